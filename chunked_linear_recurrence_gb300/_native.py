@@ -1,0 +1,232 @@
+"""ctypes binding of libsf_gdn.so (include/sf_gdn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and the current CUDA stream.  If the
+library is missing or fails to load, every call raises -- nothing falls back.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libsf_gdn.so")
+
+SF_OK, SF_ERR_INVALID_ARG, SF_ERR_UNSUPPORTED, SF_ERR_WORKSPACE, SF_ERR_CUDA, SF_ERR_TIMEOUT = range(6)
+SF_F32, SF_BF16 = 0, 1
+STATUS_NAMES = {0: "SF_OK", 1: "SF_ERR_INVALID_ARG", 2: "SF_ERR_UNSUPPORTED",
+                3: "SF_ERR_WORKSPACE", 4: "SF_ERR_CUDA", 5: "SF_ERR_TIMEOUT"}
+
+# Every symbol include/sf_gdn.h declares.
+EXPORTS = ("sf_last_error", "sf_version", "sf_gdn_fwd_workspace", "sf_gdn_chunk_fwd",
+           "sf_gdn_summary_workspace", "sf_gdn_segment_summary", "sf_state_scan",
+           "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_validate_cu_seqlens",
+           "sf_workspace_status")
+
+
+class SfError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class sf_gdn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("K", ctypes.c_int), ("V", ctypes.c_int), ("N", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsf_gdn.so not built ({path}); run "
+                               "`python -m chunked_linear_recurrence_gb300.build`")
+        lib = ctypes.CDLL(path)
+        vp, sz, st, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int
+        sp = ctypes.POINTER(sf_gdn_shape)
+        lib.sf_last_error.restype = ctypes.c_char_p
+        lib.sf_version.restype = ctypes.c_char_p
+        lib.sf_gdn_fwd_workspace.argtypes = [sp]
+        lib.sf_gdn_fwd_workspace.restype = sz
+        lib.sf_gdn_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, I, vp, vp, vp, sz, vp]
+        lib.sf_gdn_summary_workspace.argtypes = [sp, I]
+        lib.sf_gdn_summary_workspace.restype = sz
+        lib.sf_gdn_segment_summary.argtypes = [sp, vp, vp, vp, vp, vp, I, vp, vp, vp, sz, vp]
+        lib.sf_state_scan.argtypes = [I, I, I, I, vp, vp, vp, vp, vp, vp]
+        lib.sf_gdn_bwd_workspace.argtypes = [sp]
+        lib.sf_gdn_bwd_workspace.restype = sz
+        lib.sf_gdn_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.sf_validate_cu_seqlens.argtypes = [vp, I, I, vp]
+        lib.sf_workspace_status.argtypes = [vp, vp]
+        for f in ("sf_gdn_chunk_fwd", "sf_gdn_segment_summary", "sf_state_scan",
+                  "sf_gdn_chunk_bwd", "sf_validate_cu_seqlens", "sf_workspace_status"):
+            getattr(lib, f).restype = st
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != SF_OK:
+        raise SfError(rc, load().sf_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return SF_BF16
+    if dt == torch.float32:
+        return SF_F32
+    raise ValueError(f"q/k/v dtype must be bfloat16 or float32, got {dt}")
+
+
+def make_shape(q, v, cu_seqlens=None, scale=None) -> sf_gdn_shape:
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    return sf_gdn_shape(B, T, H, K, V, N, _dtype_code(q.dtype),
+                        float(scale) if scale is not None else 0.0)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Zero-initialised byte buffer (the status word must start at zero)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _f32(t):
+    if t is None:
+        return None
+    if t.dtype != torch.float32:
+        raise ValueError("gate, beta and states must be float32")
+    return t
+
+
+def sf_gdn_chunk_fwd(q, k, v, gate, beta, initial_state=None, cu_seqlens=None, scale=None,
+                     output_final_state=False, out=None, final_state=None, ws=None, stream=None):
+    """chunk_gdn forward.  Returns (out [B,T,H,V], final_state [N,H,V,K] or None)."""
+    lib = load()
+    shape = make_shape(q, v, cu_seqlens, scale)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty(shape.N, shape.H, shape.V, shape.K, dtype=torch.float32,
+                                  device=q.device)
+    need = lib.sf_gdn_fwd_workspace(ctypes.byref(shape))
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib.sf_gdn_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(_f32(gate)),
+                                _ptr(_f32(beta)), _ptr(_f32(initial_state)), _ptr(cu_seqlens),
+                                int(bool(output_final_state)), _ptr(out),
+                                _ptr(final_state) if output_final_state else None,
+                                _ptr(ws), ws.numel(), _stream(stream)))
+    return out, (final_state if output_final_state else None)
+
+
+def sf_gdn_segment_summary(k, v, gate, beta, bounds, P=None, S_ext=None, ws=None, stream=None):
+    """Affine map of each token range: returns (P [R,H,K,K], S_ext [R,H,V,K])."""
+    lib = load()
+    shape = make_shape(k, v)
+    R = bounds.shape[0]
+    if bounds.dtype != torch.int32:
+        raise ValueError("bounds must be int32 [R,2]")
+    if P is None:
+        P = torch.empty(R, shape.H, shape.K, shape.K, dtype=torch.float32, device=k.device)
+    if S_ext is None:
+        S_ext = torch.empty(R, shape.H, shape.V, shape.K, dtype=torch.float32, device=k.device)
+    need = lib.sf_gdn_summary_workspace(ctypes.byref(shape), R)
+    if ws is None:
+        ws = workspace(need, k.device)
+    _check(lib.sf_gdn_segment_summary(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(_f32(gate)),
+                                      _ptr(_f32(beta)), _ptr(bounds), R, _ptr(P), _ptr(S_ext),
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+    return P, S_ext
+
+
+def sf_state_scan(P, S_ext, S0=None, entry_states=None, final_state=None, stream=None,
+                  want_final=True):
+    """Exclusive scan of segment maps: returns (entry_states [R,H,V,K], final [H,V,K])."""
+    lib = load()
+    R, H, K, _ = P.shape
+    V = S_ext.shape[2]
+    if entry_states is None:
+        entry_states = torch.empty(R, H, V, K, dtype=torch.float32, device=P.device)
+    if want_final and final_state is None:
+        final_state = torch.empty(H, V, K, dtype=torch.float32, device=P.device)
+    _check(lib.sf_state_scan(R, H, K, V, _ptr(_f32(P)), _ptr(_f32(S_ext)), _ptr(_f32(S0)),
+                             _ptr(entry_states), _ptr(final_state), _stream(stream)))
+    return entry_states, final_state
+
+
+def sf_gdn_chunk_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state=None,
+                     cu_seqlens=None, scale=None, want_d_initial_state=True, grads=None, ws=None,
+                     stream=None):
+    """Backward of sf_gdn_chunk_fwd.  Returns dict dq, dk, dv, dgate, dbeta, d_initial_state."""
+    lib = load()
+    shape = make_shape(q, v, cu_seqlens, scale)
+    dev = q.device
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dgate=torch.empty_like(gate), dbeta=torch.empty_like(beta),
+                     d_initial_state=(torch.empty(shape.N, shape.H, shape.V, shape.K,
+                                                  dtype=torch.float32, device=dev)
+                                      if want_d_initial_state else None))
+    need = lib.sf_gdn_bwd_workspace(ctypes.byref(shape))
+    if ws is None:
+        ws = workspace(need, dev)
+    _check(lib.sf_gdn_chunk_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(_f32(gate)),
+                                _ptr(_f32(beta)), _ptr(_f32(initial_state)), _ptr(cu_seqlens),
+                                _ptr(d_out), _ptr(_f32(d_final_state)), _ptr(grads["dq"]),
+                                _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dgate"]),
+                                _ptr(grads["dbeta"]), _ptr(grads["d_initial_state"]),
+                                _ptr(ws), ws.numel(), _stream(stream)))
+    return grads
+
+
+def sf_validate_cu_seqlens(cu_seqlens, T, stream=None):
+    lib = load()
+    _check(lib.sf_validate_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(T),
+                                      _stream(stream)))
+
+
+def sf_workspace_status(ws, stream=None):
+    _check(load().sf_workspace_status(_ptr(ws), _stream(stream)))
+
+
+def fwd_workspace_bytes(shape: sf_gdn_shape) -> int:
+    return int(load().sf_gdn_fwd_workspace(ctypes.byref(shape)))
+
+
+def bwd_workspace_bytes(shape: sf_gdn_shape) -> int:
+    return int(load().sf_gdn_bwd_workspace(ctypes.byref(shape)))
+
+
+def default_scale(K: int) -> float:
+    return 1.0 / math.sqrt(K)

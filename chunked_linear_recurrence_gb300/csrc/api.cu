@@ -1,0 +1,249 @@
+// api.cu -- the C ABI (include/sf_gdn.h): argument checks, workspace layout and
+// kernel dispatch.  No entry point allocates memory or synchronises the host
+// (except the two documented synchronous helpers at the end).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/sf_gdn.h"
+#include "common.cuh"
+#include "fwd_tc.cuh"
+#include "scan.cuh"
+#include "simt_chunk.cuh"
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+sf_status fail(sf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+sf_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(SF_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr size_t kStatusBytes = 256;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-visible checks shared by every token-stream entry point.
+sf_status check_shape(const sf_gdn_shape* s, bool packed, bool need_n, const char* fn) {
+  if (!s) return fail(SF_ERR_INVALID_ARG, "%s: shape is NULL", fn);
+  if (s->B < 1 || s->T < 0 || s->H < 1 || s->K < 1 || s->V < 1)
+    return fail(SF_ERR_INVALID_ARG, "%s: need B>=1, T>=0, H>=1, K>=1, V>=1 (got B=%d T=%d H=%d K=%d V=%d)",
+                fn, s->B, s->T, s->H, s->K, s->V);
+  if (s->dtype != SF_F32 && s->dtype != SF_BF16)
+    return fail(SF_ERR_INVALID_ARG, "%s: dtype must be SF_F32 or SF_BF16", fn);
+  if (s->K != s->V || (s->K != 64 && s->K != 128))
+    return fail(SF_ERR_UNSUPPORTED, "%s: head sizes K == V in {64, 128} only (got K=%d V=%d)", fn,
+                s->K, s->V);
+  const long long elems = (long long)s->B * s->T * s->H * s->K;
+  if (elems >= (1LL << 31))
+    return fail(SF_ERR_UNSUPPORTED, "%s: tensors need int64 element offsets (%lld elements)", fn,
+                elems);
+  if (need_n) {
+    if (packed) {
+      if (s->B != 1) return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens requires B == 1", fn);
+      if (s->N < 1) return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens requires N >= 1", fn);
+    } else if (s->N != s->B) {
+      return fail(SF_ERR_INVALID_ARG, "%s: without cu_seqlens N must equal B (N=%d B=%d)", fn,
+                  s->N, s->B);
+    }
+  }
+  return SF_OK;
+}
+
+float eff_scale(const sf_gdn_shape* s) {
+  return s->scale > 0.f ? s->scale : 1.0f / std::sqrt((float)s->K);
+}
+
+int64_t bwd_slots(const sf_gdn_shape* s, bool packed) {
+  const int64_t per = (s->T + sfg::CHUNK - 1) / sfg::CHUNK;
+  return packed ? per + s->N : (int64_t)s->N * per;
+}
+
+size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sf_last_error(void) { return g_last_error.c_str(); }
+
+const char* sf_version(void) { return "sf_gdn 0.1 sm_103a"; }
+
+size_t sf_gdn_fwd_workspace(const sf_gdn_shape* shape) {
+  (void)shape;
+  return kStatusBytes;
+}
+
+sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
+                           const float* gate, const float* beta, const float* initial_state,
+                           const int32_t* cu_seqlens, int output_final_state, void* out,
+                           float* final_state, void* workspace, size_t ws_bytes,
+                           sf_stream_t stream) {
+  const char* fn = "sf_gdn_chunk_fwd";
+  sf_status st = check_shape(shape, cu_seqlens != nullptr, true, fn);
+  if (st != SF_OK) return st;
+  if (shape->T > 0 && (!q || !k || !v || !gate || !beta || !out))
+    return fail(SF_ERR_INVALID_ARG, "%s: q, k, v, gate, beta and out must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(SF_ERR_INVALID_ARG, "%s: q, k, v and out must be 16-byte aligned", fn);
+  if (output_final_state && !final_state)
+    return fail(SF_ERR_INVALID_ARG, "%s: output_final_state requires final_state", fn);
+  if (!workspace || ws_bytes < sf_gdn_fwd_workspace(shape))
+    return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn, sf_gdn_fwd_workspace(shape));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = shape->dtype == SF_BF16;
+  const int D = shape->K;
+  sfg::ChainParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = gate; p.beta = beta; p.s0 = initial_state;
+  p.cu = cu_seqlens; p.out = out; p.final_state = output_final_state ? final_state : nullptr;
+  p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
+  cudaError_t e;
+  if (bf16 && D == 128 && sfg::tc_fwd_available()) {
+    e = sfg::launch_tc_fwd(p, reinterpret_cast<int*>(workspace), cs);
+  } else {
+    e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
+size_t sf_gdn_summary_workspace(const sf_gdn_shape* shape, int R) {
+  (void)shape; (void)R;
+  return kStatusBytes;
+}
+
+sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const void* v,
+                                 const float* gate, const float* beta, const int32_t* bounds,
+                                 int R, float* P, float* S_ext, void* workspace, size_t ws_bytes,
+                                 sf_stream_t stream) {
+  const char* fn = "sf_gdn_segment_summary";
+  sf_status st = check_shape(shape, false, false, fn);
+  if (st != SF_OK) return st;
+  if (R < 0) return fail(SF_ERR_INVALID_ARG, "%s: R must be >= 0", fn);
+  if (R == 0) return SF_OK;
+  if (shape->T < 1) return fail(SF_ERR_INVALID_ARG, "%s: T must be >= 1", fn);
+  if (!k || !v || !gate || !beta || !bounds || !P || !S_ext)
+    return fail(SF_ERR_INVALID_ARG, "%s: k, v, gate, beta, bounds, P, S_ext must be non-NULL", fn);
+  if (!aligned16(k) || !aligned16(v))
+    return fail(SF_ERR_INVALID_ARG, "%s: k and v must be 16-byte aligned", fn);
+  if (!workspace || ws_bytes < sf_gdn_summary_workspace(shape, R))
+    return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn,
+                sf_gdn_summary_workspace(shape, R));
+  sfg::ChainParams p{};
+  p.k = k; p.v = v; p.g = gate; p.beta = beta; p.bounds = bounds; p.P = P; p.E = S_ext;
+  p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = R; p.scale = 1.f;
+  cudaError_t e = sfg::launch_simt_chain(p, sfg::MODE_SUMMARY, shape->dtype == SF_BF16, shape->K,
+                                         R, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
+sf_status sf_state_scan(int R, int H, int K, int V, const float* P, const float* S_ext,
+                        const float* S0, float* entry_states, float* final_state,
+                        sf_stream_t stream) {
+  const char* fn = "sf_state_scan";
+  if (R < 0 || H < 1) return fail(SF_ERR_INVALID_ARG, "%s: need R>=0 and H>=1", fn);
+  if (K != V || (K != 64 && K != 128))
+    return fail(SF_ERR_UNSUPPORTED, "%s: K == V in {64, 128} only", fn);
+  if (R > 0 && (!P || !S_ext || !entry_states))
+    return fail(SF_ERR_INVALID_ARG, "%s: P, S_ext and entry_states must be non-NULL", fn);
+  if (R == 0 && !final_state) return SF_OK;
+  cudaError_t e = sfg::launch_state_scan(R, H, K, P, S_ext, S0, entry_states, final_state,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
+size_t sf_gdn_bwd_workspace(const sf_gdn_shape* shape) {
+  if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0) return kStatusBytes;
+  // enough for both layouts: dense needs N*ceil(T/64) slots, packed (B == 1)
+  // at most ceil(T/64) + N
+  const int64_t per = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK;
+  const int64_t n = shape->N > 0 ? shape->N : shape->B;
+  int64_t slots = n * per;
+  if (shape->B == 1 && slots < per + n) slots = per + n;
+  const size_t one = (size_t)slots * shape->H * shape->K * shape->V * sizeof(float);
+  return kStatusBytes + 2 * round_up(one);
+}
+
+sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
+                           const float* gate, const float* beta, const float* initial_state,
+                           const int32_t* cu_seqlens, const void* d_out, const float* d_final_state,
+                           void* dq, void* dk, void* dv, float* dgate, float* dbeta,
+                           float* d_initial_state, void* workspace, size_t ws_bytes,
+                           sf_stream_t stream) {
+  const char* fn = "sf_gdn_chunk_bwd";
+  const bool packed = cu_seqlens != nullptr;
+  sf_status st = check_shape(shape, packed, true, fn);
+  if (st != SF_OK) return st;
+  const bool bf16 = shape->dtype == SF_BF16;
+  const int D = shape->K;
+  if (!bf16 && D != 64)
+    return fail(SF_ERR_UNSUPPORTED, "%s: FP32 inputs support K = V = 64 only", fn);
+  if (shape->T > 0 && (!q || !k || !v || !gate || !beta || !d_out || !dq || !dk || !dv || !dgate ||
+                       !dbeta))
+    return fail(SF_ERR_INVALID_ARG, "%s: inputs and gradient outputs must be non-NULL", fn);
+  const size_t need = sf_gdn_bwd_workspace(shape);
+  if (!workspace || ws_bytes < need)
+    return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn, need);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t slots = bwd_slots(shape, packed);
+  const size_t one = round_up((size_t)slots * shape->H * D * D * sizeof(float));
+  char* ws = reinterpret_cast<char*>(workspace);
+  sfg::ChainParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = gate; p.beta = beta; p.s0 = initial_state; p.cu = cu_seqlens;
+  p.ckpt = reinterpret_cast<float*>(ws + kStatusBytes);
+  p.tape = reinterpret_cast<float*>(ws + kStatusBytes + one);
+  p.dout = d_out; p.dsf = d_final_state; p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dgate;
+  p.dbeta = dbeta; p.ds0 = d_initial_state;
+  p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
+  cudaError_t e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  e = sfg::launch_simt_bwd(p, bf16, D, slots, cs);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
+sf_status sf_validate_cu_seqlens(const int32_t* cu_seqlens, int N, int T, sf_stream_t stream) {
+  const char* fn = "sf_validate_cu_seqlens";
+  if (!cu_seqlens || N < 1 || T < 0) return fail(SF_ERR_INVALID_ARG, "%s: bad arguments", fn);
+  std::string host((size_t)(N + 1) * sizeof(int32_t), '\0');
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&host[0], cu_seqlens, host.size(), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  const int32_t* c = reinterpret_cast<const int32_t*>(host.data());
+  if (c[0] != 0) return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens[0] = %d, expected 0", fn, c[0]);
+  for (int i = 0; i < N; ++i)
+    if (c[i + 1] < c[i])
+      return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens decreases at %d (%d -> %d)", fn, i, c[i],
+                  c[i + 1]);
+  if (c[N] > T) return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens[N] = %d exceeds T = %d", fn, c[N], T);
+  return SF_OK;
+}
+
+sf_status sf_workspace_status(void* workspace, sf_stream_t stream) {
+  const char* fn = "sf_workspace_status";
+  if (!workspace) return fail(SF_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
+  int word = 0;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int), cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (word != 0) return fail((sf_status)word, "%s: a kernel reported status %d", fn, word);
+  return SF_OK;
+}
+
+}  // extern "C"

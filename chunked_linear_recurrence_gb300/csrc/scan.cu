@@ -1,0 +1,68 @@
+// scan.cu -- exclusive scan of segment maps (Attention Gym "Linear Attention",
+// section "Context Parallelism": a prefix scan over the [bias; transition]
+// summaries recovers every range's entry state; Megatron-LM PR "Mamba2
+// state-passing context parallelism": exclusive causal scan of (S_ext, a_block)).
+//
+//   entry_0 = S0,  entry_{j+1} = entry_j P_j + S_ext_j,  final = entry_R
+//
+// Rows of the state are independent under right-multiplication by P, so the
+// scan is split over (head, block of RB rows); each CTA keeps its rows in
+// shared memory and walks the R segments in order.  FP32 throughout.
+#include "common.cuh"
+#include "scan.cuh"
+
+namespace sfg {
+
+template <int D, int RB>
+__global__ void __launch_bounds__(D) state_scan_kernel(int R, int H, const float* __restrict__ P,
+                                                       const float* __restrict__ E,
+                                                       const float* __restrict__ S0,
+                                                       float* __restrict__ entry,
+                                                       float* __restrict__ final_state) {
+  __shared__ float cur[RB][D];
+  const int c = threadIdx.x;                 // column owned by this thread
+  const int h = blockIdx.y, r0 = blockIdx.x * RB;
+  const size_t SZ = (size_t)D * D;
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+    cur[r][c] = S0 ? S0[(size_t)h * SZ + (size_t)(r0 + r) * D + c] : 0.f;
+  __syncthreads();
+  for (int j = 0; j < R; ++j) {
+    const size_t base = ((size_t)j * H + h) * SZ;
+    float acc[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      entry[base + (size_t)(r0 + r) * D + c] = cur[r][c];
+      acc[r] = E[base + (size_t)(r0 + r) * D + c];
+    }
+    const float* Pj = P + base;
+#pragma unroll 4
+    for (int m = 0; m < D; ++m) {
+      const float pm = Pj[(size_t)m * D + c];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) acc[r] += cur[r][m] * pm;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RB; ++r) cur[r][c] = acc[r];
+    __syncthreads();
+  }
+  if (final_state)
+#pragma unroll
+    for (int r = 0; r < RB; ++r) final_state[(size_t)h * SZ + (size_t)(r0 + r) * D + c] = cur[r][c];
+}
+
+cudaError_t launch_state_scan(int R, int H, int D, const float* P, const float* E,
+                              const float* S0, float* entry, float* final_state, cudaStream_t st) {
+  constexpr int RB = 8;
+  if (D == 64)
+    state_scan_kernel<64, RB><<<dim3(64 / RB, H), 64, 0, st>>>(R, H, P, E, S0, entry, final_state);
+  else if (D == 128)
+    state_scan_kernel<128, RB><<<dim3(128 / RB, H), 128, 0, st>>>(R, H, P, E, S0, entry,
+                                                                  final_state);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace sfg

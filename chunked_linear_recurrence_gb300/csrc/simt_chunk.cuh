@@ -1,0 +1,45 @@
+// simt_chunk.cuh -- parameters and launchers of the FP32 CUDA-core chunk kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sfg {
+
+enum { MODE_FWD = 0, MODE_SUMMARY = 1, MODE_REPLAY = 2 };
+
+// One parameter block for every chain kernel; unused members are NULL.
+struct ChainParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* s0;        // [N,H,V,K] or NULL
+  const int32_t* cu;      // [N+1] or NULL
+  const int32_t* bounds;  // [R,2] (summary)
+  void* out;              // [B,T,H,V]
+  float* final_state;     // [N,H,V,K] or NULL
+  float* P;               // [R,H,K,K] (summary)
+  float* E;               // [R,H,V,K] (summary)
+  float* ckpt;            // [slots,H,V,K] chunk-entry states (replay / backward)
+  float* tape;            // [slots,H,V,K] chunk-exit cotangents (backward)
+  const void* dout;       // [B,T,H,V] (backward)
+  const float* dsf;       // [N,H,V,K] or NULL (backward)
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dg;
+  float* dbeta;
+  float* ds0;             // [N,H,V,K] or NULL
+  int B, T, H, N;
+  float scale;
+};
+
+// Forward / summary / replay chain kernel: `items` = N (fwd, replay) or R (summary).
+cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, int items,
+                              cudaStream_t st);
+// Backward after a replay: reverse cotangent chain then per-chunk token gradients.
+cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
+                            cudaStream_t st);
+
+}  // namespace sfg

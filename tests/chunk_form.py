@@ -67,3 +67,83 @@ def summary_seq(k, v, g, beta, C=CHUNK):
         Ec = U.T @ (dec[:, None] * k[sl])
         P, E = P @ Pc, E @ Pc + Ec
     return P, E
+
+
+def bwd_chunk(q, k, v, g, beta, S, dO, dSn, scale):
+    """Chunk-form backward of one chunk (L <= 64 rows) given its entry state S
+    and the cotangent dSn of its exit state.  Returns (dq, dk, dv, dg, dbeta,
+    dS_entry).  This is the algebra the CUDA backward follows, step by step."""
+    L, Kd = k.shape
+    gam = np.cumsum(g)
+    eg = np.exp(gam)
+    dec = np.exp(gam[-1] - gam)
+    Gam = np.exp(np.minimum(gam[:, None] - gam[None, :], 0.0))
+    low = np.tril(np.ones((L, L)), -1)
+    lowd = np.tril(np.ones((L, L)))
+    Ak = low * Gam * (k @ k.T)                 # A = diag(beta) Ak
+    T = np.linalg.inv(np.eye(L) + beta[:, None] * Ak)
+    Aqk = lowd * Gam * (q @ k.T)
+    W = T @ ((beta * eg)[:, None] * k)
+    U = T @ (beta[:, None] * v)
+    Delta = U - W @ S.T
+    dgam = np.zeros(L)
+    # reverse chain pieces
+    dDelta = scale * Aqk.T @ dO + dec[:, None] * (k @ dSn.T)
+    dS_entry = eg[-1] * dSn + scale * dO.T @ (eg[:, None] * q) - dDelta.T @ W
+    # output: O = scale (diag(eg) Q S^T + Aqk Delta)
+    dAqk = scale * dO @ Delta.T
+    rho = dAqk * Aqk
+    dgam += rho.sum(1) - rho.sum(0)
+    G = dAqk * Gam * lowd
+    dQfirst = scale * eg[:, None] * (dO @ S)
+    dq = dQfirst + G @ k
+    dk = G.T @ q
+    dgam += (q * dQfirst).sum(1)
+    # exit state: S_next = eg_C S + Delta^T diag(dec) K
+    Z = Delta @ dSn
+    dk += dec[:, None] * Z
+    ddec = (k * Z).sum(1)
+    dgam -= dec * ddec
+    dgam[-1] += (dec * ddec).sum() + eg[-1] * (dSn * S).sum()
+    # Delta = U - W S^T
+    dW = -dDelta @ S
+    TtdU = T.T @ dDelta
+    dv = beta[:, None] * TtdU
+    dbeta = (v * TtdU).sum(1)
+    dT = dDelta @ (beta[:, None] * v).T
+    TtdW = T.T @ dW
+    dk += (beta * eg)[:, None] * TtdW
+    kt = (k * TtdW).sum(1)
+    dbeta += eg * kt
+    dgam += beta * eg * kt
+    dT += dW @ ((beta * eg)[:, None] * k).T
+    dA = -(T.T @ dT @ T.T) * low
+    dbeta += (dA * Ak).sum(1)
+    rhoA = dA * beta[:, None] * Ak
+    dgam += rhoA.sum(1) - rhoA.sum(0)
+    dKK = dA * beta[:, None] * Gam * low
+    dk += dKK @ k + dKK.T @ k
+    dg = np.cumsum(dgam[::-1])[::-1]
+    return dq, dk, dv, dg, dbeta, dS_entry
+
+
+def bwd_seq(q, k, v, g, beta, S0, dO, dSf, scale, C=CHUNK):
+    """Chunk-form backward of one sequence: replay entry states, then walk the
+    chunks in reverse carrying the state cotangent."""
+    L = q.shape[0]
+    starts = list(range(0, L, C))
+    ents = []
+    S = S0
+    for c0 in starts:
+        ents.append(S)
+        sl = slice(c0, min(c0 + C, L))
+        _, S = fwd_seq(q[sl], k[sl], v[sl], g[sl], beta[sl], S, scale, C)
+    grads = [np.zeros_like(x) for x in (q, k, v, g, beta)]
+    dS = dSf
+    for c0, Sc in zip(reversed(starts), reversed(ents)):
+        sl = slice(c0, min(c0 + C, L))
+        dq, dk, dv, dg, db, dS = bwd_chunk(q[sl], k[sl], v[sl], g[sl], beta[sl], Sc,
+                                          dO[sl], dS, scale)
+        for gr, x in zip(grads, (dq, dk, dv, dg, db)):
+            gr[sl] = x
+    return (*grads, dS)

@@ -1,0 +1,90 @@
+"""The C-ABI library loads without a GPU, exports every function include/*.h
+declares, and rejects bad arguments on the host before anything launches
+(these calls never reach a CUDA API, so they run on the CPU machine)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(sf_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_linear_recurrence_gb300 import _native
+    if not os.path.exists(_native.LIB_PATH):
+        from chunked_linear_recurrence_gb300 import build
+        build.build()
+    return _native.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from chunked_linear_recurrence_gb300 import _native
+    names = declared_functions()
+    assert len(names) >= 10
+    assert names <= set(_native.EXPORTS), names - set(_native.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.sf_version().decode().startswith("sf_gdn")
+
+
+def _shape(**kw):
+    from chunked_linear_recurrence_gb300._native import sf_gdn_shape
+    d = dict(B=1, T=64, H=1, K=128, V=128, N=1, dtype=1, scale=0.0)
+    d.update(kw)
+    return sf_gdn_shape(**d)
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced
+
+
+def _fwd(lib, shape, out_final=0, ws_bytes=4096, ptr=FAKE, cu=None, fin=None):
+    return lib.sf_gdn_chunk_fwd(ctypes.byref(shape), ptr, ptr, ptr, ptr, ptr, None, cu, out_final,
+                                ptr, fin, FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=96, V=96), 2), (dict(K=128, V=64), 2), (dict(T=-1), 1), (dict(H=0), 1),
+    (dict(dtype=7), 1), (dict(N=2), 1), (dict(B=40000, T=40000), 2)])
+def test_forward_rejects_bad_shapes(lib, kw, status):
+    assert _fwd(lib, _shape(**kw)) == status
+    assert len(lib.sf_last_error()) > 0
+
+
+def test_forward_rejects_bad_pointers_and_workspace(lib):
+    assert _fwd(lib, _shape(), ptr=ctypes.c_void_p(0)) == 1
+    assert _fwd(lib, _shape(), ptr=ctypes.c_void_p((1 << 20) + 4)) == 1      # misaligned
+    assert _fwd(lib, _shape(), out_final=1, fin=None) == 1
+    assert _fwd(lib, _shape(), ws_bytes=8) == 3
+    # cu_seqlens requires B == 1
+    assert _fwd(lib, _shape(B=2, N=3), cu=FAKE) == 1
+
+
+def test_other_entry_points_reject_bad_arguments(lib):
+    s = _shape()
+    assert lib.sf_gdn_segment_summary(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, -1, FAKE,
+                                      FAKE, FAKE, 4096, None) == 1
+    assert lib.sf_gdn_segment_summary(ctypes.byref(s), FAKE, None, FAKE, FAKE, FAKE, 2, FAKE,
+                                      FAKE, FAKE, 4096, None) == 1
+    assert lib.sf_state_scan(2, 1, 96, 96, FAKE, FAKE, None, FAKE, None, None) == 2
+    assert lib.sf_state_scan(2, 1, 128, 128, None, FAKE, None, FAKE, None, None) == 1
+    s32 = _shape(dtype=0)
+    assert lib.sf_gdn_chunk_bwd(ctypes.byref(s32), *([FAKE] * 5), None, None, FAKE, None,
+                                *([FAKE] * 5), None, FAKE, 1 << 40, None) == 2
+    need = lib.sf_gdn_bwd_workspace(ctypes.byref(s))
+    assert need >= 256 + 2 * 128 * 128 * 4      # one chunk: checkpoint + cotangent tape
+    assert lib.sf_gdn_chunk_bwd(ctypes.byref(s), *([FAKE] * 5), None, None, FAKE, None,
+                                *([FAKE] * 5), None, FAKE, need - 1, None) == 3

@@ -27,3 +27,18 @@ def test_chunk_form_summary_equals_probing():
     P2, E2 = summary_seq(k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0])
     np.testing.assert_allclose(P2, P[0, 0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(E2, E[0, 0], rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,K,V", [(64, 8, 8), (150, 6, 10), (1, 4, 4)])
+def test_chunk_form_backward_equals_oracle(T, K, V):
+    from chunk_form import bwd_seq
+    rng = np.random.default_rng(T * 3 + K)
+    q, k, v, g, beta, S0 = rand_inputs(1, T, 1, K, V, rng)
+    dO = rng.normal(size=(1, T, 1, V))
+    dSf = rng.normal(size=(1, 1, V, K))
+    ref = oracle.gdn_bwd(q, k, v, g, beta, S0, dO, dSf, scale=0.3)
+    got = bwd_seq(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0], S0[0, 0],
+                  dO[0, :, 0], dSf[0, 0], 0.3)
+    for name, x in zip(["dq", "dk", "dv", "dg", "dbeta"], got[:5]):
+        np.testing.assert_allclose(x, ref[name][0, :, 0], rtol=1e-9, atol=1e-11, err_msg=name)
+    np.testing.assert_allclose(got[5], ref["d_initial_state"][0, 0], rtol=1e-9, atol=1e-11)
