@@ -109,7 +109,7 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   p.cu = cu_seqlens; p.out = out; p.final_state = output_final_state ? final_state : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
-  if (bf16 && D == 128 && sfg::tc_fwd_available()) {
+  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
     e = sfg::launch_tc_fwd(p, reinterpret_cast<int*>(workspace), cs);
   } else {
     e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
