@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "fwd_tc.cuh"
+#include "solve_tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace sfg {
@@ -41,26 +42,28 @@ constexpr int D = 128;
 constexpr int NTHR = 256;
 
 // Shared-memory map (bytes from a 1024-aligned base).  Panel layout, see tc_ptx.cuh.
-constexpr uint32_t OFF_KQ = 0;          // 2 panels x 16 KB: rows 0-63 K, rows 64-127 Q
+constexpr uint32_t OFF_KQ = 0;          // 2 stages x 32 KB; a stage is 2 panels x 16 KB:
+constexpr uint32_t KQ_STAGE = 32768;    //   rows 0-63 K, rows 64-127 Q of one chunk
 constexpr uint32_t KQ_PANEL = 16384;
-constexpr uint32_t OFF_V = 32768;       // 2 panels x 8 KB: V [64 tokens][128]
+constexpr uint32_t OFF_V = 65536;       // 2 panels x 8 KB: V [64 tokens][128]
 constexpr uint32_t V_PANEL = 8192;
-constexpr uint32_t OFF_S = 49152;       // 2 panels x 16 KB: S (BF16) [128 v][128 k]
+constexpr uint32_t OFF_S = 81920;       // 2 panels x 16 KB: S (BF16) [128 v][128 k]
 constexpr uint32_t S_PANEL = 16384;
-constexpr uint32_t OFF_WT = 81920;      // 16 KB: W^T [128 k][64 i]
-constexpr uint32_t OFF_DT = 98304;      // 16 KB: Delta^T [128 v][64 j]
-constexpr uint32_t OFF_DDT = 114688;    // 16 KB: (Delta^T diag(dec)) [128 v][64 j]
-constexpr uint32_t OFF_T1 = 131072;     // 8 KB: T'  [64 i][64 j]
-constexpr uint32_t OFF_T2 = 139264;     // 8 KB: T'' [64 i][64 j]
-constexpr uint32_t OFF_AH = 147456;     // 8 KB: Ahat [64 i][64 j]
-constexpr uint32_t OFF_A32 = 155648;    // FP32 A [64][65]
-constexpr uint32_t OFF_T32 = 172288;    // FP32 T [64][65]
-constexpr uint32_t OFF_SCR = 188928;    // FP32 scratch [1024]
-constexpr uint32_t OFF_VEC = 193024;    // FP32 vectors: g, beta, gamma, e^gamma, dec (5 x 64)
-constexpr uint32_t OFF_BAR = 194304;    // mbarriers + TMEM address
+constexpr uint32_t OFF_WT = 114688;     // 16 KB: W^T [128 k][64 i]
+constexpr uint32_t OFF_DT = 131072;     // 16 KB: Delta^T [128 v][64 j]; solve scratch before
+constexpr uint32_t OFF_DDT = 147456;    // 16 KB: (Delta^T diag(dec)) [128 v][64 j]
+constexpr uint32_t OFF_T1 = 163840;     // 8 KB: T'  [64 i][64 j]   } output staging
+constexpr uint32_t OFF_T2 = 172032;     // 8 KB: T'' [64 i][64 j]   } [64][128] BF16 after
+constexpr uint32_t OFF_AH = 180224;     // 8 KB: Ahat [64 i][64 j]
+constexpr uint32_t OFF_A32 = 188416;    // FP32 A [64][SOLVE_LD]
+constexpr uint32_t OFF_T32 = 205824;    // FP32 T [64][SOLVE_LD]
+constexpr uint32_t OFF_VEC = 223232;    // FP32 vectors: g, beta, gamma, e^gamma, dec, e^+, e^- (7 x 64)
+constexpr uint32_t OFF_BAR = 225024;    // mbarriers + TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack to align the base to 1024
-constexpr int LD32 = 65;
+static_assert(OFF_A32 + 64 * SOLVE_LD * 4 <= OFF_T32, "A32");
+static_assert(OFF_T32 + 64 * SOLVE_LD * 4 <= OFF_VEC, "T32");
+static_assert(32 * SOLVE_LD * 4 <= 16384, "solve scratch fits the Delta^T tile");
 
 // TMEM columns (FP32 accumulators, 128 lanes each).
 constexpr uint32_t TM_S = 0;      // S [v][k]        128 cols
@@ -111,15 +114,19 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t sb = smem_u32(sm);
   float* sA = reinterpret_cast<float*>(sm + OFF_A32);
   float* sT = reinterpret_cast<float*>(sm + OFF_T32);
-  float* scr = reinterpret_cast<float*>(sm + OFF_SCR);
+  float* sX = reinterpret_cast<float*>(sm + OFF_DT);       // solve scratch (Delta^T tile is free then)
   float* sg = reinterpret_cast<float*>(sm + OFF_VEC);
   float* sbeta = sg + 64;
   float* sgam = sbeta + 64;
-  float* seg = sgam + 64;
-  float* sdec = seg + 64;
-  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_mma = bar_load + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_load + 2);
+  float* seg = sgam + 64;      // e^{gamma_i}
+  float* sdec = seg + 64;      // e^{gamma_C - gamma_i}
+  float* sep = sdec + 64;      // e^{gamma_i - mid}   (factorised decay, see below)
+  float* sem = sep + 64;       // e^{mid - gamma_j}
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [2] K/Q stage loaded
+  uint64_t* bar_v = bar_kq + 2;                                    // V loaded
+  uint64_t* bar_mma = bar_kq + 3;                                  // MMA batch done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 4);
+  int* flag = reinterpret_cast<int*>(tmem_slot + 1);               // per-chunk decay path
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
@@ -129,13 +136,30 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int row = q4 * 32 + lane;          // accumulator row (TMEM lane) of this thread
   const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
+  int64_t bos, eos;
+  seq_span(n, p.B, p.T, p.cu, bos, eos);
+  const int nchunks = (int)((eos - bos + CHUNK - 1) / CHUNK);
+  const size_t state_off = ((size_t)n * H + h) * D * D;
+
   if (tid == 0) {
-    mbar_init(bar_load, 1);
+    mbar_init(bar_kq, 1);
+    mbar_init(bar_kq + 1, 1);
+    mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    if (nchunks > 0) {        // prologue: chunk 0's K, Q and V
+      mbar_arrive_expect_tx(bar_kq, 4 * 8192);
+      mbar_arrive_expect_tx(bar_v, 2 * 8192);
+#pragma unroll
+      for (int pnl = 0; pnl < 2; ++pnl) {
+        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL, &tmK, bar_kq, 64 * pnl, h, (int)bos);
+        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL + 8192, &tmQ, bar_kq, 64 * pnl, h, (int)bos);
+        tma_load_3d(sm + OFF_V + pnl * V_PANEL, &tmV, bar_v, 64 * pnl, h, (int)bos);
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TM_COLS);
@@ -146,10 +170,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
   const uint32_t tl = tm + lane_off;       // this warp's lane base
-
-  int64_t bos, eos;
-  seq_span(n, p.B, p.T, p.cu, bos, eos);
-  const size_t state_off = ((size_t)n * H + h) * D * D;
 
   // initial state -> TMEM (FP32) and the BF16 operand copy
 #pragma unroll
@@ -177,18 +197,24 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
 
-  uint32_t ph_load = 0, ph_mma = 0;
+  uint32_t ph_mma = 0;
   bool ok = true;
-  for (int64_t c0 = bos; c0 < eos && ok; c0 += CHUNK) {
+  for (int c = 0; c < nchunks && ok; ++c) {
+    const int64_t c0 = bos + (int64_t)c * CHUNK;
     const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
-    // ---- load the chunk: K, Q, V tiles by TMA; gate and beta by plain loads
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_load, 6 * 8192);
+    const int st = c & 1;
+    uint8_t* kq = sm + OFF_KQ + st * KQ_STAGE;
+    const uint32_t kqa = sb + OFF_KQ + st * KQ_STAGE;
+    // ---- load the chunk: prefetch the next chunk's K/Q into the other stage
+    //      (its previous chunk is finished); gate and beta by plain loads
+    if (tid == 0 && c + 1 < nchunks) {
+      uint64_t* bn = bar_kq + (st ^ 1);
+      uint8_t* kqn = sm + OFF_KQ + (st ^ 1) * KQ_STAGE;
+      mbar_arrive_expect_tx(bn, 4 * 8192);
 #pragma unroll
       for (int pnl = 0; pnl < 2; ++pnl) {
-        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL, &tmK, bar_load, 64 * pnl, h, (int)c0);
-        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL + 8192, &tmQ, bar_load, 64 * pnl, h, (int)c0);
-        tma_load_3d(sm + OFF_V + pnl * V_PANEL, &tmV, bar_load, 64 * pnl, h, (int)c0);
+        tma_load_3d(kqn + pnl * KQ_PANEL, &tmK, bn, 64 * pnl, h, (int)(c0 + CHUNK));
+        tma_load_3d(kqn + pnl * KQ_PANEL + 8192, &tmQ, bn, 64 * pnl, h, (int)(c0 + CHUNK));
       }
     }
     if (tid < 64) {
@@ -196,8 +222,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       sg[tid] = (tid < L) ? p.g[off] : 0.f;
       sbeta[tid] = (tid < L) ? p.beta[off] : 0.f;
     }
-    if (!(ok = cta_wait(bar_load, ph_load, p.status))) break;
-    ph_load ^= 1;
+    if (!(ok = cta_wait(bar_kq + st, (uint32_t)(c >> 1) & 1u, p.status))) break;
+    if (!(ok = cta_wait(bar_v, (uint32_t)c & 1u, p.status))) break;
     if (L < CHUNK) {
       // rows past the sequence end belong to the next sequence (or are past
       // the tensor): zero them so they contribute nothing to any product
@@ -206,17 +232,38 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
         const int r = L + rem / 8, ch = rem % 8;
         const int pnl = t6 & 1, which = t6 >> 1;
-        uint32_t off = (which == 2) ? OFF_V + pnl * V_PANEL
-                                    : OFF_KQ + pnl * KQ_PANEL + (which == 1 ? 8192u : 0u);
-        *reinterpret_cast<uint4*>(sm + off + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        uint8_t* base = (which == 2) ? sm + OFF_V + pnl * V_PANEL
+                                     : kq + pnl * KQ_PANEL + (which == 1 ? 8192u : 0u);
+        *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
     }
     __syncthreads();
-    if (warp == 0) warp_cumsum64(sg, sgam, lane);
-    __syncthreads();
-    if (tid < 64) {
-      seg[tid] = expf(sgam[tid]);
-      sdec[tid] = expf(sgam[63] - sgam[tid]);
+    if (warp == 0) {
+      warp_cumsum64(sg, sgam, lane);
+      __syncwarp();
+      // decay factors: e^{gamma_i - gamma_j} = e^{gamma_i - mid} e^{mid - gamma_j} when the
+      // chunk's gamma range keeps both factors inside e^{+-40} (no overflow, no
+      // denormals); otherwise every entry takes its own exponential
+      const float a0 = sgam[2 * lane], a1 = sgam[2 * lane + 1];
+      float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      }
+      const bool fact = (mx - mn) <= 80.f;
+      const float mid = 0.5f * (mx + mn);
+      if (lane == 0) *flag = fact ? 1 : 0;
+      const float gC = sgam[63];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 2 * lane + e;
+        const float gi = sgam[i];
+        seg[i] = expf(gi);
+        sdec[i] = expf(gC - gi);
+        sep[i] = fact ? expf(gi - mid) : 0.f;
+        sem[i] = fact ? expf(mid - gi) : 0.f;
+      }
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -226,7 +273,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a = sb + OFF_KQ + (kk >> 2) * KQ_PANEL + (kk & 3) * 32;
+        const uint32_t a = kqa + (kk >> 2) * KQ_PANEL + (kk & 3) * 32;
         mma_bf16(tm + TM_KQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), ID_KQ, kk > 0);
       }
       mma_commit(bar_mma);
@@ -238,36 +285,40 @@ __global__ void __launch_bounds__(NTHR, 1)
       float x[32];
       tmem_ld32(tl + TM_KQ + 32 * half, x);
       tmem_ld_wait();
-      if (row < 64) {
-        const int i = row;
-        const float gi = sgam[i], bi = sbeta[i];
+      const bool fact = *flag != 0;
+      const int i = row & 63;
+      const float gi = sgam[i], epi = sep[i];
+      const float bi = (row < 64) ? sbeta[i] : 1.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * half + jj;
+        const float dcy = fact ? epi * sem[j] : expf(j <= i ? gi - sgam[j] : 0.f);
+        x[jj] *= bi * dcy;
+      }
+      if (row < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * half + jj;
-          sA[i * LD32 + j] = (j < i) ? bi * expf(gi - sgam[j]) * x[jj] : 0.f;
+          sA[i * SOLVE_LD + j] = (j < i) ? x[jj] : 0.f;
         }
-      } else {
-        const int i = row - 64;
-        const float gi = sgam[i];
+      } else {                 // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * half + jj;
-          x[jj] = (j <= i) ? expf(gi - sgam[j]) * x[jj] : 0.f;
-        }
+        for (int jj = 0; jj < 32; ++jj)
+          if (32 * half + jj > i) x[jj] = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_AH, i, 32 * half + 8 * e, 8192, x + 8 * e);
       }
     }
     __syncthreads();
     // ---- Pre: T = (I + A)^{-1} (FP32), then T' = T diag(beta), T'' = T diag(beta e^gamma)
-    solve_unit_lower64(sA, sT, LD32, scr, tid, NTHR, CtaBar());
+    solve64_tc(sA, sT, sX, tid, NTHR, CtaBar());
     for (int idx = tid; idx < 64 * 8; idx += NTHR) {
       const int i = idx >> 3, cg = (idx & 7) * 8;
       float t1[8], t2[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int j = cg + e;
-        const float t = sT[i * LD32 + j] * sbeta[j];
+        const float t = sT[i * SOLVE_LD + j] * sbeta[j];
         t1[e] = t;
         t2[e] = t * seg[j];
       }
@@ -281,7 +332,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tm + TM_WT, sdesc_sw128(sb + OFF_KQ + kk * 2048, KQ_PANEL, 1024),
+        mma_bf16(tm + TM_WT, sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024),
                  sdesc_sw128(sb + OFF_T2 + kk * 32, 0, 1024), ID_WT, kk > 0);
       }
 #pragma unroll
@@ -294,6 +345,12 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (!(ok = cta_wait(bar_mma, ph_mma, p.status))) break;
     ph_mma ^= 1;
     tc_fence_after();
+    if (tid == 0 && c + 1 < nchunks) {      // V is free: load the next chunk's
+      mbar_arrive_expect_tx(bar_v, 2 * 8192);
+#pragma unroll
+      for (int pnl = 0; pnl < 2; ++pnl)
+        tma_load_3d(sm + OFF_V + pnl * V_PANEL, &tmV, bar_v, 64 * pnl, h, (int)(c0 + CHUNK));
+    }
     {
       float x[32];
       tmem_ld32(tl + TM_WT + 32 * half, x);
@@ -316,7 +373,7 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t a = sb + OFF_S + (kk >> 2) * S_PANEL + (kk & 3) * 32;
-        const uint32_t b = sb + OFF_KQ + (kk >> 2) * KQ_PANEL + 8192 + (kk & 3) * 32;
+        const uint32_t b = kqa + (kk >> 2) * KQ_PANEL + 8192 + (kk & 3) * 32;
         mma_bf16(tm + TM_SQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(b, 0, 1024), ID_SQ, kk > 0);
       }
       mma_commit(bar_mma);
@@ -356,7 +413,7 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         mma_bf16(tm + TM_S, sdesc_sw128(sb + OFF_DDT + kk * 32, 0, 1024),
-                 sdesc_sw128(sb + OFF_KQ + kk * 2048, KQ_PANEL, 1024), ID_SU, 1);
+                 sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024), ID_SU, 1);
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -369,16 +426,17 @@ __global__ void __launch_bounds__(NTHR, 1)
     ph_mma ^= 1;
     tc_fence_after();
     {
+      // out[i][v] = scale (e^{gamma_i} SQ[v][i] + OA[v][i]), staged as a [64][128]
+      // BF16 row-major tile in the (now free) T'/T'' region, then stored 16 B at a time
       float sq[32], oa[32];
       tmem_ld32(tl + TM_SQ + 32 * half, sq);
       tmem_ld32(tl + TM_OA + 32 * half, oa);
       tmem_ld_wait();
-      __nv_bfloat16* orow = p.out + ((size_t)c0 * H + h) * D + row;
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + OFF_T1);
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int i = 32 * half + jj;
-        if (i < L)
-          orow[(size_t)i * H * D] = __float2bfloat16_rn(p.scale * (seg[i] * sq[jj] + oa[jj]));
+        stage[i * D + row] = __float2bfloat16_rn(p.scale * (seg[i] * sq[jj] + oa[jj]));
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -391,6 +449,15 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
     fence_proxy_async_smem();
     tc_fence_before();
+    __syncthreads();
+    {
+      const uint4* stage = reinterpret_cast<const uint4*>(sm + OFF_T1);
+      for (int idx = tid; idx < 64 * 16; idx += NTHR) {
+        const int i = idx >> 4, ch = idx & 15;
+        if (i < L)
+          *reinterpret_cast<uint4*>(p.out + ((size_t)(c0 + i) * H + h) * D + ch * 8) = stage[idx];
+      }
+    }
     __syncthreads();
     tc_fence_after();
   }
