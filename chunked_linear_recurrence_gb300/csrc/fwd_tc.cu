@@ -4,25 +4,32 @@
 //
 // One CTA per (sequence, head) chain walks its 64-token chunks in order
 // (StateFlow section 2.2, Eq. 2: Pre -> ST -> Out per chunk; section 3.1,
-// Eq. 4-5: the chunk's output state is the next chunk's input state).  Every
-// product is arranged so that its M dimension is 128 (the full TMEM lane
-// count): the state-side products run "transposed", with the value index v
-// (or the key index k) on the M axis and the 64 chunk tokens on N:
+// Eq. 4-5: a chunk's output state is the next chunk's input state).  The CTA
+// is warp-specialised so that the next chunk's preparation overlaps the
+// current chunk's state transition (the on-chip form of StateFlow's
+// split-and-overlap schedule, section 3.4.2, Eq. 17):
 //
-//   KQ   = [K; Q] K^T                       M=128 (64 key rows, 64 query rows), N=64, K=128
-//   W^T  = K^T T''^T,  T'' = T diag(beta e^gamma)                   M=128, N=64, K=64
-//   U^T  = V^T T'^T,   T'  = T diag(beta)     (into the Delta^T accumulator)
-//   Delta^T += -S W^T                                              M=128, N=64, K=128
-//   SQ   = S Q^T                                                   M=128, N=64, K=128
-//   S   <- e^{gamma_C} S + (Delta^T diag(dec)) K                   M=128, N=128, K=64
-//   OA   = Delta^T Ahat^T,  Ahat = M o Gamma o Q K^T               M=128, N=64, K=64
-//   out[i][v] = scale (e^{gamma_i} SQ[v][i] + OA[v][i])
+//   warp 0      loader: TMA of K/Q (3-stage ring) and V (2-stage ring), gate/beta
+//   warp 1      MMA issuer: one thread issues tcgen05.mma from a non-blocking
+//               priority loop (state-transition products first)
+//   warps 4-7   state: the serial chain -- Delta^T and the state S between MMAs
+//   warps 8-11  prep:  decays, A and Ahat, e^gamma-scaled Q, the triangular
+//               solve, T' and T'', the W^T tile -- for the chunk ahead
+//   warps 12-15 out:   reads the output accumulator and stores BF16 rows
 //
-// The 64x64 triangular solve T = (I + A)^{-1} runs on the CUDA cores in FP32
-// (hierarchical 16x16 blocks); its BF16 copies T', T'' are tensor-core
-// operands, as are the BF16 copies of the state, W and Delta (the state itself
-// stays FP32 in TMEM; the pages stage chunk-entry states in the Q/K/V dtype in
-// the same way).
+// Products (every M is 128, the full TMEM lane count; "A@tmem" = the A
+// operand is read from TMEM as BF16 pairs):
+//   KQ   = [K; Q] K^T                                      N=64,  K=128
+//   W^T  = K^T T''^T,   T'' = T diag(beta e^gamma)         N=64,  K=64
+//   U^T  = V^T T'^T,    T'  = T diag(beta)  -> Delta^T acc N=64,  K=64
+//   Delta^T += -S W^T                      (S A@tmem)      N=64,  K=128
+//   O    = S (diag(e^gamma) Q)^T           (S A@tmem)      N=64,  K=128
+//   S   <- e^{gamma_C} S + (Delta^T diag(dec)) K  (A@tmem) N=128, K=64
+//   O   += Delta^T Ahat^T,  Ahat = M o Gamma o Q K^T (A@tmem) N=64, K=64
+//   out[i][v] = scale O[v][i]
+// The 64x64 solve T = (I + A)^{-1} is FP32 (solve_tc.cuh).  BF16 copies of
+// S, W, Delta, T', T'' are the tensor-core operands; S itself stays FP32 in
+// TMEM (the pages stage chunk-entry states in the Q/K/V dtype the same way).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,47 +46,78 @@ namespace {
 using namespace tc;
 
 constexpr int D = 128;
-constexpr int NTHR = 256;
+constexpr int NTHR = 512;
+constexpr int BAR_STATE = 1, BAR_PREP = 2, BAR_OUT = 3;   // named barriers (128 threads each)
 
-// Shared-memory map (bytes from a 1024-aligned base).  Panel layout, see tc_ptx.cuh.
-constexpr uint32_t OFF_KQ = 0;          // 2 stages x 32 KB; a stage is 2 panels x 16 KB:
-constexpr uint32_t KQ_STAGE = 32768;    //   rows 0-63 K, rows 64-127 Q of one chunk
+// Shared-memory map (bytes from a 1024-aligned base); tiles use the panel layout of tc_ptx.cuh.
+constexpr uint32_t KQ_STAGES = 3, V_STAGES = 2;
+constexpr uint32_t OFF_KQ = 0;           // 3 x 32 KB; stage = 2 panels x 16 KB (rows 0-63 K, 64-127 Q)
+constexpr uint32_t KQ_STAGE = 32768;
 constexpr uint32_t KQ_PANEL = 16384;
-constexpr uint32_t OFF_V = 65536;       // 2 panels x 8 KB: V [64 tokens][128]
+constexpr uint32_t OFF_V = 98304;        // 2 x 16 KB; stage = 2 panels x 8 KB: V [64][128]
+constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t V_PANEL = 8192;
-constexpr uint32_t OFF_S = 81920;       // 2 panels x 16 KB: S (BF16) [128 v][128 k]
-constexpr uint32_t S_PANEL = 16384;
-constexpr uint32_t OFF_WT = 114688;     // 16 KB: W^T [128 k][64 i]
-constexpr uint32_t OFF_DT = 131072;     // 16 KB: Delta^T [128 v][64 j]; solve scratch before
-constexpr uint32_t OFF_DDT = 147456;    // 16 KB: (Delta^T diag(dec)) [128 v][64 j]
-constexpr uint32_t OFF_T1 = 163840;     // 8 KB: T'  [64 i][64 j]   } output staging
-constexpr uint32_t OFF_T2 = 172032;     // 8 KB: T'' [64 i][64 j]   } [64][128] BF16 after
-constexpr uint32_t OFF_AH = 180224;     // 8 KB: Ahat [64 i][64 j]
-constexpr uint32_t OFF_A32 = 188416;    // FP32 A [64][SOLVE_LD]
-constexpr uint32_t OFF_T32 = 205824;    // FP32 T [64][SOLVE_LD]
-constexpr uint32_t OFF_VEC = 223232;    // FP32 vectors: g, beta, gamma, e^gamma, dec, e^+, e^- (7 x 64)
-constexpr uint32_t OFF_BAR = 225024;    // mbarriers + TMEM address
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack to align the base to 1024
-static_assert(OFF_A32 + 64 * SOLVE_LD * 4 <= OFF_T32, "A32");
-static_assert(OFF_T32 + 64 * SOLVE_LD * 4 <= OFF_VEC, "T32");
-static_assert(32 * SOLVE_LD * 4 <= 16384, "solve scratch fits the Delta^T tile");
+constexpr uint32_t OFF_WT = 131072;      // 16 KB: W^T [128 k][64 i]
+constexpr uint32_t OFF_T1 = 147456;      // 8 KB: T'  [64 i][64 j]
+constexpr uint32_t OFF_T2 = 155648;      // 8 KB: T'' [64 i][64 j]
+constexpr uint32_t OFF_AH = 163840;      // 2 x 8 KB: Ahat [64 i][64 j]
+constexpr uint32_t OFF_AT = 180224;      // FP32 [64][SOLVE_LD]: A, then T (in place)
+constexpr uint32_t OFF_X = 197632;       // FP32 [32][SOLVE_LD]: solve scratch
+constexpr uint32_t OFF_VEC = 206336;     // 3 stages x 512 floats (see VEC_*)
+constexpr uint32_t OFF_BAR = 212480;     // mbarriers, TMEM address, abort flag
+constexpr uint32_t SMEM_USED = OFF_BAR + 256;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(OFF_AT + 64 * SOLVE_LD * 4 <= OFF_X, "AT");
+static_assert(OFF_X + 32 * SOLVE_LD * 4 <= OFF_VEC, "X");
+static_assert(OFF_VEC + KQ_STAGES * 512 * 4 <= OFF_BAR, "VEC");
+static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
-// TMEM columns (FP32 accumulators, 128 lanes each).
-constexpr uint32_t TM_S = 0;      // S [v][k]        128 cols
-constexpr uint32_t TM_KQ = 128;   // [K;Q] K^T       64 cols
-constexpr uint32_t TM_WT = 192;   // W^T [k][i]      64 cols
-constexpr uint32_t TM_DT = 256;   // U^T / Delta^T   64 cols
-constexpr uint32_t TM_SQ = 320;   // S Q^T [v][i]    64 cols
-constexpr uint32_t TM_OA = 384;   // Delta^T Ahat^T  64 cols
+// Per-chunk vectors (ring stage = chunk % 3): gate, beta (loader); the rest (prep).
+constexpr int VEC_G = 0, VEC_BETA = 64, VEC_GAM = 128, VEC_EG = 192, VEC_DEC = 256,
+              VEC_EP = 320, VEC_EM = 384, VEC_FLAG = 448;
+
+// TMEM columns.
+constexpr uint32_t TM_S = 0;      // S FP32 [v][k]                  128
+constexpr uint32_t TM_KQ = 128;   // [K;Q] K^T                      64
+constexpr uint32_t TM_WT = 192;   // W^T [k][i]                     64
+constexpr uint32_t TM_DT = 256;   // U^T / Delta^T FP32 [v][j]      64
+constexpr uint32_t TM_O = 320;    // O [v][i]                       64
+constexpr uint32_t TM_SB = 384;   // S BF16 pairs (A operand)       64
+constexpr uint32_t TM_DB = 448;   // Delta^T BF16 pairs             32
+constexpr uint32_t TM_DDB = 480;  // (Delta^T diag(dec)) BF16 pairs 32
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_KQ = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_WT = idesc_bf16(128, 64, true, false);        // A = K^T (MN-major)
-constexpr uint32_t ID_DT = idesc_bf16(128, 64, false, true, true);  // A = -S, B = W^T (MN-major)
+constexpr uint32_t ID_WT = idesc_bf16(128, 64, true, false);        // A = K^T / V^T (MN-major)
+constexpr uint32_t ID_DT = idesc_bf16(128, 64, false, true, true);  // -S W^T, B MN-major
 constexpr uint32_t ID_SQ = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_SU = idesc_bf16(128, 128, false, true);       // B = K (MN-major)
 constexpr uint32_t ID_OA = idesc_bf16(128, 64, false, false);
+
+// mbarrier indices
+enum {
+  B_KQFULL = 0,    // [3] K/Q tiles + gate/beta of a stage landed (33 arrivals + tx)
+  B_KQEMPTY = 3,   // [3] stage free again (MMA commit after the chunk's state update)
+  B_VFULL = 6,     // [2]
+  B_VEMPTY = 8,    // [2] (MMA commit after U^T)
+  B_KQREADY = 10,  // prep: padded rows zeroed, decay vectors written
+  B_KQDONE = 11,   // MMA: KQ complete
+  B_KQFREE = 12,   // prep: KQ accumulator read
+  B_QG = 13,       // [3] prep: Q rows of a stage scaled by e^gamma
+  B_TTREADY = 16,  // prep: T', T'', Ahat written
+  B_WTDONE = 17,   // MMA: W^T and U^T complete
+  B_WTREADY = 18,  // prep: W^T tile written
+  B_DTDONE = 19,   // MMA: Delta^T complete
+  B_DREADY = 20,   // state: Delta BF16 operands in TMEM
+  B_SUDONE = 21,   // MMA: state update complete
+  B_SREADY = 22,   // state: S BF16 operand and e^{gamma_C}-scaled S in TMEM
+  B_ODONE = 23,    // MMA: O complete
+  B_OFREE = 24,    // out: O read
+  B_AHFREE = 25,   // [2] MMA: Ahat buffer free (commit after O += Delta^T Ahat^T)
+  B_VEC = 27,      // [3] prep: decay vectors of a stage written
+  B_COUNT = 30
+};
+static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 
 struct TcParams {
   const float* g;
@@ -93,16 +131,48 @@ struct TcParams {
   float scale;
 };
 
-struct CtaBar {
-  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
+  *abort_flag = 1;
+  atomicExch(status, 5 /* SF_ERR_TIMEOUT */);
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Every thread of a 128-thread warpgroup waits, then they agree on the outcome.
+__device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, int bar_id,
+                                        volatile int* abort_flag, int* status) {
+  const bool ok = named_bar_and(bar_id, 128, wait_or_abort(bar, parity, abort_flag));
+  if (!ok && (threadIdx.x & 127) == 0) raise_abort(abort_flag, status);
+  return ok;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const bool ok = __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag)) != 0;
+  if (!ok && (threadIdx.x & 31) == 0) raise_abort(abort_flag, status);
+  return ok;
+}
+
+struct PrepBar {
+  __device__ __forceinline__ void operator()() const { named_bar(BAR_PREP, 128); }
 };
 
-// All threads agree on the outcome of a bounded wait.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* status) {
-  const bool ok = mbar_wait(bar, parity);
-  const bool all = __syncthreads_and(ok) != 0;
-  if (!all && threadIdx.x == 0) atomicExch(status, 5 /* SF_ERR_TIMEOUT */);
-  return all;
+__device__ __forceinline__ int chunk_len(int64_t bos, int64_t eos, int c) {
+  const int64_t r = eos - (bos + (int64_t)c * CHUNK);
+  return (int)(r < CHUNK ? r : CHUNK);
 }
 
 __global__ void __launch_bounds__(NTHR, 1)
@@ -112,56 +182,29 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
-  float* sA = reinterpret_cast<float*>(sm + OFF_A32);
-  float* sT = reinterpret_cast<float*>(sm + OFF_T32);
-  float* sX = reinterpret_cast<float*>(sm + OFF_DT);       // solve scratch (Delta^T tile is free then)
-  float* sg = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* sbeta = sg + 64;
-  float* sgam = sbeta + 64;
-  float* seg = sgam + 64;      // e^{gamma_i}
-  float* sdec = seg + 64;      // e^{gamma_C - gamma_i}
-  float* sep = sdec + 64;      // e^{gamma_i - mid}   (factorised decay, see below)
-  float* sem = sep + 64;       // e^{mid - gamma_j}
-  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [2] K/Q stage loaded
-  uint64_t* bar_v = bar_kq + 2;                                    // V loaded
-  uint64_t* bar_mma = bar_kq + 3;                                  // MMA batch done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 4);
-  int* flag = reinterpret_cast<int*>(tmem_slot + 1);               // per-chunk decay path
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + B_COUNT * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vecs = reinterpret_cast<float*>(sm + OFF_VEC);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   const int n = blockIdx.x / H, h = blockIdx.x % H;
-  const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-  const int half = warp >> 2;              // which half of the columns this warp handles
-  const int row = q4 * 32 + lane;          // accumulator row (TMEM lane) of this thread
-  const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-
   int64_t bos, eos;
   seq_span(n, p.B, p.T, p.cu, bos, eos);
-  const int nchunks = (int)((eos - bos + CHUNK - 1) / CHUNK);
+  const int nc = (int)((eos - bos + CHUNK - 1) / CHUNK);
   const size_t state_off = ((size_t)n * H + h) * D * D;
 
   if (tid == 0) {
-    mbar_init(bar_kq, 1);
-    mbar_init(bar_kq + 1, 1);
-    mbar_init(bar_v, 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
+    for (int s = 0; s < (int)KQ_STAGES; ++s) mbar_init(&bars[B_KQFULL + s], 33);
+    *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    if (nchunks > 0) {        // prologue: chunk 0's K, Q and V
-      mbar_arrive_expect_tx(bar_kq, 4 * 8192);
-      mbar_arrive_expect_tx(bar_v, 2 * 8192);
-#pragma unroll
-      for (int pnl = 0; pnl < 2; ++pnl) {
-        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL, &tmK, bar_kq, 64 * pnl, h, (int)bos);
-        tma_load_3d(sm + OFF_KQ + pnl * KQ_PANEL + 8192, &tmQ, bar_kq, 64 * pnl, h, (int)bos);
-        tma_load_3d(sm + OFF_V + pnl * V_PANEL, &tmV, bar_v, 64 * pnl, h, (int)bos);
-      }
-    }
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(tmem_slot, TM_COLS);
     tmem_relinquish();
   }
@@ -169,314 +212,435 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t tl = tm + lane_off;       // this warp's lane base
 
-  // initial state -> TMEM (FP32) and the BF16 operand copy
-#pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int c0 = 64 * half + 32 * cc;
-    float x[32];
-    if (p.s0) {
-      const float4* src = reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)row * D + c0);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 t = src[e];
-        x[4 * e] = t.x; x[4 * e + 1] = t.y; x[4 * e + 2] = t.z; x[4 * e + 3] = t.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = 0.f;
-    }
-    tmem_st32(tl + TM_S + c0, x);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_S, row, c0 + 8 * e, S_PANEL, x + 8 * e);
-  }
-  tmem_st_wait();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  uint32_t ph_mma = 0;
-  bool ok = true;
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int64_t c0 = bos + (int64_t)c * CHUNK;
-    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
-    const int st = c & 1;
-    uint8_t* kq = sm + OFF_KQ + st * KQ_STAGE;
-    const uint32_t kqa = sb + OFF_KQ + st * KQ_STAGE;
-    // ---- load the chunk: prefetch the next chunk's K/Q into the other stage
-    //      (its previous chunk is finished); gate and beta by plain loads
-    if (tid == 0 && c + 1 < nchunks) {
-      uint64_t* bn = bar_kq + (st ^ 1);
-      uint8_t* kqn = sm + OFF_KQ + (st ^ 1) * KQ_STAGE;
-      mbar_arrive_expect_tx(bn, 4 * 8192);
-#pragma unroll
-      for (int pnl = 0; pnl < 2; ++pnl) {
-        tma_load_3d(kqn + pnl * KQ_PANEL, &tmK, bn, 64 * pnl, h, (int)(c0 + CHUNK));
-        tma_load_3d(kqn + pnl * KQ_PANEL + 8192, &tmQ, bn, 64 * pnl, h, (int)(c0 + CHUNK));
-      }
-    }
-    if (tid < 64) {
-      const size_t off = (size_t)(c0 + tid) * H + h;
-      sg[tid] = (tid < L) ? p.g[off] : 0.f;
-      sbeta[tid] = (tid < L) ? p.beta[off] : 0.f;
-    }
-    if (!(ok = cta_wait(bar_kq + st, (uint32_t)(c >> 1) & 1u, p.status))) break;
-    if (!(ok = cta_wait(bar_v, (uint32_t)c & 1u, p.status))) break;
-    if (L < CHUNK) {
-      // rows past the sequence end belong to the next sequence (or are past
-      // the tensor): zero them so they contribute nothing to any product
-      const int rows = CHUNK - L;
-      for (int idx = tid; idx < 6 * rows * 8; idx += NTHR) {
-        const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
-        const int r = L + rem / 8, ch = rem % 8;
-        const int pnl = t6 & 1, which = t6 >> 1;
-        uint8_t* base = (which == 2) ? sm + OFF_V + pnl * V_PANEL
-                                     : kq + pnl * KQ_PANEL + (which == 1 ? 8192u : 0u);
-        *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      warp_cumsum64(sg, sgam, lane);
-      __syncwarp();
-      // decay factors: e^{gamma_i - gamma_j} = e^{gamma_i - mid} e^{mid - gamma_j} when the
-      // chunk's gamma range keeps both factors inside e^{+-40} (no overflow, no
-      // denormals); otherwise every entry takes its own exponential
-      const float a0 = sgam[2 * lane], a1 = sgam[2 * lane + 1];
-      float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      }
-      const bool fact = (mx - mn) <= 80.f;
-      const float mid = 0.5f * (mx + mn);
-      if (lane == 0) *flag = fact ? 1 : 0;
-      const float gC = sgam[63];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = 2 * lane + e;
-        const float gi = sgam[i];
-        seg[i] = expf(gi);
-        sdec[i] = expf(gC - gi);
-        sep[i] = fact ? expf(gi - mid) : 0.f;
-        sem[i] = fact ? expf(mid - gi) : 0.f;
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- Pre: KQ = [K; Q] K^T
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a = kqa + (kk >> 2) * KQ_PANEL + (kk & 3) * 32;
-        mma_bf16(tm + TM_KQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), ID_KQ, kk > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    if (!(ok = cta_wait(bar_mma, ph_mma, p.status))) break;
-    ph_mma ^= 1;
-    tc_fence_after();
-    {
-      float x[32];
-      tmem_ld32(tl + TM_KQ + 32 * half, x);
-      tmem_ld_wait();
-      const bool fact = *flag != 0;
-      const int i = row & 63;
-      const float gi = sgam[i], epi = sep[i];
-      const float bi = (row < 64) ? sbeta[i] : 1.f;
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * half + jj;
-        const float dcy = fact ? epi * sem[j] : expf(j <= i ? gi - sgam[j] : 0.f);
-        x[jj] *= bi * dcy;
-      }
-      if (row < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * half + jj;
-          sA[i * SOLVE_LD + j] = (j < i) ? x[jj] : 0.f;
-        }
-      } else {                 // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (32 * half + jj > i) x[jj] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_AH, i, 32 * half + 8 * e, 8192, x + 8 * e);
-      }
-    }
-    __syncthreads();
-    // ---- Pre: T = (I + A)^{-1} (FP32), then T' = T diag(beta), T'' = T diag(beta e^gamma)
-    solve64_tc(sA, sT, sX, tid, NTHR, CtaBar());
-    for (int idx = tid; idx < 64 * 8; idx += NTHR) {
-      const int i = idx >> 3, cg = (idx & 7) * 8;
-      float t1[8], t2[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = cg + e;
-        const float t = sT[i * SOLVE_LD + j] * sbeta[j];
-        t1[e] = t;
-        t2[e] = t * seg[j];
-      }
-      st_row8_bf16(sm + OFF_T1, i, cg, 8192, t1);
-      st_row8_bf16(sm + OFF_T2, i, cg, 8192, t2);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    // ---- W^T = K^T T''^T ; U^T = V^T T'^T (into the Delta^T accumulator)
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tm + TM_WT, sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024),
-                 sdesc_sw128(sb + OFF_T2 + kk * 32, 0, 1024), ID_WT, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tm + TM_DT, sdesc_sw128(sb + OFF_V + kk * 2048, V_PANEL, 1024),
-                 sdesc_sw128(sb + OFF_T1 + kk * 32, 0, 1024), ID_WT, kk > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    if (!(ok = cta_wait(bar_mma, ph_mma, p.status))) break;
-    ph_mma ^= 1;
-    tc_fence_after();
-    if (tid == 0 && c + 1 < nchunks) {      // V is free: load the next chunk's
-      mbar_arrive_expect_tx(bar_v, 2 * 8192);
-#pragma unroll
-      for (int pnl = 0; pnl < 2; ++pnl)
-        tma_load_3d(sm + OFF_V + pnl * V_PANEL, &tmV, bar_v, 64 * pnl, h, (int)(c0 + CHUNK));
-    }
-    {
-      float x[32];
-      tmem_ld32(tl + TM_WT + 32 * half, x);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_WT, row, 32 * half + 8 * e, 16384, x + 8 * e);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- ST: Delta^T += -S W^T ; Out: SQ = S Q^T
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a = sb + OFF_S + (kk >> 2) * S_PANEL + (kk & 3) * 32;
-        mma_bf16(tm + TM_DT, sdesc_sw128(a, 0, 1024),
-                 sdesc_sw128(sb + OFF_WT + kk * 2048, 16384, 1024), ID_DT, 1);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a = sb + OFF_S + (kk >> 2) * S_PANEL + (kk & 3) * 32;
-        const uint32_t b = kqa + (kk >> 2) * KQ_PANEL + 8192 + (kk & 3) * 32;
-        mma_bf16(tm + TM_SQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(b, 0, 1024), ID_SQ, kk > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    if (!(ok = cta_wait(bar_mma, ph_mma, p.status))) break;
-    ph_mma ^= 1;
-    tc_fence_after();
-    {
-      float x[32];
-      tmem_ld32(tl + TM_DT + 32 * half, x);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_DT, row, 32 * half + 8 * e, 16384, x + 8 * e);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] *= sdec[32 * half + jj];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_DDT, row, 32 * half + 8 * e, 16384, x + 8 * e);
-      // S <- e^{gamma_C} S in TMEM before the update accumulates on top of it
-      const float gC = seg[63];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = TM_S + 64 * half + 32 * cc;
-        tmem_ld32(tl + col, x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] *= gC;
-        tmem_st32(tl + col, x);
-      }
-      tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- ST: S += (Delta^T diag(dec)) K ; Out: OA = Delta^T Ahat^T
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tm + TM_S, sdesc_sw128(sb + OFF_DDT + kk * 32, 0, 1024),
-                 sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024), ID_SU, 1);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tm + TM_OA, sdesc_sw128(sb + OFF_DT + kk * 32, 0, 1024),
-                 sdesc_sw128(sb + OFF_AH + kk * 32, 0, 1024), ID_OA, kk > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    if (!(ok = cta_wait(bar_mma, ph_mma, p.status))) break;
-    ph_mma ^= 1;
-    tc_fence_after();
-    {
-      // out[i][v] = scale (e^{gamma_i} SQ[v][i] + OA[v][i]), staged as a [64][128]
-      // BF16 row-major tile in the (now free) T'/T'' region, then stored 16 B at a time
-      float sq[32], oa[32];
-      tmem_ld32(tl + TM_SQ + 32 * half, sq);
-      tmem_ld32(tl + TM_OA + 32 * half, oa);
-      tmem_ld_wait();
-      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + OFF_T1);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int i = 32 * half + jj;
-        stage[i * D + row] = __float2bfloat16_rn(p.scale * (seg[i] * sq[jj] + oa[jj]));
-      }
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = 64 * half + 32 * cc;
-        tmem_ld32(tl + TM_S + col, sq);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_S, row, col + 8 * e, S_PANEL, sq + 8 * e);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    {
-      const uint4* stage = reinterpret_cast<const uint4*>(sm + OFF_T1);
-      for (int idx = tid; idx < 64 * 16; idx += NTHR) {
-        const int i = idx >> 4, ch = idx & 15;
-        if (i < L)
-          *reinterpret_cast<uint4*>(p.out + ((size_t)(c0 + i) * H + h) * D + ch * 8) = stage[idx];
-      }
-    }
-    __syncthreads();
-    tc_fence_after();
-  }
-
-  if (ok && p.final_state) {
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c0 = 64 * half + 32 * cc;
-      float x[32];
-      tmem_ld32(tl + TM_S + c0, x);
-      tmem_ld_wait();
-      float4* dst = reinterpret_cast<float4*>(p.final_state + state_off + (size_t)row * D + c0);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 0) {
+    // ------------------------------------------------------------- loader
+    int last_kq[KQ_STAGES] = {-1, -1, -1}, last_v[V_STAGES] = {-1, -1};
+    for (int c = 0; c < nc; ++c) {
+      const int s = c % KQ_STAGES, sv = c & 1;
+      const int64_t c0 = bos + (int64_t)c * CHUNK;
+      const int L = chunk_len(bos, eos, c);
+      if (c >= (int)KQ_STAGES &&
+          !warp_wait(&bars[B_KQEMPTY + s], (uint32_t)((c - KQ_STAGES) / KQ_STAGES) & 1u, abort_flag,
+                     p.status))
+        break;
+      if (lane == 0) {
+        uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
+        mbar_arrive_expect_tx(&bars[B_KQFULL + s], 4 * 8192);
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl) {
+          tma_load_3d(kq + pnl * KQ_PANEL, &tmK, &bars[B_KQFULL + s], 64 * pnl, h, (int)c0);
+          tma_load_3d(kq + pnl * KQ_PANEL + 8192, &tmQ, &bars[B_KQFULL + s], 64 * pnl, h, (int)c0);
+        }
+      }
+      last_kq[s] = c;
+      float* vs = vecs + s * 512;
+#pragma unroll
+      for (int e = lane; e < 64; e += 32) {
+        const size_t off = (size_t)(c0 + e) * H + h;
+        vs[VEC_G + e] = (e < L) ? p.g[off] : 0.f;
+        vs[VEC_BETA + e] = (e < L) ? p.beta[off] : 0.f;
+      }
+      mbar_arrive(&bars[B_KQFULL + s]);
+      if (c >= (int)V_STAGES &&
+          !warp_wait(&bars[B_VEMPTY + sv], (uint32_t)((c - V_STAGES) >> 1) & 1u, abort_flag,
+                     p.status))
+        break;
+      if (lane == 0) {
+        uint8_t* vt = sm + OFF_V + sv * V_STAGE;
+        mbar_arrive_expect_tx(&bars[B_VFULL + sv], 2 * 8192);
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl)
+          tma_load_3d(vt + pnl * V_PANEL, &tmV, &bars[B_VFULL + sv], 64 * pnl, h, (int)c0);
+      }
+      last_v[sv] = c;
+    }
+    // never leave with a tile copy in flight
+    for (int s = 0; s < (int)KQ_STAGES; ++s)
+      if (last_kq[s] >= 0)
+        mbar_wait(&bars[B_KQFULL + s], (uint32_t)(last_kq[s] / KQ_STAGES) & 1u, 100000000ull);
+    for (int s = 0; s < (int)V_STAGES; ++s)
+      if (last_v[s] >= 0) mbar_wait(&bars[B_VFULL + s], (uint32_t)(last_v[s] >> 1) & 1u, 100000000ull);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && nc > 0) {
+      int nKQ = 0, nWU = 0, nDT = 0, nSQ = 0, nSU = 0;
+      uint64_t t_prog = globaltimer_ns();
+      while (nSU < nc) {
+        bool prog = false;
+        // state transition: Delta^T += -S W^T
+        if (nDT < nWU && mbar_test(&bars[B_WTREADY], nDT & 1) &&
+            mbar_test(&bars[B_SREADY], nDT & 1)) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ta(tm + TM_DT, tm + TM_SB + kk * 8,
+                        sdesc_sw128(sb + OFF_WT + kk * 2048, 16384, 1024), ID_DT, 1);
+          mma_commit(&bars[B_DTDONE]);
+          ++nDT;
+          prog = true;
+        }
+        // output, state part: O = S Qg^T
+        if (nSQ < nDT && mbar_test(&bars[B_QG + nSQ % KQ_STAGES], (nSQ / KQ_STAGES) & 1) &&
+            (nSQ == 0 || mbar_test(&bars[B_OFREE], (nSQ - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t kqa = sb + OFF_KQ + (nSQ % KQ_STAGES) * KQ_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ta(tm + TM_O, tm + TM_SB + kk * 8,
+                        sdesc_sw128(kqa + (kk >> 2) * KQ_PANEL + 8192 + (kk & 3) * 32, 0, 1024),
+                        ID_SQ, kk > 0);
+          ++nSQ;
+          prog = true;
+        }
+        // state update S += (Delta^T diag(dec)) K, then O += Delta^T Ahat^T
+        if (nSU < nSQ && mbar_test(&bars[B_DREADY], nSU & 1)) {
+          tc_fence_after();
+          const int s = nSU % KQ_STAGES;
+          const uint32_t kqa = sb + OFF_KQ + s * KQ_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8,
+                        sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024), ID_SU, 1);
+          mma_commit(&bars[B_SUDONE]);
+          mma_commit(&bars[B_KQEMPTY + s]);
+          const uint32_t ah = sb + OFF_AH + (nSU & 1) * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(tm + TM_O, tm + TM_DB + kk * 8, sdesc_sw128(ah + kk * 32, 0, 1024), ID_OA,
+                        1);
+          mma_commit(&bars[B_ODONE]);
+          mma_commit(&bars[B_AHFREE + (nSU & 1)]);
+          ++nSU;
+          prog = true;
+        }
+        // prep products of chunk nWU: W^T and U^T (U^T needs the Delta^T accumulator free)
+        if (nWU < nKQ && nSU >= nWU && mbar_test(&bars[B_TTREADY], nWU & 1)) {
+          tc_fence_after();
+          const uint32_t kqa = sb + OFF_KQ + (nWU % KQ_STAGES) * KQ_STAGE;
+          const uint32_t va = sb + OFF_V + (nWU & 1) * V_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tm + TM_WT, sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024),
+                     sdesc_sw128(sb + OFF_T2 + kk * 32, 0, 1024), ID_WT, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tm + TM_DT, sdesc_sw128(va + kk * 2048, V_PANEL, 1024),
+                     sdesc_sw128(sb + OFF_T1 + kk * 32, 0, 1024), ID_WT, kk > 0);
+          mma_commit(&bars[B_WTDONE]);
+          mma_commit(&bars[B_VEMPTY + (nWU & 1)]);
+          ++nWU;
+          prog = true;
+        }
+        // prep product of chunk nKQ: [K; Q] K^T
+        if (nKQ < nc && mbar_test(&bars[B_KQREADY], nKQ & 1) &&
+            (nKQ == 0 || mbar_test(&bars[B_KQFREE], (nKQ - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t kqa = sb + OFF_KQ + (nKQ % KQ_STAGES) * KQ_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a = kqa + (kk >> 2) * KQ_PANEL + (kk & 3) * 32;
+            mma_bf16(tm + TM_KQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), ID_KQ, kk > 0);
+          }
+          mma_commit(&bars[B_KQDONE]);
+          ++nKQ;
+          prog = true;
+        }
+        if (prog) {
+          t_prog = globaltimer_ns();
+        } else if (*abort_flag || globaltimer_ns() - t_prog > kWaitLimitNs) {
+          raise_abort(abort_flag, p.status);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // --------------------------------------------------------------- state
+    const int v = tid - 128;                         // TMEM lane = state row
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    bool ok = true;
+    if (nc == 0) {
+      if (p.final_state)
+        for (int c = 0; c < D; c += 4) {
+          float4 x = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)v * D + c)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + c) = x;
+        }
+    } else {
+      ok = wg_wait(&bars[B_VEC + 0], 0, BAR_STATE, abort_flag, p.status);
+      if (ok) {
+        const float g0 = vecs[VEC_EG + 63];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float x[32];
+          if (p.s0) {
+            const float4* src =
+                reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)v * D + 32 * cc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 t = src[e];
+              x[4 * e] = t.x; x[4 * e + 1] = t.y; x[4 * e + 2] = t.z; x[4 * e + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+          }
+          uint32_t u[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+          tmem_st16(tl + TM_SB + 16 * cc, u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] *= g0;
+          tmem_st32(tl + TM_S + 32 * cc, x);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(BAR_STATE, 128);
+        if (v == 0) mbar_arrive(&bars[B_SREADY]);
+      }
+      for (int c = 0; c < nc && ok; ++c) {
+        const float* vs = vecs + (c % KQ_STAGES) * 512;
+        if (!(ok = wg_wait(&bars[B_DTDONE], c & 1, BAR_STATE, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[32];
+          tmem_ld32(tl + TM_DT + 32 * hh, x);
+          tmem_ld_wait();
+          uint32_t u[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+          tmem_st16(tl + TM_DB + 16 * hh, u);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            u[e] = pack_bf16x2(x[2 * e] * vs[VEC_DEC + 32 * hh + 2 * e],
+                               x[2 * e + 1] * vs[VEC_DEC + 32 * hh + 2 * e + 1]);
+          tmem_st16(tl + TM_DDB + 16 * hh, u);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(BAR_STATE, 128);
+        if (v == 0) mbar_arrive(&bars[B_DREADY]);
+        if (!(ok = wg_wait(&bars[B_SUDONE], c & 1, BAR_STATE, abort_flag, p.status))) break;
+        tc_fence_after();
+        const bool last = (c + 1 == nc);
+        float gn = 0.f;
+        if (!last) {
+          if (!(ok = wg_wait(&bars[B_VEC + (c + 1) % KQ_STAGES], ((c + 1) / KQ_STAGES) & 1,
+                             BAR_STATE, abort_flag, p.status)))
+            break;
+          gn = vecs[((c + 1) % KQ_STAGES) * 512 + VEC_EG + 63];
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float x[32];
+          tmem_ld32(tl + TM_S + 32 * cc, x);
+          tmem_ld_wait();
+          if (!last) {
+            uint32_t u[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+            tmem_st16(tl + TM_SB + 16 * cc, u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] *= gn;
+            tmem_st32(tl + TM_S + 32 * cc, x);
+          } else if (p.final_state) {
+            float4* dst =
+                reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + 32 * cc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+          }
+        }
+        if (!last) {
+          tmem_st_wait();
+          tc_fence_before();
+          named_bar(BAR_STATE, 128);
+          if (v == 0) mbar_arrive(&bars[B_SREADY]);
+        }
+      }
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------------------------------------------------------- prep
+    const int pt = tid - 256;                        // 0..127 = TMEM lane row
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    float* AT = reinterpret_cast<float*>(sm + OFF_AT);
+    float* X = reinterpret_cast<float*>(sm + OFF_X);
+    for (int c = 0; c < nc; ++c) {
+      const int s = c % KQ_STAGES, sv = c & 1;
+      const int L = chunk_len(bos, eos, c);
+      float* vs = vecs + s * 512;
+      uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
+      uint8_t* vt = sm + OFF_V + sv * V_STAGE;
+      if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status)) break;
+      if (!wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status)) break;
+      if (L < CHUNK) {
+        // rows past the sequence end belong to the next sequence (or are past
+        // the tensor): zero them so they contribute nothing to any product
+        const int rows = CHUNK - L;
+        for (int idx = pt; idx < 6 * rows * 8; idx += 128) {
+          const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
+          const int r = L + rem / 8, ch = rem % 8;
+          const int pnl = t6 & 1, which = t6 >> 1;
+          uint8_t* base = (which == 2) ? vt + pnl * V_PANEL
+                                       : kq + pnl * KQ_PANEL + (which == 1 ? 8192u : 0u);
+          *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (pt < 32) {
+        warp_cumsum64(vs + VEC_G, vs + VEC_GAM, lane);
+        __syncwarp();
+        // decay factors: e^{gamma_i - gamma_j} = e^{gamma_i - mid} e^{mid - gamma_j} when the
+        // chunk's gamma range keeps both factors inside e^{+-40}; else one exponential per entry
+        const float a0 = vs[VEC_GAM + 2 * lane], a1 = vs[VEC_GAM + 2 * lane + 1];
+        float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        const bool fact = (mx - mn) <= 80.f;
+        const float mid = 0.5f * (mx + mn);
+        const float gC = vs[VEC_GAM + 63];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * lane + e;
+          const float gi = vs[VEC_GAM + i];
+          vs[VEC_EG + i] = expf(gi);
+          vs[VEC_DEC + i] = expf(gC - gi);
+          vs[VEC_EP + i] = fact ? expf(gi - mid) : 0.f;
+          vs[VEC_EM + i] = fact ? expf(mid - gi) : 0.f;
+        }
+        if (lane == 0) vs[VEC_FLAG] = fact ? 1.f : 0.f;
+      }
+      fence_proxy_async_smem();
+      named_bar(BAR_PREP, 128);
+      if (pt == 0) {
+        mbar_arrive(&bars[B_KQREADY]);
+        mbar_arrive(&bars[B_VEC + s]);
+      }
+      if (c >= 2 &&
+          !wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag, p.status))
+        break;
+      if (!wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status)) break;
+      tc_fence_after();
+      {
+        const bool fact = vs[VEC_FLAG] != 0.f;
+        const int i = pt & 63;
+        const float gi = vs[VEC_GAM + i], epi = vs[VEC_EP + i];
+        const float bi = (pt < 64) ? vs[VEC_BETA + i] : 1.f;
+        uint8_t* ah = sm + OFF_AH + (c & 1) * 8192;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[32];
+          tmem_ld32(tl + TM_KQ + 32 * hh, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * hh + jj;
+            const float dcy = fact ? epi * vs[VEC_EM + j] : expf(j <= i ? gi - vs[VEC_GAM + j] : 0.f);
+            x[jj] *= bi * dcy;
+          }
+          if (pt < 64) {       // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) AT[i * SOLVE_LD + 32 * hh + jj] = (32 * hh + jj < i) ? x[jj] : 0.f;
+          } else {             // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (32 * hh + jj > i) x[jj] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st_row8_bf16(ah, i, 32 * hh + 8 * e, 8192, x + 8 * e);
+          }
+        }
+      }
+      tc_fence_before();
+      // Q rows scaled by e^{gamma_i} in place (the KQ product has consumed them): O's
+      // state part S (diag(e^gamma) Q)^T then shares one accumulator with Delta^T Ahat^T
+      for (int idx = pt; idx < 64 * 2 * 8; idx += 128) {
+        const int r = idx >> 4, pnl = (idx >> 3) & 1, ch = idx & 7;
+        uint4* ptr = reinterpret_cast<uint4*>(kq + pnl * KQ_PANEL + 8192 + r * 128 + ch * 16);
+        const float e = vs[VEC_EG + r];
+        uint4 w = *ptr;
+        uint32_t* wu = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162*>(&wu[q2]);
+          float2 f = __bfloat1622float2(b2);
+          wu[q2] = pack_bf16x2(f.x * e, f.y * e);
+        }
+        *ptr = w;
+      }
+      fence_proxy_async_smem();
+      named_bar(BAR_PREP, 128);
+      if (pt == 0) {
+        mbar_arrive(&bars[B_KQFREE]);
+        mbar_arrive(&bars[B_QG + s]);
+      }
+      // T = (I + A)^{-1}, then T' = T diag(beta), T'' = T diag(beta e^gamma)
+      solve64_tc_inplace(AT, X, pt, 128, PrepBar());
+      for (int idx = pt; idx < 64 * 8; idx += 128) {
+        const int i = idx >> 3, cg = (idx & 7) * 8;
+        float t1[8], t2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = cg + e;
+          const float t = AT[i * SOLVE_LD + j] * vs[VEC_BETA + j];
+          t1[e] = t;
+          t2[e] = t * vs[VEC_EG + j];
+        }
+        st_row8_bf16(sm + OFF_T1, i, cg, 8192, t1);
+        st_row8_bf16(sm + OFF_T2, i, cg, 8192, t2);
+      }
+      fence_proxy_async_smem();
+      named_bar(BAR_PREP, 128);
+      if (pt == 0) mbar_arrive(&bars[B_TTREADY]);
+      if (!wg_wait(&bars[B_WTDONE], c & 1, BAR_PREP, abort_flag, p.status)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[32];
+        tmem_ld32(tl + TM_WT + 32 * hh, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_WT, pt, 32 * hh + 8 * e, 16384, x + 8 * e);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar(BAR_PREP, 128);
+      if (pt == 0) mbar_arrive(&bars[B_WTREADY]);
+    }
+  } else if (warp >= 12) {
+    // ----------------------------------------------------------------- out
+    const int v = tid - 384;
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    for (int c = 0; c < nc; ++c) {
+      if (!wg_wait(&bars[B_ODONE], c & 1, BAR_OUT, abort_flag, p.status)) break;
+      tc_fence_after();
+      float a[32], b[32];
+      tmem_ld32(tl + TM_O, a);
+      tmem_ld32(tl + TM_O + 32, b);
+      tmem_ld_wait();
+      tc_fence_before();
+      named_bar(BAR_OUT, 128);
+      if (v == 0) mbar_arrive(&bars[B_OFREE]);
+      const int64_t c0 = bos + (int64_t)c * CHUNK;
+      const int L = chunk_len(bos, eos, c);
+      __nv_bfloat16* orow = p.out + ((size_t)c0 * H + h) * D + v;
+      const size_t st = (size_t)H * D;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < L) orow[i * st] = __float2bfloat16_rn(p.scale * a[i]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (32 + i < L) orow[(32 + i) * st] = __float2bfloat16_rn(p.scale * b[i]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tm, TM_COLS);
   }

@@ -120,4 +120,68 @@ __device__ void solve64_tc(const float* A, float* T, float* X, int tid, int nthr
   bar();
 }
 
+// In-place variant: AT holds A (strictly lower) on entry and T on exit.  Each
+// stage overwrites only blocks of A that no later stage reads: the diagonal
+// blocks after every thread has its column in registers, A_10 of each 32x32
+// half after X_p = A_10 T_00, and A[32:64, 0:32] after the 64-level X.
+template <typename Bar>
+__device__ void solve64_tc_inplace(float* AT, float* X, int tid, int nthr, Bar bar) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int L = SOLVE_LD;
+  float acc[16];
+  const int b = tid >> 4, m = tid & 15, base = 16 * b;
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = (i == m) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      const float x = acc[j];
+#pragma unroll
+      for (int i = j + 1; i < 16; ++i) acc[i] -= AT[(base + i) * L + base + j] * x;
+    }
+  }
+  bar();
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) AT[(base + i) * L + base + m] = acc[i];
+  } else {
+    for (int idx = tid - 64; idx < 6 * 256; idx += nthr - 64) {
+      const int blk = idx >> 8, e = idx & 255;
+      const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      AT[(16 * br + (e >> 4)) * L + 16 * bc + (e & 15)] = 0.f;
+    }
+  }
+  bar();
+  if (warp < 4) {
+    const int p = warp >> 1, nt = warp & 1, r0 = 32 * p;
+    warp_tile_tf32(AT + (r0 + 16) * L + r0, AT + r0 * L + r0 + 8 * nt, X + 16 * p * L + 8 * nt,
+                   16, 1.f, lane);
+  }
+  bar();
+  if (warp < 4) {
+    const int p = warp >> 1, nt = warp & 1, r0 = 32 * p;
+    warp_tile_tf32(AT + (r0 + 16) * L + r0 + 16, X + 16 * p * L + 8 * nt,
+                   AT + (r0 + 16) * L + r0 + 8 * nt, 16, -1.f, lane);
+  }
+  bar();
+  if (warp < 4) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int tile = 2 * warp + s, mt = tile >> 2, nt = tile & 3;
+      warp_tile_tf32(AT + (32 + 16 * mt) * L, AT + 8 * nt, X + 16 * mt * L + 8 * nt, 32, 1.f, lane);
+    }
+  }
+  bar();
+  if (warp < 4) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int tile = 2 * warp + s, mt = tile >> 2, nt = tile & 3;
+      warp_tile_tf32(AT + (32 + 16 * mt) * L + 32, X + 8 * nt, AT + (32 + 16 * mt) * L + 8 * nt,
+                     32, -1.f, lane);
+    }
+  }
+  bar();
+}
+
 }  // namespace sfg

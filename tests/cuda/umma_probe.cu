@@ -101,8 +101,20 @@ __global__ void solve_probe_kernel(const float* __restrict__ A, float* __restric
   for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) T[i] = sT[(i >> 6) * sfg::SOLVE_LD + (i & 63)];
 }
 
-extern "C" int solve_probe(const float* A, float* T, int nthreads) {
-  solve_probe_kernel<<<1, nthreads>>>(A, T);
+__global__ void solve_inplace_probe_kernel(const float* __restrict__ A, float* __restrict__ T) {
+  __shared__ float sAT[64 * sfg::SOLVE_LD], sX[32 * sfg::SOLVE_LD];
+  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x)
+    sAT[(i >> 6) * sfg::SOLVE_LD + (i & 63)] = A[i];
+  __syncthreads();
+  sfg::solve64_tc_inplace(sAT, sX, threadIdx.x, blockDim.x, ProbeBar());
+  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) T[i] = sAT[(i >> 6) * sfg::SOLVE_LD + (i & 63)];
+}
+
+extern "C" int solve_probe(const float* A, float* T, int nthreads, int inplace) {
+  if (inplace)
+    solve_inplace_probe_kernel<<<1, nthreads>>>(A, T);
+  else
+    solve_probe_kernel<<<1, nthreads>>>(A, T);
   return (int)cudaDeviceSynchronize();
 }
 

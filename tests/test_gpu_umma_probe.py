@@ -48,17 +48,19 @@ def test_umma_layouts(probe, N, K, a_mn, b_mn, neg):
 
 
 @pytest.mark.parametrize("nthreads", [128, 256])
-def test_solve64_tc(probe, nthreads):
+@pytest.mark.parametrize("inplace", [0, 1])
+def test_solve64_tc(probe, nthreads, inplace):
     """(I + A)^{-1} of a chunk-like strictly lower A: diagonal blocks in FP32,
     block merges on TF32 tensor cores -> relative error well under BF16's."""
-    probe.solve_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    probe.solve_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     g = torch.Generator().manual_seed(nthreads)
     k = torch.nn.functional.normalize(torch.randn(64, 128, generator=g), dim=-1).double()
     beta = torch.sigmoid(torch.randn(64, generator=g)).double()
     gam = torch.cumsum(-torch.nn.functional.softplus(torch.randn(64, generator=g)), 0).double()
     A = torch.tril(beta[:, None] * torch.exp(gam[:, None] - gam[None, :]).clamp(max=1) * (k @ k.T), -1)
     Td = torch.zeros(64, 64, device="cuda")
-    assert probe.solve_probe(A.float().cuda().data_ptr(), Td.data_ptr(), nthreads) == 0
+    Ad = A.float().cuda()
+    assert probe.solve_probe(Ad.data_ptr(), Td.data_ptr(), nthreads, inplace) == 0
     ref = torch.linalg.inv(torch.eye(64, dtype=torch.float64) + A)
     err = (Td.cpu().double() - ref).abs().max().item() / ref.abs().max().item()
     assert err < 2e-3, err
@@ -76,9 +78,9 @@ def test_umma_a_from_tmem(probe, N, K, b_mn, neg):
     g = torch.Generator().manual_seed(7 * N + K + b_mn)
     A = torch.randn(128, K, generator=g).bfloat16()
     B = torch.randn(K, N, generator=g).bfloat16()
+    Ad, Bd = A.cuda(), B.cuda()      # keep the device copies alive during the call
     Dd = torch.zeros(128, N, device="cuda")
-    rc = probe.umma_probe_ta(N, K, b_mn, neg, A.cuda().data_ptr(), B.cuda().data_ptr(),
-                             Dd.data_ptr())
+    rc = probe.umma_probe_ta(N, K, b_mn, neg, Ad.data_ptr(), Bd.data_ptr(), Dd.data_ptr())
     assert rc == 0
     ref = (A.double() @ B.double()) * (-1 if neg else 1)
     err = (Dd.cpu().double() - ref).abs().max().item() / ref.abs().max().item()
