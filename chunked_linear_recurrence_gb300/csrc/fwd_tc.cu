@@ -144,8 +144,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
@@ -273,10 +272,10 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (nDT < nWU && mbar_test(&bars[B_WTREADY], nDT & 1) &&
             mbar_test(&bars[B_SREADY], nDT & 1)) {
           tc_fence_after();
+          const uint64_t bd = sdesc_sw128(sb + OFF_WT, 16384, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ta(tm + TM_DT, tm + TM_SB + kk * 8,
-                        sdesc_sw128(sb + OFF_WT + kk * 2048, 16384, 1024), ID_DT, 1);
+            mma_bf16_ta(tm + TM_DT, tm + TM_SB + kk * 8, bd + (uint64_t)(kk * 2048 >> 4), ID_DT, 1);
           mma_commit(&bars[B_DTDONE]);
           ++nDT;
           prog = true;
@@ -286,11 +285,11 @@ __global__ void __launch_bounds__(NTHR, 1)
             (nSQ == 0 || mbar_test(&bars[B_OFREE], (nSQ - 1) & 1))) {
           tc_fence_after();
           const uint32_t kqa = sb + OFF_KQ + (nSQ % KQ_STAGES) * KQ_STAGE;
+          const uint64_t bd = sdesc_sw128(kqa + 8192, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ta(tm + TM_O, tm + TM_SB + kk * 8,
-                        sdesc_sw128(kqa + (kk >> 2) * KQ_PANEL + 8192 + (kk & 3) * 32, 0, 1024),
-                        ID_SQ, kk > 0);
+                        bd + (uint64_t)(((kk >> 2) * KQ_PANEL + (kk & 3) * 32) >> 4), ID_SQ, kk > 0);
           ++nSQ;
           prog = true;
         }
@@ -299,17 +298,17 @@ __global__ void __launch_bounds__(NTHR, 1)
           tc_fence_after();
           const int s = nSU % KQ_STAGES;
           const uint32_t kqa = sb + OFF_KQ + s * KQ_STAGE;
+          const uint64_t bk = sdesc_sw128(kqa, KQ_PANEL, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8,
-                        sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024), ID_SU, 1);
+            mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_SU, 1);
           mma_commit(&bars[B_SUDONE]);
           mma_commit(&bars[B_KQEMPTY + s]);
           const uint32_t ah = sb + OFF_AH + (nSU & 1) * 8192;
+          const uint64_t ba = sdesc_sw128(ah, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ta(tm + TM_O, tm + TM_DB + kk * 8, sdesc_sw128(ah + kk * 32, 0, 1024), ID_OA,
-                        1);
+            mma_bf16_ta(tm + TM_O, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2), ID_OA, 1);
           mma_commit(&bars[B_ODONE]);
           mma_commit(&bars[B_AHFREE + (nSU & 1)]);
           ++nSU;
@@ -320,14 +319,14 @@ __global__ void __launch_bounds__(NTHR, 1)
           tc_fence_after();
           const uint32_t kqa = sb + OFF_KQ + (nWU % KQ_STAGES) * KQ_STAGE;
           const uint32_t va = sb + OFF_V + (nWU & 1) * V_STAGE;
+          const uint64_t ak = sdesc_sw128(kqa, KQ_PANEL, 1024), b2 = sdesc_sw128(sb + OFF_T2, 0, 1024);
+          const uint64_t av = sdesc_sw128(va, V_PANEL, 1024), b1 = sdesc_sw128(sb + OFF_T1, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tm + TM_WT, sdesc_sw128(kqa + kk * 2048, KQ_PANEL, 1024),
-                     sdesc_sw128(sb + OFF_T2 + kk * 32, 0, 1024), ID_WT, kk > 0);
+            mma_bf16(tm + TM_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_WT, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tm + TM_DT, sdesc_sw128(va + kk * 2048, V_PANEL, 1024),
-                     sdesc_sw128(sb + OFF_T1 + kk * 32, 0, 1024), ID_WT, kk > 0);
+            mma_bf16(tm + TM_DT, av + (uint64_t)(kk * 2048 >> 4), b1 + (uint64_t)(kk * 2), ID_WT, kk > 0);
           mma_commit(&bars[B_WTDONE]);
           mma_commit(&bars[B_VEMPTY + (nWU & 1)]);
           ++nWU;
@@ -338,10 +337,11 @@ __global__ void __launch_bounds__(NTHR, 1)
             (nKQ == 0 || mbar_test(&bars[B_KQFREE], (nKQ - 1) & 1))) {
           tc_fence_after();
           const uint32_t kqa = sb + OFF_KQ + (nKQ % KQ_STAGES) * KQ_STAGE;
+          const uint64_t bq = sdesc_sw128(kqa, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a = kqa + (kk >> 2) * KQ_PANEL + (kk & 3) * 32;
-            mma_bf16(tm + TM_KQ, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), ID_KQ, kk > 0);
+            const uint64_t d = bq + (uint64_t)(((kk >> 2) * KQ_PANEL + (kk & 3) * 32) >> 4);
+            mma_bf16(tm + TM_KQ, d, d, ID_KQ, kk > 0);
           }
           mma_commit(&bars[B_KQDONE]);
           ++nKQ;
@@ -352,6 +352,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         } else if (*abort_flag || globaltimer_ns() - t_prog > kWaitLimitNs) {
           raise_abort(abort_flag, p.status);
           break;
+        } else {
+          __nanosleep(32);     // leave issue slots to the warps sharing this sub-partition
         }
       }
     }
@@ -404,20 +406,29 @@ __global__ void __launch_bounds__(NTHR, 1)
         const float* vs = vecs + (c % KQ_STAGES) * 512;
         if (!(ok = wg_wait(&bars[B_DTDONE], c & 1, BAR_STATE, abort_flag, p.status))) break;
         tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[32];
-          tmem_ld32(tl + TM_DT + 32 * hh, x);
+        {
+          float x[64];
+          tmem_ld32(tl + TM_DT, *reinterpret_cast<float(*)[32]>(x));
+          tmem_ld32(tl + TM_DT + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           tmem_ld_wait();
           uint32_t u[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-          tmem_st16(tl + TM_DB + 16 * hh, u);
+          for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            u[e] = pack_bf16x2(x[2 * e] * vs[VEC_DEC + 32 * hh + 2 * e],
-                               x[2 * e + 1] * vs[VEC_DEC + 32 * hh + 2 * e + 1]);
-          tmem_st16(tl + TM_DDB + 16 * hh, u);
+            for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[32 * hh + 2 * e], x[32 * hh + 2 * e + 1]);
+            tmem_st16(tl + TM_DB + 16 * hh, u);
+          }
+          const float4* dec4 = reinterpret_cast<const float4*>(vs + VEC_DEC);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 d4 = dec4[8 * hh + e];
+              u[2 * e] = pack_bf16x2(x[32 * hh + 4 * e] * d4.x, x[32 * hh + 4 * e + 1] * d4.y);
+              u[2 * e + 1] = pack_bf16x2(x[32 * hh + 4 * e + 2] * d4.z, x[32 * hh + 4 * e + 3] * d4.w);
+            }
+            tmem_st16(tl + TM_DDB + 16 * hh, u);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -434,23 +445,28 @@ __global__ void __launch_bounds__(NTHR, 1)
           gn = vecs[((c + 1) % KQ_STAGES) * 512 + VEC_EG + 63];
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float x[32];
-          tmem_ld32(tl + TM_S + 32 * cc, x);
+        for (int cp = 0; cp < 2; ++cp) {
+          float x[64];
+          tmem_ld32(tl + TM_S + 64 * cp, *reinterpret_cast<float(*)[32]>(x));
+          tmem_ld32(tl + TM_S + 64 * cp + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           tmem_ld_wait();
           if (!last) {
             uint32_t u[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-            tmem_st16(tl + TM_SB + 16 * cc, u);
+            for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] *= gn;
-            tmem_st32(tl + TM_S + 32 * cc, x);
+              for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(x[32 * hh + 2 * e], x[32 * hh + 2 * e + 1]);
+              tmem_st16(tl + TM_SB + 32 * cp + 16 * hh, u);
+            }
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] *= gn;
+            tmem_st32(tl + TM_S + 64 * cp, *reinterpret_cast<float(*)[32]>(x));
+            tmem_st32(tl + TM_S + 64 * cp + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           } else if (p.final_state) {
             float4* dst =
-                reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + 32 * cc);
+                reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + 64 * cp);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
           }
         }
@@ -464,21 +480,25 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else if (warp >= 8 && warp < 12) {
     // ---------------------------------------------------------------- prep
+    // Order per chunk c: [KQ(c) epilogue -> release KQ] [head of chunk c+1, so its KQ
+    // product runs during this chunk's solve] [solve(c), T', T''] [W^T tile].
     const int pt = tid - 256;                        // 0..127 = TMEM lane row
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
     float* AT = reinterpret_cast<float*>(sm + OFF_AT);
     float* X = reinterpret_cast<float*>(sm + OFF_X);
-    for (int c = 0; c < nc; ++c) {
+    // head: the chunk's tiles have landed -> zero padded rows, gamma and decay vectors
+    auto head = [&](int c) -> bool {
       const int s = c % KQ_STAGES, sv = c & 1;
       const int L = chunk_len(bos, eos, c);
       float* vs = vecs + s * 512;
-      uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
-      uint8_t* vt = sm + OFF_V + sv * V_STAGE;
-      if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status)) break;
-      if (!wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status)) break;
+      if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status))
+        return false;
+      if (!wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status)) return false;
       if (L < CHUNK) {
         // rows past the sequence end belong to the next sequence (or are past
         // the tensor): zero them so they contribute nothing to any product
+        uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
+        uint8_t* vt = sm + OFF_V + sv * V_STAGE;
         const int rows = CHUNK - L;
         for (int idx = pt; idx < 6 * rows * 8; idx += 128) {
           const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
@@ -488,6 +508,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                        : kq + pnl * KQ_PANEL + (which == 1 ? 8192u : 0u);
           *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
       if (pt < 32) {
         warp_cumsum64(vs + VEC_G, vs + VEC_GAM, lane);
@@ -503,11 +524,11 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
         const bool fact = (mx - mn) <= 80.f;
         const float mid = 0.5f * (mx + mn);
-        const float gC = vs[VEC_GAM + 63];
+        const float gC = __shfl_sync(0xffffffffu, a1, 31);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int i = 2 * lane + e;
-          const float gi = vs[VEC_GAM + i];
+          const float gi = e ? a1 : a0;
           vs[VEC_EG + i] = expf(gi);
           vs[VEC_DEC + i] = expf(gC - gi);
           vs[VEC_EP + i] = fact ? expf(gi - mid) : 0.f;
@@ -515,44 +536,61 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
         if (lane == 0) vs[VEC_FLAG] = fact ? 1.f : 0.f;
       }
-      fence_proxy_async_smem();
       named_bar(BAR_PREP, 128);
       if (pt == 0) {
         mbar_arrive(&bars[B_KQREADY]);
         mbar_arrive(&bars[B_VEC + s]);
       }
+      return true;
+    };
+    bool ok = nc > 0 ? head(0) : true;
+    for (int c = 0; c < nc && ok; ++c) {
+      const int s = c % KQ_STAGES;
+      float* vs = vecs + s * 512;
+      uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
       if (c >= 2 &&
-          !wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag, p.status))
+          !(ok = wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag, p.status)))
         break;
-      if (!wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status)) break;
+      if (!(ok = wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status))) break;
       tc_fence_after();
       {
         const bool fact = vs[VEC_FLAG] != 0.f;
         const int i = pt & 63;
         const float gi = vs[VEC_GAM + i], epi = vs[VEC_EP + i];
         const float bi = (pt < 64) ? vs[VEC_BETA + i] : 1.f;
-        uint8_t* ah = sm + OFF_AH + (c & 1) * 8192;
+        float x[64];
+        tmem_ld32(tl + TM_KQ, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(tl + TM_KQ + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        tmem_ld_wait();
+        if (fact) {
+          const float f = bi * epi;
+          const float4* em4 = reinterpret_cast<const float4*>(vs + VEC_EM);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[32];
-          tmem_ld32(tl + TM_KQ + 32 * hh, x);
-          tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = 32 * hh + jj;
-            const float dcy = fact ? epi * vs[VEC_EM + j] : expf(j <= i ? gi - vs[VEC_GAM + j] : 0.f);
-            x[jj] *= bi * dcy;
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 e4 = em4[j4];
+            x[4 * j4] *= f * e4.x;
+            x[4 * j4 + 1] *= f * e4.y;
+            x[4 * j4 + 2] *= f * e4.z;
+            x[4 * j4 + 3] *= f * e4.w;
           }
-          if (pt < 64) {       // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+        } else {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) AT[i * SOLVE_LD + 32 * hh + jj] = (32 * hh + jj < i) ? x[jj] : 0.f;
-          } else {             // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
+          for (int j = 0; j < 64; ++j) x[j] *= bi * expf(j <= i ? gi - vs[VEC_GAM + j] : 0.f);
+        }
+        if (pt < 64) {         // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+          float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              if (32 * hh + jj > i) x[jj] = 0.f;
+          for (int j4 = 0; j4 < 16; ++j4)
+            row[j4] = make_float4(4 * j4 < i ? x[4 * j4] : 0.f, 4 * j4 + 1 < i ? x[4 * j4 + 1] : 0.f,
+                                  4 * j4 + 2 < i ? x[4 * j4 + 2] : 0.f,
+                                  4 * j4 + 3 < i ? x[4 * j4 + 3] : 0.f);
+        } else {               // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
+          uint8_t* ah = sm + OFF_AH + (c & 1) * 8192;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) st_row8_bf16(ah, i, 32 * hh + 8 * e, 8192, x + 8 * e);
-          }
+          for (int j = 0; j < 64; ++j)
+            if (j > i) x[j] = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) st_row8_bf16(ah, i, 8 * e, 8192, x + 8 * e);
         }
       }
       tc_fence_before();
@@ -578,17 +616,22 @@ __global__ void __launch_bounds__(NTHR, 1)
         mbar_arrive(&bars[B_KQFREE]);
         mbar_arrive(&bars[B_QG + s]);
       }
+      if (c + 1 < nc && !(ok = head(c + 1))) break;
       // T = (I + A)^{-1}, then T' = T diag(beta), T'' = T diag(beta e^gamma)
       solve64_tc_inplace(AT, X, pt, 128, PrepBar());
       for (int idx = pt; idx < 64 * 8; idx += 128) {
         const int i = idx >> 3, cg = (idx & 7) * 8;
+        const float4* tr = reinterpret_cast<const float4*>(AT + i * SOLVE_LD + cg);
+        const float4* b4 = reinterpret_cast<const float4*>(vs + VEC_BETA + cg);
+        const float4* g4 = reinterpret_cast<const float4*>(vs + VEC_EG + cg);
         float t1[8], t2[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = cg + e;
-          const float t = AT[i * SOLVE_LD + j] * vs[VEC_BETA + j];
-          t1[e] = t;
-          t2[e] = t * vs[VEC_EG + j];
+        for (int h4 = 0; h4 < 2; ++h4) {
+          const float4 t = tr[h4], b = b4[h4], g = g4[h4];
+          t1[4 * h4] = t.x * b.x; t1[4 * h4 + 1] = t.y * b.y;
+          t1[4 * h4 + 2] = t.z * b.z; t1[4 * h4 + 3] = t.w * b.w;
+          t2[4 * h4] = t1[4 * h4] * g.x; t2[4 * h4 + 1] = t1[4 * h4 + 1] * g.y;
+          t2[4 * h4 + 2] = t1[4 * h4 + 2] * g.z; t2[4 * h4 + 3] = t1[4 * h4 + 3] * g.w;
         }
         st_row8_bf16(sm + OFF_T1, i, cg, 8192, t1);
         st_row8_bf16(sm + OFF_T2, i, cg, 8192, t2);
@@ -596,15 +639,15 @@ __global__ void __launch_bounds__(NTHR, 1)
       fence_proxy_async_smem();
       named_bar(BAR_PREP, 128);
       if (pt == 0) mbar_arrive(&bars[B_TTREADY]);
-      if (!wg_wait(&bars[B_WTDONE], c & 1, BAR_PREP, abort_flag, p.status)) break;
+      if (!(ok = wg_wait(&bars[B_WTDONE], c & 1, BAR_PREP, abort_flag, p.status))) break;
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float x[32];
-        tmem_ld32(tl + TM_WT + 32 * hh, x);
+      {
+        float x[64];
+        tmem_ld32(tl + TM_WT, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(tl + TM_WT + 32, *reinterpret_cast<float(*)[32]>(x + 32));
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) st_row8_bf16(sm + OFF_WT, pt, 32 * hh + 8 * e, 16384, x + 8 * e);
+        for (int e = 0; e < 8; ++e) st_row8_bf16(sm + OFF_WT, pt, 8 * e, 16384, x + 8 * e);
       }
       fence_proxy_async_smem();
       tc_fence_before();

@@ -128,9 +128,10 @@ template <typename Bar>
 __device__ void solve64_tc_inplace(float* AT, float* X, int tid, int nthr, Bar bar) {
   const int warp = tid >> 5, lane = tid & 31;
   const int L = SOLVE_LD;
+  // diagonal blocks: warp b (< 4) inverts block b, lane m (and m + 16, redundantly) owns column m
   float acc[16];
-  const int b = tid >> 4, m = tid & 15, base = 16 * b;
-  if (tid < 64) {
+  const int m = lane & 15, base = 16 * (warp & 3);
+  if (warp < 4) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = (i == m) ? 1.f : 0.f;
 #pragma unroll
@@ -141,17 +142,21 @@ __device__ void solve64_tc_inplace(float* AT, float* X, int tid, int nthr, Bar b
     }
   }
   bar();
-  if (tid < 64) {
+  if (warp < 4) {
+    if (lane < 16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) AT[(base + i) * L + base + m] = acc[i];
-  } else {
-    for (int idx = tid - 64; idx < 6 * 256; idx += nthr - 64) {
-      const int blk = idx >> 8, e = idx & 255;
-      const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      AT[(16 * br + (e >> 4)) * L + 16 * bc + (e & 15)] = 0.f;
+      for (int i = 0; i < 16; ++i) AT[(base + i) * L + base + m] = acc[i];
+    } else {
+      // zero the six 16x16 blocks above the block diagonal (64 threads)
+      for (int idx = warp * 16 + lane - 16; idx < 6 * 256; idx += 64) {
+        const int blk = idx >> 8, e = idx & 255;
+        const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        AT[(16 * br + (e >> 4)) * L + 16 * bc + (e & 15)] = 0.f;
+      }
     }
   }
+  (void)nthr;
   bar();
   if (warp < 4) {
     const int p = warp >> 1, nt = warp & 1, r0 = 32 * p;
