@@ -212,7 +212,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
 
-  if (warp == 0) {
+  // Roles, each with its own register budget (launch: 128 per thread = the whole
+  // register file; budgets sum to 480 x 128 threads <= 65536):
+  // loader/issuer 56, state 136, prep 192, out 96.
+  if (warp < 4) {
+   reg_dealloc<56>();
+   if (warp == 0) {
     // ------------------------------------------------------------- loader
     int last_kq[KQ_STAGES] = {-1, -1, -1}, last_v[V_STAGES] = {-1, -1};
     for (int c = 0; c < nc; ++c) {
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int s = 0; s < (int)V_STAGES; ++s)
       if (last_v[s] >= 0) mbar_wait(&bars[B_VFULL + s], (uint32_t)(last_v[s] >> 1) & 1u, 100000000ull);
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nc > 0) {
       int nKQ = 0, nWU = 0, nDT = 0, nSQ = 0, nSU = 0;
@@ -358,7 +363,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+   }
+  } else if (warp < 8) {
+    reg_alloc<136>();
     // --------------------------------------------------------------- state
     const int v = tid - 128;                         // TMEM lane = state row
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
@@ -478,7 +485,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if (warp < 12) {
+    reg_alloc<192>();
     // ---------------------------------------------------------------- prep
     // Order per chunk c: [KQ(c) epilogue -> release KQ] [head of chunk c+1, so its KQ
     // product runs during this chunk's solve] [solve(c), T', T''] [W^T tile].
@@ -654,7 +662,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       named_bar(BAR_PREP, 128);
       if (pt == 0) mbar_arrive(&bars[B_WTREADY]);
     }
-  } else if (warp >= 12) {
+  } else {
+    reg_dealloc<96>();
     // ----------------------------------------------------------------- out
     const int v = tid - 384;
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
