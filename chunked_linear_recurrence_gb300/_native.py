@@ -24,8 +24,8 @@ STATUS_NAMES = {0: "SF_OK", 1: "SF_ERR_INVALID_ARG", 2: "SF_ERR_UNSUPPORTED",
 # Every symbol include/sf_gdn.h declares.
 EXPORTS = ("sf_last_error", "sf_version", "sf_gdn_fwd_workspace", "sf_gdn_chunk_fwd",
            "sf_gdn_summary_workspace", "sf_gdn_segment_summary", "sf_state_scan",
-           "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_validate_cu_seqlens",
-           "sf_workspace_status")
+           "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc",
+           "sf_validate_cu_seqlens", "sf_workspace_status")
 
 
 class SfError(RuntimeError):
@@ -69,10 +69,13 @@ def load(path: str = LIB_PATH):
         lib.sf_gdn_bwd_workspace.restype = sz
         lib.sf_gdn_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.sf_gdn_chunk_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 vp, vp, vp, vp, vp, vp, vp]
         lib.sf_validate_cu_seqlens.argtypes = [vp, I, I, vp]
         lib.sf_workspace_status.argtypes = [vp, vp]
         for f in ("sf_gdn_chunk_fwd", "sf_gdn_segment_summary", "sf_state_scan",
-                  "sf_gdn_chunk_bwd", "sf_validate_cu_seqlens", "sf_workspace_status"):
+                  "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc", "sf_validate_cu_seqlens",
+                  "sf_workspace_status"):
             getattr(lib, f).restype = st
         _lib = lib
         return lib
@@ -207,6 +210,28 @@ def sf_gdn_chunk_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state=No
                                 _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dgate"]),
                                 _ptr(grads["dbeta"]), _ptr(grads["d_initial_state"]),
                                 _ptr(ws), ws.numel(), _stream(stream)))
+    return grads
+
+
+def sf_gdn_chunk_bwd_noalloc(q, k, v, gate, beta, initial_state, d_out, d_final_state=None,
+                             cu_seqlens=None, scale=None, want_d_initial_state=True, grads=None,
+                             stream=None):
+    """sf_gdn_chunk_bwd with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory at this point; see
+    include/sf_gdn.h for the size limit and the sharing rules)."""
+    lib = load()
+    shape = make_shape(q, v, cu_seqlens, scale)
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dgate=torch.empty_like(gate), dbeta=torch.empty_like(beta),
+                     d_initial_state=(torch.empty(shape.N, shape.H, shape.V, shape.K,
+                                                  dtype=torch.float32, device=q.device)
+                                      if want_d_initial_state else None))
+    _check(lib.sf_gdn_chunk_bwd_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(_f32(gate)), _ptr(_f32(beta)),
+        _ptr(_f32(initial_state)), _ptr(cu_seqlens), _ptr(d_out), _ptr(_f32(d_final_state)),
+        _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dgate"]),
+        _ptr(grads["dbeta"]), _ptr(grads["d_initial_state"]), _stream(stream)))
     return grads
 
 

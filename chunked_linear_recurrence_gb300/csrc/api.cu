@@ -7,6 +7,7 @@
 #include <string>
 
 #include "../../include/sf_gdn.h"
+#include "api_internal.cuh"
 #include "common.cuh"
 #include "fwd_tc.cuh"
 #include "scan.cuh"
@@ -25,6 +26,20 @@ sf_status fail(sf_status s, const char* fmt, ...) {
   g_last_error = buf;
   return s;
 }
+
+}  // namespace
+
+sf_status sfg::report(sf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+namespace {
 
 sf_status cuda_fail(cudaError_t e, const char* where) {
   return fail(SF_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));

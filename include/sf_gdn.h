@@ -18,7 +18,9 @@
  * ---------------------------------------
  *  * Every tensor pointer is a DEVICE pointer owned by the caller.  The library
  *    allocates no device or host memory in any entry point; scratch comes from
- *    the caller's `workspace` (size from the matching *_workspace query).
+ *    the caller's `workspace` (size from the matching *_workspace query), or,
+ *    for sf_gdn_chunk_bwd_noalloc only, from a fixed array built into the
+ *    library.
  *  * Layouts are contiguous, row-major:
  *        q, k    [B, T, H, K]      v, out, d_out  [B, T, H, V]
  *        gate, beta, dgate, dbeta  [B, T, H]  (FP32)
@@ -163,6 +165,36 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape *shape, const void *q, const void 
                            void *dk, void *dv, float *dgate, float *dbeta,
                            float *d_initial_state, void *workspace, size_t ws_bytes,
                            sf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Backward without a workspace.  The pages have no counterpart of this entry
+ * point; it exists for callers that cannot allocate device memory where they
+ * need gradients -- code recording a CUDA graph (an allocation is not part of
+ * the captured work), host runtimes that freeze their allocator after
+ * warm-up, embedders that own all device memory themselves.  Same arguments
+ * and results as sf_gdn_chunk_bwd, minus the workspace: the scratch (chunk
+ * checkpoints and cotangent tape) is a fixed device array of
+ * SF_BWD_NOALLOC_SCRATCH_BYTES built into the library, present on every GPU
+ * that loads it until the process exits.  No CUDA, library or other
+ * allocating routine is called.
+ *  * Limit: shapes whose sf_gdn_bwd_workspace() exceeds
+ *    SF_BWD_NOALLOC_SCRATCH_BYTES return SF_ERR_UNSUPPORTED (e.g. K = V = 128:
+ *    at most 255 chunk-heads, i.e. sequences x heads x ceil(T/64), plus one per
+ *    sequence when packed).
+ *  * The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress, with the device current); make that first
+ *    call before any stream capture.
+ *  * Every call shares the one array: calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on it.  Nothing in it has to
+ *    start at zero; each call writes every scratch value before reading it.
+ * ---------------------------------------------------------------------- */
+#define SF_BWD_NOALLOC_SCRATCH_BYTES (32ull << 20)
+sf_status sf_gdn_chunk_bwd_noalloc(const sf_gdn_shape *shape, const void *q, const void *k,
+                                   const void *v, const float *gate, const float *beta,
+                                   const float *initial_state, const int32_t *cu_seqlens,
+                                   const void *d_out, const float *d_final_state, void *dq,
+                                   void *dk, void *dv, float *dgate, float *dbeta,
+                                   float *d_initial_state, sf_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Helpers (not on the hot path).
