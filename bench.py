@@ -48,6 +48,29 @@ SUM_BYTES_PER_TH = 520           # k, v, gate, beta
 STATE_BYTES = 128 * 128 * 4      # one [V,K] FP32 state
 
 
+def fwd_traffic():
+    """DRAM bytes per launch of the forward kernel from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    import hashlib
+    csrc = os.path.join(ROOT, "chunked_linear_recurrence_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("fwd_tc.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    try:
+        rec = {}
+        with open(os.path.join(ROOT, "profiles", "gdn_fwd_tc_traffic.txt")) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("source_sha256") == h.hexdigest():
+            return float(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -219,7 +242,7 @@ def run_ours(args):
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                 "algorithmic_bytes": fwd_bytes,
-                "traffic": args.traffic if args.traffic else None,
+                "traffic": fwd_traffic(),
                 "flops": th * FWD_FLOP_PER_TH,
                 "tensor_frac": round(th * FWD_FLOP_PER_TH / (ms * 1e-3) / (tflops * 1e12), 4)}
 
@@ -356,28 +379,26 @@ def bench_state_passing(args, W, dev, ws_n, hbm, peak_src):
 
 
 def oracle_baseline(inp, w, target_s=10.0):
-    """The FP64 oracle on a bounded sample of the workload: the first batch row,
-    all heads, the first `t` tokens, grown until ~target_s of CPU time."""
-    import numpy as np
-
+    """The FP64 oracle on a bounded sample of the workload: the whole workload
+    (every batch row, head and token) repeated until about `target_s` seconds
+    of CPU time have been spent."""
     import oracle
 
     def f64(t):
         return t.detach().cpu().double().numpy()
 
-    q, k, v, g, b = (f64(inp[n][:1]) for n in ("q", "k", "v", "gate", "beta"))
-    s0 = f64(inp["initial_state"][:1])
-    t = 256
-    while True:
+    q, k, v, g, b = (f64(inp[n]) for n in ("q", "k", "v", "gate", "beta"))
+    s0 = f64(inp["initial_state"])
+    reps, el = 0, 0.0
+    while el < target_s:
         t0 = time.perf_counter()
-        oracle.gdn_fwd(q[:, :t], k[:, :t], v[:, :t], g[:, :t], b[:, :t], s0)
-        el = time.perf_counter() - t0
-        if el >= target_s / 4 or t >= w.T:
-            break
-        t = min(w.T, t * 4)
-    return {"value": t / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"first batch row, all {w.H} heads, first {t} of {w.T} tokens "
-                      f"({el:.2f} s, FP64 token-by-token, OpenMP over heads)"}
+        oracle.gdn_fwd(q, k, v, g, b, s0)
+        el += time.perf_counter() - t0
+        reps += 1
+    tokens = reps * w.B * w.T
+    return {"value": tokens / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole workload (B={w.B}, T={w.T}, H={w.H}) x {reps} passes, "
+                      f"{el:.1f} s, FP64 token-by-token, OpenMP over (sequence, head) chains"}
 
 
 def run_reference(args):
@@ -395,9 +416,9 @@ def run_reference(args):
     def f64(t):
         return t.detach().double().numpy()
 
-    # each step: the oracle forward on the first batch row, all heads, a bounded
-    # number of tokens (so the whole --steps/--warmup run ends in minutes)
-    t_tok = args.ref_tokens
+    # each step: the oracle forward on one batch row (all heads, all tokens) -- a
+    # bounded sample, so the whole --steps/--warmup run ends within minutes
+    t_tok = min(args.ref_tokens, w.T)
     arrs = [f64(inp[n][:1, :t_tok]) for n in ("q", "k", "v", "gate", "beta")]
     s0 = f64(inp["initial_state"][:1])
     for _ in range(args.warmup):
@@ -409,7 +430,8 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = t_tok / (ms * 1e-3)
-    sample = f"first batch row, all {w.H} heads, first {t_tok} of {w.T} tokens per step"
+    sample = (f"one batch row per step: all {w.H} heads, {t_tok} of {w.T} tokens "
+              f"(FP64 token-by-token, OpenMP over heads)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -430,9 +452,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--fwd-only", action="store_true", help="skip the fwd+bwd and state-passing lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-tokens", type=int, default=256)
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per launch of the forward kernel from an ncu capture")
+    ap.add_argument("--ref-tokens", type=int, default=4096,
+                    help="tokens of one batch row the reference arm runs per step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
