@@ -125,7 +125,7 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
-    e = sfg::launch_tc_fwd(p, reinterpret_cast<int*>(workspace), cs);
+    e = sfg::launch_tc(p, sfg::TC_MODE_FWD, reinterpret_cast<int*>(workspace), cs);
   } else {
     e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
   }
@@ -158,8 +158,13 @@ sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const
   sfg::ChainParams p{};
   p.k = k; p.v = v; p.g = gate; p.beta = beta; p.bounds = bounds; p.P = P; p.E = S_ext;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = R; p.scale = 1.f;
-  cudaError_t e = sfg::launch_simt_chain(p, sfg::MODE_SUMMARY, shape->dtype == SF_BF16, shape->K,
-                                         R, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = shape->dtype == SF_BF16;
+  cudaError_t e;
+  if (bf16 && shape->K == 128 && sfg::tc_fwd_available())
+    e = sfg::launch_tc(p, sfg::TC_MODE_SUMMARY, reinterpret_cast<int*>(workspace), cs);
+  else
+    e = sfg::launch_simt_chain(p, sfg::MODE_SUMMARY, bf16, shape->K, R, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return SF_OK;
 }
@@ -223,7 +228,11 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   p.dout = d_out; p.dsf = d_final_state; p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dgate;
   p.dbeta = dbeta; p.ds0 = d_initial_state;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
-  cudaError_t e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
+  cudaError_t e;
+  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available())
+    e = sfg::launch_tc(p, sfg::TC_MODE_REPLAY, reinterpret_cast<int*>(workspace), cs);
+  else
+    e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   e = sfg::launch_simt_bwd(p, bf16, D, slots, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);

@@ -129,6 +129,12 @@ struct TcParams {
   int* status;
   int B, T, H, N;
   float scale;
+  int mode;                 // TC_MODE_*
+  const int32_t* bounds;    // summary: [R,2] token ranges
+  float* P;                 // summary: [R,H,K,K]
+  float* E;                 // summary: [R,H,V,K]
+  float* ckpt;              // replay: [slots,H,V,K] chunk-entry states
+  int R;
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -188,9 +194,37 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
-  const int n = blockIdx.x / H, h = blockIdx.x % H;
-  int64_t bos, eos;
-  seq_span(n, p.B, p.T, p.cu, bos, eos);
+  // Work item.  FWD / REPLAY: one (sequence, head) chain.  SUMMARY: one (range,
+  // head) pair; the first R*H CTAs build S_ext (zero entry state, value term on),
+  // the next R*H build P (identity entry state, value term off) -- the probing
+  // construction of the Attention Gym "Context Parallelism" section.
+  int n, h;
+  int64_t bos = 0, eos = 0;
+  bool valid = true, value_on = true;
+  const bool has_out = (p.mode == TC_MODE_FWD);
+  int init_kind = p.s0 ? 1 : 0;              // 0: zero, 1: initial state, 2: identity
+  float* final_dst = (p.mode == TC_MODE_FWD) ? p.final_state : nullptr;
+  if (p.mode == TC_MODE_SUMMARY) {
+    const int per = p.R * H;
+    const bool second = (int)blockIdx.x >= per;
+    const int bx = (int)blockIdx.x - (second ? per : 0);
+    n = bx / H;
+    h = bx % H;
+    const int64_t total = (int64_t)p.B * p.T;
+    const int64_t r0 = p.bounds[2 * n], r1 = p.bounds[2 * n + 1];
+    valid = (r0 >= 0 && r1 >= r0 && r1 <= total && (r1 == r0 || r0 / p.T == (r1 - 1) / p.T));
+    if (valid) {
+      bos = r0;
+      eos = r1;
+    }
+    value_on = !second;
+    init_kind = second ? 2 : 0;
+    final_dst = second ? p.P : p.E;
+  } else {
+    n = blockIdx.x / H;
+    h = blockIdx.x % H;
+    seq_span(n, p.B, p.T, p.cu, bos, eos);
+  }
   const int nc = (int)((eos - bos + CHUNK - 1) / CHUNK);
   const size_t state_off = ((size_t)n * H + h) * D * D;
 
@@ -230,11 +264,13 @@ __global__ void __launch_bounds__(NTHR, 1)
         break;
       if (lane == 0) {
         uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
-        mbar_arrive_expect_tx(&bars[B_KQFULL + s], 4 * 8192);
+        mbar_arrive_expect_tx(&bars[B_KQFULL + s], (has_out ? 4 : 2) * 8192);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
           tma_load_3d(kq + pnl * KQ_PANEL, &tmK, &bars[B_KQFULL + s], 64 * pnl, h, (int)c0);
-          tma_load_3d(kq + pnl * KQ_PANEL + 8192, &tmQ, &bars[B_KQFULL + s], 64 * pnl, h, (int)c0);
+          if (has_out)
+            tma_load_3d(kq + pnl * KQ_PANEL + 8192, &tmQ, &bars[B_KQFULL + s], 64 * pnl, h,
+                        (int)c0);
         }
       }
       last_kq[s] = c;
@@ -246,6 +282,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         vs[VEC_BETA + e] = (e < L) ? p.beta[off] : 0.f;
       }
       mbar_arrive(&bars[B_KQFULL + s]);
+      if (!value_on) continue;
       if (c >= (int)V_STAGES &&
           !warp_wait(&bars[B_VEMPTY + sv], (uint32_t)((c - V_STAGES) >> 1) & 1u, abort_flag,
                      p.status))
@@ -280,13 +317,14 @@ __global__ void __launch_bounds__(NTHR, 1)
           const uint64_t bd = sdesc_sw128(sb + OFF_WT, 16384, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ta(tm + TM_DT, tm + TM_SB + kk * 8, bd + (uint64_t)(kk * 2048 >> 4), ID_DT, 1);
+            mma_bf16_ta(tm + TM_DT, tm + TM_SB + kk * 8, bd + (uint64_t)(kk * 2048 >> 4), ID_DT,
+                        (value_on || kk > 0) ? 1u : 0u);
           mma_commit(&bars[B_DTDONE]);
           ++nDT;
           prog = true;
         }
         // output, state part: O = S Qg^T
-        if (nSQ < nDT && mbar_test(&bars[B_QG + nSQ % KQ_STAGES], (nSQ / KQ_STAGES) & 1) &&
+        if (has_out && nSQ < nDT && mbar_test(&bars[B_QG + nSQ % KQ_STAGES], (nSQ / KQ_STAGES) & 1) &&
             (nSQ == 0 || mbar_test(&bars[B_OFREE], (nSQ - 1) & 1))) {
           tc_fence_after();
           const uint32_t kqa = sb + OFF_KQ + (nSQ % KQ_STAGES) * KQ_STAGE;
@@ -299,7 +337,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           prog = true;
         }
         // state update S += (Delta^T diag(dec)) K, then O += Delta^T Ahat^T
-        if (nSU < nSQ && mbar_test(&bars[B_DREADY], nSU & 1)) {
+        if (nSU < (has_out ? nSQ : nDT) && mbar_test(&bars[B_DREADY], nSU & 1)) {
           tc_fence_after();
           const int s = nSU % KQ_STAGES;
           const uint32_t kqa = sb + OFF_KQ + s * KQ_STAGE;
@@ -309,13 +347,15 @@ __global__ void __launch_bounds__(NTHR, 1)
             mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_SU, 1);
           mma_commit(&bars[B_SUDONE]);
           mma_commit(&bars[B_KQEMPTY + s]);
-          const uint32_t ah = sb + OFF_AH + (nSU & 1) * 8192;
-          const uint64_t ba = sdesc_sw128(ah, 0, 1024);
+          if (has_out) {
+            const uint32_t ah = sb + OFF_AH + (nSU & 1) * 8192;
+            const uint64_t ba = sdesc_sw128(ah, 0, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ta(tm + TM_O, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2), ID_OA, 1);
-          mma_commit(&bars[B_ODONE]);
-          mma_commit(&bars[B_AHFREE + (nSU & 1)]);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ta(tm + TM_O, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2), ID_OA, 1);
+            mma_commit(&bars[B_ODONE]);
+            mma_commit(&bars[B_AHFREE + (nSU & 1)]);
+          }
           ++nSU;
           prog = true;
         }
@@ -329,11 +369,14 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tm + TM_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_WT, kk > 0);
+          if (value_on) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tm + TM_DT, av + (uint64_t)(kk * 2048 >> 4), b1 + (uint64_t)(kk * 2), ID_WT, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tm + TM_DT, av + (uint64_t)(kk * 2048 >> 4), b1 + (uint64_t)(kk * 2), ID_WT,
+                       kk > 0);
+          }
           mma_commit(&bars[B_WTDONE]);
-          mma_commit(&bars[B_VEMPTY + (nWU & 1)]);
+          if (value_on) mma_commit(&bars[B_VEMPTY + (nWU & 1)]);
           ++nWU;
           prog = true;
         }
@@ -370,13 +413,28 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int v = tid - 128;                         // TMEM lane = state row
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
     bool ok = true;
+    // entry state row v, 4 consecutive columns starting at c
+    auto init4 = [&](int c) -> float4 {
+      if (init_kind == 1)
+        return *reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)v * D + c);
+      if (init_kind == 2)
+        return make_float4(v == c ? 1.f : 0.f, v == c + 1 ? 1.f : 0.f, v == c + 2 ? 1.f : 0.f,
+                           v == c + 3 ? 1.f : 0.f);
+      return make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    // replay: chunk-entry states go to ckpt[slot][h] (unscaled FP32)
+    float* ckpt = (p.mode == TC_MODE_REPLAY)
+                      ? p.ckpt + ((size_t)chunk_slot_base(n, p.B, p.T, p.cu) * H + h) * D * D +
+                            (size_t)v * D
+                      : nullptr;
+    const size_t ckpt_stride = (size_t)H * D * D;
     if (nc == 0) {
-      if (p.final_state)
-        for (int c = 0; c < D; c += 4) {
-          float4 x = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)v * D + c)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + c) = x;
-        }
+      if (final_dst) {
+        const float nanv = __int_as_float(0x7fc00000);
+        for (int c = 0; c < D; c += 4)
+          *reinterpret_cast<float4*>(final_dst + state_off + (size_t)v * D + c) =
+              valid ? init4(c) : make_float4(nanv, nanv, nanv, nanv);
+      }
     } else {
       ok = wg_wait(&bars[B_VEC + 0], 0, BAR_STATE, abort_flag, p.status);
       if (ok) {
@@ -384,17 +442,16 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           float x[32];
-          if (p.s0) {
-            const float4* src =
-                reinterpret_cast<const float4*>(p.s0 + state_off + (size_t)v * D + 32 * cc);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 t = src[e];
-              x[4 * e] = t.x; x[4 * e + 1] = t.y; x[4 * e + 2] = t.z; x[4 * e + 3] = t.w;
-            }
-          } else {
+          for (int e = 0; e < 8; ++e) {
+            const float4 t = init4(32 * cc + 4 * e);
+            x[4 * e] = t.x; x[4 * e + 1] = t.y; x[4 * e + 2] = t.z; x[4 * e + 3] = t.w;
+          }
+          if (ckpt) {
+            float4* dst = reinterpret_cast<float4*>(ckpt + 32 * cc);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = 0.f;
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
           }
           uint32_t u[16];
 #pragma unroll
@@ -458,6 +515,12 @@ __global__ void __launch_bounds__(NTHR, 1)
           tmem_ld32(tl + TM_S + 64 * cp + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           tmem_ld_wait();
           if (!last) {
+            if (ckpt) {
+              float4* dst = reinterpret_cast<float4*>(ckpt + (size_t)(c + 1) * ckpt_stride + 64 * cp);
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+            }
             uint32_t u[16];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -469,9 +532,9 @@ __global__ void __launch_bounds__(NTHR, 1)
             for (int e = 0; e < 64; ++e) x[e] *= gn;
             tmem_st32(tl + TM_S + 64 * cp, *reinterpret_cast<float(*)[32]>(x));
             tmem_st32(tl + TM_S + 64 * cp + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-          } else if (p.final_state) {
+          } else if (final_dst) {
             float4* dst =
-                reinterpret_cast<float4*>(p.final_state + state_off + (size_t)v * D + 64 * cp);
+                reinterpret_cast<float4*>(final_dst + state_off + (size_t)v * D + 64 * cp);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
@@ -501,14 +564,16 @@ __global__ void __launch_bounds__(NTHR, 1)
       float* vs = vecs + s * 512;
       if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status))
         return false;
-      if (!wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status)) return false;
+      if (value_on &&
+          !wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status))
+        return false;
       if (L < CHUNK) {
         // rows past the sequence end belong to the next sequence (or are past
         // the tensor): zero them so they contribute nothing to any product
         uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
         uint8_t* vt = sm + OFF_V + sv * V_STAGE;
         const int rows = CHUNK - L;
-        for (int idx = pt; idx < 6 * rows * 8; idx += 128) {
+        for (int idx = pt; idx < (value_on ? 6 : 4) * rows * 8; idx += 128) {
           const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
           const int r = L + rem / 8, ch = rem % 8;
           const int pnl = t6 & 1, which = t6 >> 1;
@@ -556,7 +621,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int s = c % KQ_STAGES;
       float* vs = vecs + s * 512;
       uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
-      if (c >= 2 &&
+      if (has_out && c >= 2 &&
           !(ok = wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag, p.status)))
         break;
       if (!(ok = wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status))) break;
@@ -592,7 +657,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             row[j4] = make_float4(4 * j4 < i ? x[4 * j4] : 0.f, 4 * j4 + 1 < i ? x[4 * j4 + 1] : 0.f,
                                   4 * j4 + 2 < i ? x[4 * j4 + 2] : 0.f,
                                   4 * j4 + 3 < i ? x[4 * j4 + 3] : 0.f);
-        } else {               // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
+        } else if (has_out) {  // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
           uint8_t* ah = sm + OFF_AH + (c & 1) * 8192;
 #pragma unroll
           for (int j = 0; j < 64; ++j)
@@ -604,7 +669,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_before();
       // Q rows scaled by e^{gamma_i} in place (the KQ product has consumed them): O's
       // state part S (diag(e^gamma) Q)^T then shares one accumulator with Delta^T Ahat^T
-      for (int idx = pt; idx < 64 * 2 * 8; idx += 128) {
+      for (int idx = pt; has_out && idx < 64 * 2 * 8; idx += 128) {
         const int r = idx >> 4, pnl = (idx >> 3) & 1, ch = idx & 7;
         uint4* ptr = reinterpret_cast<uint4*>(kq + pnl * KQ_PANEL + 8192 + r * 128 + ch * 16);
         const float e = vs[VEC_EG + r];
@@ -667,7 +732,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     // ----------------------------------------------------------------- out
     const int v = tid - 384;
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
-    for (int c = 0; c < nc; ++c) {
+    for (int c = 0; has_out && c < nc; ++c) {
       if (!wg_wait(&bars[B_ODONE], c & 1, BAR_OUT, abort_flag, p.status)) break;
       tc_fence_after();
       float a[32], b[32];
@@ -729,14 +794,16 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int H) {
 
 bool tc_fwd_available() { return encode_fn() != nullptr; }
 
-cudaError_t launch_tc_fwd(const ChainParams& cp, int* status, cudaStream_t st) {
+cudaError_t launch_tc(const ChainParams& cp, int mode, int* status, cudaStream_t st) {
   const int rows = cp.B * cp.T;
   if (rows <= 0) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, cp.q, rows, cp.H) || !make_map(&mk, cp.k, rows, cp.H) ||
+  // without an output the query tiles are never loaded; the K map stands in
+  const void* qsrc = (mode == TC_MODE_FWD) ? cp.q : cp.k;
+  if (!make_map(&mq, qsrc, rows, cp.H) || !make_map(&mk, cp.k, rows, cp.H) ||
       !make_map(&mv, cp.v, rows, cp.H))
     return cudaErrorInvalidValue;
-  TcParams p;
+  TcParams p{};
   p.g = cp.g;
   p.beta = cp.beta;
   p.s0 = cp.s0;
@@ -749,10 +816,17 @@ cudaError_t launch_tc_fwd(const ChainParams& cp, int* status, cudaStream_t st) {
   p.H = cp.H;
   p.N = cp.N;
   p.scale = cp.scale;
+  p.mode = mode;
+  p.bounds = cp.bounds;
+  p.P = cp.P;
+  p.E = cp.E;
+  p.ckpt = cp.ckpt;
+  p.R = cp.N;
   cudaError_t e = cudaFuncSetAttribute(gdn_fwd_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  gdn_fwd_tc_kernel<<<cp.N * cp.H, NTHR, SMEM_ALLOC, st>>>(mq, mk, mv, p);
+  const int ctas = (mode == TC_MODE_SUMMARY ? 2 : 1) * cp.N * cp.H;
+  if (ctas > 0) gdn_fwd_tc_kernel<<<ctas, NTHR, SMEM_ALLOC, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// fwd_tc.cuh -- launcher of the tensor-core (tcgen05 / TMEM / TMA) forward for
+// fwd_tc.cuh -- launcher of the tensor-core (tcgen05 / TMEM / TMA) chunk kernel for
 // BF16 q/k/v with K = V = 128.
 #pragma once
 #include <cuda_runtime.h>
@@ -6,8 +6,15 @@
 #include "simt_chunk.cuh"
 
 namespace sfg {
-// True when this build contains the tensor-core forward.
+
+// FWD: outputs + final state.  SUMMARY: per (range, head) the affine map's S_ext and
+// P (p.bounds, p.N = number of ranges, results in p.E / p.P).  REPLAY: chunk-entry
+// states into p.ckpt (the backward's state replay).
+enum { TC_MODE_FWD = 0, TC_MODE_SUMMARY = 1, TC_MODE_REPLAY = 2 };
+
+// True when this build can encode TMA descriptors (the tensor-core kernel is usable).
 bool tc_fwd_available();
 // status: device int the kernel sets to a nonzero code when a bounded wait expires.
-cudaError_t launch_tc_fwd(const ChainParams& p, int* status, cudaStream_t st);
+cudaError_t launch_tc(const ChainParams& p, int mode, int* status, cudaStream_t st);
+
 }  // namespace sfg
