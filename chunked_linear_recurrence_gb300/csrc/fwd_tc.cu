@@ -47,7 +47,7 @@ using namespace tc;
 
 constexpr int D = 128;
 constexpr int NTHR = 512;
-constexpr int BAR_STATE = 1, BAR_PREP = 2, BAR_OUT = 3;   // named barriers (128 threads each)
+constexpr int BAR_STATE = 1, BAR_PREP = 2;   // named barriers: state (128 threads), prep (256)
 
 // Shared-memory map (bytes from a 1024-aligned base); tiles use the panel layout of tc_ptx.cuh.
 constexpr uint32_t KQ_STAGES = 3, V_STAGES = 2;
@@ -137,7 +137,10 @@ struct TcParams {
   int R;
 };
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Wait limit in SM clock cycles (about 2 s at the GB300's clocks).  The cycle
+// counter is read instead of the global timer: it costs a few cycles, so the
+// issuer's polling loop stays responsive.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
   *abort_flag = 1;
@@ -148,19 +151,20 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* statu
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 
-// Every thread of a 128-thread warpgroup waits, then they agree on the outcome.
+// Every thread of a role (nthr threads on named barrier bar_id) waits, then they
+// agree on the outcome.
 __device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, int bar_id,
-                                        volatile int* abort_flag, int* status) {
-  const bool ok = named_bar_and(bar_id, 128, wait_or_abort(bar, parity, abort_flag));
-  if (!ok && (threadIdx.x & 127) == 0) raise_abort(abort_flag, status);
+                                        volatile int* abort_flag, int* status, int nthr = 128) {
+  const bool ok = named_bar_and(bar_id, nthr, wait_or_abort(bar, parity, abort_flag));
+  if (!ok && (threadIdx.x & (nthr - 1)) == 0) raise_abort(abort_flag, status);
   return ok;
 }
 
@@ -171,8 +175,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+constexpr int PREP_THREADS = 256;   // warps 8-15
 struct PrepBar {
-  __device__ __forceinline__ void operator()() const { named_bar(BAR_PREP, 128); }
+  __device__ __forceinline__ void operator()() const { named_bar(BAR_PREP, PREP_THREADS); }
 };
 
 __device__ __forceinline__ int chunk_len(int64_t bos, int64_t eos, int c) {
@@ -247,8 +252,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t tm = *tmem_slot;
 
   // Roles, each with its own register budget (launch: 128 per thread = the whole
-  // register file; budgets sum to 480 x 128 threads <= 65536):
-  // loader/issuer 56, state 136, prep 192, out 96.
+  // register file; budgets sum to 512 x 128 threads = 65536):
+  // loader/issuer 56, state (+ output stores) 136, prep (two warpgroups) 160.
   if (warp < 4) {
    reg_dealloc<56>();
    if (warp == 0) {
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nc > 0) {
       int nKQ = 0, nWU = 0, nDT = 0, nSQ = 0, nSU = 0;
-      uint64_t t_prog = globaltimer_ns();
+      long long t_prog = clock64();
       while (nSU < nc) {
         bool prog = false;
         // state transition: Delta^T += -S W^T
@@ -396,12 +401,10 @@ __global__ void __launch_bounds__(NTHR, 1)
           prog = true;
         }
         if (prog) {
-          t_prog = globaltimer_ns();
-        } else if (*abort_flag || globaltimer_ns() - t_prog > kWaitLimitNs) {
+          t_prog = clock64();
+        } else if (*abort_flag || clock64() - t_prog > kWaitLimitCycles) {
           raise_abort(abort_flag, p.status);
           break;
-        } else {
-          __nanosleep(32);     // leave issue slots to the warps sharing this sub-partition
         }
       }
     }
@@ -546,14 +549,37 @@ __global__ void __launch_bounds__(NTHR, 1)
           named_bar(BAR_STATE, 128);
           if (v == 0) mbar_arrive(&bars[B_SREADY]);
         }
+        if (has_out) {
+          // out[i][v] = scale O[v][i]: one warp writes 32 consecutive v of a token row
+          if (!(ok = wg_wait(&bars[B_ODONE], c & 1, BAR_STATE, abort_flag, p.status))) break;
+          tc_fence_after();
+          float a[64];
+          tmem_ld32(tl + TM_O, *reinterpret_cast<float(*)[32]>(a));
+          tmem_ld32(tl + TM_O + 32, *reinterpret_cast<float(*)[32]>(a + 32));
+          tmem_ld_wait();
+          tc_fence_before();
+          named_bar(BAR_STATE, 128);
+          if (v == 0) mbar_arrive(&bars[B_OFREE]);
+          const int64_t c0 = bos + (int64_t)c * CHUNK;
+          const int L = chunk_len(bos, eos, c);
+          __nv_bfloat16* orow = p.out + ((size_t)c0 * H + h) * D + v;
+          const size_t rs = (size_t)H * D;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < L) orow[i * rs] = __float2bfloat16_rn(p.scale * a[i]);
+        }
       }
     }
-  } else if (warp < 12) {
-    reg_alloc<192>();
+  } else {
+    reg_alloc<160>();
     // ---------------------------------------------------------------- prep
-    // Order per chunk c: [KQ(c) epilogue -> release KQ] [head of chunk c+1, so its KQ
-    // product runs during this chunk's solve] [solve(c), T', T''] [W^T tile].
-    const int pt = tid - 256;                        // 0..127 = TMEM lane row
+    // Warps 8-15 prepare the chunk ahead.  Order per chunk c: [KQ(c) epilogue ->
+    // release KQ] [head of chunk c+1, so its KQ product runs during this chunk's
+    // solve] [solve(c), T', T''] [W^T tile].  A thread owns TMEM row `lrow` and the
+    // column half `half` of it.
+    const int pt = tid - 256;                        // 0..255
+    const int half = pt >> 7;
+    const int lrow = ((warp & 3) << 5) + lane;
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
     float* AT = reinterpret_cast<float*>(sm + OFF_AT);
     float* X = reinterpret_cast<float*>(sm + OFF_X);
@@ -562,10 +588,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int s = c % KQ_STAGES, sv = c & 1;
       const int L = chunk_len(bos, eos, c);
       float* vs = vecs + s * 512;
-      if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status))
+      if (!wg_wait(&bars[B_KQFULL + s], (c / KQ_STAGES) & 1, BAR_PREP, abort_flag, p.status,
+                   PREP_THREADS))
         return false;
-      if (value_on &&
-          !wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status))
+      if (value_on && !wg_wait(&bars[B_VFULL + sv], (c >> 1) & 1, BAR_PREP, abort_flag, p.status,
+                               PREP_THREADS))
         return false;
       if (L < CHUNK) {
         // rows past the sequence end belong to the next sequence (or are past
@@ -573,7 +600,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
         uint8_t* vt = sm + OFF_V + sv * V_STAGE;
         const int rows = CHUNK - L;
-        for (int idx = pt; idx < (value_on ? 6 : 4) * rows * 8; idx += 128) {
+        for (int idx = pt; idx < (value_on ? 6 : 4) * rows * 8; idx += PREP_THREADS) {
           const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
           const int r = L + rem / 8, ch = rem % 8;
           const int pnl = t6 & 1, which = t6 >> 1;
@@ -586,8 +613,6 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (pt < 32) {
         warp_cumsum64(vs + VEC_G, vs + VEC_GAM, lane);
         __syncwarp();
-        // decay factors: e^{gamma_i - gamma_j} = e^{gamma_i - mid} e^{mid - gamma_j} when the
-        // chunk's gamma range keeps both factors inside e^{+-40}; else one exponential per entry
         const float a0 = vs[VEC_GAM + 2 * lane], a1 = vs[VEC_GAM + 2 * lane + 1];
         float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
 #pragma unroll
@@ -595,21 +620,24 @@ __global__ void __launch_bounds__(NTHR, 1)
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         }
-        const bool fact = (mx - mn) <= 80.f;
-        const float mid = 0.5f * (mx + mn);
-        const float gC = __shfl_sync(0xffffffffu, a1, 31);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 2 * lane + e;
-          const float gi = e ? a1 : a0;
-          vs[VEC_EG + i] = expf(gi);
-          vs[VEC_DEC + i] = expf(gC - gi);
-          vs[VEC_EP + i] = fact ? expf(gi - mid) : 0.f;
-          vs[VEC_EM + i] = fact ? expf(mid - gi) : 0.f;
+        // decay factors: e^{gamma_i - gamma_j} = e^{gamma_i - mid} e^{mid - gamma_j} when
+        // the chunk's gamma range keeps both factors inside e^{+-40}; else one
+        // exponential per entry
+        if (lane == 0) {
+          vs[VEC_FLAG] = (mx - mn) <= 80.f ? 1.f : 0.f;
+          vs[VEC_FLAG + 1] = 0.5f * (mx + mn);
         }
-        if (lane == 0) vs[VEC_FLAG] = fact ? 1.f : 0.f;
       }
-      named_bar(BAR_PREP, 128);
+      named_bar(BAR_PREP, PREP_THREADS);
+      if (pt < 64) {
+        const bool fact = vs[VEC_FLAG] != 0.f;
+        const float mid = vs[VEC_FLAG + 1], gi = vs[VEC_GAM + pt], gC = vs[VEC_GAM + 63];
+        vs[VEC_EG + pt] = expf(gi);
+        vs[VEC_DEC + pt] = expf(gC - gi);
+        vs[VEC_EP + pt] = fact ? expf(gi - mid) : 0.f;
+        vs[VEC_EM + pt] = fact ? expf(mid - gi) : 0.f;
+      }
+      named_bar(BAR_PREP, PREP_THREADS);
       if (pt == 0) {
         mbar_arrive(&bars[B_KQREADY]);
         mbar_arrive(&bars[B_VEC + s]);
@@ -622,24 +650,25 @@ __global__ void __launch_bounds__(NTHR, 1)
       float* vs = vecs + s * 512;
       uint8_t* kq = sm + OFF_KQ + s * KQ_STAGE;
       if (has_out && c >= 2 &&
-          !(ok = wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag, p.status)))
+          !(ok = wg_wait(&bars[B_AHFREE + (c & 1)], ((c - 2) >> 1) & 1, BAR_PREP, abort_flag,
+                         p.status, PREP_THREADS)))
         break;
-      if (!(ok = wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status))) break;
+      if (!(ok = wg_wait(&bars[B_KQDONE], c & 1, BAR_PREP, abort_flag, p.status, PREP_THREADS)))
+        break;
       tc_fence_after();
       {
         const bool fact = vs[VEC_FLAG] != 0.f;
-        const int i = pt & 63;
+        const int i = lrow & 63, j0 = 32 * half;
         const float gi = vs[VEC_GAM + i], epi = vs[VEC_EP + i];
-        const float bi = (pt < 64) ? vs[VEC_BETA + i] : 1.f;
-        float x[64];
-        tmem_ld32(tl + TM_KQ, *reinterpret_cast<float(*)[32]>(x));
-        tmem_ld32(tl + TM_KQ + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        const float bi = (lrow < 64) ? vs[VEC_BETA + i] : 1.f;
+        float x[32];
+        tmem_ld32(tl + TM_KQ + j0, x);
         tmem_ld_wait();
         if (fact) {
           const float f = bi * epi;
-          const float4* em4 = reinterpret_cast<const float4*>(vs + VEC_EM);
+          const float4* em4 = reinterpret_cast<const float4*>(vs + VEC_EM + j0);
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
+          for (int j4 = 0; j4 < 8; ++j4) {
             const float4 e4 = em4[j4];
             x[4 * j4] *= f * e4.x;
             x[4 * j4 + 1] *= f * e4.y;
@@ -648,28 +677,30 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) x[j] *= bi * expf(j <= i ? gi - vs[VEC_GAM + j] : 0.f);
+          for (int jj = 0; jj < 32; ++jj)
+            x[jj] *= bi * expf(j0 + jj <= i ? gi - vs[VEC_GAM + j0 + jj] : 0.f);
         }
-        if (pt < 64) {         // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
-          float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD);
+        if (lrow < 64) {       // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+          float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD + j0);
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4)
-            row[j4] = make_float4(4 * j4 < i ? x[4 * j4] : 0.f, 4 * j4 + 1 < i ? x[4 * j4 + 1] : 0.f,
-                                  4 * j4 + 2 < i ? x[4 * j4 + 2] : 0.f,
-                                  4 * j4 + 3 < i ? x[4 * j4 + 3] : 0.f);
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const int j = j0 + 4 * j4;
+            row[j4] = make_float4(j < i ? x[4 * j4] : 0.f, j + 1 < i ? x[4 * j4 + 1] : 0.f,
+                                  j + 2 < i ? x[4 * j4 + 2] : 0.f, j + 3 < i ? x[4 * j4 + 3] : 0.f);
+          }
         } else if (has_out) {  // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
           uint8_t* ah = sm + OFF_AH + (c & 1) * 8192;
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j > i) x[j] = 0.f;
+          for (int jj = 0; jj < 32; ++jj)
+            if (j0 + jj > i) x[jj] = 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) st_row8_bf16(ah, i, 8 * e, 8192, x + 8 * e);
+          for (int e = 0; e < 4; ++e) st_row8_bf16(ah, i, j0 + 8 * e, 8192, x + 8 * e);
         }
       }
       tc_fence_before();
       // Q rows scaled by e^{gamma_i} in place (the KQ product has consumed them): O's
       // state part S (diag(e^gamma) Q)^T then shares one accumulator with Delta^T Ahat^T
-      for (int idx = pt; has_out && idx < 64 * 2 * 8; idx += 128) {
+      for (int idx = pt; has_out && idx < 64 * 2 * 8; idx += PREP_THREADS) {
         const int r = idx >> 4, pnl = (idx >> 3) & 1, ch = idx & 7;
         uint4* ptr = reinterpret_cast<uint4*>(kq + pnl * KQ_PANEL + 8192 + r * 128 + ch * 16);
         const float e = vs[VEC_EG + r];
@@ -684,15 +715,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         *ptr = w;
       }
       fence_proxy_async_smem();
-      named_bar(BAR_PREP, 128);
+      named_bar(BAR_PREP, PREP_THREADS);
       if (pt == 0) {
         mbar_arrive(&bars[B_KQFREE]);
         mbar_arrive(&bars[B_QG + s]);
       }
       if (c + 1 < nc && !(ok = head(c + 1))) break;
       // T = (I + A)^{-1}, then T' = T diag(beta), T'' = T diag(beta e^gamma)
-      solve64_tc_inplace(AT, X, pt, 128, PrepBar());
-      for (int idx = pt; idx < 64 * 8; idx += 128) {
+      solve64_tc_inplace(AT, X, pt, PREP_THREADS, PrepBar());
+      for (int idx = pt; idx < 64 * 8; idx += PREP_THREADS) {
         const int i = idx >> 3, cg = (idx & 7) * 8;
         const float4* tr = reinterpret_cast<const float4*>(AT + i * SOLVE_LD + cg);
         const float4* b4 = reinterpret_cast<const float4*>(vs + VEC_BETA + cg);
@@ -710,48 +741,23 @@ __global__ void __launch_bounds__(NTHR, 1)
         st_row8_bf16(sm + OFF_T2, i, cg, 8192, t2);
       }
       fence_proxy_async_smem();
-      named_bar(BAR_PREP, 128);
+      named_bar(BAR_PREP, PREP_THREADS);
       if (pt == 0) mbar_arrive(&bars[B_TTREADY]);
-      if (!(ok = wg_wait(&bars[B_WTDONE], c & 1, BAR_PREP, abort_flag, p.status))) break;
+      if (!(ok = wg_wait(&bars[B_WTDONE], c & 1, BAR_PREP, abort_flag, p.status, PREP_THREADS)))
+        break;
       tc_fence_after();
       {
-        float x[64];
-        tmem_ld32(tl + TM_WT, *reinterpret_cast<float(*)[32]>(x));
-        tmem_ld32(tl + TM_WT + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        float x[32];
+        tmem_ld32(tl + TM_WT + 32 * half, x);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) st_row8_bf16(sm + OFF_WT, pt, 8 * e, 16384, x + 8 * e);
+        for (int e = 0; e < 4; ++e)
+          st_row8_bf16(sm + OFF_WT, lrow, 32 * half + 8 * e, 16384, x + 8 * e);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar(BAR_PREP, 128);
+      named_bar(BAR_PREP, PREP_THREADS);
       if (pt == 0) mbar_arrive(&bars[B_WTREADY]);
-    }
-  } else {
-    reg_dealloc<96>();
-    // ----------------------------------------------------------------- out
-    const int v = tid - 384;
-    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
-    for (int c = 0; has_out && c < nc; ++c) {
-      if (!wg_wait(&bars[B_ODONE], c & 1, BAR_OUT, abort_flag, p.status)) break;
-      tc_fence_after();
-      float a[32], b[32];
-      tmem_ld32(tl + TM_O, a);
-      tmem_ld32(tl + TM_O + 32, b);
-      tmem_ld_wait();
-      tc_fence_before();
-      named_bar(BAR_OUT, 128);
-      if (v == 0) mbar_arrive(&bars[B_OFREE]);
-      const int64_t c0 = bos + (int64_t)c * CHUNK;
-      const int L = chunk_len(bos, eos, c);
-      __nv_bfloat16* orow = p.out + ((size_t)c0 * H + h) * D + v;
-      const size_t st = (size_t)H * D;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < L) orow[i * st] = __float2bfloat16_rn(p.scale * a[i]);
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (32 + i < L) orow[(32 + i) * st] = __float2bfloat16_rn(p.scale * b[i]);
     }
   }
 

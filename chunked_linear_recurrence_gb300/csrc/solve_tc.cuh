@@ -156,7 +156,6 @@ __device__ void solve64_tc_inplace(float* AT, float* X, int tid, int nthr, Bar b
       }
     }
   }
-  (void)nthr;
   bar();
   if (warp < 4) {
     const int p = warp >> 1, nt = warp & 1, r0 = 32 * p;
@@ -170,21 +169,16 @@ __device__ void solve64_tc_inplace(float* AT, float* X, int tid, int nthr, Bar b
                    AT + (r0 + 16) * L + r0 + 8 * nt, 16, -1.f, lane);
   }
   bar();
-  if (warp < 4) {
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int tile = 2 * warp + s, mt = tile >> 2, nt = tile & 3;
-      warp_tile_tf32(AT + (32 + 16 * mt) * L, AT + 8 * nt, X + 16 * mt * L + 8 * nt, 32, 1.f, lane);
-    }
+  const int nw = nthr >> 5;
+  for (int tile = warp; tile < 8; tile += nw) {
+    const int mt = tile >> 2, nt = tile & 3;
+    warp_tile_tf32(AT + (32 + 16 * mt) * L, AT + 8 * nt, X + 16 * mt * L + 8 * nt, 32, 1.f, lane);
   }
   bar();
-  if (warp < 4) {
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int tile = 2 * warp + s, mt = tile >> 2, nt = tile & 3;
-      warp_tile_tf32(AT + (32 + 16 * mt) * L + 32, X + 8 * nt, AT + (32 + 16 * mt) * L + 8 * nt,
-                     32, -1.f, lane);
-    }
+  for (int tile = warp; tile < 8; tile += nw) {
+    const int mt = tile >> 2, nt = tile & 3;
+    warp_tile_tf32(AT + (32 + 16 * mt) * L + 32, X + 8 * nt, AT + (32 + 16 * mt) * L + 8 * nt, 32,
+                   -1.f, lane);
   }
   bar();
 }
