@@ -218,7 +218,8 @@ def run_ours(args):
     inp = make_inputs(w1, dev)
     out = torch.empty_like(inp["v"])
     fin = torch.empty(w1.N, w1.H, w1.V, w1.K, dtype=torch.float32, device=dev)
-    wsb = _native.workspace(256, dev)
+    wsb = _native.workspace(_native.fwd_workspace_bytes(_native.make_shape(inp["q"], inp["v"])),
+                            dev)
     stream = torch.cuda.current_stream()
 
     def fwd():
@@ -230,6 +231,7 @@ def run_ours(args):
     t0 = time.time()
     ms = time_loop(fwd, args.steps, args.warmup, ws_n, stream=stream)
     t1 = time.time()
+    _native.sf_workspace_status(wsb)     # raises if a kernel reported a timeout
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
@@ -304,7 +306,7 @@ def bench_fwd_bwd(args, W, dev, ws_n, hbm, peak_src):
     out = torch.empty_like(inp["v"])
     fin = torch.empty(w.N, w.H, w.V, w.K, dtype=torch.float32, device=dev)
     shape = _native.make_shape(inp["q"], inp["v"])
-    wsf = _native.workspace(256, dev)
+    wsf = _native.workspace(_native.fwd_workspace_bytes(shape), dev)
     wsb = _native.workspace(_native.bwd_workspace_bytes(shape), dev)
     grads = dict(dq=torch.empty_like(inp["q"]), dk=torch.empty_like(inp["k"]),
                  dv=torch.empty_like(inp["v"]), dgate=torch.empty_like(inp["gate"]),
@@ -324,6 +326,8 @@ def bench_fwd_bwd(args, W, dev, ws_n, hbm, peak_src):
     steps = max(3, min(args.steps, 10))
     ms_f = time_loop(fwd, steps, args.warmup, ws_n)
     ms_b = time_loop(bwd, steps, args.warmup, ws_n)
+    _native.sf_workspace_status(wsf)
+    _native.sf_workspace_status(wsb)
     tokens = w.B * w.T
     th = tokens * w.H
     bb = th * BWD_BYTES_PER_TH + 4 * w.N * w.H * STATE_BYTES
@@ -357,7 +361,8 @@ def bench_state_passing(args, W, dev, ws_n, hbm, peak_src):
     fin = torch.empty(w.H, w.V, w.K, dtype=torch.float32, device=dev)
     out = torch.empty_like(inp["v"])
     seg_fin = torch.empty_like(E)
-    wss = _native.workspace(256, dev)
+    wss = _native.workspace(_native.fwd_workspace_bytes(_native.make_shape(inp["q"], inp["v"])),
+                            dev)
 
     def step():
         sf.sf_gdn_segment_summary(inp["k"], inp["v"], inp["gate"], inp["beta"], bounds, P=P,
@@ -369,6 +374,7 @@ def bench_state_passing(args, W, dev, ws_n, hbm, peak_src):
 
     steps = max(3, min(args.steps, 5))
     ms = time_loop(step, steps, min(args.warmup, 3), ws_n)
+    _native.sf_workspace_status(wss)
     th = w.T * w.H
     bytes_ = (th * (SUM_BYTES_PER_TH + FWD_BYTES_PER_TH) + 4 * R * w.H * STATE_BYTES)
     return {"workload": w.name, "segments": R, "tokens_per_step": w.T,

@@ -9,6 +9,7 @@
 #include "../../include/sf_gdn.h"
 #include "api_internal.cuh"
 #include "common.cuh"
+#include "fwd_split.cuh"
 #include "fwd_tc.cuh"
 #include "scan.cuh"
 #include "simt_chunk.cuh"
@@ -96,7 +97,10 @@ const char* sf_last_error(void) { return g_last_error.c_str(); }
 const char* sf_version(void) { return "sf_gdn 0.1 sm_103a"; }
 
 size_t sf_gdn_fwd_workspace(const sf_gdn_shape* shape) {
-  (void)shape;
+  // BF16 with K = V = 128 may run on the split forward, which passes chunk records
+  // between its CTAs through a ring in the workspace.
+  if (shape && shape->dtype == SF_BF16 && shape->K == 128 && shape->V == 128)
+    return sfg::split_fwd_workspace(shape->N > 0 ? shape->N : shape->B, shape->H > 0 ? shape->H : 1);
   return kStatusBytes;
 }
 
@@ -125,7 +129,7 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
-    e = sfg::launch_tc(p, sfg::TC_MODE_FWD, reinterpret_cast<int*>(workspace), cs);
+    e = sfg::launch_split_fwd(p, workspace, cs);
   } else {
     e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
   }

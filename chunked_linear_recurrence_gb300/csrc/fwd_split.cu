@@ -1,0 +1,1167 @@
+// fwd_split.cu -- forward of the chunked gated delta rule for dense BF16 q/k/v with
+// K = V = 128 on sm_103a, split across the GPU by role.
+//
+// The per-chunk work of the chunk-parallel form (StateFlow section 2.2, Eq. 2) has
+// two parts with very different shapes:
+//   Pre  (fully parallel over chunks): the decays, [K;Q] K^T, the triangular solve
+//        T = (I + A)^{-1}, and the factors W = T diag(beta e^gamma) K,
+//        U = T diag(beta) V, Qg = diag(e^gamma) Q, Ahat = M o Gamma o Q K^T;
+//   ST + Out (serial along a chain): Delta = U - W S^T, O = Qg S^T + Ahat Delta,
+//        S <- e^{gamma_C} S + Delta^T diag(dec) K.
+// One cooperative persistent launch gives each kind its own SMs.  The first `nch`
+// CTAs are state-chain CTAs, each owning a fixed list of (sequence, head) chains and
+// walking their chunks in order; the other CTAs are preparation CTAs that turn
+// chunks into "records" (the chunk's factors as ready-made BF16 tensor-core tiles) in
+// the order the chains consume them, two chunks in flight per CTA.  Records pass
+// through a per-chain-CTA ring of NSLOT slots in global memory (small enough to stay
+// in L2); a slot's `ready` flag (release/acquire) hands it to the chain CTA, which
+// copies it into shared memory with a bulk copy and hands the slot back through its
+// `consumed` counter.  This is StateFlow's split of Pre from ST (section 3.4.2,
+// Eq. 17: the next chunk's Pre overlaps the current ST) carried across SMs: the
+// serial chain no longer waits on the preparation of its own chunks.
+//
+// Record of one chunk (BF16 tiles in the 128-byte-swizzled panel layout of tc_ptx.cuh):
+//   WQ   [128 k][128 n]: n < 64: (-W)^T, n >= 64: Qg^T      (B of the merged product)
+//   U^T  [128 v][64 i]                                      (added to -S W^T)
+//   Ahat [64 i][64 j]                                       (B of O += Delta^T Ahat^T)
+//   dec[64] = e^{gamma_C - gamma_j}, e^{gamma_C}            (FP32)
+// Chain products per chunk (all M = 128; S, Delta as BF16 A operands in TMEM):
+//   [-(S W^T) | S Qg^T] = S [(-W)^T | Qg^T]         N = 128, K = 128  (one product)
+//   Delta^T = U^T - S W^T                           (CUDA cores, while O is pending)
+//   S <- e^{gamma_C} S + (Delta^T diag(dec)) K      N = 128, K = 64
+//   O += Delta^T Ahat^T                             N = 64,  K = 64
+//   out[i][v] = scale O[v][i]
+// Preparation products per chunk: KQ = [K;Q] K^T, Qg^T = Q^T diag(e^gamma),
+// (-W)^T = K^T (-T'')^T, U^T = V^T T'^T (all N = 64), T' = T diag(beta),
+// T'' = T diag(beta e^gamma), the 64x64 solve in FP32 (solve_tc.cuh).
+//
+// Every wait (mbarrier or global flag) is bounded; a CTA that gives up raises a
+// global abort flag that every other CTA polls, writes SF_ERR_TIMEOUT to the status
+// word, lets its own copies land, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "fwd_split.cuh"
+#include "fwd_tc.cuh"
+#include "solve_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace sfg {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int NTHR = 512;
+constexpr int NSLOT = 8;          // ring slots per chain CTA
+constexpr int NBUF = 3;           // record buffers in a chain CTA's shared memory
+constexpr int MAX_NCH = 64;       // chain CTAs at most
+
+// ---- record (global ring slot, and the chain CTA's shared-memory copy) ----
+constexpr uint32_t R_WQ = 0;          // 2 panels x 16 KB
+constexpr uint32_t R_WQ_PANEL = 16384;
+constexpr uint32_t R_U = 32768;       // 16 KB
+constexpr uint32_t R_AH = 49152;      // 8 KB
+constexpr uint32_t R_VEC = 57344;     // dec[64], then e^{gamma_C} at +256
+constexpr uint32_t REC_BYTES = 57856;
+constexpr uint32_t REC_PART = REC_BYTES / 4;   // the slot is fetched in 4 bulk copies
+static_assert(REC_PART % 16 == 0, "bulk copy granularity");
+
+// ---- chain CTA shared memory: NBUF record buffers, each followed by its K tile ----
+constexpr uint32_t C_K = 58368;       // K tile [64 tok][128 k]: 2 panels x 8 KB
+constexpr uint32_t C_K_PANEL = 8192;
+constexpr uint32_t C_BUF = 74752;     // buffer stride (1024-aligned)
+constexpr uint32_t C_BAR = NBUF * C_BUF;
+static_assert(C_K >= REC_BYTES && C_K % 1024 == 0 && C_BUF % 1024 == 0, "chain smem");
+
+// ---- preparation CTA shared memory, per pipeline (two pipelines) ----
+constexpr uint32_t P_KQ = 0;          // [K;Q]: 2 panels x 16 KB (rows 0-63 K, 64-127 Q)
+constexpr uint32_t P_KQ_PANEL = 16384;
+constexpr uint32_t P_V = 32768;       // V: 2 panels x 8 KB
+constexpr uint32_t P_V_PANEL = 8192;
+constexpr uint32_t P_T1 = 49152;      // T'  [64 i][64 j]
+constexpr uint32_t P_T2 = 57344;      // -T'' [64 i][64 j]
+constexpr uint32_t P_DG = 65536;      // diag(e^gamma) [64][64]
+constexpr uint32_t P_AT = 73728;      // FP32 [64][SOLVE_LD]: A, then T
+constexpr uint32_t P_X = 91136;       // FP32 [32][SOLVE_LD]: solve scratch
+constexpr uint32_t P_VEC = 99840;     // 2 slots x 512 floats (items alternate)
+constexpr uint32_t P_VEC_SLOT = 2048;
+constexpr uint32_t P_STRIDE = 104448;
+constexpr uint32_t P_BAR = 2 * P_STRIDE;
+static_assert(P_AT + 64 * SOLVE_LD * 4 <= P_X && P_X + 32 * SOLVE_LD * 4 <= P_VEC, "prep smem");
+static_assert(P_VEC + 2 * P_VEC_SLOT <= P_STRIDE && P_STRIDE % 1024 == 0, "prep smem");
+static_assert(64 * SOLVE_LD * 4 >= 4 * 4096, "the A/T area doubles as the store staging area");
+
+constexpr uint32_t BAR_BYTES = 512;
+constexpr uint32_t GEO_BYTES = 2 * 64 * 4;   // stream lengths and their order (packed inputs)
+constexpr uint32_t SMEM_USED = (P_BAR > C_BAR ? P_BAR : C_BAR) + BAR_BYTES + GEO_BYTES;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 232448, "shared memory");
+
+// per-pipeline vectors (floats)
+constexpr int VEC_BETA = 64, VEC_GAM = 128, VEC_EG = 192, VEC_DEC = 256,
+              VEC_EP = 320, VEC_EM = 384, VEC_FLAG = 448;
+
+// ---- TMEM columns ----
+// chain: S FP32, S BF16 pairs, Delta^T BF16 pairs, Delta^T diag(dec) BF16 pairs, two
+// buffers of [ -S W^T (64) | O (64) ].
+constexpr uint32_t TM_S = 0, TM_SB = 128, TM_DB = 192, TM_DDB = 224, TM_BUF = 256;
+// preparation, per pipeline p at 256 p: KQ, Qg^T, (-W)^T, U^T
+constexpr uint32_t TP_KQ = 0, TP_QG = 64, TP_WT = 128, TP_UT = 192;
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint32_t ID_N64 = idesc_bf16(128, 64, false, false);   // both K-major
+constexpr uint32_t ID_AMN = idesc_bf16(128, 64, true, false);    // A MN-major (X^T from a tile)
+constexpr uint32_t ID_MG = idesc_bf16(128, 128, false, true);    // A@tmem, B MN-major, N = 128
+
+// ---- mbarriers ----
+enum {
+  // chain CTA
+  C_RECFULL = 0,   // [NBUF] record + K tile landed (tx)
+  C_RECFREE = 3,   // [NBUF] MMA commit after the chunk's last product reading the buffer
+  C_MERGED = 6,    // MMA: [-S W^T | S Qg^T] complete
+  C_DREADY = 7,    // state: Delta BF16 operands in TMEM (and K padding zeroed)
+  C_SUDONE = 8,    // MMA: state update complete
+  C_SREADY = 9,    // state: S BF16 operand in TMEM
+  C_SSCALED = 10,  // state: TMEM S scaled by e^{gamma_C} of the chunk
+  C_ODONE = 11,    // [2] MMA: O of a TMEM buffer complete
+  C_OFREE = 13,    // [2] out: O of a TMEM buffer read
+  C_COUNT = 15,
+  // preparation CTA
+  P_FULL = 0,      // [2] tiles + gate/beta landed (33 arrivals + tx)
+  P_HEAD = 2,      // [2] loader: decay vectors, diag(e^gamma), padding rows zeroed
+  P_KQDONE = 4,    // [2]
+  P_QGDONE = 6,    // [2]
+  P_TT = 8,        // [2] T', -T'' written
+  P_WUDONE = 10,   // [2]
+  P_ITEMFREE = 12, // [2] MMA commit after the item's last product (tiles free)
+  P_TMFREE = 14,   // [2] item finished: TMEM region read out, vector slot free
+  P_PUB = 16,      // [2] item's record written: the publisher may release it
+  P_SLOTOK = 18,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
+  P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out
+  P_VECFREE = 22,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
+  P_COUNT = 26
+};
+static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
+
+// named barriers
+constexpr int BAR_STATE = 1, BAR_OUT = 2;       // chain: 256, 128 threads
+constexpr int BAR_PREP0 = 1;                    // preparation pipeline p: BAR_PREP0 + p
+
+struct SplitParams {
+  const float* g;
+  const float* beta;
+  const float* s0;           // [N,H,V,K] or NULL
+  __nv_bfloat16* out;
+  float* final_state;        // or NULL
+  int* status;               // workspace status word
+  int* abort_g;              // global abort flag
+  uint32_t* consumed;        // [nch] records consumed (copied out) per chain CTA
+  uint32_t* ready;           // [nch][NSLOT] stream position + 1 of the record in the slot
+  uint8_t* ring;             // [nch][NSLOT][REC_BYTES]
+  const int32_t* cu;         // packed sequences: cu_seqlens [N+1], else NULL
+  int* sstart;               // packed: [N*H] first stream position of each chain in its CTA
+  int* lenj;                 // packed: [nch] stream length of each chain CTA
+  int* sortj;                // packed: [nch] chain CTAs by stream length, longest first
+  int B, T, H, N;
+  int nch, nprep;
+  float scale;
+};
+
+// About 2 s at the GB300's clocks.
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
+struct Ctx {
+  volatile int* abort_l;     // CTA-local abort flag (shared memory)
+  const SplitParams* p;
+};
+
+__device__ __forceinline__ void raise_abort(const Ctx& cx) {
+  *cx.abort_l = 1;
+  atomicExch(cx.p->abort_g, 1);
+  atomicExch(cx.p->status, 5 /* SF_ERR_TIMEOUT */);
+}
+
+__device__ __forceinline__ bool aborted(const Ctx& cx) {
+  return *cx.abort_l || ld_volatile_s32(cx.p->abort_g);
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*cx.abort_l) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+// All `nthr` threads on named barrier `id` wait; they agree on the outcome.
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int id, int nthr,
+                                           const Ctx& cx) {
+  const bool ok = named_bar_and(id, nthr, wait_bar(bar, parity, cx));
+  if (!ok && (threadIdx.x & (nthr - 1)) == 0) raise_abort(cx);
+  return ok;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctx& cx) {
+  const bool ok = __all_sync(0xffffffffu, wait_bar(bar, parity, cx)) != 0;
+  if (!ok && (threadIdx.x & 31) == 0) raise_abort(cx);
+  return ok;
+}
+
+// One thread waits until the global counter reaches `target`.
+__device__ __forceinline__ bool poll_ge(const uint32_t* f, uint32_t target, const Ctx& cx) {
+  if (ld_acquire_u32(f) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(32);
+    if (ld_acquire_u32(f) >= target) return true;
+    if (aborted(cx)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(x));
+  tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+  tmem_ld_wait();
+}
+
+// Geometry.  Chain CTA j owns the chains x = j + nch t (t = 0, 1, ...; x = n H + h) and
+// walks their chunks in order: its stream position s is chunk c of one of them.  Records
+// are produced in the order (s, j): every chain CTA's position s before any s + 1, the
+// CTAs with the longer streams first.  Dense inputs have closed forms; packed inputs use
+// the per-chain stream starts and per-CTA stream lengths built by split_setup_kernel.
+struct Geo {
+  const SplitParams* p;
+  int H, NH, nch, ncd, q, r;
+  bool packed;
+  const int* lenj;           // packed: shared-memory copy
+  const int* sortj;
+  long long full, total;
+  __device__ void init(const SplitParams& pr, const int* len_s, const int* sort_s) {
+    p = &pr;
+    H = pr.H;
+    NH = pr.N * pr.H;
+    nch = pr.nch;
+    packed = pr.cu != nullptr;
+    ncd = (pr.T + CHUNK - 1) / CHUNK;
+    q = NH / nch;
+    r = NH % nch;
+    full = (long long)q * ncd * nch;
+    lenj = len_s;
+    sortj = sort_s;
+    if (packed) {
+      total = 0;
+      for (int i = 0; i < nch; ++i) total += lenj[i];
+    } else {
+      total = (long long)NH * ncd;
+    }
+  }
+  __device__ int chains_of(int j) const { return (NH - j + nch - 1) / nch; }
+  __device__ void span(int x, int64_t& bos, int64_t& eos) const {
+    seq_span(x / H, p->B, p->T, p->cu, bos, eos);
+  }
+  __device__ int len_of(int j) const { return packed ? lenj[j] : chains_of(j) * ncd; }
+  // records at stream positions below s, over all chain CTAs
+  __device__ long long before(int s) const {
+    long long a = 0;
+    for (int i = 0; i < nch; ++i) a += min(lenj[i], s);
+    return a;
+  }
+  // w-th record in production order -> (chain CTA, stream position)
+  __device__ void item(long long w, int& j, int& s) const {
+    if (!packed) {
+      if (w < full) {
+        s = (int)(w / nch);
+        j = (int)(w % nch);
+      } else {
+        const long long w2 = w - full;
+        s = q * ncd + (int)(w2 / r);
+        j = (int)(w2 % r);
+      }
+      return;
+    }
+    int lo = 0, hi = lenj[sortj[0]];
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (before(mid) <= w) lo = mid; else hi = mid;
+    }
+    s = lo;
+    j = sortj[(int)(w - before(lo))];
+  }
+  // stream position s of chain CTA j -> chain x and its chunk c
+  __device__ void locate(int j, int s, int& x, int& c) const {
+    if (!packed) {
+      const int t = s / ncd;
+      x = j + nch * t;
+      c = s - t * ncd;
+      return;
+    }
+    int lo = 0, hi = chains_of(j);
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p->sstart[j + nch * mid] <= s) lo = mid; else hi = mid;
+    }
+    x = j + nch * lo;
+    c = s - p->sstart[x];
+  }
+};
+
+struct NamedBar {
+  int id, n;
+  __device__ __forceinline__ void operator()() const { named_bar(id, n); }
+};
+
+// --------------------------------------------------------------------------
+// State-chain CTA.  warp 0: record / K-tile loader; warp 1: MMA issuer; warps 4-11:
+// the state (two warpgroups, one column half each); warps 12-15: output stores.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitParams& p,
+                                          const Geo& geo, uint8_t* sm, uint32_t sb,
+                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = blockIdx.x, H = p.H;
+  const int cnt = geo.chains_of(j);
+  const int len = geo.len_of(j);
+  const uint8_t* ringj = p.ring + (size_t)j * NSLOT * REC_BYTES;
+  const uint32_t* readyj = p.ready + (size_t)j * NSLOT;
+
+  if (warp < 4) {
+    reg_dealloc<56>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ loader
+      if (lane == 0) {
+        // Up to NBUF copies in flight.  A ring slot is handed back (consumed) once its
+        // record has landed in shared memory: at the latest when the buffer is needed
+        // again (then the chunk that used it is done), earlier if the copy is seen landed.
+        int issued = 0, rel = 0;
+        bool ok = true;
+        auto release_to = [&](int n) {
+          fence_proxy_async_all();
+          st_release_u32(p.consumed + j, (uint32_t)n);
+          rel = n;
+        };
+        int s = 0, t = 0, c = 0, ncx = 0;
+        int64_t bos = 0, eos = 0;
+        for (; s < len; ++s, ++c) {
+          while (c >= ncx) {      // next chain with chunks
+            const int x = j + geo.nch * (t++);
+            geo.span(x, bos, eos);
+            ncx = (int)n_chunks(eos - bos);
+            c = 0;
+          }
+          const int b = s % NBUF;
+          if (s >= NBUF) {
+            if (!(ok = wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx))) break;
+            if (rel < s - NBUF + 1) release_to(s - NBUF + 1);
+          }
+          // the K tile does not depend on the record: fetch it first
+          uint8_t* buf = sm + b * C_BUF;
+          const int row0 = (int)(bos + (int64_t)c * CHUNK), h = (j + geo.nch * (t - 1)) % H;
+          mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
+          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, h, row0);
+          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, h, row0);
+          issued = s + 1;
+          if (!(ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx))) break;
+          fence_proxy_async_all();
+          const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, &bars[C_RECFULL + b]);
+          while (rel < s && mbar_test(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1))
+            release_to(rel + 1);
+        }
+        while (ok && rel < len) {
+          if (!(ok = wait_bar(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1, cx))) break;
+          release_to(rel + 1);
+        }
+        if (!ok) {
+          raise_abort(cx);
+          // let every copy still in flight land before leaving
+          for (int q = issued > NBUF ? issued - NBUF : 0; q < issued; ++q)
+            mbar_wait(&bars[C_RECFULL + q % NBUF], (q / NBUF) & 1, 100000000ull);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      // The chain's products come in a fixed order, so the issuer blocks on each
+      // condition in turn (a suspended wait leaves the issue slots to the other warps).
+      if (lane == 0) {
+        for (int s = 0; s < len; ++s) {
+          const int b = s & 1, rb = s % NBUF;
+          const uint32_t buf = sb + rb * C_BUF;
+          // [-S W^T | S Qg^T] = S [(-W)^T | Qg^T]
+          if (!wait_bar(&bars[C_SREADY], s & 1, cx) ||
+              !wait_bar(&bars[C_RECFULL + rb], (s / NBUF) & 1, cx) ||
+              (s >= 2 && !wait_bar(&bars[C_OFREE + b], ((s - 2) >> 1) & 1, cx))) {
+            raise_abort(cx);
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bw = sdesc_sw128(buf + R_WQ, R_WQ_PANEL, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ta(tm + TM_BUF + 128 * b, tm + TM_SB + kk * 8, bw + (uint64_t)(kk * 2048 >> 4),
+                        ID_MG, kk > 0 ? 1u : 0u);
+          mma_commit(&bars[C_MERGED]);
+          // S <- e^{gamma_C} S + (Delta^T diag(dec)) K, then O += Delta^T Ahat^T
+          if (!wait_bar(&bars[C_DREADY], s & 1, cx) || !wait_bar(&bars[C_SSCALED], s & 1, cx)) {
+            raise_abort(cx);
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bk = sdesc_sw128(buf + C_K, C_K_PANEL, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_MG, 1u);
+          mma_commit(&bars[C_SUDONE]);
+          const uint64_t ba = sdesc_sw128(buf + R_AH, 0, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(tm + TM_BUF + 128 * b + 64, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2),
+                        ID_N64, 1u);
+          mma_commit(&bars[C_ODONE + b]);
+          mma_commit(&bars[C_RECFREE + rb]);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp < 12) {
+    reg_alloc<168>();
+    // -------------------------------------------------------------- state
+    const int st_t = tid - 128;                       // 0..255
+    const int w = st_t >> 7;                          // column half
+    const int v = ((warp & 3) << 5) + lane;           // TMEM lane = state row
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    bool ok = true;
+    int sbase = 0;
+    for (int t = 0; t < cnt && ok; ++t) {
+      const int x = j + geo.nch * t;
+      const size_t soff = ((size_t)x * D + v) * D + 64 * w;   // states [N*H, V, K]
+      int64_t bos, eos;
+      geo.span(x, bos, eos);
+      const int nc = (int)n_chunks(eos - bos);
+      if (nc == 0) {
+        // an empty sequence passes its initial state through
+        if (p.final_state) {
+          float4* dst = reinterpret_cast<float4*>(p.final_state + soff);
+          const float4* src = reinterpret_cast<const float4*>(p.s0 + soff);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dst[e] = p.s0 ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      if (!(ok = group_wait(&bars[C_RECFULL + sbase % NBUF], (sbase / NBUF) & 1, BAR_STATE, 256,
+                            cx)))
+        break;
+      {
+        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NBUF) * C_BUF + R_VEC + 256);
+        float xv[64];
+        if (p.s0) {
+          const float4* src = reinterpret_cast<const float4*>(p.s0 + soff);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float4 f = src[e];
+            xv[4 * e] = f.x; xv[4 * e + 1] = f.y; xv[4 * e + 2] = f.z; xv[4 * e + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) xv[e] = 0.f;
+        }
+        uint32_t u[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
+          tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
+        }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) xv[e] *= g0;
+        tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
+        tmem_st32(tl + TM_S + 64 * w + 32, *reinterpret_cast<float(*)[32]>(xv + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(BAR_STATE, 256);
+        if (st_t == 0) {
+          mbar_arrive(&bars[C_SREADY]);
+          mbar_arrive(&bars[C_SSCALED]);
+        }
+      }
+      for (int c = 0; c < nc && ok; ++c) {
+        const int s = sbase + c, b = s & 1;
+        uint8_t* buf = sm + (s % NBUF) * C_BUF;
+        const int64_t rem = eos - (bos + (int64_t)c * CHUNK);
+        const int L = rem < CHUNK ? (int)rem : CHUNK;
+        if (!(ok = group_wait(&bars[C_MERGED], s & 1, BAR_STATE, 256, cx))) break;
+        tc_fence_after();
+        {
+          // Delta^T = U^T - S W^T for columns [32w, 32w + 32)
+          float a[32];
+          tmem_ld32(tl + TM_BUF + 128 * b + 32 * w, a);
+          const uint4* urow = reinterpret_cast<const uint4*>(buf + R_U + v * 128);
+          uint4 uu[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) uu[e] = urow[(4 * w + e) ^ (v & 7)];
+          const float* dec = reinterpret_cast<const float*>(buf + R_VEC) + 32 * w;
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uu[e]);
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[q2]));
+              a[8 * e + 2 * q2] += f.x;
+              a[8 * e + 2 * q2 + 1] += f.y;
+            }
+          }
+          uint32_t d1[16], d2[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            d1[e] = pack_bf16x2(a[2 * e], a[2 * e + 1]);
+            d2[e] = pack_bf16x2(a[2 * e] * dec[2 * e], a[2 * e + 1] * dec[2 * e + 1]);
+          }
+          tmem_st16(tl + TM_DB + 16 * w, d1);
+          tmem_st16(tl + TM_DDB + 16 * w, d2);
+        }
+        if (L < CHUNK) {
+          // K rows past the sequence end: zero, so they add nothing to the state update
+          const int rows = CHUNK - L;
+          for (int idx = st_t; idx < 2 * rows * 8; idx += 256) {
+            const int pnl = idx / (rows * 8), rem = idx % (rows * 8);
+            *reinterpret_cast<uint4*>(buf + C_K + pnl * C_K_PANEL + (L + rem / 8) * 128 +
+                                      (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(BAR_STATE, 256);
+        if (st_t == 0) mbar_arrive(&bars[C_DREADY]);
+        if (!(ok = group_wait(&bars[C_SUDONE], s & 1, BAR_STATE, 256, cx))) break;
+        tc_fence_after();
+        float xv[64];
+        tmem_ld64(tl + TM_S + 64 * w, xv);
+        if (c + 1 == nc) {
+          if (p.final_state) {
+            float4* dst = reinterpret_cast<float4*>(p.final_state + soff);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
+          }
+        } else {
+          uint32_t u[16];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
+            tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          named_bar(BAR_STATE, 256);
+          if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
+          const int s1 = s + 1;
+          if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))
+            break;
+          const float gn = *reinterpret_cast<const float*>(sm + (s1 % NBUF) * C_BUF + R_VEC + 256);
+#pragma unroll
+          for (int e = 0; e < 64; ++e) xv[e] *= gn;
+          tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
+          tmem_st32(tl + TM_S + 64 * w + 32, *reinterpret_cast<float(*)[32]>(xv + 32));
+          tmem_st_wait();
+          tc_fence_before();
+          named_bar(BAR_STATE, 256);
+          if (st_t == 0) mbar_arrive(&bars[C_SSCALED]);
+        }
+      }
+      sbase += nc;
+    }
+  } else {
+    reg_dealloc<120>();
+    // -------------------------------------------------------------- output
+    const int v = ((warp & 3) << 5) + lane;
+    const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
+    const size_t rs = (size_t)H * D;
+    bool ok = true;
+    int s = 0;
+    for (int t = 0; t < cnt && ok; ++t) {
+      const int x = j + geo.nch * t, h = x % H;
+      int64_t bos, eos;
+      geo.span(x, bos, eos);
+      const int nc = (int)n_chunks(eos - bos);
+      for (int c = 0; c < nc; ++c, ++s) {
+        const int b = s & 1;
+        if (!(ok = group_wait(&bars[C_ODONE + b], (s >> 1) & 1, BAR_OUT, 128, cx))) break;
+        tc_fence_after();
+        float o[64];
+        tmem_ld64(tl + TM_BUF + 128 * b + 64, o);
+        tc_fence_before();
+        named_bar(BAR_OUT, 128);
+        if (v == 0) mbar_arrive(&bars[C_OFREE + b]);
+        const int64_t row0 = bos + (int64_t)c * CHUNK;
+        const int L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
+        __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i < L) orow[i * rs] = __float2bfloat16_rn(p.scale * o[i]);
+      }
+    }
+  }
+}
+
+// One warp stores 32 consecutive rows (row0 % 32 == 0, this lane's row = row0 + lane) of a
+// panel-layout BF16 tile into global memory with full-line writes: each lane parks its
+// 128-byte line in the warp's 4 KB of shared memory (already in the tile's swizzled
+// order), then every store instruction writes four whole lines.
+__device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* stage, int row0,
+                                           const uint32_t (&u)[32], int lane) {
+  uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    mine[e ^ (lane & 7)] = make_uint4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int ln = 4 * it + (lane >> 3);
+    const uint4 v = reinterpret_cast<const uint4*>(stage + ln * 128)[lane & 7];
+    reinterpret_cast<uint4*>(gtile + (size_t)(row0 + ln) * 128)[lane & 7] = v;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void pack64(const float (&x)[64], uint32_t (&u)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+}
+
+// --------------------------------------------------------------------------
+// Preparation CTA.  warp 0: loader (gate/beta and the chunk's decay vectors, then the
+// K/Q/V tiles by TMA); warp 1: MMA issuer; warps 2 and 3: publishers of pipelines 0
+// and 1 (ring-slot check, then the release of a finished record); warps 4-7 and 8-11:
+// two pipelines, each preparing every other item of this CTA; warps 12-15 idle.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                         const CUtensorMap* tmV, const SplitParams& p,
+                                         const Geo& geo, uint8_t* sm, uint32_t sb,
+                                         uint64_t* bars, uint32_t tm, const Ctx& cx) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pc = blockIdx.x - p.nch, H = p.H;
+  const int nk = (pc < geo.total) ? (int)((geo.total - pc + p.nprep - 1) / p.nprep) : 0;
+  // item k of this CTA -> (chain CTA, stream position, head, first row, length)
+  auto item = [&](int k, int& jj, int& s, int& h, int& row0, int& L) {
+    geo.item(pc + (long long)k * p.nprep, jj, s);
+    int x, c;
+    geo.locate(jj, s, x, c);
+    int64_t bos, eos;
+    geo.span(x, bos, eos);
+    h = x % H;
+    row0 = (int)(bos + (int64_t)c * CHUNK);
+    L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
+  };
+  auto vec_of = [&](int pp, int use) {
+    return reinterpret_cast<float*>(sm + pp * P_STRIDE + P_VEC + (use & 1) * P_VEC_SLOT);
+  };
+
+  if (warp < 4) {
+    reg_dealloc<56>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ loader
+      for (int idx = lane; idx < 2 * 512; idx += 32)
+        reinterpret_cast<uint4*>(sm + (idx >> 9) * P_STRIDE + P_DG)[idx & 511] = make_uint4(0, 0, 0, 0);
+      int last[2] = {-1, -1};
+      for (int k = 0; k < nk; ++k) {
+        const int pp = k & 1, use = k >> 1;
+        int jj, s, h, row0, L;
+        item(k, jj, s, h, row0, L);
+        (void)jj;
+        (void)s;
+        // the vector slot is free once the item two uses back has finished (one barrier
+        // per slot, so a phase can never be mistaken for the one two items later)
+        if (use >= 2 && !warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx))
+          break;
+        float* vs = vec_of(pp, use);
+        {
+          // gamma = in-chunk cumulative gate; decays e^{gamma}, e^{gamma_C - gamma}, and
+          // the factors e^{+-(gamma - mid)} (used when the chunk's gamma range is <= 80)
+          const int e0 = 2 * lane, e1 = e0 + 1;
+          const size_t o0 = (size_t)(row0 + e0) * H + h, o1 = (size_t)(row0 + e1) * H + h;
+          const float g0 = e0 < L ? p.g[o0] : 0.f, g1 = e1 < L ? p.g[o1] : 0.f;
+          const float b0 = e0 < L ? p.beta[o0] : 0.f, b1 = e1 < L ? p.beta[o1] : 0.f;
+          float sum = g0 + g1;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, sum, o);
+            if (lane >= o) sum += t;
+          }
+          const float excl = sum - (g0 + g1);
+          const float a0 = excl + g0, a1 = excl + g0 + g1;
+          float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          }
+          const bool fact = (mx - mn) <= 80.f;
+          const float mid = 0.5f * (mx + mn);
+          const float gC = __shfl_sync(0xffffffffu, a1, 31);
+          vs[VEC_BETA + e0] = b0;
+          vs[VEC_BETA + e1] = b1;
+          vs[VEC_GAM + e0] = a0;
+          vs[VEC_GAM + e1] = a1;
+          vs[VEC_EG + e0] = expf(a0);
+          vs[VEC_EG + e1] = expf(a1);
+          vs[VEC_DEC + e0] = expf(gC - a0);
+          vs[VEC_DEC + e1] = expf(gC - a1);
+          vs[VEC_EP + e0] = fact ? expf(a0 - mid) : 0.f;
+          vs[VEC_EP + e1] = fact ? expf(a1 - mid) : 0.f;
+          vs[VEC_EM + e0] = fact ? expf(mid - a0) : 0.f;
+          vs[VEC_EM + e1] = fact ? expf(mid - a1) : 0.f;
+          if (lane == 0) {
+            vs[VEC_FLAG] = fact ? 1.f : 0.f;
+            vs[VEC_FLAG + 1] = mid;
+          }
+        }
+        __syncwarp();
+        if (use >= 1 && !warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx)) break;
+        uint8_t* base = sm + pp * P_STRIDE;
+        // diag(e^gamma), the B operand of Qg^T (the previous item's products are complete)
+        for (int e = lane; e < 64; e += 32)
+          *reinterpret_cast<__nv_bfloat16*>(base + P_DG + sw128_off(e, e, 8192)) =
+              __float2bfloat16_rn(vs[VEC_EG + e]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[P_FULL + pp], 3 * 16384);
+#pragma unroll
+          for (int pnl = 0; pnl < 2; ++pnl) {
+            tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
+            tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + 8192, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
+                        row0);
+            tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULL + pp], 64 * pnl, h, row0);
+          }
+        }
+        mbar_arrive(&bars[P_FULL + pp]);
+        last[pp] = k;
+        if (L < CHUNK) {
+          // rows past the sequence end: zero K, Q and V so they add nothing to any product
+          if (!warp_wait(&bars[P_FULL + pp], use & 1, cx)) break;
+          const int rows = CHUNK - L;
+          for (int idx = lane; idx < 6 * rows * 8; idx += 32) {
+            const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
+            const int row = L + rem / 8, ch = rem % 8, pnl = t6 & 1, which = t6 >> 1;
+            uint8_t* tb = (which == 2) ? base + P_V + pnl * P_V_PANEL
+                                       : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? 8192u : 0u);
+            *reinterpret_cast<uint4*>(tb + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[P_HEAD + pp]);
+      }
+      // never leave with a tile copy in flight
+      for (int pp = 0; pp < 2; ++pp)
+        if (last[pp] >= 0) mbar_wait(&bars[P_FULL + pp], (last[pp] >> 1) & 1, 100000000ull);
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && nk > 0) {
+        int nK = 0, nQ = 0, nW = 0;
+        long long t_prog = clock64();
+        while (nW < nk) {
+          bool prog = false;
+          if (nW < nK && mbar_test(&bars[P_TT + (nW & 1)], (nW >> 1) & 1)) {
+            tc_fence_after();
+            const int pp = nW & 1;
+            const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+            // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
+            const uint64_t ak = sdesc_sw128(base + P_KQ, P_KQ_PANEL, 1024);
+            const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_AMN,
+                       kk > 0 ? 1u : 0u);
+            const uint64_t av = sdesc_sw128(base + P_V, P_V_PANEL, 1024);
+            const uint64_t b1 = sdesc_sw128(base + P_T1, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tp + TP_UT, av + (uint64_t)(kk * 2048 >> 4), b1 + (uint64_t)(kk * 2), ID_AMN,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(&bars[P_WUDONE + pp]);
+            mma_commit(&bars[P_ITEMFREE + pp]);
+            ++nW;
+            prog = true;
+          }
+          // KQ of item nK needs only the KQ accumulator of item nK - 2 read out; its Qg^T
+          // (issued next) needs that item finished
+          if (nQ < nK && mbar_test(&bars[P_TMFREE + (nQ & 1)], ((nQ >> 1) - 1) & 1)) {
+            tc_fence_after();
+            const int pp = nQ & 1;
+            const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+            // Qg^T = Q^T diag(e^gamma)
+            const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
+            const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2), ID_AMN,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(&bars[P_QGDONE + pp]);
+            ++nQ;
+            prog = true;
+          }
+          if (nK < nk && nK < nW + 2 && nQ == nK) {
+            const int pp = nK & 1, use = nK >> 1;
+            if (mbar_test(&bars[P_HEAD + pp], use & 1) && mbar_test(&bars[P_FULL + pp], use & 1) &&
+                (use == 0 || mbar_test(&bars[P_KQFREE + pp], (use - 1) & 1))) {
+              tc_fence_after();
+              const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+              // KQ = [K; Q] K^T
+              const uint64_t bq = sdesc_sw128(base + P_KQ, 0, 1024);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t d = bq + (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
+                mma_bf16(tp + TP_KQ, d, d, ID_N64, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&bars[P_KQDONE + pp]);
+              ++nK;
+              prog = true;
+              if (use == 0) {
+                // the pipeline's first item: nothing to wait for
+                const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
+                const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2),
+                           ID_AMN, kk > 0 ? 1u : 0u);
+                mma_commit(&bars[P_QGDONE + pp]);
+                ++nQ;
+              }
+            }
+          }
+          if (prog) {
+            t_prog = clock64();
+          } else if (aborted(cx) || clock64() - t_prog > kWaitLimitCycles) {
+            raise_abort(cx);
+            break;
+          } else {
+            __nanosleep(64);   // leave the issue slots to the pipelines meanwhile
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ publishers
+      const int pp = warp - 2;
+      if (lane == 0) {
+        for (int k = pp; k < nk; k += 2) {
+          const int use = k >> 1;
+          int jj, s, h, row0, L;
+          item(k, jj, s, h, row0, L);
+          // the record's ring slot must have been copied out by its chain CTA
+          if (s >= NSLOT && !poll_ge(p.consumed + jj, (uint32_t)(s - NSLOT + 1), cx)) {
+            raise_abort(cx);
+            break;
+          }
+          mbar_arrive(&bars[P_SLOTOK + pp]);
+          if (!wait_bar(&bars[P_PUB + pp], use & 1, cx)) {
+            raise_abort(cx);
+            break;
+          }
+          st_release_u32(p.ready + (size_t)jj * NSLOT + s % NSLOT, (uint32_t)s + 1);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp < 12) {
+    reg_alloc<216>();
+    // ---------------------------------------------------------- pipelines
+    const int pp = (warp - 4) >> 2;
+    const int r = ((warp & 3) << 5) + lane;          // TMEM lane
+    const int bid = BAR_PREP0 + pp;
+    const uint32_t tl = tm + 256 * pp + ((uint32_t)((warp & 3) * 32) << 16);
+    uint8_t* base = sm + pp * P_STRIDE;
+    float* AT = reinterpret_cast<float*>(base + P_AT);
+    float* X = reinterpret_cast<float*>(base + P_X);
+    // the A/T area, once T' and T'' are built, is this warp's store staging (4 KB)
+    uint8_t* stage = base + P_AT + (warp & 3) * 4096;
+    bool ok = true;
+    for (int k = pp; k < nk && ok; k += 2) {
+      const int use = k >> 1;
+      int jj, s, h, row0, L;
+      item(k, jj, s, h, row0, L);
+      (void)h;
+      (void)row0;
+      (void)L;
+      const float* vs = vec_of(pp, use);
+      // the loader's vectors for this item (HEAD) and the chunk's [K;Q] K^T
+      if (!(ok = group_wait(&bars[P_HEAD + pp], use & 1, bid, 128, cx))) break;
+      if (!(ok = group_wait(&bars[P_KQDONE + pp], use & 1, bid, 128, cx))) break;
+      tc_fence_after();
+      uint32_t ah[32];     // rows 64-127: this row of Ahat (BF16 pairs), stored at the end
+      {
+        const bool fact = vs[VEC_FLAG] != 0.f;
+        const int i = r & 63;
+        const float gi = vs[VEC_GAM + i], epi = vs[VEC_EP + i];
+        const float bi = (r < 64) ? vs[VEC_BETA + i] : 1.f;
+        float x[64];
+        tmem_ld64(tl + TP_KQ, x);
+        if (fact) {
+          const float f = bi * epi;
+          const float4* em4 = reinterpret_cast<const float4*>(vs + VEC_EM);
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 e4 = em4[j4];
+            x[4 * j4] *= f * e4.x;
+            x[4 * j4 + 1] *= f * e4.y;
+            x[4 * j4 + 2] *= f * e4.z;
+            x[4 * j4 + 3] *= f * e4.w;
+          }
+        } else {
+#pragma unroll
+          for (int jx = 0; jx < 64; ++jx) x[jx] *= bi * expf(jx <= i ? gi - vs[VEC_GAM + jx] : 0.f);
+        }
+        if (r < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+          float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD);
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const int jx = 4 * j4;
+            row[j4] = make_float4(jx < i ? x[jx] : 0.f, jx + 1 < i ? x[jx + 1] : 0.f,
+                                  jx + 2 < i ? x[jx + 2] : 0.f, jx + 3 < i ? x[jx + 3] : 0.f);
+          }
+        } else {               // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
+#pragma unroll
+          for (int jx = 0; jx < 64; ++jx)
+            if (jx > i) x[jx] = 0.f;
+          pack64(x, ah);
+        }
+      }
+      tc_fence_before();
+      named_bar(bid, 128);
+      if (r == 0) mbar_arrive(&bars[P_KQFREE + pp]);
+      // T = (I + A)^{-1}; T' = T diag(beta), -T'' = -T diag(beta e^gamma)
+      solve64_tc_inplace(AT, X, r, 128, NamedBar{bid, 128});
+      for (int idx = r; idx < 64 * 8; idx += 128) {
+        const int i = idx >> 3, cg = (idx & 7) * 8;
+        const float4* tr = reinterpret_cast<const float4*>(AT + i * SOLVE_LD + cg);
+        const float4* b4 = reinterpret_cast<const float4*>(vs + VEC_BETA + cg);
+        const float4* g4 = reinterpret_cast<const float4*>(vs + VEC_EG + cg);
+        float t1[8], t2[8];
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4) {
+          const float4 tv = tr[h4], bv = b4[h4], gv = g4[h4];
+          t1[4 * h4] = tv.x * bv.x; t1[4 * h4 + 1] = tv.y * bv.y;
+          t1[4 * h4 + 2] = tv.z * bv.z; t1[4 * h4 + 3] = tv.w * bv.w;
+          t2[4 * h4] = -t1[4 * h4] * gv.x; t2[4 * h4 + 1] = -t1[4 * h4 + 1] * gv.y;
+          t2[4 * h4 + 2] = -t1[4 * h4 + 2] * gv.z; t2[4 * h4 + 3] = -t1[4 * h4 + 3] * gv.w;
+        }
+        st_row8_bf16(base + P_T1, i, cg, 8192, t1);
+        st_row8_bf16(base + P_T2, i, cg, 8192, t2);
+      }
+      fence_proxy_async_smem();
+      named_bar(bid, 128);
+      if (r == 0) mbar_arrive(&bars[P_TT + pp]);
+      // the record goes to ring slot s % NSLOT once the publisher has seen it free
+      if (!(ok = group_wait(&bars[P_SLOTOK + pp], use & 1, bid, 128, cx))) break;
+      uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
+      if (r >= 64) store_rows(rec + R_AH, stage, (warp & 3) * 32 - 64, ah, lane);
+      if (!(ok = group_wait(&bars[P_QGDONE + pp], use & 1, bid, 128, cx))) break;
+      tc_fence_after();
+      {
+        float x[64];
+        uint32_t u[32];
+        tmem_ld64(tl + TP_QG, x);
+        pack64(x, u);
+        store_rows(rec + R_WQ + R_WQ_PANEL, stage, (warp & 3) * 32, u, lane);
+      }
+      if (!(ok = group_wait(&bars[P_WUDONE + pp], use & 1, bid, 128, cx))) break;
+      tc_fence_after();
+      {
+        float x[64];
+        uint32_t u[32];
+        tmem_ld64(tl + TP_WT, x);
+        pack64(x, u);
+        store_rows(rec + R_WQ, stage, (warp & 3) * 32, u, lane);
+        tmem_ld64(tl + TP_UT, x);
+        pack64(x, u);
+        store_rows(rec + R_U, stage, (warp & 3) * 32, u, lane);
+      }
+      if (r < 64) reinterpret_cast<float*>(rec + R_VEC)[r] = vs[VEC_DEC + r];
+      if (r == 0) reinterpret_cast<float*>(rec + R_VEC)[64] = vs[VEC_EG + 63];
+      tc_fence_before();
+      named_bar(bid, 128);
+      if (r == 0) {
+        mbar_arrive(&bars[P_PUB + pp]);
+        mbar_arrive(&bars[P_TMFREE + pp]);
+        mbar_arrive(&bars[P_VECFREE + 2 * pp + (use & 1)]);
+      }
+    }
+  } else {
+    reg_dealloc<24>();
+  }
+}
+
+__global__ void __launch_bounds__(NTHR, 1)
+    gdn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  const bool is_chain = (int)blockIdx.x < p.nch;
+  uint8_t* bar_area = sm + (is_chain ? C_BAR : P_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 256);
+  volatile int* abort_l = reinterpret_cast<volatile int*>(bar_area + 264);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  int* len_s = reinterpret_cast<int*>(bar_area + BAR_BYTES);
+  int* sort_s = len_s + 64;
+  if (p.cu && tid < p.nch) {
+    len_s[tid] = p.lenj[tid];
+    sort_s[tid] = p.sortj[tid];
+  }
+  Geo geo;
+  const Ctx cx{abort_l, &p};
+
+  if (tid == 0) {
+    if (is_chain) {
+      for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
+    } else {
+      for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
+      mbar_init(&bars[P_FULL], 33);
+      mbar_init(&bars[P_FULL + 1], 33);
+    }
+    *abort_l = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmK);
+    if (!is_chain) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmV);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_slot;
+  geo.init(p, len_s, sort_s);
+
+  if (is_chain)
+    chain_cta(&tmK, p, geo, sm, sb, bars, tm, cx);
+  else
+    prep_cta(&tmQ, &tmK, &tmV, p, geo, sm, sb, bars, tm, cx);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tm, TM_COLS);
+  }
+}
+
+// Packed inputs: each chain's first stream position in its chain CTA, each chain CTA's
+// stream length, and the chain CTAs ordered by stream length (longest first).  One CTA.
+__global__ void split_setup_kernel(const SplitParams p) {
+  __shared__ int len_s[MAX_NCH];
+  const int NH = p.N * p.H, nch = p.nch, tid = threadIdx.x;
+  for (int x = tid; x < NH; x += blockDim.x) {
+    int64_t b, e;
+    seq_span(x / p.H, p.B, p.T, p.cu, b, e);
+    p.sstart[x] = (int)n_chunks(e - b);
+  }
+  __syncthreads();
+  if (tid < nch) {
+    int acc = 0;
+    for (int x = tid; x < NH; x += nch) {
+      const int n = p.sstart[x];
+      p.sstart[x] = acc;
+      acc += n;
+    }
+    len_s[tid] = acc;
+    p.lenj[tid] = acc;
+  }
+  __syncthreads();
+  if (tid < nch) {
+    int r = 0;
+    for (int i = 0; i < nch; ++i)
+      r += (len_s[i] > len_s[tid]) || (len_s[i] == len_s[tid] && i < tid);
+    p.sortj[r] = tid;
+  }
+}
+
+// Workspace: [0, 256) status word; [256, 260) abort flag; [512, 768) consumed[MAX_NCH];
+// ready[MAX_NCH][NSLOT] from 768; the ring from 4096; then (packed inputs) the chain
+// stream starts [N*H], stream lengths [64] and their order [64].
+constexpr size_t WS_ABORT = 256, WS_CONSUMED = 512, WS_READY = 768;
+constexpr size_t WS_FLAGS_END = WS_READY + (size_t)MAX_NCH * NSLOT * 4;
+constexpr size_t WS_RING = 4096;
+static_assert(WS_FLAGS_END <= WS_RING, "workspace flags");
+
+}  // namespace
+
+constexpr size_t WS_GEO = WS_RING + (size_t)MAX_NCH * NSLOT * REC_BYTES;
+
+size_t split_fwd_workspace(int N, int H) {
+  return WS_GEO + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
+}
+
+cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, cudaStream_t st) {
+  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1)) return cudaErrorInvalidValue;
+  int dev = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int NH = cp.N * cp.H;
+  const int nch = NH < MAX_NCH ? NH : MAX_NCH;
+  const int nprep = nsm - nch;
+  if (nprep < 1) return cudaErrorInvalidConfiguration;
+  const int rows = cp.B * cp.T;
+  CUtensorMap mq, mk, mv;
+  if (!make_bf16_map(&mq, cp.q, rows, cp.H) || !make_bf16_map(&mk, cp.k, rows, cp.H) ||
+      !make_bf16_map(&mv, cp.v, rows, cp.H))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(gdn_fwd_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  char* w = reinterpret_cast<char*>(ws);
+  e = cudaMemsetAsync(w + WS_ABORT, 0, WS_FLAGS_END - WS_ABORT, st);
+  if (e != cudaSuccess) return e;
+  SplitParams p{};
+  p.g = cp.g;
+  p.beta = cp.beta;
+  p.s0 = cp.s0;
+  p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
+  p.final_state = cp.final_state;
+  p.status = reinterpret_cast<int*>(w);
+  p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
+  p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
+  p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
+  p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
+  p.cu = cp.cu;
+  p.sstart = reinterpret_cast<int*>(w + WS_GEO);
+  p.lenj = p.sstart + (size_t)NH;
+  p.sortj = p.lenj + MAX_NCH;
+  p.B = cp.B;
+  p.T = cp.T;
+  p.H = cp.H;
+  p.N = cp.N;
+  p.nch = nch;
+  p.nprep = nprep;
+  p.scale = cp.scale;
+  if (p.cu) {
+    split_setup_kernel<<<1, 256, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  void* args[] = {&mq, &mk, &mv, &p};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
+                                     dim3(nch + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
+}
+
+}  // namespace sfg

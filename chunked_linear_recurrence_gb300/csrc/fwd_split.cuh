@@ -1,0 +1,17 @@
+// fwd_split.cuh -- launcher of the split forward (preparation CTAs feeding state-chain CTAs
+// through an L2-resident ring) for dense BF16 q/k/v with K = V = 128.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "simt_chunk.cuh"
+
+namespace sfg {
+
+// Workspace bytes the split forward needs for N sequences of H heads (status word included).
+size_t split_fwd_workspace(int N, int H);
+// Dense (p.cu == NULL) or packed (p.cu != NULL, p.B == 1) inputs, p.T > 0.  ws: workspace
+// of split_fwd_workspace(p.N, p.H) bytes; its first int is the status word.
+cudaError_t launch_split_fwd(const ChainParams& p, void* ws, cudaStream_t st);
+
+}  // namespace sfg

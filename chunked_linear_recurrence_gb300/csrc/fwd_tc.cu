@@ -800,6 +800,10 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int H) {
 
 bool tc_fwd_available() { return encode_fn() != nullptr; }
 
+bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int H) {
+  return make_map(m, base, rows, H);
+}
+
 cudaError_t launch_tc(const ChainParams& cp, int mode, int* status, cudaStream_t st) {
   const int rows = cp.B * cp.T;
   if (rows <= 0) return cudaErrorInvalidValue;

@@ -16,10 +16,16 @@ def _lib():
 
 
 def run_fwd(inp, **kw):
+    """Forward through the C ABI; also checks that no kernel reported a timeout."""
     sf = _lib()
-    return sf.sf_gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["gate"], inp["beta"],
-                               inp.get("initial_state"), cu_seqlens=inp.get("cu_seqlens"),
-                               output_final_state=True, **kw)
+    from chunked_linear_recurrence_gb300 import _native
+    shape = _native.make_shape(inp["q"], inp["v"], inp.get("cu_seqlens"))
+    ws = _native.workspace(_native.fwd_workspace_bytes(shape), inp["q"].device)
+    res = sf.sf_gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["gate"], inp["beta"],
+                              inp.get("initial_state"), cu_seqlens=inp.get("cu_seqlens"),
+                              output_final_state=True, ws=ws, **kw)
+    _native.sf_workspace_status(ws)
+    return res
 
 
 def check_fwd(inp, tol=None):
