@@ -361,7 +361,8 @@ def bench_state_passing(args, W, dev, ws_n, hbm, peak_src):
     fin = torch.empty(w.H, w.V, w.K, dtype=torch.float32, device=dev)
     out = torch.empty_like(inp["v"])
     seg_fin = torch.empty_like(E)
-    wss = _native.workspace(_native.fwd_workspace_bytes(_native.make_shape(inp["q"], inp["v"])),
+    wss = _native.workspace(max(_native.fwd_workspace_bytes(_native.make_shape(inp["q"], inp["v"], cu)),
+                                _native.summary_workspace_bytes(_native.make_shape(inp["k"], inp["v"]), R)),
                             dev)
 
     def step():

@@ -249,6 +249,10 @@ def fwd_workspace_bytes(shape: sf_gdn_shape) -> int:
     return int(load().sf_gdn_fwd_workspace(ctypes.byref(shape)))
 
 
+def summary_workspace_bytes(shape: sf_gdn_shape, R: int) -> int:
+    return int(load().sf_gdn_summary_workspace(ctypes.byref(shape), int(R)))
+
+
 def bwd_workspace_bytes(shape: sf_gdn_shape) -> int:
     return int(load().sf_gdn_bwd_workspace(ctypes.byref(shape)))
 

@@ -1,0 +1,471 @@
+// bwd_grad_mma.cu -- token gradients of one chunk of the chunked gated delta rule on the
+// warp-level tensor cores (mma.sync m16n8k8, TF32 operands, FP32 accumulation).
+//
+// StateFlow section 3.4.2, Eq. 18 ("OutputGrad" and "PrepGrad"): given the chunk's entry
+// state S (state replay) and the cotangent dSn of its exit state (reverse state chain),
+// the chunk's factors are recomputed and the gradient is pushed back through Out, ST and
+// Pre -- the chunk algebra of common.cuh differentiated term by term:
+//
+//   Ak = Gamma o K K^T (strict), Aqk = Gamma o Q K^T (incl. diagonal), A = diag(beta) Ak
+//   T = (I + A)^-1, W = T diag(beta e^gamma) K, U = T diag(beta) V, Delta = U - W S^T
+//   dDelta = scale Aqk^T dO + diag(dec) K dSn^T
+//   dAqk = scale dO Delta^T -> G = dAqk o Gamma,   dq = scale diag(e^gamma) dO S + G K
+//   dk  = G^T Q + diag(dec) (Delta dSn) + diag(beta e^gamma) T^T dW + dKK K + dKK^T K
+//   dW  = -dDelta S,   dv = diag(beta) T^T dDelta,   dT = dDelta (beta V)^T + dW (beta e^gamma K)^T
+//   dA  = -(T^T dT T^T) strictly lower,  dKK = dA o (beta Gamma)
+//   dgate = reverse cumulative sum of dgamma (collected from every decay factor), dbeta.
+//
+// Every product is a set of 16x8 output tiles per warp; a warp owns the same tiles of
+// every 64 x D product, so dq and dk accumulate in its registers across products.  The
+// shared-memory tiles and the order of the steps are those of simt_bwd_grad_kernel.
+#include "common.cuh"
+#include "simt_chunk.cuh"
+#include "solve_tc.cuh"
+
+namespace sfg {
+namespace {
+
+constexpr int NTG = 256;   // 8 warps
+
+// Element (r, c) views of the operands.
+template <typename T>
+struct View {
+  const T* p;
+  int sr, sc;
+  __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[r * sr + c * sc]); }
+};
+template <typename T>
+__device__ __forceinline__ View<T> view(const T* p, int sr, int sc) { return View<T>{p, sr, sc}; }
+// rows scaled by s[r]
+template <typename V>
+struct RowScaled {
+  V v;
+  const float* s;
+  __device__ __forceinline__ float operator()(int r, int c) const { return s[r] * v(r, c); }
+};
+// columns scaled by s[c]
+template <typename V>
+struct ColScaled {
+  V v;
+  const float* s;
+  __device__ __forceinline__ float operator()(int r, int c) const { return s[c] * v(r, c); }
+};
+template <typename V>
+__device__ __forceinline__ RowScaled<V> rows_scaled(V v, const float* s) { return RowScaled<V>{v, s}; }
+template <typename V>
+__device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { return ColScaled<V>{v, s}; }
+
+// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + 8 ti
+// of an output with NTN 8-column tiles per 16-row band.
+template <int NTILE, int NTN, typename AV, typename BV>
+__device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
+                                     int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll 4
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      const uint32_t a[4] = {f2tf32(A(m0 + g, k0 + t)), f2tf32(A(m0 + g + 8, k0 + t)),
+                             f2tf32(A(m0 + g, k0 + t + 4)), f2tf32(A(m0 + g + 8, k0 + t + 4))};
+      const uint32_t b[2] = {f2tf32(B(k0 + t, n0 + g)), f2tf32(B(k0 + t + 4, n0 + g))};
+      mma_tf32_16x8x8(acc[ti], a, b);
+    }
+  }
+}
+
+template <int NTILE>
+__device__ __forceinline__ void zero(float (&acc)[NTILE][4]) {
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[ti][e] = 0.f;
+}
+
+// Calls f(row, col, value&) for every element this warp holds.
+template <int NTILE, int NTN, typename F>
+__device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane, F&& f) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f(m0 + g + 8 * (e >> 1), n0 + 2 * t + (e & 1), acc[ti][e]);
+  }
+}
+
+// vec[row] += sum over this warp's columns of w(row, col) acc(row, col) (4-lane reduction,
+// then one shared-memory atomic per row segment).
+template <int NTILE, int NTN, typename W>
+__device__ __forceinline__ void row_dot(const float (&acc)[NTILE][4], const W& w, float* vec,
+                                        int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = m0 + g + 8 * hr, c = n0 + 2 * t;
+      float s = acc[ti][2 * hr] * w(r, c) + acc[ti][2 * hr + 1] * w(r, c + 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (t == 0) atomicAdd(&vec[r], s);
+    }
+  }
+}
+
+struct CtaBarG {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+}  // namespace
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) {
+  constexpr int LDI = D + 8;      // input tiles (Tin)
+  constexpr int LDF = D + 1;      // fp32 [64][D] tiles
+  constexpr int LD6 = 65;
+  constexpr int NTD = D / 8;      // 8-column tiles of a 64 x D output
+  constexpr int TD = 4 * NTD / 8; // tiles per warp of a 64 x D output
+  extern __shared__ float sm[];
+  float* sT = sm;
+  float* sM = sT + 64 * LD6;      // Ak (Gamma o K K^T, strict)
+  float* sP = sM + 64 * LD6;      // Aqk -> G -> dT -> dKK
+  float* B1 = sP + 64 * LD6;      // W -> dW -> X1
+  float* B2 = B1 + 64 * LDF;      // U -> Delta -> T^T dDelta -> dA
+  float* B3 = B2 + 64 * LDF;      // solve input, then dDelta
+  float* sg = B3 + 64 * LDF;
+  float* sb = sg + 64;
+  float* sgam = sb + 64;
+  float* seg = sgam + 64;
+  float* sdec = seg + 64;
+  float* sdgam = sdec + 64;
+  float* sred = sdgam + 64;       // dbeta accumulator
+  float* sz = sred + 64;          // per-row sums of K o (Delta dSn)
+  float* sbeg = sz + 64;          // beta e^gamma
+  float* ssc = sbeg + 64;         // scale e^gamma
+  Tin* sQ = reinterpret_cast<Tin*>(ssc + 64);
+  Tin* sK = sQ + 64 * LDI;
+  Tin* sV = sK + 64 * LDI;
+  Tin* sdO = sV + 64 * LDI;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
+  const int64_t slot = blockIdx.x;
+  int n = -1;
+  int64_t bos = 0, eos = 0, ci = 0;
+  if (!p.cu) {
+    const int64_t nc = n_chunks(p.T);
+    n = (int)(slot / nc);
+    ci = slot % nc;
+    if (n >= p.N) return;
+    seq_span(n, p.B, p.T, nullptr, bos, eos);
+  } else {
+    int64_t s = 0;
+    for (int m = 0; m < p.N; ++m) {
+      int64_t b, e;
+      seq_span(m, p.B, p.T, p.cu, b, e);
+      const int64_t c = n_chunks(e - b);
+      if (slot < s + c) { n = m; ci = slot - s; bos = b; eos = e; break; }
+      s += c;
+    }
+    if (n < 0) return;
+  }
+  const int64_t c0 = bos + ci * CHUNK;
+  const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+  const float* S = p.ckpt + ((size_t)slot * H + h) * D * D;
+  const float* dSn = p.tape + ((size_t)slot * H + h) * D * D;
+  const Tin* q = (const Tin*)p.q;
+  const Tin* k = (const Tin*)p.k;
+  const Tin* v = (const Tin*)p.v;
+  const Tin* dO = (const Tin*)p.dout;
+  const float scale = p.scale;
+
+  for (int idx = tid; idx < 64 * D; idx += NTG) {
+    const int i = idx / D, c = idx % D;
+    const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+    const Tin z = from_f<Tin>(0.f);
+    sQ[i * LDI + c] = (i < L) ? q[off] : z;
+    sK[i * LDI + c] = (i < L) ? k[off] : z;
+    sV[i * LDI + c] = (i < L) ? v[off] : z;
+    sdO[i * LDI + c] = (i < L) ? dO[off] : z;
+  }
+  if (tid < 64) {
+    const size_t off = (size_t)(c0 + tid) * H + h;
+    sg[tid] = (tid < L) ? p.g[off] : 0.f;
+    sb[tid] = (tid < L) ? p.beta[off] : 0.f;
+    sdgam[tid] = 0.f;
+    sred[tid] = 0.f;
+    sz[tid] = 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) warp_cumsum64(sg, sgam, tid);
+  __syncthreads();
+  if (tid < 64) {
+    const float eg = expf(sgam[tid]);
+    seg[tid] = eg;
+    sdec[tid] = expf(sgam[63] - sgam[tid]);
+    sbeg[tid] = sb[tid] * eg;
+    ssc[tid] = scale * eg;
+  }
+  __syncthreads();
+  const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), Vv = view(sV, LDI, 1),
+             dOv = view(sdO, LDI, 1);
+  const auto KvT = view(sK, 1, LDI), VvT = view(sV, 1, LDI);
+  const auto Sv = view(S, D, 1), SvT = view(S, 1, D), dSnT = view(dSn, 1, D),
+             dSnv = view(dSn, D, 1);
+
+  // Ak = Gamma o K K^T (strict lower), Aqk = Gamma o Q K^T (lower incl. diagonal)
+  {
+    float a1[4][4], a2[4][4];
+    zero(a1);
+    zero(a2);
+    gemm<4, 8>(a1, Kv, KvT, D, warp, lane);
+    gemm<4, 8>(a2, Qv, KvT, D, warp, lane);
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) {
+      sM[i * LD6 + j] = (j < i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
+    });
+    each<4, 8>(a2, warp, lane, [&](int i, int j, float& x) {
+      sP[i * LD6 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
+    });
+  }
+  __syncthreads();
+  // A = diag(beta) Ak into B3 (as a [64][65] tile), T = (I + A)^-1 into sT (scratch B2)
+  for (int idx = tid; idx < 64 * 64; idx += NTG) {
+    const int i = idx >> 6, j = idx & 63;
+    B3[i * LD6 + j] = sb[i] * sM[i * LD6 + j];
+  }
+  __syncthreads();
+  solve_unit_lower64(B3, sT, LD6, B2, tid, NTG, CtaBarG());
+  const auto Tv = view(sT, LD6, 1), TvT = view(sT, 1, LD6);
+  // W = T diag(beta e^gamma) K -> B1 ; U = T diag(beta) V -> B2
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, cols_scaled(Tv, sbeg), Kv, 64, warp, lane);
+    each<TD, NTD>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = x; });
+    zero(acc);
+    gemm<TD, NTD>(acc, cols_scaled(Tv, sb), Vv, 64, warp, lane);
+    each<TD, NTD>(acc, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
+  }
+  __syncthreads();
+  const auto B1v = view(B1, LDF, 1), B2v = view(B2, LDF, 1), B3v = view(B3, LDF, 1);
+  // Delta = U - W S^T (B2);  dDelta = scale Aqk^T dO + diag(dec) K dSn^T (B3)
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, B1v, SvT, D, warp, lane);
+    float acc2[TD][4];
+    zero(acc2);
+    gemm<TD, NTD>(acc2, view(sP, 1, LD6), dOv, 64, warp, lane);
+    float acc3[TD][4];
+    zero(acc3);
+    gemm<TD, NTD>(acc3, Kv, dSnT, D, warp, lane);
+    __syncthreads();   // every warp has read W (B1), U (B2) as operands of its own tiles only
+    each<TD, NTD>(acc, warp, lane, [&](int i, int r, float& x) { B2[i * LDF + r] -= x; });
+    each<TD, NTD>(acc3, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
+#pragma unroll
+    for (int ti = 0; ti < TD; ++ti)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc2[ti][e] = scale * acc2[ti][e] + acc3[ti][e];
+    each<TD, NTD>(acc2, warp, lane, [&](int i, int r, float& x) { B3[i * LDF + r] = x; });
+  }
+  __syncthreads();
+  float dq[TD][4], dk[TD][4];
+  zero(dq);
+  zero(dk);
+  // dAqk = scale dO Delta^T; rho = dAqk o Aqk -> dgamma; G = dAqk o Gamma (into sP)
+  {
+    float a1[4][4];
+    zero(a1);
+    gemm<4, 8>(a1, dOv, view(B2, 1, LDF), D, warp, lane);
+    __syncthreads();   // sP (Aqk) fully read as an operand before it is overwritten
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) {
+      float gval = 0.f;
+      if (j <= i) {
+        const float dA = scale * x;
+        const float rho = dA * sP[i * LD6 + j];
+        atomicAdd(&sdgam[i], rho);
+        atomicAdd(&sdgam[j], -rho);
+        gval = dA * expf(sgam[i] - sgam[j]);
+      }
+      sP[i * LD6 + j] = gval;
+    });
+  }
+  __syncthreads();
+  // dq += scale e^gamma (dO S) + G K ; dk += G^T Q ; dgamma += q . (scale e^gamma dO S)
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, rows_scaled(dOv, ssc), Sv, D, warp, lane);
+    row_dot<TD, NTD>(acc, Qv, sdgam, warp, lane);
+#pragma unroll
+    for (int ti = 0; ti < TD; ++ti)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dq[ti][e] += acc[ti][e];
+    gemm<TD, NTD>(dq, view(sP, LD6, 1), Kv, 64, warp, lane);
+    gemm<TD, NTD>(dk, view(sP, 1, LD6), Qv, 64, warp, lane);
+  }
+  // exit state: Z = Delta dSn ; dk += dec o Z ; ddec = rowsum(K o Z)
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, B2v, dSnv, D, warp, lane);
+    row_dot<TD, NTD>(acc, Kv, sz, warp, lane);
+    each<TD, NTD>(acc, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
+#pragma unroll
+    for (int ti = 0; ti < TD; ++ti)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dk[ti][e] += acc[ti][e];
+  }
+  // <dSn, S> for the e^{gamma_C} S term
+  {
+    float part = 0.f;
+    for (int idx = tid; idx < D * D; idx += NTG) part += dSn[idx] * S[idx];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) atomicAdd(&sdgam[63], seg[63] * part);
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const float t = sdec[tid] * sz[tid];
+    atomicAdd(&sdgam[tid], -t);
+    atomicAdd(&sdgam[63], t);
+  }
+  // dW = -dDelta S (B1) ;  X = T^T dDelta (B2, Delta no longer needed)
+  {
+    float acc[TD][4], acc2[TD][4];
+    zero(acc);
+    zero(acc2);
+    gemm<TD, NTD>(acc, B3v, Sv, D, warp, lane);
+    gemm<TD, NTD>(acc2, TvT, B3v, 64, warp, lane);
+    __syncthreads();
+    each<TD, NTD>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = -x; });
+    each<TD, NTD>(acc2, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
+  }
+  __syncthreads();
+  // dv = beta X ; dbeta += rowsum(V o X)
+  {
+    Tin* dv = (Tin*)p.dv;
+    for (int idx = tid; idx < 64 * D; idx += NTG) {
+      const int i = idx / D, c = idx % D;
+      const float t = B2[i * LDF + c];
+      if (i < L) dv[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(sb[i] * t);
+      atomicAdd(&sred[i], Vv(i, c) * t);
+    }
+  }
+  // dT = dDelta (diag(beta) V)^T + dW (diag(beta e^gamma) K)^T  (into sP)
+  {
+    float a1[4][4];
+    zero(a1);
+    gemm<4, 8>(a1, B3v, cols_scaled(VvT, sb), D, warp, lane);
+    gemm<4, 8>(a1, B1v, cols_scaled(KvT, sbeg), D, warp, lane);
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) { sP[i * LD6 + j] = x; });
+  }
+  __syncthreads();
+  // Y = T^T dW ; dk += beta e^gamma Y ; kt = rowsum(K o Y) -> dbeta += e^gamma kt,
+  // dgamma += beta e^gamma kt
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, TvT, B1v, 64, warp, lane);
+    if (tid < 64) sz[tid] = 0.f;
+    __syncthreads();
+    row_dot<TD, NTD>(acc, Kv, sz, warp, lane);
+    each<TD, NTD>(acc, warp, lane, [&](int i, int, float& x) { x *= sbeg[i]; });
+#pragma unroll
+    for (int ti = 0; ti < TD; ++ti)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dk[ti][e] += acc[ti][e];
+  }
+  __syncthreads();
+  if (tid < 64) {
+    sred[tid] += seg[tid] * sz[tid];
+    sdgam[tid] += sbeg[tid] * sz[tid];
+  }
+  // dA = -(T^T dT T^T) strictly lower: X1 = dT T^T (B1 as [64][65]), dA = -T^T X1 (B2)
+  {
+    float a1[4][4];
+    zero(a1);
+    gemm<4, 8>(a1, view(sP, LD6, 1), TvT, 64, warp, lane);
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) { B1[i * LD6 + j] = x; });
+  }
+  __syncthreads();
+  {
+    float a1[4][4];
+    zero(a1);
+    gemm<4, 8>(a1, TvT, view(B1, LD6, 1), 64, warp, lane);
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) { B2[i * LD6 + j] = (j < i) ? -x : 0.f; });
+  }
+  __syncthreads();
+  // from A_ij = beta_i Ak_ij: dbeta_i += sum_j dA_ij Ak_ij; dgamma_i/j +- dA beta Ak;
+  // dKK_ij = dA_ij beta_i Gamma_ij (into sP)
+  for (int idx = tid; idx < 64 * 64; idx += NTG) {
+    const int i = idx >> 6, j = idx & 63;
+    float dkk = 0.f;
+    if (j < i) {
+      const float dA = B2[i * LD6 + j], ak = sM[i * LD6 + j];
+      atomicAdd(&sred[i], dA * ak);
+      const float rho = dA * sb[i] * ak;
+      atomicAdd(&sdgam[i], rho);
+      atomicAdd(&sdgam[j], -rho);
+      dkk = dA * sb[i] * expf(sgam[i] - sgam[j]);
+    }
+    sP[i * LD6 + j] = dkk;
+  }
+  __syncthreads();
+  // dk += dKK K + dKK^T K
+  gemm<TD, NTD>(dk, view(sP, LD6, 1), Kv, 64, warp, lane);
+  gemm<TD, NTD>(dk, view(sP, 1, LD6), Kv, 64, warp, lane);
+  // write dq, dk
+  {
+    Tin* dqo = (Tin*)p.dq;
+    Tin* dko = (Tin*)p.dk;
+    each<TD, NTD>(dq, warp, lane, [&](int i, int c, float& x) {
+      if (i < L) dqo[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
+    });
+    each<TD, NTD>(dk, warp, lane, [&](int i, int c, float& x) {
+      if (i < L) dko[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
+    });
+  }
+  __syncthreads();
+  // dgate = reverse cumulative sum of dgamma; dbeta
+  if (tid < 32) {
+    const float a = sdgam[63 - 2 * lane], b = sdgam[62 - 2 * lane];
+    float s = a + b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += t;
+    }
+    const float excl = s - (a + b);
+    sgam[63 - 2 * lane] = excl + a;
+    sgam[62 - 2 * lane] = excl + a + b;
+  }
+  __syncthreads();
+  if (tid < L) {
+    const size_t off = (size_t)(c0 + tid) * H + h;
+    p.dg[off] = sgam[tid];
+    p.dbeta[off] = sred[tid];
+  }
+}
+
+template <typename Tin, int D>
+static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 11 * 64) +
+                      sizeof(Tin) * 4 * 64 * (D + 8);
+  auto kern = mma_bwd_grad_kernel<Tin, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTG, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
+                                cudaStream_t st) {
+  if (bf16 && D == 64) return launch_grad_t<__nv_bfloat16, 64>(p, slots, st);
+  if (bf16 && D == 128) return launch_grad_t<__nv_bfloat16, 128>(p, slots, st);
+  if (!bf16 && D == 64) return launch_grad_t<float, 64>(p, slots, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sfg

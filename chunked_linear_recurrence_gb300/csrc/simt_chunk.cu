@@ -11,6 +11,8 @@
 // dimension, so a (sequence, head) chain runs as D/BV CTAs, each owning BV
 // rows of the [V,K] state -- rows of the state evolve independently given
 // the chunk's factors, which every CTA recomputes).
+#include <type_traits>
+
 #include "common.cuh"
 #include "simt_chunk.cuh"
 
@@ -738,26 +740,25 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 template <typename Tin, int D>
 static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
   constexpr int BV = 32;
-  {
-    const size_t smem = sizeof(float) * (3 * 64 * (D + 1) + 2 * 64 * (BV + 1) + BV * (D + 1) +
-                                         3 * 64 * 65 + 5 * 64);
-    auto kern = simt_bwd_chain_kernel<Tin, D, BV>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3(D / BV, p.H, p.N), NT, smem, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    const size_t smem = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 7 * 64) +
-                        sizeof(Tin) * 4 * 64 * (D + 8);
-    auto kern = simt_bwd_grad_kernel<Tin, D>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NT, smem, st>>>(p);
-    return cudaGetLastError();
-  }
+  const size_t smem = sizeof(float) * (3 * 64 * (D + 1) + 2 * 64 * (BV + 1) + BV * (D + 1) +
+                                       3 * 64 * 65 + 5 * 64);
+  auto kern = simt_bwd_chain_kernel<Tin, D, BV>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(D / BV, p.H, p.N), NT, smem, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // token gradients of every chunk, fully parallel: BF16 inputs on the warp-level tensor
+  // cores (TF32 products); FP32 inputs keep FP32 products on the CUDA cores
+  if (std::is_same<Tin, __nv_bfloat16>::value)
+    return launch_mma_bwd_grad(p, true, D, slots, st);
+  const size_t smem2 = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 7 * 64) +
+                       sizeof(Tin) * 4 * 64 * (D + 8);
+  auto kern2 = simt_bwd_grad_kernel<Tin, D>;
+  e = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+  if (e != cudaSuccess) return e;
+  if (slots > 0) kern2<<<dim3((unsigned)slots, p.H), NT, smem2, st>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,

@@ -41,5 +41,8 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 // Backward after a replay: reverse cotangent chain then per-chunk token gradients.
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
                             cudaStream_t st);
+// Per-chunk token gradients on the warp-level tensor cores (bwd_grad_mma.cu).
+cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
+                                cudaStream_t st);
 
 }  // namespace sfg
