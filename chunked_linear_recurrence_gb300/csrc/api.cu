@@ -88,6 +88,31 @@ int64_t bwd_slots(const sf_gdn_shape* s, bool packed) {
 
 size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Backward workspace: status word | chunk-entry states | exit cotangents (FP32
+// [slots,H,V,K] each) | BF16 only: per-chunk factors [slots,H] and, for head size 128, the
+// split forward's ring (state replay).
+struct BwdLayout {
+  size_t one, fac, split, total;
+};
+
+BwdLayout bwd_layout(const sf_gdn_shape* shape) {
+  BwdLayout l{0, 0, 0, kStatusBytes};
+  if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0) return l;
+  // enough for both layouts: dense needs N*ceil(T/64) slots, packed (B == 1)
+  // at most ceil(T/64) + N
+  const int64_t per = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK;
+  const int64_t n = shape->N > 0 ? shape->N : shape->B;
+  int64_t slots = n * per;
+  if (shape->B == 1 && slots < per + n) slots = per + n;
+  l.one = round_up((size_t)slots * shape->H * shape->K * shape->V * sizeof(float));
+  if (shape->dtype == SF_BF16 && (shape->K == 64 || shape->K == 128))
+    l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));
+  if (shape->dtype == SF_BF16 && shape->K == 128 && shape->V == 128)
+    l.split = sfg::split_fwd_workspace((int)n, shape->H);
+  l.total = kStatusBytes + 2 * l.one + l.fac + l.split;
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
@@ -129,7 +154,7 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
-    e = sfg::launch_split_fwd(p, workspace, cs);
+    e = sfg::launch_split_fwd(p, workspace, reinterpret_cast<int*>(workspace), cs);
   } else {
     e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
   }
@@ -189,17 +214,7 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float* P, const float*
   return SF_OK;
 }
 
-size_t sf_gdn_bwd_workspace(const sf_gdn_shape* shape) {
-  if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0) return kStatusBytes;
-  // enough for both layouts: dense needs N*ceil(T/64) slots, packed (B == 1)
-  // at most ceil(T/64) + N
-  const int64_t per = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK;
-  const int64_t n = shape->N > 0 ? shape->N : shape->B;
-  int64_t slots = n * per;
-  if (shape->B == 1 && slots < per + n) slots = per + n;
-  const size_t one = (size_t)slots * shape->H * shape->K * shape->V * sizeof(float);
-  return kStatusBytes + 2 * round_up(one);
-}
+size_t sf_gdn_bwd_workspace(const sf_gdn_shape* shape) { return bwd_layout(shape).total; }
 
 sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
                            const float* gate, const float* beta, const float* initial_state,
@@ -223,7 +238,8 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
     return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn, need);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int64_t slots = bwd_slots(shape, packed);
-  const size_t one = round_up((size_t)slots * shape->H * D * D * sizeof(float));
+  const BwdLayout lay = bwd_layout(shape);
+  const size_t one = lay.one;
   char* ws = reinterpret_cast<char*>(workspace);
   sfg::ChainParams p{};
   p.q = q; p.k = k; p.v = v; p.g = gate; p.beta = beta; p.s0 = initial_state; p.cu = cu_seqlens;
@@ -231,10 +247,12 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   p.tape = reinterpret_cast<float*>(ws + kStatusBytes + one);
   p.dout = d_out; p.dsf = d_final_state; p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dgate;
   p.dbeta = dbeta; p.ds0 = d_initial_state;
+  p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + 2 * one) : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available())
-    e = sfg::launch_tc(p, sfg::TC_MODE_REPLAY, reinterpret_cast<int*>(workspace), cs);
+    e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
+                              reinterpret_cast<int*>(workspace), cs);
   else
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);

@@ -1,0 +1,281 @@
+// bwd_chain_mma.cu -- the backward's reverse state-cotangent chain for BF16 inputs on the
+// warp-level tensor cores (mma.sync m16n8k8, TF32 operands, FP32 carry).
+//
+// StateFlow section 3.1, Eq. 6-7: the cotangent of a chunk's entry state is the cotangent
+// of the previous chunk's exit state; walking a sequence backwards, per chunk with exit
+// cotangent dSn:
+//     dDelta   = scale Aqk^T dO + diag(dec) K dSn^T
+//     dS_entry = e^{gamma_C} dSn + scale dO^T diag(e^gamma) Q - dDelta^T W
+// (the chunk algebra of common.cuh, differentiated).  Two kernels:
+//   * mma_bwd_factor_kernel, fully parallel over chunks, computes each chunk's Aqk and W
+//     (the [K;Q] K^T contractions, the triangular solve) once;
+//   * mma_bwd_chain_kernel walks each (sequence, head) chain backwards, tiled along V
+//     (StateFlow section 3.4.1, Eq. 16: rows of the cotangent evolve independently given
+//     the chunk factors), with the cotangent rows FP32 in shared memory.  Each chunk's
+//     exit cotangent goes to the tape for the token-gradient kernel; the cotangent at the
+//     sequence start is d_initial_state.
+#include <type_traits>
+
+#include "common.cuh"
+#include "mma_tiles.cuh"
+#include "simt_chunk.cuh"
+#include "solve_tc.cuh"
+
+namespace sfg {
+namespace {
+
+using namespace mt;
+constexpr int NTB = 256;   // 8 warps
+
+struct CtaBarB {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// Locates chunk `slot` (dense: n * ceil(T/64) + c; packed: running sum over sequences).
+__device__ __forceinline__ bool locate_slot(const ChainParams& p, int64_t slot, int& n,
+                                            int64_t& bos, int64_t& eos, int64_t& ci) {
+  if (!p.cu) {
+    const int64_t nc = n_chunks(p.T);
+    n = (int)(slot / nc);
+    ci = slot % nc;
+    if (n >= p.N) return false;
+    seq_span(n, p.B, p.T, nullptr, bos, eos);
+    return true;
+  }
+  int64_t s = 0;
+  for (int m = 0; m < p.N; ++m) {
+    int64_t b, e;
+    seq_span(m, p.B, p.T, p.cu, b, e);
+    const int64_t c = n_chunks(e - b);
+    if (slot < s + c) {
+      n = m;
+      ci = slot - s;
+      bos = b;
+      eos = e;
+      return true;
+    }
+    s += c;
+  }
+  return false;
+}
+
+}  // namespace
+
+// Per-chunk factors of the backward chain: fac[(slot * H + h)] = { Aqk [64][64], W [64][D],
+// e^gamma [64], dec [64] } (FP32; rows past the sequence end are zero).
+template <int D>
+__host__ __device__ constexpr size_t fac_bytes() { return 4 * (64 * 64 + 64 * D + 128); }
+
+template <int D>
+__global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p, float* fac) {
+  constexpr int LDI = D + 8, LD6 = 65, NTD = D / 8, TD = 4 * NTD / 8;
+  extern __shared__ float sm[];
+  float* sA = sm;                 // A = diag(beta) Ak, then scratch of the solve
+  float* sT = sA + 64 * LD6;
+  float* sX = sT + 64 * LD6;      // solve scratch (1024 floats)
+  float* sg = sX + 64 * LD6;
+  float* sb = sg + 64;
+  float* sgam = sb + 64;
+  float* sbeg = sgam + 64;
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sbeg + 64);
+  __nv_bfloat16* sK = sQ + 64 * LDI;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
+  const int64_t slot = blockIdx.x;
+  int n;
+  int64_t bos, eos, ci;
+  if (!locate_slot(p, slot, n, bos, eos, ci)) return;
+  const int64_t c0 = bos + ci * CHUNK;
+  const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+  const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
+  const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
+  for (int idx = tid; idx < 64 * D; idx += NTB) {
+    const int i = idx / D, c = idx % D;
+    const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+    const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+    sQ[i * LDI + c] = (i < L) ? q[off] : z;
+    sK[i * LDI + c] = (i < L) ? k[off] : z;
+  }
+  if (tid < 64) {
+    const size_t off = (size_t)(c0 + tid) * H + h;
+    sg[tid] = (tid < L) ? p.g[off] : 0.f;
+    sb[tid] = (tid < L) ? p.beta[off] : 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) warp_cumsum64(sg, sgam, tid);
+  __syncthreads();
+  float* out = fac + (size_t)(slot * H + h) * (fac_bytes<D>() / 4);
+  float* oAqk = out;
+  float* oW = out + 64 * 64;
+  float* ovec = oW + 64 * D;
+  if (tid < 64) {
+    const float eg = expf(sgam[tid]);
+    sbeg[tid] = sb[tid] * eg;
+    ovec[tid] = eg;
+    ovec[64 + tid] = expf(sgam[63] - sgam[tid]);
+  }
+  const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), KvT = view(sK, 1, LDI);
+  {
+    float a1[4][4], a2[4][4];
+    zero(a1);
+    zero(a2);
+    gemm<4, 8>(a1, Kv, KvT, D, warp, lane);
+    gemm<4, 8>(a2, Qv, KvT, D, warp, lane);
+    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) {
+      sA[i * LD6 + j] = (j < i) ? sb[i] * expf(sgam[i] - sgam[j]) * x : 0.f;
+    });
+    each<4, 8>(a2, warp, lane, [&](int i, int j, float& x) {
+      oAqk[i * 64 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
+    });
+  }
+  __syncthreads();
+  solve_unit_lower64(sA, sT, LD6, sX, tid, NTB, CtaBarB());
+  {
+    float acc[TD][4];
+    zero(acc);
+    gemm<TD, NTD>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
+    each<TD, NTD>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
+  }
+}
+
+// Reverse chain: grid (D / BV, H, N); CTA (rv, h, n) owns cotangent rows [BV rv, BV rv + BV).
+template <int D, int BV>
+__global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p, const float* fac) {
+  constexpr int LDS = D + 1, LD6 = 65, LDI = D + 8, LDO = BV + 8, LDW = D + 1;
+  constexpr int MB = BV / 16;                 // 16-row bands of the cotangent tile
+  constexpr int T64 = MB * 8 / 8;             // tiles per warp of a BV x 64 output
+  constexpr int TDD = MB * (D / 8) / 8;       // tiles per warp of a BV x D output
+  static_assert(MB * 8 % 8 == 0 && MB * (D / 8) % 8 == 0, "tiles per warp");
+  extern __shared__ float sm[];
+  float* dS = sm;                             // [BV][LDS] running cotangent rows
+  float* dDT = dS + BV * LDS;                 // [BV][LD6] dDelta^T
+  float* sAqk = dDT + BV * LD6;               // [64][LD6]
+  float* sW = sAqk + 64 * LD6;                // [64][LDW]
+  float* sdec = sW + 64 * LDW;
+  float* ssc = sdec + 64;                     // scale e^gamma
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(ssc + 64);
+  __nv_bfloat16* sK = sQ + 64 * LDI;
+  __nv_bfloat16* sdO = sK + 64 * LDI;         // [64][LDO]: dO rows, columns [r0, r0 + BV)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, n = blockIdx.z, r0 = blockIdx.x * BV, H = p.H;
+  const float scale = p.scale;
+  const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
+  const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
+  const __nv_bfloat16* dO = (const __nv_bfloat16*)p.dout;
+  int64_t bos, eos;
+  seq_span(n, p.B, p.T, p.cu, bos, eos);
+  const int64_t nc = n_chunks(eos - bos);
+  const int64_t slot0 = chunk_slot_base(n, p.B, p.T, p.cu);
+
+  for (int idx = tid; idx < BV * D; idx += NTB) {
+    const int r = idx / D, c = idx % D;
+    dS[r * LDS + c] = p.dsf ? p.dsf[(((size_t)n * H + h) * D + r0 + r) * D + c] : 0.f;
+  }
+  const auto dOT = view(sdO, 1, LDO);        // dO^T (v, i)
+  for (int64_t ci = nc - 1; ci >= 0; --ci) {
+    const int64_t c0 = bos + ci * CHUNK;
+    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+    const size_t slot = (size_t)(slot0 + ci);
+    const float* f = fac + (slot * H + h) * (fac_bytes<D>() / 4);
+    __syncthreads();
+    {
+      float* dst = p.tape + (slot * H + h) * D * D;
+      for (int idx = tid; idx < BV * D; idx += NTB) {
+        const int r = idx / D, c = idx % D;
+        dst[(size_t)(r0 + r) * D + c] = dS[r * LDS + c];
+      }
+    }
+    for (int idx = tid; idx < 64 * D; idx += NTB) {
+      const int i = idx / D, c = idx % D;
+      const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+      const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+      sQ[i * LDI + c] = (i < L) ? q[off] : z;
+      sK[i * LDI + c] = (i < L) ? k[off] : z;
+      sW[i * LDW + c] = f[64 * 64 + i * D + c];
+    }
+    for (int idx = tid; idx < 64 * BV; idx += NTB) {
+      const int i = idx / BV, c = idx % BV;
+      sdO[i * LDO + c] = (i < L) ? dO[((size_t)(c0 + i) * H + h) * D + r0 + c]
+                                 : __float2bfloat16_rn(0.f);
+    }
+    for (int idx = tid; idx < 64 * 64; idx += NTB) sAqk[(idx >> 6) * LD6 + (idx & 63)] = f[idx];
+    if (tid < 64) {
+      ssc[tid] = scale * f[64 * 64 + 64 * D + tid];
+      sdec[tid] = f[64 * 64 + 64 * D + 64 + tid];
+    }
+    __syncthreads();
+    const float gC = f[64 * 64 + 64 * D + 63];   // e^{gamma_C}
+    // dDelta^T [v][j] = scale (dO^T Aqk)[v][j] + dec_j (dS K^T)[v][j]
+    {
+      float a1[T64][4], a2[T64][4];
+      zero(a1);
+      zero(a2);
+      gemm<T64, 8>(a1, dOT, view(sAqk, LD6, 1), 64, warp, lane);
+      gemm<T64, 8>(a2, view(dS, LDS, 1), view(sK, 1, LDI), D, warp, lane);
+#pragma unroll
+      for (int ti = 0; ti < T64; ++ti)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a1[ti][e] *= scale;
+      each<T64, 8>(a2, warp, lane, [&](int, int j, float& x) { x *= sdec[j]; });
+#pragma unroll
+      for (int ti = 0; ti < T64; ++ti)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a1[ti][e] += a2[ti][e];
+      each<T64, 8>(a1, warp, lane, [&](int v, int j, float& x) { dDT[v * LD6 + j] = x; });
+    }
+    __syncthreads();
+    // dS <- e^{gamma_C} dS + (dO^T diag(scale e^gamma)) Q - dDelta^T W
+    {
+      float a3[TDD][4], a4[TDD][4];
+      zero(a3);
+      zero(a4);
+      gemm<TDD, D / 8>(a3, cols_scaled(dOT, ssc), view(sQ, LDI, 1), 64, warp, lane);
+      gemm<TDD, D / 8>(a4, view(dDT, LD6, 1), view(sW, LDW, 1), 64, warp, lane);
+#pragma unroll
+      for (int ti = 0; ti < TDD; ++ti)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a3[ti][e] -= a4[ti][e];
+      each<TDD, D / 8>(a3, warp, lane, [&](int v, int c, float& x) {
+        dS[v * LDS + c] = gC * dS[v * LDS + c] + x;
+      });
+    }
+  }
+  __syncthreads();
+  if (p.ds0)
+    for (int idx = tid; idx < BV * D; idx += NTB) {
+      const int r = idx / D, c = idx % D;
+      p.ds0[(((size_t)n * H + h) * D + r0 + r) * D + c] = dS[r * LDS + c];
+    }
+}
+
+size_t mma_bwd_fac_bytes(int D) { return D == 128 ? fac_bytes<128>() : fac_bytes<64>(); }
+
+template <int D>
+static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slots, cudaStream_t st) {
+  constexpr int BV = 32;
+  {
+    const size_t smem = sizeof(float) * (3 * 64 * 65 + 4 * 64) + 2 * 2 * 64 * (D + 8);
+    auto kern = mma_bwd_factor_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTB, smem, st>>>(p, fac);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t smem = sizeof(float) * (BV * (D + 1) + BV * 65 + 64 * 65 + 64 * (D + 1) + 128) +
+                      2 * (2 * 64 * (D + 8) + 64 * (BV + 8));
+  auto kern = mma_bwd_chain_kernel<D, BV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(D / BV, p.H, p.N), NTB, smem, st>>>(p, fac);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_t slots,
+                                 cudaStream_t st) {
+  if (D == 128) return launch_chain_d<128>(p, fac, slots, st);
+  if (D == 64) return launch_chain_d<64>(p, fac, slots, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sfg

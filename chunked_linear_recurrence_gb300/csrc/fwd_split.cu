@@ -155,8 +155,9 @@ struct SplitParams {
   const float* g;
   const float* beta;
   const float* s0;           // [N,H,V,K] or NULL
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;        // or NULL (state replay: no output)
   float* final_state;        // or NULL
+  float* ckpt;               // state replay: [slots,H,V,K] chunk-entry states, else NULL
   int* status;               // workspace status word
   int* abort_g;              // global abort flag
   uint32_t* consumed;        // [nch] records consumed (copied out) per chain CTA
@@ -447,6 +448,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
       int64_t bos, eos;
       geo.span(x, bos, eos);
       const int nc = (int)n_chunks(eos - bos);
+      // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c]
+      float* ck = p.ckpt ? p.ckpt + ((size_t)chunk_slot_base(x / H, p.B, p.T, p.cu) * H + x % H) * D * D +
+                               (size_t)v * D + 64 * w
+                         : nullptr;
+      const size_t ck_stride = (size_t)H * D * D;
       if (nc == 0) {
         // an empty sequence passes its initial state through
         if (p.final_state) {
@@ -473,6 +479,12 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
         } else {
 #pragma unroll
           for (int e = 0; e < 64; ++e) xv[e] = 0.f;
+        }
+        if (ck) {
+          float4* dst = reinterpret_cast<float4*>(ck);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
         }
         uint32_t u[16];
 #pragma unroll
@@ -562,6 +574,12 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
             for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
             tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
           }
+          if (ck) {
+            float4* dst = reinterpret_cast<float4*>(ck + (size_t)(c + 1) * ck_stride);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
+          }
           tmem_st_wait();
           tc_fence_before();
           named_bar(BAR_STATE, 256);
@@ -604,6 +622,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
         tc_fence_before();
         named_bar(BAR_OUT, 128);
         if (v == 0) mbar_arrive(&bars[C_OFREE + b]);
+        if (!p.out) continue;
         const int64_t row0 = bos + (int64_t)c * CHUNK;
         const int L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
         __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
@@ -1106,20 +1125,24 @@ static_assert(WS_FLAGS_END <= WS_RING, "workspace flags");
 
 }  // namespace
 
-constexpr size_t WS_GEO = WS_RING + (size_t)MAX_NCH * NSLOT * REC_BYTES;
+int chain_ctas(int N, int H) {
+  const long long nh = (long long)N * H;
+  return (int)(nh < MAX_NCH ? nh : MAX_NCH);
+}
+size_t ws_geo(int N, int H) { return WS_RING + (size_t)chain_ctas(N, H) * NSLOT * REC_BYTES; }
 
 size_t split_fwd_workspace(int N, int H) {
-  return WS_GEO + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
+  return ws_geo(N, H) + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
 }
 
-cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, cudaStream_t st) {
+cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
   if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1)) return cudaErrorInvalidValue;
   int dev = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int NH = cp.N * cp.H;
-  const int nch = NH < MAX_NCH ? NH : MAX_NCH;
+  const int nch = chain_ctas(cp.N, cp.H);
   const int nprep = nsm - nch;
   if (nprep < 1) return cudaErrorInvalidConfiguration;
   const int rows = cp.B * cp.T;
@@ -1139,13 +1162,14 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, cudaStream_t st) {
   p.s0 = cp.s0;
   p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
   p.final_state = cp.final_state;
-  p.status = reinterpret_cast<int*>(w);
+  p.status = status;
+  p.ckpt = cp.ckpt;
   p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
   p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
   p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
   p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
   p.cu = cp.cu;
-  p.sstart = reinterpret_cast<int*>(w + WS_GEO);
+  p.sstart = reinterpret_cast<int*>(w + ws_geo(cp.N, cp.H));
   p.lenj = p.sstart + (size_t)NH;
   p.sortj = p.lenj + MAX_NCH;
   p.B = cp.B;

@@ -1,0 +1,100 @@
+// mma_tiles.cuh -- warp-level tensor-core tiles (mma.sync m16n8k8, TF32 operands, FP32
+// accumulation) for the backward kernels: element views of shared/global operands, a
+// tile GEMM over a warp's fixed set of 16x8 output tiles, and tile epilogues.
+#pragma once
+
+#include "common.cuh"
+#include "solve_tc.cuh"
+
+namespace sfg {
+namespace mt {
+
+// Element (r, c) views of the operands.
+template <typename T>
+struct View {
+  const T* p;
+  int sr, sc;
+  __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[r * sr + c * sc]); }
+};
+template <typename T>
+__device__ __forceinline__ View<T> view(const T* p, int sr, int sc) { return View<T>{p, sr, sc}; }
+// rows scaled by s[r]
+template <typename V>
+struct RowScaled {
+  V v;
+  const float* s;
+  __device__ __forceinline__ float operator()(int r, int c) const { return s[r] * v(r, c); }
+};
+// columns scaled by s[c]
+template <typename V>
+struct ColScaled {
+  V v;
+  const float* s;
+  __device__ __forceinline__ float operator()(int r, int c) const { return s[c] * v(r, c); }
+};
+template <typename V>
+__device__ __forceinline__ RowScaled<V> rows_scaled(V v, const float* s) { return RowScaled<V>{v, s}; }
+template <typename V>
+__device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { return ColScaled<V>{v, s}; }
+
+// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + 8 ti
+// of an output with NTN 8-column tiles per 16-row band.
+template <int NTILE, int NTN, typename AV, typename BV>
+__device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
+                                     int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll 4
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      const uint32_t a[4] = {f2tf32(A(m0 + g, k0 + t)), f2tf32(A(m0 + g + 8, k0 + t)),
+                             f2tf32(A(m0 + g, k0 + t + 4)), f2tf32(A(m0 + g + 8, k0 + t + 4))};
+      const uint32_t b[2] = {f2tf32(B(k0 + t, n0 + g)), f2tf32(B(k0 + t + 4, n0 + g))};
+      mma_tf32_16x8x8(acc[ti], a, b);
+    }
+  }
+}
+
+template <int NTILE>
+__device__ __forceinline__ void zero(float (&acc)[NTILE][4]) {
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[ti][e] = 0.f;
+}
+
+// Calls f(row, col, value&) for every element this warp holds.
+template <int NTILE, int NTN, typename F>
+__device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane, F&& f) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f(m0 + g + 8 * (e >> 1), n0 + 2 * t + (e & 1), acc[ti][e]);
+  }
+}
+
+// vec[row] += sum over this warp's columns of w(row, col) acc(row, col) (4-lane reduction,
+// then one shared-memory atomic per row segment).
+template <int NTILE, int NTN, typename W>
+__device__ __forceinline__ void row_dot(const float (&acc)[NTILE][4], const W& w, float* vec,
+                                        int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = m0 + g + 8 * hr, c = n0 + 2 * t;
+      float s = acc[ti][2 * hr] * w(r, c) + acc[ti][2 * hr + 1] * w(r, c + 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (t == 0) atomicAdd(&vec[r], s);
+    }
+  }
+}
+
+}  // namespace mt
+}  // namespace sfg

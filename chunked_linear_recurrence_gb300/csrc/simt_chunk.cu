@@ -739,19 +739,21 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 
 template <typename Tin, int D>
 static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
+  cudaError_t e;
+  if (std::is_same<Tin, __nv_bfloat16>::value) {
+    // BF16: reverse chain and token gradients on the warp-level tensor cores
+    if ((e = launch_mma_bwd_chain(p, p.fac, D, slots, st)) != cudaSuccess) return e;
+    return launch_mma_bwd_grad(p, true, D, slots, st);
+  }
+  // FP32 inputs keep FP32 products on the CUDA cores (1e-4 parity)
   constexpr int BV = 32;
   const size_t smem = sizeof(float) * (3 * 64 * (D + 1) + 2 * 64 * (BV + 1) + BV * (D + 1) +
                                        3 * 64 * 65 + 5 * 64);
   auto kern = simt_bwd_chain_kernel<Tin, D, BV>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(D / BV, p.H, p.N), NT, smem, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // token gradients of every chunk, fully parallel: BF16 inputs on the warp-level tensor
-  // cores (TF32 products); FP32 inputs keep FP32 products on the CUDA cores
-  if (std::is_same<Tin, __nv_bfloat16>::value)
-    return launch_mma_bwd_grad(p, true, D, slots, st);
   const size_t smem2 = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 7 * 64) +
                        sizeof(Tin) * 4 * 64 * (D + 8);
   auto kern2 = simt_bwd_grad_kernel<Tin, D>;

@@ -31,6 +31,7 @@ struct ChainParams {
   float* dg;
   float* dbeta;
   float* ds0;             // [N,H,V,K] or NULL
+  float* fac;             // [slots,H] per-chunk backward factors (BF16 backward)
   int B, T, H, N;
   float scale;
 };
@@ -41,6 +42,11 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 // Backward after a replay: reverse cotangent chain then per-chunk token gradients.
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
                             cudaStream_t st);
+// BF16 backward's reverse cotangent chain on the warp-level tensor cores
+// (bwd_chain_mma.cu): per-chunk factors into p.fac, then the chain (tape, ds0).
+size_t mma_bwd_fac_bytes(int D);
+cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_t slots,
+                                 cudaStream_t st);
 // Per-chunk token gradients on the warp-level tensor cores (bwd_grad_mma.cu).
 cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
                                 cudaStream_t st);
