@@ -95,14 +95,29 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   const Tin* dO = (const Tin*)p.dout;
   const float scale = p.scale;
 
-  for (int idx = tid; idx < 64 * D; idx += NTG) {
-    const int i = idx / D, c = idx % D;
-    const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
-    const Tin z = from_f<Tin>(0.f);
-    sQ[i * LDI + c] = (i < L) ? q[off] : z;
-    sK[i * LDI + c] = (i < L) ? k[off] : z;
-    sV[i * LDI + c] = (i < L) ? v[off] : z;
-    sdO[i * LDI + c] = (i < L) ? dO[off] : z;
+  {
+    // 16-byte loads, all of a thread's issued together
+    constexpr int PV = 16 / sizeof(Tin);          // elements per 16 bytes
+    constexpr int NV = 64 * D / PV / NTG;         // 16-byte pieces per thread per tile
+    uint4 vq[NV], vk[NV], vv[NV], vo[NV];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = (tid + NTG * e) * PV, i = idx / D, c = idx % D;
+      const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      vq[e] = (i < L) ? *reinterpret_cast<const uint4*>(q + off) : z;
+      vk[e] = (i < L) ? *reinterpret_cast<const uint4*>(k + off) : z;
+      vv[e] = (i < L) ? *reinterpret_cast<const uint4*>(v + off) : z;
+      vo[e] = (i < L) ? *reinterpret_cast<const uint4*>(dO + off) : z;
+    }
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = (tid + NTG * e) * PV, i = idx / D, c = idx % D;
+      *reinterpret_cast<uint4*>(sQ + i * LDI + c) = vq[e];
+      *reinterpret_cast<uint4*>(sK + i * LDI + c) = vk[e];
+      *reinterpret_cast<uint4*>(sV + i * LDI + c) = vv[e];
+      *reinterpret_cast<uint4*>(sdO + i * LDI + c) = vo[e];
+    }
   }
   if (tid < 64) {
     const size_t off = (size_t)(c0 + tid) * H + h;
@@ -235,7 +250,13 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   // <dSn, S> for the e^{gamma_C} S term
   {
     float part = 0.f;
-    for (int idx = tid; idx < D * D; idx += NTG) part += dSn[idx] * S[idx];
+    const float4* a4 = reinterpret_cast<const float4*>(dSn);
+    const float4* b4 = reinterpret_cast<const float4*>(S);
+#pragma unroll 8
+    for (int idx = tid; idx < D * D / 4; idx += NTG) {
+      const float4 x = a4[idx], y = b4[idx];
+      part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) atomicAdd(&sdgam[63], seg[63] * part);
@@ -258,14 +279,18 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     each<TD, NTD>(acc2, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
   }
   __syncthreads();
-  // dv = beta X ; dbeta += rowsum(V o X)
+  // dv = beta X ; dbeta += rowsum(V o X)  (a warp covers 32 columns of one row: warp sum,
+  // then one atomic per row segment)
   {
     Tin* dv = (Tin*)p.dv;
     for (int idx = tid; idx < 64 * D; idx += NTG) {
       const int i = idx / D, c = idx % D;
       const float t = B2[i * LDF + c];
       if (i < L) dv[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(sb[i] * t);
-      atomicAdd(&sred[i], Vv(i, c) * t);
+      float r = Vv(i, c) * t;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+      if (lane == 0) atomicAdd(&sred[i], r);
     }
   }
   // dT = dDelta (diag(beta) V)^T + dW (diag(beta e^gamma) K)^T  (into sP)
@@ -314,16 +339,25 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   __syncthreads();
   // from A_ij = beta_i Ak_ij: dbeta_i += sum_j dA_ij Ak_ij; dgamma_i/j +- dA beta Ak;
   // dKK_ij = dA_ij beta_i Gamma_ij (into sP)
+  // (a warp covers 32 columns j of one row i: the row-i sums go through a warp sum)
   for (int idx = tid; idx < 64 * 64; idx += NTG) {
     const int i = idx >> 6, j = idx & 63;
-    float dkk = 0.f;
+    float dkk = 0.f, r1 = 0.f, rho = 0.f;
     if (j < i) {
       const float dA = B2[i * LD6 + j], ak = sM[i * LD6 + j];
-      atomicAdd(&sred[i], dA * ak);
-      const float rho = dA * sb[i] * ak;
-      atomicAdd(&sdgam[i], rho);
+      r1 = dA * ak;
+      rho = dA * sb[i] * ak;
       atomicAdd(&sdgam[j], -rho);
       dkk = dA * sb[i] * expf(sgam[i] - sgam[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+      rho += __shfl_xor_sync(0xffffffffu, rho, o);
+    }
+    if (lane == 0) {
+      atomicAdd(&sred[i], r1);
+      atomicAdd(&sdgam[i], rho);
     }
     sP[i * LD6 + j] = dkk;
   }

@@ -38,21 +38,27 @@ template <typename V>
 __device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { return ColScaled<V>{v, s}; }
 
 // acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + 8 ti
-// of an output with NTN 8-column tiles per 16-row band.
+// of an output with NTN 8-column tiles per 16-row band.  The k loop is outermost and every
+// tile's operands of a k step are loaded before its products, so that a warp has all of
+// them in flight at once (operands in global memory take an L2 round trip).
 template <int NTILE, int NTN, typename AV, typename BV>
 __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
                                      int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a[NTILE][4], b[NTILE][2];
 #pragma unroll
-  for (int ti = 0; ti < NTILE; ++ti) {
-    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
-#pragma unroll 4
-    for (int k0 = 0; k0 < K; k0 += 8) {
-      const uint32_t a[4] = {f2tf32(A(m0 + g, k0 + t)), f2tf32(A(m0 + g + 8, k0 + t)),
-                             f2tf32(A(m0 + g, k0 + t + 4)), f2tf32(A(m0 + g + 8, k0 + t + 4))};
-      const uint32_t b[2] = {f2tf32(B(k0 + t, n0 + g)), f2tf32(B(k0 + t + 4, n0 + g))};
-      mma_tf32_16x8x8(acc[ti], a, b);
+    for (int ti = 0; ti < NTILE; ++ti) {
+      const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+      a[ti][0] = f2tf32(A(m0 + g, k0 + t));
+      a[ti][1] = f2tf32(A(m0 + g + 8, k0 + t));
+      a[ti][2] = f2tf32(A(m0 + g, k0 + t + 4));
+      a[ti][3] = f2tf32(A(m0 + g + 8, k0 + t + 4));
+      b[ti][0] = f2tf32(B(k0 + t, n0 + g));
+      b[ti][1] = f2tf32(B(k0 + t + 4, n0 + g));
     }
+#pragma unroll
+    for (int ti = 0; ti < NTILE; ++ti) mma_tf32_16x8x8(acc[ti], a[ti], b[ti]);
   }
 }
 
