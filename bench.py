@@ -54,12 +54,12 @@ def fwd_traffic():
     import hashlib
     csrc = os.path.join(ROOT, "chunked_linear_recurrence_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("fwd_tc.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
+    for f in ("fwd_split.cu", "fwd_tc.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     try:
         rec = {}
-        with open(os.path.join(ROOT, "profiles", "gdn_fwd_tc_traffic.txt")) as fh:
+        with open(os.path.join(ROOT, "profiles", "gdn_fwd_split_traffic.txt")) as fh:
             for line in fh:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
@@ -240,7 +240,7 @@ def run_ours(args):
     th = w1.B * w1.T * w1.H
     fwd_bytes = th * FWD_BYTES_PER_TH + 2 * w1.N * w1.H * STATE_BYTES
     achieved = fwd_bytes / (ms * 1e-3) / 1e9
-    roofline = {"kernel": "gdn_fwd (one launch per step)", "bound": "hbm",
+    roofline = {"kernel": "gdn_fwd_split_kernel (one launch per step)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                 "algorithmic_bytes": fwd_bytes,
