@@ -33,7 +33,7 @@
 //   out[i][v] = scale O[v][i]
 // Preparation products per chunk: KQ = [K;Q] K^T, Qg^T = Q^T diag(e^gamma),
 // (-W)^T = K^T (-T'')^T, U^T = V^T T'^T (all N = 64), T' = T diag(beta),
-// T'' = T diag(beta e^gamma), the 64x64 solve in FP32 (solve_tc.cuh).
+// T'' = T diag(beta e^gamma), the 64x64 solve in FP32 with TF32 merges (solve::).
 //
 // Every wait (mbarrier or global flag) is bounded; a CTA that gives up raises a
 // global abort flag that every other CTA polls, writes SF_ERR_TIMEOUT to the status
@@ -59,6 +59,7 @@ constexpr int NTHR = 512;
 constexpr int NSLOT = 8;          // ring slots per chain CTA
 constexpr int NBUF = 3;           // record buffers in a chain CTA's shared memory
 constexpr int MAX_NCH = 64;       // chain CTAs at most
+constexpr int FLAG_STRIDE = 32;   // words between chain CTAs' flags: one 128-byte line each
 
 // ---- record (global ring slot, and the chain CTA's shared-memory copy) ----
 constexpr uint32_t R_WQ = 0;          // 2 panels x 16 KB
@@ -86,14 +87,21 @@ constexpr uint32_t P_T1 = 49152;      // T'  [64 i][64 j]
 constexpr uint32_t P_T2 = 57344;      // -T'' [64 i][64 j]
 constexpr uint32_t P_DG = 65536;      // diag(e^gamma) [64][64]
 constexpr uint32_t P_AT = 73728;      // FP32 [64][SOLVE_LD]: A, then T
-constexpr uint32_t P_X = 91136;       // FP32 [32][SOLVE_LD]: solve scratch
+constexpr uint32_t P_X = 91136;       // staging of the Ahat rows (2 warps x 4 KB)
 constexpr uint32_t P_VEC = 99840;     // 2 slots x 512 floats (items alternate)
 constexpr uint32_t P_VEC_SLOT = 2048;
 constexpr uint32_t P_STRIDE = 104448;
 constexpr uint32_t P_BAR = 2 * P_STRIDE;
-static_assert(P_AT + 64 * SOLVE_LD * 4 <= P_X && P_X + 32 * SOLVE_LD * 4 <= P_VEC, "prep smem");
+static_assert(P_AT + 64 * SOLVE_LD * 4 <= P_X && P_X + 2 * 4096 <= P_VEC, "prep smem");
 static_assert(P_VEC + 2 * P_VEC_SLOT <= P_STRIDE && P_STRIDE % 1024 == 0, "prep smem");
 static_assert(64 * SOLVE_LD * 4 >= 4 * 4096, "the A/T area doubles as the store staging area");
+
+// Registers per thread after setmaxnreg, by role.  Each CTA is launched with 128 per
+// thread (512 threads, the SM's 64K), and the roles' shares must add up to no more.
+constexpr int RC_CTL = 56, RC_STATE = 168, RC_OUT = 120;        // chain: 4, 8, 4 warps
+constexpr int RP_CTL = 88, RP_PIPE = 200, RP_IDLE = 24;         // preparation: 4, 8, 4 warps
+static_assert(4 * RC_CTL + 8 * RC_STATE + 4 * RC_OUT <= 16 * 128, "chain register split");
+static_assert(4 * RP_CTL + 8 * RP_PIPE + 4 * RP_IDLE <= 16 * 128, "preparation register split");
 
 constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t GEO_BYTES = 2 * 64 * 4;   // stream lengths and their order (packed inputs)
@@ -103,7 +111,8 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
 // per-pipeline vectors (floats)
 constexpr int VEC_BETA = 64, VEC_GAM = 128, VEC_EG = 192, VEC_DEC = 256,
-              VEC_EP = 320, VEC_EM = 384, VEC_FLAG = 448;
+              VEC_EP = 320, VEC_EM = 384, VEC_FLAG = 448,
+              VEC_ITEM = 450;   // the use's item (int), -1: the pipeline has no more items
 
 // ---- TMEM columns ----
 // chain: S FP32, S BF16 pairs, Delta^T BF16 pairs, Delta^T diag(dec) BF16 pairs, two
@@ -141,7 +150,7 @@ enum {
   P_TMFREE = 14,   // [2] item finished: TMEM region read out, vector slot free
   P_PUB = 16,      // [2] item's record written: the publisher may release it
   P_SLOTOK = 18,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
-  P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out
+  P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
   P_VECFREE = 22,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
   P_COUNT = 26
 };
@@ -160,8 +169,9 @@ struct SplitParams {
   float* ckpt;               // state replay: [slots,H,V,K] chunk-entry states, else NULL
   int* status;               // workspace status word
   int* abort_g;              // global abort flag
-  uint32_t* consumed;        // [nch] records consumed (copied out) per chain CTA
-  uint32_t* ready;           // [nch][NSLOT] stream position + 1 of the record in the slot
+  uint32_t* next_item;       // items claimed so far by the preparation CTAs
+  uint32_t* consumed;        // [nch] records consumed (copied out), one line per chain CTA
+  uint32_t* ready;           // [nch] lines: [NSLOT] stream position + 1 of the slot's record
   uint8_t* ring;             // [nch][NSLOT][REC_BYTES]
   const int32_t* cu;         // packed sequences: cu_seqlens [N+1], else NULL
   int* sstart;               // packed: [N*H] first stream position of each chain in its CTA
@@ -186,8 +196,10 @@ __device__ __forceinline__ void raise_abort(const Ctx& cx) {
   atomicExch(cx.p->status, 5 /* SF_ERR_TIMEOUT */);
 }
 
-__device__ __forceinline__ bool aborted(const Ctx& cx) {
-  return *cx.abort_l || ld_volatile_s32(cx.p->abort_g);
+// The CTA's own flag is read every time; the global flag, on a line that every polling
+// thread of the grid would otherwise keep hot, only on every 64th call of a wait loop.
+__device__ __forceinline__ bool aborted(const Ctx& cx, uint32_t n) {
+  return *cx.abort_l || ((n & 63) == 0 && ld_volatile_s32(cx.p->abort_g));
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
@@ -218,10 +230,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ bool poll_ge(const uint32_t* f, uint32_t target, const Ctx& cx) {
   if (ld_acquire_u32(f) >= target) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     __nanosleep(32);
     if (ld_acquire_u32(f) >= target) return true;
-    if (aborted(cx)) return false;
+    if (aborted(cx, n)) return false;
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
@@ -313,11 +325,6 @@ struct Geo {
   }
 };
 
-struct NamedBar {
-  int id, n;
-  __device__ __forceinline__ void operator()() const { named_bar(id, n); }
-};
-
 // --------------------------------------------------------------------------
 // State-chain CTA.  warp 0: record / K-tile loader; warp 1: MMA issuer; warps 4-11:
 // the state (two warpgroups, one column half each); warps 12-15: output stores.
@@ -330,21 +337,23 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
   const int cnt = geo.chains_of(j);
   const int len = geo.len_of(j);
   const uint8_t* ringj = p.ring + (size_t)j * NSLOT * REC_BYTES;
-  const uint32_t* readyj = p.ready + (size_t)j * NSLOT;
+  const uint32_t* readyj = p.ready + (size_t)j * FLAG_STRIDE;
 
   if (warp < 4) {
-    reg_dealloc<56>();
+    reg_dealloc<RC_CTL>();
     if (warp == 0) {
       // ------------------------------------------------------------ loader
       if (lane == 0) {
         // Up to NBUF copies in flight.  A ring slot is handed back (consumed) once its
         // record has landed in shared memory: at the latest when the buffer is needed
-        // again (then the chunk that used it is done), earlier if the copy is seen landed.
+        // again (then the chunk that used it is done), earlier if the copy is seen landed;
+        // the slots landed by then go back with one release.  The loader's own path per
+        // record is: ready flag, buffer free, proxy fence, copies.
         int issued = 0, rel = 0;
         bool ok = true;
         auto release_to = [&](int n) {
-          fence_proxy_async_all();
-          st_release_u32(p.consumed + j, (uint32_t)n);
+          fence_proxy_async_global();
+          st_release_u32(p.consumed + (size_t)j * FLAG_STRIDE, (uint32_t)n);
           rel = n;
         };
         int s = 0, t = 0, c = 0, ncx = 0;
@@ -357,25 +366,26 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
             c = 0;
           }
           const int b = s % NBUF;
-          if (s >= NBUF) {
-            if (!(ok = wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx))) break;
-            if (rel < s - NBUF + 1) release_to(s - NBUF + 1);
-          }
-          // the K tile does not depend on the record: fetch it first
+          if (!(ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx))) break;
+          if (s >= NBUF && !(ok = wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx))) break;
+          // the producer's plain stores before its release, then our bulk reads
+          fence_proxy_async_global();
           uint8_t* buf = sm + b * C_BUF;
           const int row0 = (int)(bos + (int64_t)c * CHUNK), h = (j + geo.nch * (t - 1)) % H;
-          mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
-          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, h, row0);
-          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, h, row0);
-          issued = s + 1;
-          if (!(ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx))) break;
-          fence_proxy_async_all();
           const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
+          mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, &bars[C_RECFULL + b]);
-          while (rel < s && mbar_test(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1))
-            release_to(rel + 1);
+          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, h, row0);
+          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, h, row0);
+          issued = s + 1;
+          // records up to s - NBUF have landed (their buffers came back); later ones are
+          // tested against their buffers' current phases
+          int n = rel;
+          if (s >= NBUF && n < s - NBUF + 1) n = s - NBUF + 1;
+          while (n < s && mbar_test(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1)) ++n;
+          if (n > rel) release_to(n);
         }
         while (ok && rel < len) {
           if (!(ok = wait_bar(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1, cx))) break;
@@ -434,7 +444,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
       __syncwarp();
     }
   } else if (warp < 12) {
-    reg_alloc<168>();
+    reg_alloc<RC_STATE>();
     // -------------------------------------------------------------- state
     const int st_t = tid - 128;                       // 0..255
     const int w = st_t >> 7;                          // column half
@@ -601,7 +611,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
       sbase += nc;
     }
   } else {
-    reg_dealloc<120>();
+    reg_dealloc<RC_OUT>();
     // -------------------------------------------------------------- output
     const int v = ((warp & 3) << 5) + lane;
     const uint32_t tl = tm + ((uint32_t)((warp & 3) * 32) << 16);
@@ -660,21 +670,175 @@ __device__ __forceinline__ void pack64(const float (&x)[64], uint32_t (&u)[32]) 
 }
 
 // --------------------------------------------------------------------------
-// Preparation CTA.  warp 0: loader (gate/beta and the chunk's decay vectors, then the
-// K/Q/V tiles by TMA); warp 1: MMA issuer; warps 2 and 3: publishers of pipelines 0
-// and 1 (ring-slot check, then the release of a finished record); warps 4-7 and 8-11:
-// two pipelines, each preparing every other item of this CTA; warps 12-15 idle.
+// The chunk's triangular solve on a preparation pipeline (four warps).
+//
+// T = (I + A)^{-1} for the strictly lower 64x64 A (FP32 rows in shared memory, leading
+// dimension SOLVE_LD), delivered as the BF16 B operands T' = T diag(beta) and
+// -T'' = -T diag(beta e^gamma) of the U and W products.  The blocking is that of
+// solve_tc.cuh -- 16x16 diagonal blocks by substitution in FP32, then
+// T_10 = -T_11 A_10 T_00 for the 32x32 halves and for the 64x64 matrix on TF32 mma --
+// arranged for four warps and a single barrier:
+//  phase 1: warp p (p = 0, 1), which wrote rows 32p..32p+31 of A, inverts the half's
+//           two diagonal blocks (lanes 0-15 and 16-31, one column per lane, the block's
+//           A in registers) and merges them into the half's lower-left block;
+//  phase 2: warp w forms block (2 + w/2, w%2) of T[32:64, 0:32] =
+//           -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]).
+// A product whose B operand is the previous product is taken in two steps: first the
+// transpose X^T = N^T M^T of the inner product (both operands from shared memory), then
+// the outer product with X^T's accumulator fragments as its B fragments -- valid once the
+// k index of both outer operands is permuted (k-slot t <-> 2t, t + 4 <-> 2t + 1 within
+// each 8-wide step), which keeps the intermediate in registers.
+// --------------------------------------------------------------------------
+namespace solve {
+
+constexpr int L = SOLVE_LD;
+
+__device__ __forceinline__ void mma4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                     uint32_t a3, uint32_t b0, uint32_t b1) {
+  const uint32_t a[4] = {a0, a1, a2, a3};
+  const uint32_t b[2] = {b0, b1};
+  mma_tf32_16x8x8(d, a, b);
+}
+
+// xt += M^T N^T for 16x16 blocks M (rows k, columns c) and N (rows n, columns k) in shared
+// memory: xt[nt] are the C fragments of the 16x16 result [c][n], n in 8nt..8nt+7.
+__device__ __forceinline__ void acc_tt(float (&xt)[2][4], const float* M, const float* N, int g,
+                                       int t) {
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const float* mk = M + (8 * s + t) * L;
+    const uint32_t a0 = f2tf32(mk[g]), a1 = f2tf32(mk[g + 8]);
+    const uint32_t a2 = f2tf32(mk[4 * L + g]), a3 = f2tf32(mk[4 * L + g + 8]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float* nr = N + (8 * nt + g) * L + 8 * s + t;
+      mma4(xt[nt], a0, a1, a2, a3, f2tf32(nr[0]), f2tf32(nr[4]));
+    }
+  }
+}
+
+// o += M X for a 16x16 block M in shared memory (rows i, columns k) and X given by the C
+// fragments xt[s] of its transpose (X^T[n][k], k in 8s..8s+7); the k-slot permutation
+// makes those fragments X's B fragments.  o[nt]: C fragments of [i][n], n in 8nt..8nt+7.
+__device__ __forceinline__ void acc_nx(float (&o)[2][4], const float* M, const float (&xt)[2][4],
+                                       int g, int t) {
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const float2 r0 = *reinterpret_cast<const float2*>(M + g * L + 8 * s + 2 * t);
+    const float2 r1 = *reinterpret_cast<const float2*>(M + (g + 8) * L + 8 * s + 2 * t);
+    const uint32_t a0 = f2tf32(r0.x), a2 = f2tf32(r0.y), a1 = f2tf32(r1.x), a3 = f2tf32(r1.y);
+    mma4(o[0], a0, a1, a2, a3, f2tf32(xt[s][0]), f2tf32(xt[s][1]));
+    mma4(o[1], a0, a1, a2, a3, f2tf32(xt[s][2]), f2tf32(xt[s][3]));
+  }
+}
+
+// Block (R0.., C0..) of T from the C fragments of -T: FP32 into the T area (when `at`)
+// and the BF16 operands T' and -T''.
+__device__ __forceinline__ void put_block(float* at, uint8_t* t1, uint8_t* t2, const float* vs,
+                                          int R0, int C0, const float (&o)[2][4], int g, int t) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int col = C0 + 8 * nt + 2 * t;
+    const float2 b = *reinterpret_cast<const float2*>(vs + VEC_BETA + col);
+    const float2 e = *reinterpret_cast<const float2*>(vs + VEC_EG + col);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int row = R0 + g + 8 * hf;
+      const float x0 = -o[nt][2 * hf], x1 = -o[nt][2 * hf + 1];
+      if (at) *reinterpret_cast<float2*>(at + row * L + col) = make_float2(x0, x1);
+      const float p0 = x0 * b.x, p1 = x1 * b.y;
+      const uint32_t off = sw128_off(row, col, 8192);
+      *reinterpret_cast<uint32_t*>(t1 + off) = pack_bf16x2(p0, p1);
+      *reinterpret_cast<uint32_t*>(t2 + off) = pack_bf16x2(-p0 * e.x, -p1 * e.y);
+    }
+  }
+}
+
+// Phase 1 for half p (one warp).
+__device__ __forceinline__ void half(float* AT, uint8_t* t1, uint8_t* t2, const float* vs, int p,
+                                     int lane) {
+  {
+    // diagonal block at o: this lane's column m of its inverse, by forward substitution
+    const int m = lane & 15, o = 32 * p + 16 * (lane >> 4);
+    float a[120];                      // A[o + i][o + j], j < i, at i (i - 1) / 2 + j
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+#pragma unroll
+      for (int q = 0; q < (i + 3) / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(AT + (o + i) * L + o + 4 * q);
+        const int b = i * (i - 1) / 2 + 4 * q;
+        a[b] = v.x;
+        if (4 * q + 1 < i) a[b + 1] = v.y;
+        if (4 * q + 2 < i) a[b + 2] = v.z;
+        if (4 * q + 3 < i) a[b + 3] = v.w;
+      }
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = (i == m) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      const float x = acc[j];
+#pragma unroll
+      for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(-a[i * (i - 1) / 2 + j], x, acc[i]);
+    }
+    __syncwarp();                      // every lane has its block's A in registers
+    const float bm = vs[VEC_BETA + o + m], em = vs[VEC_EG + o + m];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      AT[(o + i) * L + o + m] = acc[i];
+      const float p1 = acc[i] * bm;
+      const uint32_t off = sw128_off(o + i, o + m, 8192);
+      *reinterpret_cast<__nv_bfloat16*>(t1 + off) = __float2bfloat16_rn(p1);
+      *reinterpret_cast<__nv_bfloat16*>(t2 + off) = __float2bfloat16_rn(-p1 * em);
+    }
+  }
+  __syncwarp();
+  // T_10 = -T_11 (A_10 T_00): Y^T = T_00^T A_10^T, then T_11 Y
+  const int g = lane >> 2, t = lane & 3, o0 = 32 * p, o1 = o0 + 16;
+  float yt[2][4] = {}, ob[2][4] = {};
+  acc_tt(yt, AT + o0 * L + o0, AT + o1 * L + o0, g, t);
+  acc_nx(ob, AT + o1 * L + o1, yt, g, t);
+  __syncwarp();                        // A_10 read by every lane before T_10 replaces it
+  put_block(AT, t1, t2, vs, o1, o0, ob, g, t);
+}
+
+// Phase 2 for the block (2 + MT, c) of T (one warp).
+template <int MT>
+__device__ __forceinline__ void lower(const float* AT, uint8_t* t1, uint8_t* t2, const float* vs,
+                                      int c, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  // X^T[c][kb] = sum_{j >= c} T[j][c]^T A[2 + kb][j]^T  (16x16 blocks, kb <= MT)
+  float xt[MT + 1][2][4] = {};
+#pragma unroll
+  for (int kb = 0; kb <= MT; ++kb)
+    for (int j = c; j < 2; ++j)
+      acc_tt(xt[kb], AT + 16 * j * L + 16 * c, AT + (32 + 16 * kb) * L + 16 * j, g, t);
+  float ob[2][4] = {};
+#pragma unroll
+  for (int kb = 0; kb <= MT; ++kb) acc_nx(ob, AT + (32 + 16 * MT) * L + 32 + 16 * kb, xt[kb], g, t);
+  put_block(nullptr, t1, t2, vs, 32 + 16 * MT, 16 * c, ob, g, t);
+}
+
+}  // namespace solve
+
+// --------------------------------------------------------------------------
+// Preparation CTA.  Items (chunk records) are claimed one at a time, in stream order,
+// from a grid-wide counter, so that a pipeline waiting for a full ring slot holds up
+// only the chain that slot belongs to.  warps 0 and 2: controllers of pipelines 0 and 1
+// (claim, gate/beta and the chunk's decay vectors, the K/Q/V tiles by TMA, the ring-slot
+// check, the release of the finished record); warps 1 and 3: MMA issuers of pipelines 0
+// and 1; warps 4-7 and 8-11: the two pipelines; warps 12-15 idle.
 // --------------------------------------------------------------------------
 __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                          const CUtensorMap* tmV, const SplitParams& p,
                                          const Geo& geo, uint8_t* sm, uint32_t sb,
                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pc = blockIdx.x - p.nch, H = p.H;
-  const int nk = (pc < geo.total) ? (int)((geo.total - pc + p.nprep - 1) / p.nprep) : 0;
-  // item k of this CTA -> (chain CTA, stream position, head, first row, length)
-  auto item = [&](int k, int& jj, int& s, int& h, int& row0, int& L) {
-    geo.item(pc + (long long)k * p.nprep, jj, s);
+  const int H = p.H;
+  // item g -> (chain CTA, stream position, head, first row, length)
+  auto item = [&](long long g, int& jj, int& s, int& h, int& row0, int& L) {
+    geo.item(g, jj, s);
     int x, c;
     geo.locate(jj, s, x, c);
     int64_t bos, eos;
@@ -688,24 +852,47 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
   };
 
   if (warp < 4) {
-    reg_dealloc<56>();
-    if (warp == 0) {
-      // ------------------------------------------------------------ loader
-      for (int idx = lane; idx < 2 * 512; idx += 32)
-        reinterpret_cast<uint4*>(sm + (idx >> 9) * P_STRIDE + P_DG)[idx & 511] = make_uint4(0, 0, 0, 0);
-      int last[2] = {-1, -1};
-      for (int k = 0; k < nk; ++k) {
-        const int pp = k & 1, use = k >> 1;
+    reg_dealloc<RP_CTL>();
+    if (warp == 0 || warp == 2) {
+      // ------------------------------------------------------------ controller
+      const int pp = warp >> 1;
+      uint8_t* base = sm + pp * P_STRIDE;
+      for (int idx = lane; idx < 512; idx += 32)
+        reinterpret_cast<uint4*>(base + P_DG)[idx] = make_uint4(0, 0, 0, 0);
+      auto claim = [&]() -> long long {
+        int g = 0;
+        if (lane == 0) g = (int)atomicAdd(p.next_item, 1u);
+        return (long long)__shfl_sync(0xffffffffu, g, 0);
+      };
+      auto prefetch = [&](long long g) {
+        if (g >= geo.total || lane != 0) return;
         int jj, s, h, row0, L;
-        item(k, jj, s, h, row0, L);
-        (void)jj;
-        (void)s;
+        item(g, jj, s, h, row0, L);
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl) {
+          tma_prefetch_l2_3d(tmK, 64 * pnl, h, row0);
+          tma_prefetch_l2_3d(tmQ, 64 * pnl, h, row0);
+          tma_prefetch_l2_3d(tmV, 64 * pnl, h, row0);
+        }
+      };
+      int last = -1;                 // last use with a tile copy
+      int pj = -1, ps = 0;           // the previous use's record (chain CTA, position)
+      bool ok = true;
+      long long g = claim();
+      prefetch(g);
+      for (int use = 0; ok; ++use) {
+        const bool done = g >= geo.total;
+        int jj = 0, s = 0, h = 0, row0 = 0, L = 0;
+        if (!done) item(g, jj, s, h, row0, L);
+        // the item after this one (claimed now, so that its tiles can be warmed in L2)
+        const long long gn = done ? g : claim();
+        prefetch(gn);
         // the vector slot is free once the item two uses back has finished (one barrier
         // per slot, so a phase can never be mistaken for the one two items later)
-        if (use >= 2 && !warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx))
+        if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx)))
           break;
         float* vs = vec_of(pp, use);
-        {
+        if (!done) {
           // gamma = in-chunk cumulative gate; decays e^{gamma}, e^{gamma_C - gamma}, and
           // the factors e^{+-(gamma - mid)} (used when the chunk's gamma range is <= 80)
           const int e0 = 2 * lane, e1 = e0 + 1;
@@ -746,58 +933,85 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             vs[VEC_FLAG + 1] = mid;
           }
         }
+        if (lane == 0) reinterpret_cast<int*>(vs)[VEC_ITEM] = done ? -1 : (int)g;
         __syncwarp();
-        if (use >= 1 && !warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx)) break;
-        uint8_t* base = sm + pp * P_STRIDE;
-        // diag(e^gamma), the B operand of Qg^T (the previous item's products are complete)
-        for (int e = lane; e < 64; e += 32)
-          *reinterpret_cast<__nv_bfloat16*>(base + P_DG + sw128_off(e, e, 8192)) =
-              __float2bfloat16_rn(vs[VEC_EG + e]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[P_FULL + pp], 3 * 16384);
-#pragma unroll
-          for (int pnl = 0; pnl < 2; ++pnl) {
-            tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
-            tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + 8192, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
-                        row0);
-            tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULL + pp], 64 * pnl, h, row0);
-          }
-        }
-        mbar_arrive(&bars[P_FULL + pp]);
-        last[pp] = k;
-        if (L < CHUNK) {
-          // rows past the sequence end: zero K, Q and V so they add nothing to any product
-          if (!warp_wait(&bars[P_FULL + pp], use & 1, cx)) break;
-          const int rows = CHUNK - L;
-          for (int idx = lane; idx < 6 * rows * 8; idx += 32) {
-            const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
-            const int row = L + rem / 8, ch = rem % 8, pnl = t6 & 1, which = t6 >> 1;
-            uint8_t* tb = (which == 2) ? base + P_V + pnl * P_V_PANEL
-                                       : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? 8192u : 0u);
-            *reinterpret_cast<uint4*>(tb + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-          }
+        // the pipeline's previous item has had its last product (its tiles are free)
+        if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
+        if (!done) {
+          // diag(e^gamma), the B operand of Qg^T
+          for (int e = lane; e < 64; e += 32)
+            *reinterpret_cast<__nv_bfloat16*>(base + P_DG + sw128_off(e, e, 8192)) =
+                __float2bfloat16_rn(vs[VEC_EG + e]);
           fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[P_FULL + pp], 3 * 16384);
+#pragma unroll
+            for (int pnl = 0; pnl < 2; ++pnl) {
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + 8192, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
+                          row0);
+              tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULL + pp], 64 * pnl, h, row0);
+            }
+          }
+          mbar_arrive(&bars[P_FULL + pp]);
+          last = use;
+          if (L < CHUNK) {
+            // rows past the sequence end: zero K, Q and V so they add nothing to any product
+            if (!(ok = warp_wait(&bars[P_FULL + pp], use & 1, cx))) break;
+            const int rows = CHUNK - L;
+            for (int idx = lane; idx < 6 * rows * 8; idx += 32) {
+              const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
+              const int row = L + rem / 8, ch = rem % 8, pnl = t6 & 1, which = t6 >> 1;
+              uint8_t* tb = (which == 2) ? base + P_V + pnl * P_V_PANEL
+                                         : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? 8192u : 0u);
+              *reinterpret_cast<uint4*>(tb + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[P_HEAD + pp]);
+        // release the previous record once written (before this item's slot check: a
+        // record that its own chain is waiting for must never sit behind that check)
+        if (pj >= 0) {
+          if (!(ok = warp_wait(&bars[P_PUB + pp], (use - 1) & 1, cx))) break;
+          if (lane == 0) st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
+          pj = -1;
+        }
+        if (done) break;
+        // this record's ring slot must have been copied out by its chain CTA
+        if (lane == 0) {
+          ok = s < NSLOT || poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx);
+          if (ok) mbar_arrive(&bars[P_SLOTOK + pp]);
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) {
+          if (lane == 0) raise_abort(cx);
+          break;
+        }
+        pj = jj;
+        ps = s;
+        g = gn;
       }
       // never leave with a tile copy in flight
-      for (int pp = 0; pp < 2; ++pp)
-        if (last[pp] >= 0) mbar_wait(&bars[P_FULL + pp], (last[pp] >> 1) & 1, 100000000ull);
+      if (last >= 0) mbar_wait(&bars[P_FULL + pp], last & 1, 100000000ull);
       __syncwarp();
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0 && nk > 0) {
-        int nK = 0, nQ = 0, nW = 0;
+    } else {
+      // ------------------------------------------------------------ MMA issuers
+      // warp 1 issues pipeline 0's products, warp 3 pipeline 1's, each in its pipeline's
+      // item order (an issue waits for the tensor pipe, so one thread serving both
+      // pipelines would hold each up behind the other).  A pipeline ends at the use
+      // whose item slot says -1.
+      const int pp = warp >> 1;
+      if (lane == 0) {
+        const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+        int uK = 0, uQ = 0, uW = 0;   // next use per product
+        bool fin = false;
         long long t_prog = clock64();
-        while (nW < nk) {
+        while (!(fin && uW == uK)) {
           bool prog = false;
-          if (nW < nK && mbar_test(&bars[P_TT + (nW & 1)], (nW >> 1) & 1)) {
+          if (uW < uK && mbar_test(&bars[P_TT + pp], uW & 1)) {
             tc_fence_after();
-            const int pp = nW & 1;
-            const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
             // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
             const uint64_t ak = sdesc_sw128(base + P_KQ, P_KQ_PANEL, 1024);
             const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
@@ -813,15 +1027,12 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
                        kk > 0 ? 1u : 0u);
             mma_commit(&bars[P_WUDONE + pp]);
             mma_commit(&bars[P_ITEMFREE + pp]);
-            ++nW;
+            ++uW;
             prog = true;
           }
-          // KQ of item nK needs only the KQ accumulator of item nK - 2 read out; its Qg^T
-          // (issued next) needs that item finished
-          if (nQ < nK && mbar_test(&bars[P_TMFREE + (nQ & 1)], ((nQ >> 1) - 1) & 1)) {
+          // Qg^T of an item needs the Qg^T accumulator of the previous item read (TMFREE)
+          if (uQ < uK && (uQ == 0 || mbar_test(&bars[P_TMFREE + pp], (uQ - 1) & 1))) {
             tc_fence_after();
-            const int pp = nQ & 1;
-            const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
             // Qg^T = Q^T diag(e^gamma)
             const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
             const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
@@ -830,15 +1041,19 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
               mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2), ID_AMN,
                        kk > 0 ? 1u : 0u);
             mma_commit(&bars[P_QGDONE + pp]);
-            ++nQ;
+            ++uQ;
             prog = true;
           }
-          if (nK < nk && nK < nW + 2 && nQ == nK) {
-            const int pp = nK & 1, use = nK >> 1;
-            if (mbar_test(&bars[P_HEAD + pp], use & 1) && mbar_test(&bars[P_FULL + pp], use & 1) &&
-                (use == 0 || mbar_test(&bars[P_KQFREE + pp], (use - 1) & 1))) {
+          // KQ of an item: its item slot and vectors are in (HEAD), its tiles are in
+          // (FULL), the previous item has had all its products issued and its KQ
+          // accumulator read out (KQFREE)
+          if (!fin && uW == uK && uQ == uK && mbar_test(&bars[P_HEAD + pp], uK & 1)) {
+            const int gi = reinterpret_cast<const int*>(vec_of(pp, uK))[VEC_ITEM];
+            if (gi < 0) {
+              fin = true;
+            } else if (mbar_test(&bars[P_FULL + pp], uK & 1) &&
+                       (uK == 0 || mbar_test(&bars[P_KQFREE + pp], (uK - 1) & 1))) {
               tc_fence_after();
-              const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
               // KQ = [K; Q] K^T
               const uint64_t bq = sdesc_sw128(base + P_KQ, 0, 1024);
 #pragma unroll
@@ -847,57 +1062,24 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
                 mma_bf16(tp + TP_KQ, d, d, ID_N64, kk > 0 ? 1u : 0u);
               }
               mma_commit(&bars[P_KQDONE + pp]);
-              ++nK;
+              ++uK;
               prog = true;
-              if (use == 0) {
-                // the pipeline's first item: nothing to wait for
-                const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
-                const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2),
-                           ID_AMN, kk > 0 ? 1u : 0u);
-                mma_commit(&bars[P_QGDONE + pp]);
-                ++nQ;
-              }
             }
           }
           if (prog) {
             t_prog = clock64();
-          } else if (aborted(cx) || clock64() - t_prog > kWaitLimitCycles) {
+          } else if (*cx.abort_l || clock64() - t_prog > kWaitLimitCycles) {
             raise_abort(cx);
             break;
           } else {
-            __nanosleep(64);   // leave the issue slots to the pipelines meanwhile
+            __nanosleep(16);   // leave most issue slots to the pipelines meanwhile
           }
-        }
-      }
-      __syncwarp();
-    } else {
-      // ------------------------------------------------------------ publishers
-      const int pp = warp - 2;
-      if (lane == 0) {
-        for (int k = pp; k < nk; k += 2) {
-          const int use = k >> 1;
-          int jj, s, h, row0, L;
-          item(k, jj, s, h, row0, L);
-          // the record's ring slot must have been copied out by its chain CTA
-          if (s >= NSLOT && !poll_ge(p.consumed + jj, (uint32_t)(s - NSLOT + 1), cx)) {
-            raise_abort(cx);
-            break;
-          }
-          mbar_arrive(&bars[P_SLOTOK + pp]);
-          if (!wait_bar(&bars[P_PUB + pp], use & 1, cx)) {
-            raise_abort(cx);
-            break;
-          }
-          st_release_u32(p.ready + (size_t)jj * NSLOT + s % NSLOT, (uint32_t)s + 1);
         }
       }
       __syncwarp();
     }
   } else if (warp < 12) {
-    reg_alloc<216>();
+    reg_alloc<RP_PIPE>();
     // ---------------------------------------------------------- pipelines
     const int pp = (warp - 4) >> 2;
     const int r = ((warp & 3) << 5) + lane;          // TMEM lane
@@ -905,20 +1087,28 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     const uint32_t tl = tm + 256 * pp + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t* base = sm + pp * P_STRIDE;
     float* AT = reinterpret_cast<float*>(base + P_AT);
-    float* X = reinterpret_cast<float*>(base + P_X);
-    // the A/T area, once T' and T'' are built, is this warp's store staging (4 KB)
+    // the A/T area, once T' and T'' are built, is this warp's store staging (4 KB); the
+    // Ahat rows, stored during phase 1 of the solve, are staged in the X area
     uint8_t* stage = base + P_AT + (warp & 3) * 4096;
+    uint8_t* stage_ah = base + P_X + ((warp & 3) - 2) * 4096;
+    // T' and -T'' are zero above the diagonal blocks for every item: the solve writes only
+    // the blocks on and below the diagonal
+    for (int idx = r; idx < 2 * 512; idx += 128)
+      reinterpret_cast<uint4*>(base + P_T1)[idx] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     bool ok = true;
-    for (int k = pp; k < nk && ok; k += 2) {
-      const int use = k >> 1;
+    for (int use = 0; ok; ++use) {
+      const float* vs = vec_of(pp, use);
+      // the controller's item slot and vectors for this use (HEAD), then the chunk's
+      // [K;Q] K^T
+      if (!(ok = group_wait(&bars[P_HEAD + pp], use & 1, bid, 128, cx))) break;
+      const int gi = reinterpret_cast<const int*>(vs)[VEC_ITEM];
+      if (gi < 0) break;
       int jj, s, h, row0, L;
-      item(k, jj, s, h, row0, L);
+      item(gi, jj, s, h, row0, L);
       (void)h;
       (void)row0;
       (void)L;
-      const float* vs = vec_of(pp, use);
-      // the loader's vectors for this item (HEAD) and the chunk's [K;Q] K^T
-      if (!(ok = group_wait(&bars[P_HEAD + pp], use & 1, bid, 128, cx))) break;
       if (!(ok = group_wait(&bars[P_KQDONE + pp], use & 1, bid, 128, cx))) break;
       tc_fence_after();
       uint32_t ah[32];     // rows 64-127: this row of Ahat (BF16 pairs), stored at the end
@@ -944,13 +1134,13 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
 #pragma unroll
           for (int jx = 0; jx < 64; ++jx) x[jx] *= bi * expf(jx <= i ? gi - vs[VEC_GAM + jx] : 0.f);
         }
-        if (r < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i
+        if (r < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i (the solve
+                               // reads nothing on or above the diagonal)
           float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD);
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const int jx = 4 * j4;
-            row[j4] = make_float4(jx < i ? x[jx] : 0.f, jx + 1 < i ? x[jx + 1] : 0.f,
-                                  jx + 2 < i ? x[jx + 2] : 0.f, jx + 3 < i ? x[jx + 3] : 0.f);
+            if (jx < i) row[j4] = make_float4(x[jx], x[jx + 1], x[jx + 2], x[jx + 3]);
           }
         } else {               // Ahat_ij = Gamma_ij (q_i . k_j), j <= i
 #pragma unroll
@@ -959,35 +1149,32 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           pack64(x, ah);
         }
       }
+      // this warp's part of the KQ accumulator is read out (four arrivals)
       tc_fence_before();
-      named_bar(bid, 128);
-      if (r == 0) mbar_arrive(&bars[P_KQFREE + pp]);
-      // T = (I + A)^{-1}; T' = T diag(beta), -T'' = -T diag(beta e^gamma)
-      solve64_tc_inplace(AT, X, r, 128, NamedBar{bid, 128});
-      for (int idx = r; idx < 64 * 8; idx += 128) {
-        const int i = idx >> 3, cg = (idx & 7) * 8;
-        const float4* tr = reinterpret_cast<const float4*>(AT + i * SOLVE_LD + cg);
-        const float4* b4 = reinterpret_cast<const float4*>(vs + VEC_BETA + cg);
-        const float4* g4 = reinterpret_cast<const float4*>(vs + VEC_EG + cg);
-        float t1[8], t2[8];
-#pragma unroll
-        for (int h4 = 0; h4 < 2; ++h4) {
-          const float4 tv = tr[h4], bv = b4[h4], gv = g4[h4];
-          t1[4 * h4] = tv.x * bv.x; t1[4 * h4 + 1] = tv.y * bv.y;
-          t1[4 * h4 + 2] = tv.z * bv.z; t1[4 * h4 + 3] = tv.w * bv.w;
-          t2[4 * h4] = -t1[4 * h4] * gv.x; t2[4 * h4 + 1] = -t1[4 * h4 + 1] * gv.y;
-          t2[4 * h4 + 2] = -t1[4 * h4 + 2] * gv.z; t2[4 * h4 + 3] = -t1[4 * h4 + 3] * gv.w;
-        }
-        st_row8_bf16(base + P_T1, i, cg, 8192, t1);
-        st_row8_bf16(base + P_T2, i, cg, 8192, t2);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[P_KQFREE + pp]);
+      // T = (I + A)^{-1} as T' = T diag(beta) and -T'' = -T diag(beta e^gamma).  Phase 1
+      // needs only the rows this warp wrote; meanwhile the Ahat warps store their rows to
+      // the record's ring slot once the publisher has seen it free (s % NSLOT).
+      uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
+      bool ok1 = true;
+      if (r < 64) {
+        solve::half(AT, base + P_T1, base + P_T2, vs, warp & 3, lane);
+      } else {
+        ok1 = __all_sync(0xffffffffu, wait_bar(&bars[P_SLOTOK + pp], use & 1, cx)) != 0;
+        if (ok1) store_rows(rec + R_AH, stage_ah, (warp & 3) * 32 - 64, ah, lane);
       }
+      if (!(ok = named_bar_and(bid, 128, ok1))) {
+        if (r == 0) raise_abort(cx);
+        break;
+      }
+      if ((warp & 3) < 2)
+        solve::lower<0>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
+      else
+        solve::lower<1>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
       fence_proxy_async_smem();
       named_bar(bid, 128);
       if (r == 0) mbar_arrive(&bars[P_TT + pp]);
-      // the record goes to ring slot s % NSLOT once the publisher has seen it free
-      if (!(ok = group_wait(&bars[P_SLOTOK + pp], use & 1, bid, 128, cx))) break;
-      uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
-      if (r >= 64) store_rows(rec + R_AH, stage, (warp & 3) * 32 - 64, ah, lane);
       if (!(ok = group_wait(&bars[P_QGDONE + pp], use & 1, bid, 128, cx))) break;
       tc_fence_after();
       {
@@ -1020,7 +1207,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       }
     }
   } else {
-    reg_dealloc<24>();
+    reg_dealloc<RP_IDLE>();
   }
 }
 
@@ -1053,6 +1240,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
       mbar_init(&bars[P_FULL], 33);
       mbar_init(&bars[P_FULL + 1], 33);
+      mbar_init(&bars[P_KQFREE], 4);
+      mbar_init(&bars[P_KQFREE + 1], 4);
     }
     *abort_l = 0;
     fence_mbar_init();
@@ -1115,12 +1304,14 @@ __global__ void split_setup_kernel(const SplitParams p) {
   }
 }
 
-// Workspace: [0, 256) status word; [256, 260) abort flag; [512, 768) consumed[MAX_NCH];
-// ready[MAX_NCH][NSLOT] from 768; the ring from 4096; then (packed inputs) the chain
-// stream starts [N*H], stream lengths [64] and their order [64].
-constexpr size_t WS_ABORT = 256, WS_CONSUMED = 512, WS_READY = 768;
-constexpr size_t WS_FLAGS_END = WS_READY + (size_t)MAX_NCH * NSLOT * 4;
-constexpr size_t WS_RING = 4096;
+// Workspace: [0, 256) status word; [256, 260) abort flag; [384, 388) the item counter of
+// the preparation CTAs; from 512 consumed, then ready
+// (one 128-byte line per chain CTA each: the flags polled by different CTAs never share
+// a line); the ring from 20480; then (packed inputs) the chain stream starts [N*H],
+// stream lengths [64] and their order [64].
+constexpr size_t WS_ABORT = 256, WS_NEXT = 384, WS_CONSUMED = 512, WS_READY = WS_CONSUMED + MAX_NCH * 128;
+constexpr size_t WS_FLAGS_END = WS_READY + (size_t)MAX_NCH * 128;
+constexpr size_t WS_RING = 20480;
 static_assert(WS_FLAGS_END <= WS_RING, "workspace flags");
 
 }  // namespace
@@ -1165,6 +1356,7 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaS
   p.status = status;
   p.ckpt = cp.ckpt;
   p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
+  p.next_item = reinterpret_cast<uint32_t*>(w + WS_NEXT);
   p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
   p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
   p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);

@@ -133,6 +133,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
+// Warms L2 with a tile that a later tma_load_3d of the same box will read (no completion
+// signal; coordinates outside the tensor are ignored).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -145,6 +153,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // e.g. a flag acquire, against its later async-proxy copies, and back).
 __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
+}
+// Orders this thread's generic-proxy and async-proxy accesses to global memory only (no
+// wait on its shared-memory async operations in flight).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of
 // 16); completes `bytes` of transaction count on `bar`.
