@@ -140,7 +140,7 @@ enum {
   C_OFREE = 13,    // [2] out: O of a TMEM buffer read
   C_COUNT = 15,
   // preparation CTA
-  P_FULL = 0,      // [2] tiles + gate/beta landed (33 arrivals + tx)
+  P_FULL = 0,      // [2] K and Q tiles landed, diag(e^gamma) written (33 arrivals + tx)
   P_HEAD = 2,      // [2] loader: decay vectors, diag(e^gamma), padding rows zeroed
   P_KQDONE = 4,    // [2]
   P_QGDONE = 6,    // [2]
@@ -148,11 +148,12 @@ enum {
   P_WUDONE = 10,   // [2]
   P_ITEMFREE = 12, // [2] MMA commit after the item's last product (tiles free)
   P_TMFREE = 14,   // [2] item finished: TMEM region read out, vector slot free
-  P_PUB = 16,      // [2] item's record written: the publisher may release it
+  P_PUB = 16,      // [2] item's record landed (one arrival per warp): it may be released
   P_SLOTOK = 18,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
   P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
   P_VECFREE = 22,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
-  P_COUNT = 26
+  P_FULLV = 26,    // [2] V tile landed (tx)
+  P_COUNT = 28
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
 
@@ -645,21 +646,39 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
 }
 
 // One warp stores 32 consecutive rows (row0 % 32 == 0, this lane's row = row0 + lane) of a
-// panel-layout BF16 tile into global memory with full-line writes: each lane parks its
-// 128-byte line in the warp's 4 KB of shared memory (already in the tile's swizzled
-// order), then every store instruction writes four whole lines.
+// panel-layout BF16 tile into global memory: each lane parks its 128-byte line in the
+// warp's 4 KB of shared memory (already in the tile's swizzled order), and lane 0 sends
+// the 4 KB with one bulk copy (whole lines into L2).  The staging area is reused only
+// after the previous copy from it has been read; record_landed() waits for every copy.
 __device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* stage, int row0,
                                            const uint32_t (&u)[32], int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
   uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll
   for (int e = 0; e < 8; ++e)
     mine[e ^ (lane & 7)] = make_uint4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+  fence_proxy_async_smem();
   __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int ln = 4 * it + (lane >> 3);
-    const uint4 v = reinterpret_cast<const uint4*>(stage + ln * 128)[lane & 7];
-    reinterpret_cast<uint4*>(gtile + (size_t)(row0 + ln) * 128)[lane & 7] = v;
+  if (lane == 0) {
+    bulk_s2g(gtile + (size_t)row0 * 128, stage, 4096);
+    bulk_commit();
+  }
+}
+
+// The warp's record stores have read their staging areas.
+__device__ __forceinline__ void record_read(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+
+// The warp's record stores have landed in global memory; then lane 0 counts the warp in
+// on `pub` (four arrivals: the record may be released).
+__device__ __forceinline__ void record_landed(int lane, uint64_t* pub) {
+  if (lane == 0) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+    mbar_arrive(pub);
   }
   __syncwarp();
 }
@@ -859,34 +878,46 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       uint8_t* base = sm + pp * P_STRIDE;
       for (int idx = lane; idx < 512; idx += 32)
         reinterpret_cast<uint4*>(base + P_DG)[idx] = make_uint4(0, 0, 0, 0);
-      auto claim = [&]() -> long long {
+      auto claim = [&]() -> int {
         int g = 0;
         if (lane == 0) g = (int)atomicAdd(p.next_item, 1u);
-        return (long long)__shfl_sync(0xffffffffu, g, 0);
+        return __shfl_sync(0xffffffffu, g, 0);
       };
-      auto prefetch = [&](long long g) {
-        if (g >= geo.total || lane != 0) return;
-        int jj, s, h, row0, L;
-        item(g, jj, s, h, row0, L);
+      // An item's geometry, its gate/beta values (two tokens per lane, loaded one use
+      // ahead so that their latency overlaps the waits), and its tiles warmed in L2.
+      struct Next {
+        int g, jj, s, h, row0, L;
+        float g0, g1, b0, b1;
+      };
+      auto fetch = [&](int g) {
+        Next n{g, 0, 0, 0, 0, 0, 0.f, 0.f, 0.f, 0.f};
+        if (g >= geo.total) return n;
+        item(g, n.jj, n.s, n.h, n.row0, n.L);
+        const int e0 = 2 * lane, e1 = e0 + 1;
+        const size_t o0 = (size_t)(n.row0 + e0) * H + n.h, o1 = (size_t)(n.row0 + e1) * H + n.h;
+        if (e0 < n.L) { n.g0 = p.g[o0]; n.b0 = p.beta[o0]; }
+        if (e1 < n.L) { n.g1 = p.g[o1]; n.b1 = p.beta[o1]; }
+        if (lane == 0) {
 #pragma unroll
-        for (int pnl = 0; pnl < 2; ++pnl) {
-          tma_prefetch_l2_3d(tmK, 64 * pnl, h, row0);
-          tma_prefetch_l2_3d(tmQ, 64 * pnl, h, row0);
-          tma_prefetch_l2_3d(tmV, 64 * pnl, h, row0);
+          for (int pnl = 0; pnl < 2; ++pnl) {
+            tma_prefetch_l2_3d(tmK, 64 * pnl, n.h, n.row0);
+            tma_prefetch_l2_3d(tmQ, 64 * pnl, n.h, n.row0);
+            tma_prefetch_l2_3d(tmV, 64 * pnl, n.h, n.row0);
+          }
         }
+        return n;
       };
       int last = -1;                 // last use with a tile copy
       int pj = -1, ps = 0;           // the previous use's record (chain CTA, position)
       bool ok = true;
-      long long g = claim();
-      prefetch(g);
+      // items are claimed two uses ahead: `cur` is this use's, `nxt` the next one's
+      Next cur = fetch(claim());
+      int gnn = claim();
       for (int use = 0; ok; ++use) {
-        const bool done = g >= geo.total;
-        int jj = 0, s = 0, h = 0, row0 = 0, L = 0;
-        if (!done) item(g, jj, s, h, row0, L);
-        // the item after this one (claimed now, so that its tiles can be warmed in L2)
-        const long long gn = done ? g : claim();
-        prefetch(gn);
+        const bool done = cur.g >= geo.total;
+        const Next nxt = fetch(done ? cur.g : gnn);
+        if (!done && nxt.g < geo.total) gnn = claim();
+        const int jj = cur.jj, s = cur.s, h = cur.h, row0 = cur.row0, L = cur.L;
         // the vector slot is free once the item two uses back has finished (one barrier
         // per slot, so a phase can never be mistaken for the one two items later)
         if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx)))
@@ -896,9 +927,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           // gamma = in-chunk cumulative gate; decays e^{gamma}, e^{gamma_C - gamma}, and
           // the factors e^{+-(gamma - mid)} (used when the chunk's gamma range is <= 80)
           const int e0 = 2 * lane, e1 = e0 + 1;
-          const size_t o0 = (size_t)(row0 + e0) * H + h, o1 = (size_t)(row0 + e1) * H + h;
-          const float g0 = e0 < L ? p.g[o0] : 0.f, g1 = e1 < L ? p.g[o1] : 0.f;
-          const float b0 = e0 < L ? p.beta[o0] : 0.f, b1 = e1 < L ? p.beta[o1] : 0.f;
+          const float g0 = cur.g0, g1 = cur.g1, b0 = cur.b0, b1 = cur.b1;
           float sum = g0 + g1;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -933,7 +962,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             vs[VEC_FLAG + 1] = mid;
           }
         }
-        if (lane == 0) reinterpret_cast<int*>(vs)[VEC_ITEM] = done ? -1 : (int)g;
+        if (lane == 0) reinterpret_cast<int*>(vs)[VEC_ITEM] = done ? -1 : cur.g;
         __syncwarp();
         // the pipeline's previous item has had its last product (its tiles are free)
         if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
@@ -945,20 +974,25 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[P_FULL + pp], 3 * 16384);
+            // K and Q first (the first product needs only them), V on its own barrier
+            mbar_arrive_expect_tx(&bars[P_FULL + pp], 2 * 16384);
 #pragma unroll
             for (int pnl = 0; pnl < 2; ++pnl) {
               tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
               tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + 8192, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
                           row0);
-              tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULL + pp], 64 * pnl, h, row0);
             }
+            mbar_arrive_expect_tx(&bars[P_FULLV + pp], 16384);
+#pragma unroll
+            for (int pnl = 0; pnl < 2; ++pnl)
+              tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULLV + pp], 64 * pnl, h, row0);
           }
           mbar_arrive(&bars[P_FULL + pp]);
           last = use;
           if (L < CHUNK) {
             // rows past the sequence end: zero K, Q and V so they add nothing to any product
-            if (!(ok = warp_wait(&bars[P_FULL + pp], use & 1, cx))) break;
+            if (!(ok = warp_wait(&bars[P_FULL + pp], use & 1, cx) && warp_wait(&bars[P_FULLV + pp], use & 1, cx)))
+              break;
             const int rows = CHUNK - L;
             for (int idx = lane; idx < 6 * rows * 8; idx += 32) {
               const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
@@ -991,10 +1025,13 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         }
         pj = jj;
         ps = s;
-        g = gn;
+        cur = nxt;
       }
       // never leave with a tile copy in flight
-      if (last >= 0) mbar_wait(&bars[P_FULL + pp], last & 1, 100000000ull);
+      if (last >= 0) {
+        mbar_wait(&bars[P_FULL + pp], last & 1, 100000000ull);
+        mbar_wait(&bars[P_FULLV + pp], last & 1, 100000000ull);
+      }
       __syncwarp();
     } else {
       // ------------------------------------------------------------ MMA issuers
@@ -1010,7 +1047,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         long long t_prog = clock64();
         while (!(fin && uW == uK)) {
           bool prog = false;
-          if (uW < uK && mbar_test(&bars[P_TT + pp], uW & 1)) {
+          if (uW < uK && mbar_test(&bars[P_TT + pp], uW & 1) && mbar_test(&bars[P_FULLV + pp], uW & 1)) {
             tc_fence_after();
             // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
             const uint64_t ak = sdesc_sw128(base + P_KQ, P_KQ_PANEL, 1024);
@@ -1097,11 +1134,14 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       reinterpret_cast<uint4*>(base + P_T1)[idx] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     bool ok = true;
+    bool pend = false;     // the previous item's record stores may be in flight
     for (int use = 0; ok; ++use) {
       const float* vs = vec_of(pp, use);
       // the controller's item slot and vectors for this use (HEAD), then the chunk's
-      // [K;Q] K^T
+      // [K;Q] K^T; meanwhile the previous record's stores land (then it may be released)
       if (!(ok = group_wait(&bars[P_HEAD + pp], use & 1, bid, 128, cx))) break;
+      if (pend) record_landed(lane, &bars[P_PUB + pp]);
+      pend = false;
       const int gi = reinterpret_cast<const int*>(vs)[VEC_ITEM];
       if (gi < 0) break;
       int jj, s, h, row0, L;
@@ -1198,14 +1238,18 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       }
       if (r < 64) reinterpret_cast<float*>(rec + R_VEC)[r] = vs[VEC_DEC + r];
       if (r == 0) reinterpret_cast<float*>(rec + R_VEC)[64] = vs[VEC_EG + 63];
+      record_read(lane);     // the A/T and X areas are written again by the next item
+      pend = true;
       tc_fence_before();
       named_bar(bid, 128);
       if (r == 0) {
-        mbar_arrive(&bars[P_PUB + pp]);
         mbar_arrive(&bars[P_TMFREE + pp]);
         mbar_arrive(&bars[P_VECFREE + 2 * pp + (use & 1)]);
       }
     }
+    // the last record (and, on the abort path, every bulk store) lands before leaving
+    if (pend) record_landed(lane, &bars[P_PUB + pp]);
+    else if (lane == 0) bulk_wait_all();
   } else {
     reg_dealloc<RP_IDLE>();
   }
@@ -1242,6 +1286,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       mbar_init(&bars[P_FULL + 1], 33);
       mbar_init(&bars[P_KQFREE], 4);
       mbar_init(&bars[P_KQFREE + 1], 4);
+      mbar_init(&bars[P_PUB], 4);
+      mbar_init(&bars[P_PUB + 1], 4);
     }
     *abort_l = 0;
     fence_mbar_init();
