@@ -26,6 +26,11 @@ namespace {
 
 using namespace mt;
 constexpr int NTB = 256;   // 8 warps
+// Leading dimensions (floats) of the FP32 tiles: 4 mod 32, so that the mma fragment loads
+// (8 rows x 4 columns per instruction) fall on distinct banks.
+constexpr int C_LD6 = 68;
+template <int D>
+constexpr int c_ldd() { return D + 4; }
 
 struct CtaBarB {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
@@ -68,7 +73,7 @@ __host__ __device__ constexpr size_t fac_bytes() { return 4 * (64 * 64 + 64 * D 
 
 template <int D>
 __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p, float* fac) {
-  constexpr int LDI = D + 8, LD6 = 65, NTD = D / 8, TD = 4 * NTD / 8;
+  constexpr int LDI = D + 8, LD6 = C_LD6, NTD = D / 8, TD = 4 * NTD / 8;
   extern __shared__ float sm[];
   float* sA = sm;                 // A = diag(beta) Ak, then scratch of the solve
   float* sT = sA + 64 * LD6;
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
 // Reverse chain: grid (D / BV, H, N); CTA (rv, h, n) owns cotangent rows [BV rv, BV rv + BV).
 template <int D, int BV>
 __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p, const float* fac) {
-  constexpr int LDS = D + 1, LD6 = 65, LDI = D + 8, LDO = BV + 8, LDW = D + 1;
+  constexpr int LDS = c_ldd<D>(), LD6 = C_LD6, LDI = D + 8, LDO = BV + 8, LDW = c_ldd<D>();
   constexpr int MB = BV / 16;                 // 16-row bands of the cotangent tile
   constexpr int T64 = MB * 8 / 8;             // tiles per warp of a BV x 64 output
   constexpr int TDD = MB * (D / 8) / 8;       // tiles per warp of a BV x D output
@@ -255,14 +260,14 @@ template <int D>
 static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slots, cudaStream_t st) {
   constexpr int BV = 32;
   {
-    const size_t smem = sizeof(float) * (3 * 64 * 65 + 4 * 64) + 2 * 2 * 64 * (D + 8);
+    const size_t smem = sizeof(float) * (3 * 64 * C_LD6 + 4 * 64) + 2 * 2 * 64 * (D + 8);
     auto kern = mma_bwd_factor_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTB, smem, st>>>(p, fac);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const size_t smem = sizeof(float) * (BV * (D + 1) + BV * 65 + 64 * 65 + 64 * (D + 1) + 128) +
+  const size_t smem = sizeof(float) * (BV * c_ldd<D>() + BV * C_LD6 + 64 * C_LD6 + 64 * c_ldd<D>() + 128) +
                       2 * (2 * 64 * (D + 8) + 64 * (BV + 8));
   auto kern = mma_bwd_chain_kernel<D, BV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -28,6 +28,11 @@ namespace {
 
 using namespace mt;
 constexpr int NTG = 256;   // 8 warps
+// Leading dimensions (floats) of the FP32 tiles: 4 mod 32, so that the mma fragment loads
+// (8 rows x 4 columns per instruction) fall on distinct banks.
+constexpr int G_LD6 = 68;
+template <int D>
+constexpr int g_ldf() { return D + 4; }
 
 struct CtaBarG {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
@@ -38,8 +43,8 @@ struct CtaBarG {
 template <typename Tin, int D>
 __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) {
   constexpr int LDI = D + 8;      // input tiles (Tin)
-  constexpr int LDF = D + 1;      // fp32 [64][D] tiles
-  constexpr int LD6 = 65;
+  constexpr int LDF = g_ldf<D>();  // fp32 [64][D] tiles
+  constexpr int LD6 = G_LD6;
   constexpr int NTD = D / 8;      // 8-column tiles of a 64 x D output
   constexpr int TD = 4 * NTD / 8; // tiles per warp of a 64 x D output
   extern __shared__ float sm[];
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
 
 template <typename Tin, int D>
 static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
-  const size_t smem = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 11 * 64) +
+  const size_t smem = sizeof(float) * (3 * 64 * G_LD6 + 3 * 64 * g_ldf<D>() + 11 * 64) +
                       sizeof(Tin) * 4 * 64 * (D + 8);
   auto kern = mma_bwd_grad_kernel<Tin, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
