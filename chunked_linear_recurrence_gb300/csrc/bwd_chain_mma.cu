@@ -30,7 +30,7 @@ constexpr int NTB = 256;   // 8 warps
 // (8 rows x 4 columns per instruction) fall on distinct banks.
 constexpr int C_LD6 = 68;
 template <int D>
-constexpr int c_ldd() { return D + 4; }
+__host__ __device__ constexpr int c_ldd() { return D + 4; }
 
 struct CtaBarB {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
@@ -143,24 +143,46 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
   }
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Shared-memory operands of one chunk of the reverse chain (two of them: the next chunk's
+// arrive while the current one is used).
+template <int D, int BV>
+struct ChainBuf {
+  static constexpr int LDI = D + 8, LDO = BV + 8;
+  static constexpr size_t Q = 0;                                   // [64][LDI] bf16
+  static constexpr size_t K = Q + 2 * 64 * LDI;                    // [64][LDI] bf16
+  static constexpr size_t W = K + 2 * 64 * LDI;                    // [64][c_ldd] f32
+  static constexpr size_t AQK = W + 4 * 64 * c_ldd<D>();           // [64][C_LD6] f32
+  static constexpr size_t DO = AQK + 4 * 64 * C_LD6;               // [64][LDO] bf16
+  static constexpr size_t VEC = DO + 2 * 64 * LDO;                 // e^gamma [64], dec [64]
+  static constexpr size_t BYTES = VEC + 4 * 128;
+  static_assert(K % 16 == 0 && W % 16 == 0 && AQK % 16 == 0 && DO % 16 == 0 && VEC % 16 == 0 &&
+                    BYTES % 16 == 0,
+                "16-byte copies");
+};
+
 // Reverse chain: grid (D / BV, H, N); CTA (rv, h, n) owns cotangent rows [BV rv, BV rv + BV).
 template <int D, int BV>
 __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p, const float* fac) {
-  constexpr int LDS = c_ldd<D>(), LD6 = C_LD6, LDI = D + 8, LDO = BV + 8, LDW = c_ldd<D>();
+  using B = ChainBuf<D, BV>;
+  constexpr int LDS = c_ldd<D>(), LD6 = C_LD6, LDI = B::LDI, LDO = B::LDO, LDW = c_ldd<D>();
   constexpr int MB = BV / 16;                 // 16-row bands of the cotangent tile
   constexpr int T64 = MB * 8 / 8;             // tiles per warp of a BV x 64 output
   constexpr int TDD = MB * (D / 8) / 8;       // tiles per warp of a BV x D output
   static_assert(MB * 8 % 8 == 0 && MB * (D / 8) % 8 == 0, "tiles per warp");
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* dS = sm;                             // [BV][LDS] running cotangent rows
   float* dDT = dS + BV * LDS;                 // [BV][LD6] dDelta^T
-  float* sAqk = dDT + BV * LD6;               // [64][LD6]
-  float* sW = sAqk + 64 * LD6;                // [64][LDW]
-  float* sdec = sW + 64 * LDW;
-  float* ssc = sdec + 64;                     // scale e^gamma
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(ssc + 64);
-  __nv_bfloat16* sK = sQ + 64 * LDI;
-  __nv_bfloat16* sdO = sK + 64 * LDI;         // [64][LDO]: dO rows, columns [r0, r0 + BV)
+  uint8_t* bufs = reinterpret_cast<uint8_t*>(dDT + BV * LD6);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, n = blockIdx.z, r0 = blockIdx.x * BV, H = p.H;
@@ -173,44 +195,73 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
   const int64_t nc = n_chunks(eos - bos);
   const int64_t slot0 = chunk_slot_base(n, p.B, p.T, p.cu);
 
+  // chunk ci's operands into buffer `buf` (one commit group)
+  auto stage = [&](int64_t ci, int buf) {
+    uint8_t* base = bufs + (size_t)buf * B::BYTES;
+    const int64_t c0 = bos + ci * CHUNK;
+    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+    const float* f = fac + ((size_t)(slot0 + ci) * H + h) * (fac_bytes<D>() / 4);
+    constexpr int QP = D / 8;                 // 16-byte pieces per q/k row
+    for (int idx = tid; idx < 64 * QP; idx += NTB) {
+      const int i = idx / QP, c = (idx % QP) * 8;
+      const size_t off = ((size_t)(c0 + (i < L ? i : 0)) * H + h) * D + c;
+      const int nb = i < L ? 16 : 0;
+      cp_async16(base + B::Q + 2 * (i * LDI + c), q + off, nb);
+      cp_async16(base + B::K + 2 * (i * LDI + c), k + off, nb);
+    }
+    constexpr int WP = D / 4;                 // 16-byte pieces per W row
+    for (int idx = tid; idx < 64 * WP; idx += NTB) {
+      const int i = idx / WP, c = (idx % WP) * 4;
+      cp_async16(base + B::W + 4 * (i * LDW + c), f + 64 * 64 + i * D + c, 16);
+    }
+    for (int idx = tid; idx < 64 * 16; idx += NTB) {
+      const int i = idx >> 4, c = (idx & 15) * 4;
+      cp_async16(base + B::AQK + 4 * (i * LD6 + c), f + i * 64 + c, 16);
+    }
+    constexpr int OP = BV / 8;                // 16-byte pieces per dO row segment
+    for (int idx = tid; idx < 64 * OP; idx += NTB) {
+      const int i = idx / OP, c = (idx % OP) * 8;
+      const size_t off = ((size_t)(c0 + (i < L ? i : 0)) * H + h) * D + r0 + c;
+      cp_async16(base + B::DO + 2 * (i * LDO + c), dO + off, i < L ? 16 : 0);
+    }
+    if (tid < 32) cp_async16(base + B::VEC + 16 * tid, f + 64 * 64 + 64 * D + 4 * tid, 16);
+    cp_async_commit();
+  };
+
   for (int idx = tid; idx < BV * D; idx += NTB) {
     const int r = idx / D, c = idx % D;
     dS[r * LDS + c] = p.dsf ? p.dsf[(((size_t)n * H + h) * D + r0 + r) * D + c] : 0.f;
   }
-  const auto dOT = view(sdO, 1, LDO);        // dO^T (v, i)
+  if (nc > 0) stage(nc - 1, 0);
   for (int64_t ci = nc - 1; ci >= 0; --ci) {
-    const int64_t c0 = bos + ci * CHUNK;
-    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+    const int buf = (int)((nc - 1 - ci) & 1);
     const size_t slot = (size_t)(slot0 + ci);
-    const float* f = fac + (slot * H + h) * (fac_bytes<D>() / 4);
-    __syncthreads();
+    __syncthreads();                          // the other buffer's last reader is done
+    if (ci > 0) {
+      stage(ci - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();                          // this chunk's operands have landed
+    const uint8_t* base = bufs + (size_t)buf * B::BYTES;
+    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(base + B::Q);
+    const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(base + B::K);
+    const float* sW = reinterpret_cast<const float*>(base + B::W);
+    const float* sAqk = reinterpret_cast<const float*>(base + B::AQK);
+    const __nv_bfloat16* sdO = reinterpret_cast<const __nv_bfloat16*>(base + B::DO);
+    const float* seg = reinterpret_cast<const float*>(base + B::VEC);
+    const float* sdec = seg + 64;
+    const auto dOT = view(sdO, 1, LDO);       // dO^T (v, i)
     {
-      float* dst = p.tape + (slot * H + h) * D * D;
-      for (int idx = tid; idx < BV * D; idx += NTB) {
-        const int r = idx / D, c = idx % D;
-        dst[(size_t)(r0 + r) * D + c] = dS[r * LDS + c];
+      float4* dst = reinterpret_cast<float4*>(p.tape + (slot * H + h) * D * D + (size_t)r0 * D);
+      for (int idx = tid; idx < BV * D / 4; idx += NTB) {
+        const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+        dst[idx] = make_float4(dS[r * LDS + c], dS[r * LDS + c + 1], dS[r * LDS + c + 2],
+                               dS[r * LDS + c + 3]);
       }
     }
-    for (int idx = tid; idx < 64 * D; idx += NTB) {
-      const int i = idx / D, c = idx % D;
-      const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
-      const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-      sQ[i * LDI + c] = (i < L) ? q[off] : z;
-      sK[i * LDI + c] = (i < L) ? k[off] : z;
-      sW[i * LDW + c] = f[64 * 64 + i * D + c];
-    }
-    for (int idx = tid; idx < 64 * BV; idx += NTB) {
-      const int i = idx / BV, c = idx % BV;
-      sdO[i * LDO + c] = (i < L) ? dO[((size_t)(c0 + i) * H + h) * D + r0 + c]
-                                 : __float2bfloat16_rn(0.f);
-    }
-    for (int idx = tid; idx < 64 * 64; idx += NTB) sAqk[(idx >> 6) * LD6 + (idx & 63)] = f[idx];
-    if (tid < 64) {
-      ssc[tid] = scale * f[64 * 64 + 64 * D + tid];
-      sdec[tid] = f[64 * 64 + 64 * D + 64 + tid];
-    }
-    __syncthreads();
-    const float gC = f[64 * 64 + 64 * D + 63];   // e^{gamma_C}
+    const float gC = seg[63];                 // e^{gamma_C}
     // dDelta^T [v][j] = scale (dO^T Aqk)[v][j] + dec_j (dS K^T)[v][j]
     {
       float a1[T64][4], a2[T64][4];
@@ -218,29 +269,25 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
       zero(a2);
       gemm<T64, 8>(a1, dOT, view(sAqk, LD6, 1), 64, warp, lane);
       gemm<T64, 8>(a2, view(dS, LDS, 1), view(sK, 1, LDI), D, warp, lane);
-#pragma unroll
-      for (int ti = 0; ti < T64; ++ti)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a1[ti][e] *= scale;
       each<T64, 8>(a2, warp, lane, [&](int, int j, float& x) { x *= sdec[j]; });
 #pragma unroll
       for (int ti = 0; ti < T64; ++ti)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a1[ti][e] += a2[ti][e];
+        for (int e = 0; e < 4; ++e) a1[ti][e] = scale * a1[ti][e] + a2[ti][e];
       each<T64, 8>(a1, warp, lane, [&](int v, int j, float& x) { dDT[v * LD6 + j] = x; });
     }
     __syncthreads();
-    // dS <- e^{gamma_C} dS + (dO^T diag(scale e^gamma)) Q - dDelta^T W
+    // dS <- e^{gamma_C} dS + scale (dO^T diag(e^gamma)) Q - dDelta^T W
     {
       float a3[TDD][4], a4[TDD][4];
       zero(a3);
       zero(a4);
-      gemm<TDD, D / 8>(a3, cols_scaled(dOT, ssc), view(sQ, LDI, 1), 64, warp, lane);
+      gemm<TDD, D / 8>(a3, cols_scaled(dOT, seg), view(sQ, LDI, 1), 64, warp, lane);
       gemm<TDD, D / 8>(a4, view(dDT, LD6, 1), view(sW, LDW, 1), 64, warp, lane);
 #pragma unroll
       for (int ti = 0; ti < TDD; ++ti)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a3[ti][e] -= a4[ti][e];
+        for (int e = 0; e < 4; ++e) a3[ti][e] = scale * a3[ti][e] - a4[ti][e];
       each<TDD, D / 8>(a3, warp, lane, [&](int v, int c, float& x) {
         dS[v * LDS + c] = gC * dS[v * LDS + c] + x;
       });
@@ -267,8 +314,7 @@ static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slot
     if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTB, smem, st>>>(p, fac);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const size_t smem = sizeof(float) * (BV * c_ldd<D>() + BV * C_LD6 + 64 * C_LD6 + 64 * c_ldd<D>() + 128) +
-                      2 * (2 * 64 * (D + 8) + 64 * (BV + 8));
+  const size_t smem = sizeof(float) * (BV * c_ldd<D>() + BV * C_LD6) + 2 * ChainBuf<D, BV>::BYTES;
   auto kern = mma_bwd_chain_kernel<D, BV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

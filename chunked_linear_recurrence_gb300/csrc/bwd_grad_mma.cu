@@ -32,7 +32,7 @@ constexpr int NTG = 256;   // 8 warps
 // (8 rows x 4 columns per instruction) fall on distinct banks.
 constexpr int G_LD6 = 68;
 template <int D>
-constexpr int g_ldf() { return D + 4; }
+__host__ __device__ constexpr int g_ldf() { return D + 4; }
 
 struct CtaBarG {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
