@@ -37,11 +37,11 @@ __device__ __forceinline__ RowScaled<V> rows_scaled(V v, const float* s) { retur
 template <typename V>
 __device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { return ColScaled<V>{v, s}; }
 
-// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + 8 ti
-// of an output with NTN 8-column tiles per 16-row band.  The k loop is outermost and every
+// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + NW ti
+// of an output with NTN 8-column tiles per 16-row band (NW warps share the output).  The k loop is outermost and every
 // tile's operands of a k step are loaded before its products, so that a warp has all of
 // them in flight at once (operands in global memory take an L2 round trip).
-template <int NTILE, int NTN, typename AV, typename BV>
+template <int NTILE, int NTN, int NW = 8, typename AV, typename BV>
 __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
                                      int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
@@ -49,7 +49,7 @@ __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const 
     uint32_t a[NTILE][4], b[NTILE][2];
 #pragma unroll
     for (int ti = 0; ti < NTILE; ++ti) {
-      const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+      const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
       a[ti][0] = f2tf32(A(m0 + g, k0 + t));
       a[ti][1] = f2tf32(A(m0 + g + 8, k0 + t));
       a[ti][2] = f2tf32(A(m0 + g, k0 + t + 4));
@@ -71,12 +71,12 @@ __device__ __forceinline__ void zero(float (&acc)[NTILE][4]) {
 }
 
 // Calls f(row, col, value&) for every element this warp holds.
-template <int NTILE, int NTN, typename F>
+template <int NTILE, int NTN, int NW = 8, typename F>
 __device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane, F&& f) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ti = 0; ti < NTILE; ++ti) {
-    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+    const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
 #pragma unroll
     for (int e = 0; e < 4; ++e) f(m0 + g + 8 * (e >> 1), n0 + 2 * t + (e & 1), acc[ti][e]);
   }
@@ -84,13 +84,13 @@ __device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane,
 
 // vec[row] += sum over this warp's columns of w(row, col) acc(row, col) (4-lane reduction,
 // then one shared-memory atomic per row segment).
-template <int NTILE, int NTN, typename W>
+template <int NTILE, int NTN, int NW = 8, typename W>
 __device__ __forceinline__ void row_dot(const float (&acc)[NTILE][4], const W& w, float* vec,
                                         int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ti = 0; ti < NTILE; ++ti) {
-    const int id = warp + 8 * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+    const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int r = m0 + g + 8 * hr, c = n0 + 2 * t;
