@@ -104,7 +104,9 @@ static_assert(4 * RC_CTL + 8 * RC_STATE + 4 * RC_OUT <= 16 * 128, "chain registe
 static_assert(4 * RP_CTL + 8 * RP_PIPE + 4 * RP_IDLE <= 16 * 128, "preparation register split");
 
 constexpr uint32_t BAR_BYTES = 512;
-constexpr uint32_t GEO_BYTES = 2 * 64 * 4;   // stream lengths and their order (packed inputs)
+// packed inputs: stream lengths and their order (2 x 64 ints), then the production-order
+// table (65 stream positions as ints, 65 record counts as long longs)
+constexpr uint32_t GEO_BYTES = 2 * 64 * 4 + 65 * 4 + 4 + 65 * 8;
 constexpr uint32_t SMEM_USED = (P_BAR > C_BAR ? P_BAR : C_BAR) + BAR_BYTES + GEO_BYTES;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
@@ -112,7 +114,8 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory");
 // per-pipeline vectors (floats)
 constexpr int VEC_BETA = 64, VEC_GAM = 128, VEC_EG = 192, VEC_DEC = 256,
               VEC_EP = 320, VEC_EM = 384, VEC_FLAG = 448,
-              VEC_ITEM = 450;   // the use's item (int), -1: the pipeline has no more items
+              VEC_ITEM = 450;   // the use's item, -1: no more items; then its chain CTA and
+                                // stream position (ints)
 
 // ---- TMEM columns ----
 // chain: S FP32, S BF16 pairs, Delta^T BF16 pairs, Delta^T diag(dec) BF16 pairs, two
@@ -257,6 +260,11 @@ struct Geo {
   const int* lenj;           // packed: shared-memory copy
   const int* sortj;
   long long full, total;
+  // packed: production order in intervals of stream positions with a constant number of
+  // active chain CTAs -- interval m (m = 0 .. nch-1) has nch - m of them, starts at
+  // position seg_s(m) and at record seg_w(m); the table follows sortj in shared memory
+  __device__ const int* seg_s() const { return sortj + 64; }
+  __device__ const long long* seg_w() const { return reinterpret_cast<const long long*>(sortj + 64 + 66); }
   __device__ void init(const SplitParams& pr, const int* len_s, const int* sort_s) {
     p = &pr;
     H = pr.H;
@@ -281,12 +289,6 @@ struct Geo {
     seq_span(x / H, p->B, p->T, p->cu, bos, eos);
   }
   __device__ int len_of(int j) const { return packed ? lenj[j] : chains_of(j) * ncd; }
-  // records at stream positions below s, over all chain CTAs
-  __device__ long long before(int s) const {
-    long long a = 0;
-    for (int i = 0; i < nch; ++i) a += min(lenj[i], s);
-    return a;
-  }
   // w-th record in production order -> (chain CTA, stream position)
   __device__ void item(long long w, int& j, int& s) const {
     if (!packed) {
@@ -300,13 +302,29 @@ struct Geo {
       }
       return;
     }
-    int lo = 0, hi = lenj[sortj[0]];
+    // the last interval starting at or before record w
+    int lo = 0, hi = nch;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (before(mid) <= w) lo = mid; else hi = mid;
+      if (seg_w()[mid] <= w) lo = mid; else hi = mid;
     }
-    s = lo;
-    j = sortj[(int)(w - before(lo))];
+    const int k = nch - lo;
+    const long long off = w - seg_w()[lo];
+    s = seg_s()[lo] + (int)(off / k);
+    j = sortj[(int)(off % k)];
+  }
+  // fills the production-order table from the stream lengths (one thread)
+  __device__ static void build_table(int nch, const int* lenj, const int* sortj, int* sg_s,
+                                     long long* sg_w) {
+    long long w = 0;
+    for (int m = 0; m < nch; ++m) {
+      const int k = nch - m;                               // active chain CTAs
+      const int lo = (m == 0) ? 0 : lenj[sortj[k]];        // shortest stream still ahead ends
+      const int hi = lenj[sortj[k - 1]];
+      sg_s[m] = lo;
+      sg_w[m] = w;
+      w += (long long)k * (hi > lo ? hi - lo : 0);
+    }
   }
   // stream position s of chain CTA j -> chain x and its chunk c
   __device__ void locate(int j, int s, int& x, int& c) const {
@@ -962,7 +980,12 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             vs[VEC_FLAG + 1] = mid;
           }
         }
-        if (lane == 0) reinterpret_cast<int*>(vs)[VEC_ITEM] = done ? -1 : cur.g;
+        if (lane == 0) {
+          int* vi = reinterpret_cast<int*>(vs) + VEC_ITEM;
+          vi[0] = done ? -1 : cur.g;
+          vi[1] = jj;
+          vi[2] = s;
+        }
         __syncwarp();
         // the pipeline's previous item has had its last product (its tiles are free)
         if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
@@ -1144,11 +1167,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       pend = false;
       const int gi = reinterpret_cast<const int*>(vs)[VEC_ITEM];
       if (gi < 0) break;
-      int jj, s, h, row0, L;
-      item(gi, jj, s, h, row0, L);
-      (void)h;
-      (void)row0;
-      (void)L;
+      const int jj = reinterpret_cast<const int*>(vs)[VEC_ITEM + 1];
+      const int s = reinterpret_cast<const int*>(vs)[VEC_ITEM + 2];
       if (!(ok = group_wait(&bars[P_KQDONE + pp], use & 1, bid, 128, cx))) break;
       tc_fence_after();
       uint32_t ah[32];     // rows 64-127: this row of Ahat (BF16 pairs), stored at the end
@@ -1270,6 +1290,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int tid = threadIdx.x, warp = tid >> 5;
   int* len_s = reinterpret_cast<int*>(bar_area + BAR_BYTES);
   int* sort_s = len_s + 64;
+  int* seg_s = sort_s + 64;
+  long long* seg_w = reinterpret_cast<long long*>(seg_s + 66);
   if (p.cu && tid < p.nch) {
     len_s[tid] = p.lenj[tid];
     sort_s[tid] = p.sortj[tid];
@@ -1304,6 +1326,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.cu) {
+    if (tid == 0) Geo::build_table(p.nch, len_s, sort_s, seg_s, seg_w);
+    __syncthreads();
+  }
   const uint32_t tm = *tmem_slot;
   geo.init(p, len_s, sort_s);
 
