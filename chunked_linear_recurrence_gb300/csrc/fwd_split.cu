@@ -133,7 +133,7 @@ constexpr uint32_t ID_MG = idesc_bf16(128, 128, false, true);    // A@tmem, B MN
 enum {
   // chain CTA
   C_RECFULL = 0,   // [NBUF] record + K tile landed (tx)
-  C_RECFREE = 3,   // [NBUF] MMA commit after the chunk's last product reading the buffer
+  C_RECFREE = 3,   // [NBUF] the chunk's last product done (MMA commit) + its output tile out
   C_MERGED = 6,    // MMA: [-S W^T | S Qg^T] complete
   C_DREADY = 7,    // state: Delta BF16 operands in TMEM (and K padding zeroed)
   C_SUDONE = 8,    // MMA: state update complete
@@ -348,7 +348,8 @@ struct Geo {
 // State-chain CTA.  warp 0: record / K-tile loader; warp 1: MMA issuer; warps 4-11:
 // the state (two warpgroups, one column half each); warps 12-15: output stores.
 // --------------------------------------------------------------------------
-__device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitParams& p,
+__device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensorMap* tmO,
+                                          const SplitParams& p,
                                           const Geo& geo, uint8_t* sm, uint32_t sb,
                                           uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -603,16 +604,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
             for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
             tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
           }
+          tmem_st_wait();
+          tc_fence_before();
+          named_bar(BAR_STATE, 256);
+          if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
           if (ck) {
+            // state replay: the next chunk's entry state, written while its first product runs
             float4* dst = reinterpret_cast<float4*>(ck + (size_t)(c + 1) * ck_stride);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
           }
-          tmem_st_wait();
-          tc_fence_before();
-          named_bar(BAR_STATE, 256);
-          if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
           const int s1 = s + 1;
           if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))
             break;
@@ -651,15 +653,36 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const SplitPar
         tc_fence_before();
         named_bar(BAR_OUT, 128);
         if (v == 0) mbar_arrive(&bars[C_OFREE + b]);
-        if (!p.out) continue;
+        const int rb = s % NBUF;
         const int64_t row0 = bos + (int64_t)c * CHUNK;
         const int L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
-        __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
+        if (p.out && L == CHUNK) {
+          // the record's U^T area (read by the Delta step, long done) stages the [64 token]
+          // [128 v] tile in the panel layout; one TMA store sends it out
+          uint8_t* st = sm + rb * C_BUF + R_U;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i < L) orow[i * rs] = __float2bfloat16_rn(p.scale * o[i]);
+          for (int i = 0; i < 64; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(st + sw128_off(i, v, 8192)) =
+                __float2bfloat16_rn(p.scale * o[i]);
+          fence_proxy_async_smem();
+          named_bar(BAR_OUT, 128);
+          if (v == 0) {
+            tma_store_3d(tmO, st, 0, h, (int)row0);
+            tma_store_3d(tmO, st + 8192, 64, h, (int)row0);
+            bulk_commit();
+            bulk_wait_read_all();   // the buffer may take the next record
+          }
+        } else if (p.out) {
+          // a chunk cut short by the sequence end: only its own rows are written
+          __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < L) orow[i * rs] = __float2bfloat16_rn(p.scale * o[i]);
+        }
+        if (v == 0) mbar_arrive(&bars[C_RECFREE + rb]);
       }
     }
+    if (v == 0) bulk_wait_all();   // every output store has landed before the CTA leaves
   }
 }
 
@@ -1278,7 +1301,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
 __global__ void __launch_bounds__(NTHR, 1)
     gdn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1302,6 +1326,9 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (tid == 0) {
     if (is_chain) {
       for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
+      // a record buffer is free once its chunk's products are done (MMA commit) and its
+      // output tile, staged in it, has been read out (output warps)
+      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], 2);
     } else {
       for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
       mbar_init(&bars[P_FULL], 33);
@@ -1314,6 +1341,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     *abort_l = 0;
     fence_mbar_init();
     prefetch_tmap(&tmK);
+    if (is_chain && p.out) prefetch_tmap(&tmO);
     if (!is_chain) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmV);
@@ -1334,7 +1362,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   geo.init(p, len_s, sort_s);
 
   if (is_chain)
-    chain_cta(&tmK, p, geo, sm, sb, bars, tm, cx);
+    chain_cta(&tmK, &tmO, p, geo, sm, sb, bars, tm, cx);
   else
     prep_cta(&tmQ, &tmK, &tmV, p, geo, sm, sb, bars, tm, cx);
 
@@ -1447,7 +1475,10 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaS
     split_setup_kernel<<<1, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  void* args[] = {&mq, &mk, &mv, &p};
+  // the output map (the K map stands in when there is no output: it is never used then)
+  CUtensorMap mo = mk;
+  if (cp.out && !make_bf16_map(&mo, cp.out, rows, cp.H)) return cudaErrorInvalidValue;
+  void* args[] = {&mq, &mk, &mv, &mo, &p};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
                                      dim3(nch + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
 }
