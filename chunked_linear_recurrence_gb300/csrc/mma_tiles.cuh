@@ -41,12 +41,16 @@ __device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { retur
 // of an output with NTN 8-column tiles per 16-row band (NW warps share the output).  The k loop is outermost and every
 // tile's operands of a k step are loaded before its products, so that a warp has all of
 // them in flight at once (operands in global memory take an L2 round trip).
+// When NW is a multiple of NTN every tile of a warp lies in the same 8-column band, and its
+// B fragment is loaded once per k step for all of them.
 template <int NTILE, int NTN, int NW = 8, typename AV, typename BV>
 __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
                                      int warp, int lane) {
+  constexpr bool kShareB = (NW % NTN) == 0;
+  constexpr int NB = kShareB ? 1 : NTILE;
   const int g = lane >> 2, t = lane & 3;
   for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t a[NTILE][4], b[NTILE][2];
+    uint32_t a[NTILE][4], b[NB][2];
 #pragma unroll
     for (int ti = 0; ti < NTILE; ++ti) {
       const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
@@ -54,11 +58,13 @@ __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const 
       a[ti][1] = f2tf32(A(m0 + g + 8, k0 + t));
       a[ti][2] = f2tf32(A(m0 + g, k0 + t + 4));
       a[ti][3] = f2tf32(A(m0 + g + 8, k0 + t + 4));
-      b[ti][0] = f2tf32(B(k0 + t, n0 + g));
-      b[ti][1] = f2tf32(B(k0 + t + 4, n0 + g));
+      if (!kShareB || ti == 0) {
+        b[kShareB ? 0 : ti][0] = f2tf32(B(k0 + t, n0 + g));
+        b[kShareB ? 0 : ti][1] = f2tf32(B(k0 + t + 4, n0 + g));
+      }
     }
 #pragma unroll
-    for (int ti = 0; ti < NTILE; ++ti) mma_tf32_16x8x8(acc[ti], a[ti], b[ti]);
+    for (int ti = 0; ti < NTILE; ++ti) mma_tf32_16x8x8(acc[ti], a[ti], b[kShareB ? 0 : ti]);
   }
 }
 
