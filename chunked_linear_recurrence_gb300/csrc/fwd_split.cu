@@ -1010,15 +1010,18 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           vi[2] = s;
         }
         __syncwarp();
-        // the pipeline's previous item has had its last product (its tiles are free)
-        if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
         if (!done) {
-          // diag(e^gamma), the B operand of Qg^T
+          // diag(e^gamma), the B operand of Qg^T, once the previous item's Qg^T is done
+          if (use >= 1 && !(ok = warp_wait(&bars[P_QGDONE + pp], (use - 1) & 1, cx))) break;
           for (int e = lane; e < 64; e += 32)
             *reinterpret_cast<__nv_bfloat16*>(base + P_DG + sw128_off(e, e, 8192)) =
                 __float2bfloat16_rn(vs[VEC_EG + e]);
           fence_proxy_async_smem();
           __syncwarp();
+        }
+        // the pipeline's previous item has had its last product (its tiles are free)
+        if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
+        if (!done) {
           if (lane == 0) {
             // K and Q first (the first product needs only them), V on its own barrier
             mbar_arrive_expect_tx(&bars[P_FULL + pp], 2 * 16384);
@@ -1081,20 +1084,54 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       __syncwarp();
     } else {
       // ------------------------------------------------------------ MMA issuers
-      // warp 1 issues pipeline 0's products, warp 3 pipeline 1's, each in its pipeline's
-      // item order (an issue waits for the tensor pipe, so one thread serving both
-      // pipelines would hold each up behind the other).  A pipeline ends at the use
-      // whose item slot says -1.
+      // warp 1 issues pipeline 0's products, warp 3 pipeline 1's (an issue waits for the
+      // tensor pipe, so one thread serving both pipelines would hold each up behind the
+      // other).  Per item, in order: KQ, Qg^T, then (-W)^T and U^T; each waits (suspended)
+      // for exactly what it needs.  A pipeline ends at the use whose item slot says -1.
       const int pp = warp >> 1;
       if (lane == 0) {
         const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
-        int uK = 0, uQ = 0, uW = 0;   // next use per product
-        bool fin = false;
-        long long t_prog = clock64();
-        while (!(fin && uW == uK)) {
-          bool prog = false;
-          if (uW < uK && mbar_test(&bars[P_TT + pp], uW & 1) && mbar_test(&bars[P_FULLV + pp], uW & 1)) {
-            tc_fence_after();
+        for (int u = 0;; ++u) {
+          // KQ: the item slot and vectors (HEAD), the K and Q tiles (FULL), the previous
+          // item's KQ accumulator read out (KQFREE)
+          if (!wait_bar(&bars[P_HEAD + pp], u & 1, cx)) { raise_abort(cx); break; }
+          if (reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0) break;
+          if (!wait_bar(&bars[P_FULL + pp], u & 1, cx) ||
+              (u > 0 && !wait_bar(&bars[P_KQFREE + pp], (u - 1) & 1, cx))) {
+            raise_abort(cx);
+            break;
+          }
+          tc_fence_after();
+          {
+            // KQ = [K; Q] K^T
+            const uint64_t bq = sdesc_sw128(base + P_KQ, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t d = bq + (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
+              mma_bf16(tp + TP_KQ, d, d, ID_N64, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars[P_KQDONE + pp]);
+          }
+          // Qg^T: the previous item's Qg^T accumulator read out (TMFREE)
+          if (u > 0 && !wait_bar(&bars[P_TMFREE + pp], (u - 1) & 1, cx)) { raise_abort(cx); break; }
+          tc_fence_after();
+          {
+            // Qg^T = Q^T diag(e^gamma)
+            const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
+            const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2), ID_AMN,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(&bars[P_QGDONE + pp]);
+          }
+          // (-W)^T, U^T: T' and -T'' (TT), the V tile (FULLV)
+          if (!wait_bar(&bars[P_TT + pp], u & 1, cx) || !wait_bar(&bars[P_FULLV + pp], u & 1, cx)) {
+            raise_abort(cx);
+            break;
+          }
+          tc_fence_after();
+          {
             // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
             const uint64_t ak = sdesc_sw128(base + P_KQ, P_KQ_PANEL, 1024);
             const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
@@ -1110,52 +1147,6 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
                        kk > 0 ? 1u : 0u);
             mma_commit(&bars[P_WUDONE + pp]);
             mma_commit(&bars[P_ITEMFREE + pp]);
-            ++uW;
-            prog = true;
-          }
-          // Qg^T of an item needs the Qg^T accumulator of the previous item read (TMFREE)
-          if (uQ < uK && (uQ == 0 || mbar_test(&bars[P_TMFREE + pp], (uQ - 1) & 1))) {
-            tc_fence_after();
-            // Qg^T = Q^T diag(e^gamma)
-            const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
-            const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2), ID_AMN,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(&bars[P_QGDONE + pp]);
-            ++uQ;
-            prog = true;
-          }
-          // KQ of an item: its item slot and vectors are in (HEAD), its tiles are in
-          // (FULL), the previous item has had all its products issued and its KQ
-          // accumulator read out (KQFREE)
-          if (!fin && uW == uK && uQ == uK && mbar_test(&bars[P_HEAD + pp], uK & 1)) {
-            const int gi = reinterpret_cast<const int*>(vec_of(pp, uK))[VEC_ITEM];
-            if (gi < 0) {
-              fin = true;
-            } else if (mbar_test(&bars[P_FULL + pp], uK & 1) &&
-                       (uK == 0 || mbar_test(&bars[P_KQFREE + pp], (uK - 1) & 1))) {
-              tc_fence_after();
-              // KQ = [K; Q] K^T
-              const uint64_t bq = sdesc_sw128(base + P_KQ, 0, 1024);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t d = bq + (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
-                mma_bf16(tp + TP_KQ, d, d, ID_N64, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&bars[P_KQDONE + pp]);
-              ++uK;
-              prog = true;
-            }
-          }
-          if (prog) {
-            t_prog = clock64();
-          } else if (*cx.abort_l || clock64() - t_prog > kWaitLimitCycles) {
-            raise_abort(cx);
-            break;
-          } else {
-            __nanosleep(16);   // leave most issue slots to the pipelines meanwhile
           }
         }
       }
