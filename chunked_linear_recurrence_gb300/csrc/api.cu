@@ -250,10 +250,11 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + 2 * one) : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   cudaError_t e;
-  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available())
+  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
+    p.ckpt_tiled = 1;   // the split kernel writes its checkpoints in its threads' order
     e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
                               reinterpret_cast<int*>(workspace), cs);
-  else
+  } else
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   e = sfg::launch_simt_bwd(p, bf16, D, slots, cs);

@@ -39,10 +39,21 @@ struct CtaBarG {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
 
+// Element (r, c) of a D = 128 checkpoint block in the split kernel's thread order (TR:
+// the transpose).
+template <bool TR>
+struct TiledState {
+  const float* p;
+  __device__ __forceinline__ float operator()(int r, int c) const {
+    return TR ? p[ckpt_tiled_off(c, r)] : p[ckpt_tiled_off(r, c)];
+  }
+};
+
 }  // namespace
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool kTiled>
 __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) {
+  static_assert(!kTiled || D == 128, "tiled checkpoints have D = 128");
   constexpr int LDI = D + 8;      // input tiles (Tin)
   constexpr int LDF = g_ldf<D>();  // fp32 [64][D] tiles
   constexpr int LD6 = G_LD6;
@@ -148,8 +159,13 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), Vv = view(sV, LDI, 1),
              dOv = view(sdO, LDI, 1);
   const auto KvT = view(sK, 1, LDI), VvT = view(sV, 1, LDI);
-  const auto Sv = view(S, D, 1), SvT = view(S, 1, D), dSnT = view(dSn, 1, D),
-             dSnv = view(dSn, D, 1);
+  const auto dSnT = view(dSn, 1, D), dSnv = view(dSn, D, 1);
+  const auto Sv = [&] {
+    if constexpr (kTiled) return TiledState<false>{S}; else return view(S, D, 1);
+  }();
+  const auto SvT = [&] {
+    if constexpr (kTiled) return TiledState<true>{S}; else return view(S, 1, D);
+  }();
 
   // Ak = Gamma o K K^T (strict lower), Aqk = Gamma o Q K^T (lower incl. diagonal)
   {
@@ -261,7 +277,10 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     const float4* b4 = reinterpret_cast<const float4*>(S);
 #pragma unroll 8
     for (int idx = tid; idx < D * D / 4; idx += NTG) {
-      const float4 x = a4[idx], y = b4[idx];
+      // S's float4 idx holds (v, k0 .. k0 + 3) of the tiled order, or the row-major ones
+      const int v = kTiled ? (idx & 127) : 0;
+      const int k0 = kTiled ? ((idx >> 7) & 1) * 64 + (idx >> 8) * 4 : 0;
+      const float4 x = a4[kTiled ? (v * D + k0) / 4 : idx], y = b4[idx];
       part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
     }
 #pragma unroll
@@ -405,11 +424,11 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   }
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool kTiled = false>
 static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
   const size_t smem = sizeof(float) * (3 * 64 * G_LD6 + 3 * 64 * g_ldf<D>() + 11 * 64) +
                       sizeof(Tin) * 4 * 64 * (D + 8);
-  auto kern = mma_bwd_grad_kernel<Tin, D>;
+  auto kern = mma_bwd_grad_kernel<Tin, D, kTiled>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTG, smem, st>>>(p);
@@ -419,7 +438,9 @@ static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream
 cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
                                 cudaStream_t st) {
   if (bf16 && D == 64) return launch_grad_t<__nv_bfloat16, 64>(p, slots, st);
-  if (bf16 && D == 128) return launch_grad_t<__nv_bfloat16, 128>(p, slots, st);
+  if (bf16 && D == 128)
+    return p.ckpt_tiled ? launch_grad_t<__nv_bfloat16, 128, true>(p, slots, st)
+                        : launch_grad_t<__nv_bfloat16, 128>(p, slots, st);
   if (!bf16 && D == 64) return launch_grad_t<float, 64>(p, slots, st);
   return cudaErrorInvalidValue;
 }

@@ -479,8 +479,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       geo.span(x, bos, eos);
       const int nc = (int)n_chunks(eos - bos);
       // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c]
+      // (checkpoint blocks in the threads' order: float4 e of thread st_t at 256 e + st_t)
       float* ck = p.ckpt ? p.ckpt + ((size_t)chunk_slot_base(x / H, p.B, p.T, p.cu) * H + x % H) * D * D +
-                               (size_t)v * D + 64 * w
+                               (size_t)4 * st_t
                          : nullptr;
       const size_t ck_stride = (size_t)H * D * D;
       if (nc == 0) {
@@ -514,7 +515,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           float4* dst = reinterpret_cast<float4*>(ck);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
+            dst[256 * e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
         }
         uint32_t u[16];
 #pragma unroll
@@ -613,7 +614,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
             float4* dst = reinterpret_cast<float4*>(ck + (size_t)(c + 1) * ck_stride);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
+              dst[256 * e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
           }
           const int s1 = s + 1;
           if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))

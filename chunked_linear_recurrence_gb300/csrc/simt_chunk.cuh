@@ -22,6 +22,7 @@ struct ChainParams {
   float* P;               // [R,H,K,K] (summary)
   float* E;               // [R,H,V,K] (summary)
   float* ckpt;            // [slots,H,V,K] chunk-entry states (replay / backward)
+  int ckpt_tiled;         // ckpt blocks in the state-thread order of ckpt_tiled_off (D = 128)
   float* tape;            // [slots,H,V,K] chunk-exit cotangents (backward)
   const void* dout;       // [B,T,H,V] (backward)
   const float* dsf;       // [N,H,V,K] or NULL (backward)
@@ -40,6 +41,14 @@ struct ChainParams {
 cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, int items,
                               cudaStream_t st);
 // Backward after a replay: reverse cotangent chain then per-chunk token gradients.
+// Offset (floats) of state element (v, k) in a D = 128 checkpoint block written by the
+// split kernel's state threads: thread t = 128 (k / 64) + v stores its 64 values as 16
+// float4 at float4 index 256 e + t (e = (k mod 64) / 4), so that every store instruction
+// of a warp covers 512 contiguous bytes.
+__host__ __device__ inline int ckpt_tiled_off(int v, int k) {
+  return ((((k & 63) >> 2) << 8) + ((k >> 6) << 7) + v) * 4 + (k & 3);
+}
+
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
                             cudaStream_t st);
 // BF16 backward's reverse cotangent chain on the warp-level tensor cores
