@@ -172,12 +172,12 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     float a1[T6][4], a2[T6][4];
     zero(a1);
     zero(a2);
-    gemm<T6, 8, NWG>(a1, Kv, KvT, D, warp, lane);
-    gemm<T6, 8, NWG>(a2, Qv, KvT, D, warp, lane);
-    each<T6, 8, NWG>(a1, warp, lane, [&](int i, int j, float& x) {
+    gemm<T6, 8, NWG, true>(a1, Kv, KvT, D, warp, lane);
+    gemm<T6, 8, NWG, true>(a2, Qv, KvT, D, warp, lane);
+    each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) {
       sM[i * LD6 + j] = (j < i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
     });
-    each<T6, 8, NWG>(a2, warp, lane, [&](int i, int j, float& x) {
+    each<T6, 8, NWG, true>(a2, warp, lane, [&](int i, int j, float& x) {
       sP[i * LD6 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
     });
   }
@@ -194,11 +194,11 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, cols_scaled(Tv, sbeg), Kv, 64, warp, lane);
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = x; });
+    gemm<TD, NTD, NWG, true>(acc, cols_scaled(Tv, sbeg), Kv, 64, warp, lane);
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = x; });
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, cols_scaled(Tv, sb), Vv, 64, warp, lane);
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
+    gemm<TD, NTD, NWG, true>(acc, cols_scaled(Tv, sb), Vv, 64, warp, lane);
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
   }
   __syncthreads();
   const auto B1v = view(B1, LDF, 1), B2v = view(B2, LDF, 1), B3v = view(B3, LDF, 1);
@@ -206,21 +206,21 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, B1v, SvT, D, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc, B1v, SvT, D, warp, lane);
     float acc2[TD][4];
     zero(acc2);
-    gemm<TD, NTD, NWG>(acc2, view(sP, 1, LD6), dOv, 64, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc2, view(sP, 1, LD6), dOv, 64, warp, lane);
     float acc3[TD][4];
     zero(acc3);
-    gemm<TD, NTD, NWG>(acc3, Kv, dSnT, D, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc3, Kv, dSnT, D, warp, lane);
     __syncthreads();   // every warp has read W (B1), U (B2) as operands of its own tiles only
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int r, float& x) { B2[i * LDF + r] -= x; });
-    each<TD, NTD, NWG>(acc3, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int r, float& x) { B2[i * LDF + r] -= x; });
+    each<TD, NTD, NWG, true>(acc3, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
 #pragma unroll
     for (int ti = 0; ti < TD; ++ti)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc2[ti][e] = scale * acc2[ti][e] + acc3[ti][e];
-    each<TD, NTD, NWG>(acc2, warp, lane, [&](int i, int r, float& x) { B3[i * LDF + r] = x; });
+    each<TD, NTD, NWG, true>(acc2, warp, lane, [&](int i, int r, float& x) { B3[i * LDF + r] = x; });
   }
   __syncthreads();
   float dq[TD][4], dk[TD][4];
@@ -230,9 +230,9 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG>(a1, dOv, view(B2, 1, LDF), D, warp, lane);
+    gemm<T6, 8, NWG, true>(a1, dOv, view(B2, 1, LDF), D, warp, lane);
     __syncthreads();   // sP (Aqk) fully read as an operand before it is overwritten
-    each<T6, 8, NWG>(a1, warp, lane, [&](int i, int j, float& x) {
+    each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) {
       float gval = 0.f;
       if (j <= i) {
         const float dA = scale * x;
@@ -249,22 +249,22 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, rows_scaled(dOv, ssc), Sv, D, warp, lane);
-    row_dot<TD, NTD, NWG>(acc, Qv, sdgam, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc, rows_scaled(dOv, ssc), Sv, D, warp, lane);
+    row_dot<TD, NTD, NWG, true>(acc, Qv, sdgam, warp, lane);
 #pragma unroll
     for (int ti = 0; ti < TD; ++ti)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dq[ti][e] += acc[ti][e];
-    gemm<TD, NTD, NWG>(dq, view(sP, LD6, 1), Kv, 64, warp, lane);
-    gemm<TD, NTD, NWG>(dk, view(sP, 1, LD6), Qv, 64, warp, lane);
+    gemm<TD, NTD, NWG, true>(dq, view(sP, LD6, 1), Kv, 64, warp, lane);
+    gemm<TD, NTD, NWG, true>(dk, view(sP, 1, LD6), Qv, 64, warp, lane);
   }
   // exit state: Z = Delta dSn ; dk += dec o Z ; ddec = rowsum(K o Z)
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, B2v, dSnv, D, warp, lane);
-    row_dot<TD, NTD, NWG>(acc, Kv, sz, warp, lane);
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
+    gemm<TD, NTD, NWG, true>(acc, B2v, dSnv, D, warp, lane);
+    row_dot<TD, NTD, NWG, true>(acc, Kv, sz, warp, lane);
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
 #pragma unroll
     for (int ti = 0; ti < TD; ++ti)
 #pragma unroll
@@ -298,11 +298,11 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     float acc[TD][4], acc2[TD][4];
     zero(acc);
     zero(acc2);
-    gemm<TD, NTD, NWG>(acc, B3v, Sv, D, warp, lane);
-    gemm<TD, NTD, NWG>(acc2, TvT, B3v, 64, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc, B3v, Sv, D, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc2, TvT, B3v, 64, warp, lane);
     __syncthreads();
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = -x; });
-    each<TD, NTD, NWG>(acc2, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = -x; });
+    each<TD, NTD, NWG, true>(acc2, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
   }
   __syncthreads();
   // dv = beta X ; dbeta += rowsum(V o X)  (a warp covers 32 columns of one row: warp sum,
@@ -323,9 +323,9 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG>(a1, B3v, cols_scaled(VvT, sb), D, warp, lane);
-    gemm<T6, 8, NWG>(a1, B1v, cols_scaled(KvT, sbeg), D, warp, lane);
-    each<T6, 8, NWG>(a1, warp, lane, [&](int i, int j, float& x) { sP[i * LD6 + j] = x; });
+    gemm<T6, 8, NWG, true>(a1, B3v, cols_scaled(VvT, sb), D, warp, lane);
+    gemm<T6, 8, NWG, true>(a1, B1v, cols_scaled(KvT, sbeg), D, warp, lane);
+    each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) { sP[i * LD6 + j] = x; });
   }
   __syncthreads();
   // Y = T^T dW ; dk += beta e^gamma Y ; kt = rowsum(K o Y) -> dbeta += e^gamma kt,
@@ -333,11 +333,11 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG>(acc, TvT, B1v, 64, warp, lane);
+    gemm<TD, NTD, NWG, true>(acc, TvT, B1v, 64, warp, lane);
     if (tid < 64) sz[tid] = 0.f;
     __syncthreads();
-    row_dot<TD, NTD, NWG>(acc, Kv, sz, warp, lane);
-    each<TD, NTD, NWG>(acc, warp, lane, [&](int i, int, float& x) { x *= sbeg[i]; });
+    row_dot<TD, NTD, NWG, true>(acc, Kv, sz, warp, lane);
+    each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int, float& x) { x *= sbeg[i]; });
 #pragma unroll
     for (int ti = 0; ti < TD; ++ti)
 #pragma unroll
@@ -352,15 +352,15 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG>(a1, view(sP, LD6, 1), TvT, 64, warp, lane);
-    each<T6, 8, NWG>(a1, warp, lane, [&](int i, int j, float& x) { B1[i * LD6 + j] = x; });
+    gemm<T6, 8, NWG, true>(a1, view(sP, LD6, 1), TvT, 64, warp, lane);
+    each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) { B1[i * LD6 + j] = x; });
   }
   __syncthreads();
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG>(a1, TvT, view(B1, LD6, 1), 64, warp, lane);
-    each<T6, 8, NWG>(a1, warp, lane, [&](int i, int j, float& x) { B2[i * LD6 + j] = (j < i) ? -x : 0.f; });
+    gemm<T6, 8, NWG, true>(a1, TvT, view(B1, LD6, 1), 64, warp, lane);
+    each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) { B2[i * LD6 + j] = (j < i) ? -x : 0.f; });
   }
   __syncthreads();
   // from A_ij = beta_i Ak_ij: dbeta_i += sum_j dA_ij Ak_ij; dgamma_i/j +- dA beta Ak;
@@ -389,16 +389,16 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   }
   __syncthreads();
   // dk += dKK K + dKK^T K
-  gemm<TD, NTD, NWG>(dk, view(sP, LD6, 1), Kv, 64, warp, lane);
-  gemm<TD, NTD, NWG>(dk, view(sP, 1, LD6), Kv, 64, warp, lane);
+  gemm<TD, NTD, NWG, true>(dk, view(sP, LD6, 1), Kv, 64, warp, lane);
+  gemm<TD, NTD, NWG, true>(dk, view(sP, 1, LD6), Kv, 64, warp, lane);
   // write dq, dk
   {
     Tin* dqo = (Tin*)p.dq;
     Tin* dko = (Tin*)p.dk;
-    each<TD, NTD, NWG>(dq, warp, lane, [&](int i, int c, float& x) {
+    each<TD, NTD, NWG, true>(dq, warp, lane, [&](int i, int c, float& x) {
       if (i < L) dqo[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
     });
-    each<TD, NTD, NWG>(dk, warp, lane, [&](int i, int c, float& x) {
+    each<TD, NTD, NWG, true>(dk, warp, lane, [&](int i, int c, float& x) {
       if (i < L) dko[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
     });
   }

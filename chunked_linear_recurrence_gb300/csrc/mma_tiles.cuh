@@ -37,34 +37,65 @@ __device__ __forceinline__ RowScaled<V> rows_scaled(V v, const float* s) { retur
 template <typename V>
 __device__ __forceinline__ ColScaled<V> cols_scaled(V v, const float* s) { return ColScaled<V>{v, s}; }
 
-// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles: tile id = warp + NW ti
-// of an output with NTN 8-column tiles per 16-row band (NW warps share the output).  The k loop is outermost and every
-// tile's operands of a k step are loaded before its products, so that a warp has all of
-// them in flight at once (operands in global memory take an L2 round trip).
-// When NW is a multiple of NTN every tile of a warp lies in the same 8-column band, and its
-// B fragment is loaded once per k step for all of them.
-template <int NTILE, int NTN, int NW = 8, typename AV, typename BV>
+// Which 16x8 output tiles a warp owns.  Plain (BLK = false): tile id = warp + NW ti of an
+// output with NTN 8-column tiles per 16-row band.  Blocked (BLK = true): each warp owns a
+// WM x WN block of tiles (WM 16-row bands, WN 8-column tiles), so that every A fragment it
+// loads serves WN products and every B fragment WM of them.
+template <int NTILE, int NTN, int NW, bool BLK>
+struct TileMap {
+  static constexpr int MBANDS = NW * NTILE / NTN;
+  static constexpr int WM = (BLK && NTILE >= 4 && NTILE % 2 == 0 && MBANDS % 2 == 0) ? 2 : 1;
+  static constexpr int WN = BLK ? NTILE / WM : 1;
+  static_assert(!BLK || (MBANDS / WM) * (NTN / WN) == NW, "warp blocks tile the output");
+  __device__ static __forceinline__ void at(int warp, int ti, int& m0, int& n0) {
+    if (BLK) {
+      const int wm = warp / (NTN / WN), wn = warp % (NTN / WN);
+      m0 = (wm * WM + ti / WN) * 16;
+      n0 = (wn * WN + ti % WN) * 8;
+    } else {
+      const int id = warp + NW * ti;
+      m0 = (id / NTN) * 16;
+      n0 = (id % NTN) * 8;
+    }
+  }
+};
+
+// acc[ti] += A[m0:m0+16, 0:K] B[0:K, n0:n0+8] for this warp's tiles (TileMap).  The k loop
+// is outermost and all of a k step's fragments are loaded before its products, so that a
+// warp has them all in flight at once (operands in global memory take an L2 round trip).
+template <int NTILE, int NTN, int NW = 8, bool BLK = false, typename AV, typename BV>
 __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
                                      int warp, int lane) {
-  constexpr bool kShareB = (NW % NTN) == 0;
-  constexpr int NB = kShareB ? 1 : NTILE;
+  using M = TileMap<NTILE, NTN, NW, BLK>;
+  // distinct A fragments (16-row bands) and B fragments (8-column tiles) of the warp's tiles
+  constexpr int NA = BLK ? M::WM : NTILE;
+  constexpr bool kShareB = !BLK && (NW % NTN) == 0;
+  constexpr int NB = BLK ? M::WN : (kShareB ? 1 : NTILE);
   const int g = lane >> 2, t = lane & 3;
   for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t a[NTILE][4], b[NB][2];
+    uint32_t a[NA][4], b[NB][2];
 #pragma unroll
-    for (int ti = 0; ti < NTILE; ++ti) {
-      const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
-      a[ti][0] = f2tf32(A(m0 + g, k0 + t));
-      a[ti][1] = f2tf32(A(m0 + g + 8, k0 + t));
-      a[ti][2] = f2tf32(A(m0 + g, k0 + t + 4));
-      a[ti][3] = f2tf32(A(m0 + g + 8, k0 + t + 4));
-      if (!kShareB || ti == 0) {
-        b[kShareB ? 0 : ti][0] = f2tf32(B(k0 + t, n0 + g));
-        b[kShareB ? 0 : ti][1] = f2tf32(B(k0 + t + 4, n0 + g));
-      }
+    for (int ia = 0; ia < NA; ++ia) {
+      int m0, n0;
+      M::at(warp, BLK ? ia * M::WN : ia, m0, n0);
+      a[ia][0] = f2tf32(A(m0 + g, k0 + t));
+      a[ia][1] = f2tf32(A(m0 + g + 8, k0 + t));
+      a[ia][2] = f2tf32(A(m0 + g, k0 + t + 4));
+      a[ia][3] = f2tf32(A(m0 + g + 8, k0 + t + 4));
     }
 #pragma unroll
-    for (int ti = 0; ti < NTILE; ++ti) mma_tf32_16x8x8(acc[ti], a[ti], b[kShareB ? 0 : ti]);
+    for (int ib = 0; ib < NB; ++ib) {
+      int m0, n0;
+      M::at(warp, ib, m0, n0);
+      b[ib][0] = f2tf32(B(k0 + t, n0 + g));
+      b[ib][1] = f2tf32(B(k0 + t + 4, n0 + g));
+    }
+#pragma unroll
+    for (int ti = 0; ti < NTILE; ++ti) {
+      const int ia = BLK ? ti / M::WN : ti;
+      const int ib = BLK ? ti % M::WN : (kShareB ? 0 : ti);
+      mma_tf32_16x8x8(acc[ti], a[ia], b[ib]);
+    }
   }
 }
 
@@ -77,12 +108,13 @@ __device__ __forceinline__ void zero(float (&acc)[NTILE][4]) {
 }
 
 // Calls f(row, col, value&) for every element this warp holds.
-template <int NTILE, int NTN, int NW = 8, typename F>
+template <int NTILE, int NTN, int NW = 8, bool BLK = false, typename F>
 __device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane, F&& f) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ti = 0; ti < NTILE; ++ti) {
-    const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+    int m0, n0;
+    TileMap<NTILE, NTN, NW, BLK>::at(warp, ti, m0, n0);
 #pragma unroll
     for (int e = 0; e < 4; ++e) f(m0 + g + 8 * (e >> 1), n0 + 2 * t + (e & 1), acc[ti][e]);
   }
@@ -90,13 +122,14 @@ __device__ __forceinline__ void each(float (&acc)[NTILE][4], int warp, int lane,
 
 // vec[row] += sum over this warp's columns of w(row, col) acc(row, col) (4-lane reduction,
 // then one shared-memory atomic per row segment).
-template <int NTILE, int NTN, int NW = 8, typename W>
+template <int NTILE, int NTN, int NW = 8, bool BLK = false, typename W>
 __device__ __forceinline__ void row_dot(const float (&acc)[NTILE][4], const W& w, float* vec,
                                         int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ti = 0; ti < NTILE; ++ti) {
-    const int id = warp + NW * ti, m0 = (id / NTN) * 16, n0 = (id % NTN) * 8;
+    int m0, n0;
+    TileMap<NTILE, NTN, NW, BLK>::at(warp, ti, m0, n0);
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int r = m0 + g + 8 * hr, c = n0 + 2 * t;
