@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
     });
   }
   __syncthreads();
-  solve_unit_lower64(sA, sT, LD6, sX, tid, NTB, CtaBarB());
+  static_assert(LD6 == SOLVE_LD, "solve layout");
+  solve64_tc(sA, sT, sX, tid, NTB, CtaBarB());   // merges on TF32 mma, as in the forward
   {
     float acc[TD][4];
     zero(acc);

@@ -18,6 +18,8 @@
 // Every product is a set of 16x8 output tiles per warp (16 warps); a warp owns the same tiles of
 // every 64 x D product, so dq and dk accumulate in its registers across products.  The
 // shared-memory tiles and the order of the steps are those of simt_bwd_grad_kernel.
+#include <type_traits>
+
 #include "common.cuh"
 #include "mma_tiles.cuh"
 #include "simt_chunk.cuh"
@@ -188,7 +190,13 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     B3[i * LD6 + j] = sb[i] * sM[i * LD6 + j];
   }
   __syncthreads();
-  solve_unit_lower64(B3, sT, LD6, B2, tid, NTG, CtaBarG());
+  // BF16 inputs: the off-diagonal merges on TF32 mma (the forward's solve); FP32 inputs
+  // keep the FP32 substitution
+  static_assert(LD6 == SOLVE_LD, "solve layout");
+  if constexpr (std::is_same<Tin, __nv_bfloat16>::value)
+    solve64_tc(B3, sT, B2, tid, NTG, CtaBarG());
+  else
+    solve_unit_lower64(B3, sT, LD6, B2, tid, NTG, CtaBarG());
   const auto Tv = view(sT, LD6, 1), TvT = view(sT, 1, LD6);
   // W = T diag(beta e^gamma) K -> B1 ; U = T diag(beta) V -> B2
   {
