@@ -99,7 +99,7 @@ static_assert(64 * SOLVE_LD * 4 >= 4 * 4096, "the A/T area doubles as the store 
 // Registers per thread after setmaxnreg, by role.  Each CTA is launched with 128 per
 // thread (512 threads, the SM's 64K), and the roles' shares must add up to no more.
 constexpr int RC_CTL = 56, RC_STATE = 168, RC_OUT = 120;        // chain: 4, 8, 4 warps
-constexpr int RP_CTL = 88, RP_PIPE = 200, RP_IDLE = 24;         // preparation: 4, 8, 4 warps
+constexpr int RP_CTL = 96, RP_PIPE = 192, RP_IDLE = 24;         // preparation: 4, 8, 4 warps
 static_assert(4 * RC_CTL + 8 * RC_STATE + 4 * RC_OUT <= 16 * 128, "chain register split");
 static_assert(4 * RP_CTL + 8 * RP_PIPE + 4 * RP_IDLE <= 16 * 128, "preparation register split");
 
@@ -918,6 +918,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // ------------------------------------------------------------ controller
       const int pp = warp >> 1;
       uint8_t* base = sm + pp * P_STRIDE;
+      // pipeline 0 keeps [K;Q] in its tile rows, pipeline 1 [Q;K] (see the pipelines)
+      const uint32_t kq_k = pp ? 8192u : 0u, kq_q = pp ? 0u : 8192u;
       for (int idx = lane; idx < 512; idx += 32)
         reinterpret_cast<uint4*>(base + P_DG)[idx] = make_uint4(0, 0, 0, 0);
       auto claim = [&]() -> int {
@@ -1028,8 +1030,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             mbar_arrive_expect_tx(&bars[P_FULL + pp], 2 * 16384);
 #pragma unroll
             for (int pnl = 0; pnl < 2; ++pnl) {
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + 8192, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
                           row0);
             }
             mbar_arrive_expect_tx(&bars[P_FULLV + pp], 16384);
@@ -1048,7 +1050,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
               const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
               const int row = L + rem / 8, ch = rem % 8, pnl = t6 & 1, which = t6 >> 1;
               uint8_t* tb = (which == 2) ? base + P_V + pnl * P_V_PANEL
-                                         : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? 8192u : 0u);
+                                         : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? kq_q : kq_k);
               *reinterpret_cast<uint4*>(tb + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
@@ -1092,6 +1094,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       const int pp = warp >> 1;
       if (lane == 0) {
         const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+        const uint32_t kq_k = pp ? 8192u : 0u, kq_q = pp ? 0u : 8192u;
         for (int u = 0;; ++u) {
           // KQ: the item slot and vectors (HEAD), the K and Q tiles (FULL), the previous
           // item's KQ accumulator read out (KQFREE)
@@ -1105,11 +1108,12 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           tc_fence_after();
           {
             // KQ = [K; Q] K^T
-            const uint64_t bq = sdesc_sw128(base + P_KQ, 0, 1024);
+            const uint64_t aq = sdesc_sw128(base + P_KQ, 0, 1024);
+            const uint64_t bk = sdesc_sw128(base + P_KQ + kq_k, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t d = bq + (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
-              mma_bf16(tp + TP_KQ, d, d, ID_N64, kk > 0 ? 1u : 0u);
+              const uint64_t o = (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
+              mma_bf16(tp + TP_KQ, aq + o, bk + o, ID_N64, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bars[P_KQDONE + pp]);
           }
@@ -1118,7 +1122,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           tc_fence_after();
           {
             // Qg^T = Q^T diag(e^gamma)
-            const uint64_t aq = sdesc_sw128(base + P_KQ + 8192, P_KQ_PANEL, 1024);
+            const uint64_t aq = sdesc_sw128(base + P_KQ + kq_q, P_KQ_PANEL, 1024);
             const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -1134,7 +1138,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           tc_fence_after();
           {
             // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
-            const uint64_t ak = sdesc_sw128(base + P_KQ, P_KQ_PANEL, 1024);
+            const uint64_t ak = sdesc_sw128(base + P_KQ + kq_k, P_KQ_PANEL, 1024);
             const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -1165,7 +1169,10 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     // the A/T area, once T' and T'' are built, is this warp's store staging (4 KB); the
     // Ahat rows, stored during phase 1 of the solve, are staged in the X area
     uint8_t* stage = base + P_AT + (warp & 3) * 4096;
-    uint8_t* stage_ah = base + P_X + ((warp & 3) - 2) * 4096;
+    uint8_t* stage_ah = base + P_X + ((warp & 3) & 1) * 4096;
+    // TMEM lanes (rows of [K;Q] K^T) of this pipeline's A rows: pipeline 1 holds [Q;K], so
+    // its solve's phase 1 runs on the other two SM sub-partitions than pipeline 0's
+    const bool arow = (pp == 0) == (r < 64);
     // T' and -T'' are zero above the diagonal blocks for every item: the solve writes only
     // the blocks on and below the diagonal
     for (int idx = r; idx < 2 * 512; idx += 128)
@@ -1191,7 +1198,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         const bool fact = vs[VEC_FLAG] != 0.f;
         const int i = r & 63;
         const float gi = vs[VEC_GAM + i], epi = vs[VEC_EP + i];
-        const float bi = (r < 64) ? vs[VEC_BETA + i] : 1.f;
+        const float bi = arow ? vs[VEC_BETA + i] : 1.f;
         float x[64];
         tmem_ld64(tl + TP_KQ, x);
         if (fact) {
@@ -1209,7 +1216,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
 #pragma unroll
           for (int jx = 0; jx < 64; ++jx) x[jx] *= bi * expf(jx <= i ? gi - vs[VEC_GAM + jx] : 0.f);
         }
-        if (r < 64) {          // A_ij = beta_i Gamma_ij (k_i . k_j), j < i (the solve
+        if (arow) {            // A_ij = beta_i Gamma_ij (k_i . k_j), j < i (the solve
                                // reads nothing on or above the diagonal)
           float4* row = reinterpret_cast<float4*>(AT + i * SOLVE_LD);
 #pragma unroll
@@ -1233,11 +1240,11 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // the record's ring slot once the publisher has seen it free (s % NSLOT).
       uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
       bool ok1 = true;
-      if (r < 64) {
-        solve::half(AT, base + P_T1, base + P_T2, vs, warp & 3, lane);
+      if (arow) {
+        solve::half(AT, base + P_T1, base + P_T2, vs, (warp & 3) & 1, lane);
       } else {
         ok1 = __all_sync(0xffffffffu, wait_bar(&bars[P_SLOTOK + pp], use & 1, cx)) != 0;
-        if (ok1) store_rows(rec + R_AH, stage_ah, (warp & 3) * 32 - 64, ah, lane);
+        if (ok1) store_rows(rec + R_AH, stage_ah, ((warp & 3) * 32) & 63, ah, lane);
       }
       if (!(ok = named_bar_and(bid, 128, ok1))) {
         if (r == 0) raise_abort(cx);
