@@ -1250,7 +1250,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (r == 0) raise_abort(cx);
         break;
       }
-      if ((warp & 3) < 2)
+      // the two heavier blocks (row block 3) go to sub-partitions 2, 3 in pipeline 0 and to
+      // 0, 1 in pipeline 1, so that each sub-partition gets one of them
+      if (((warp & 3) < 2) == (pp == 0))
         solve::lower<0>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
       else
         solve::lower<1>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
