@@ -124,12 +124,12 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
     float a1[4][4], a2[4][4];
     zero(a1);
     zero(a2);
-    gemm<4, 8>(a1, Kv, KvT, D, warp, lane);
-    gemm<4, 8>(a2, Qv, KvT, D, warp, lane);
-    each<4, 8>(a1, warp, lane, [&](int i, int j, float& x) {
+    gemm<4, 8, 8, true>(a1, Kv, KvT, D, warp, lane);
+    gemm<4, 8, 8, true>(a2, Qv, KvT, D, warp, lane);
+    each<4, 8, 8, true>(a1, warp, lane, [&](int i, int j, float& x) {
       sA[i * LD6 + j] = (j < i) ? sb[i] * expf(sgam[i] - sgam[j]) * x : 0.f;
     });
-    each<4, 8>(a2, warp, lane, [&](int i, int j, float& x) {
+    each<4, 8, 8, true>(a2, warp, lane, [&](int i, int j, float& x) {
       oAqk[i * 64 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
     });
   }
@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
-    each<TD, NTD>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
+    gemm<TD, NTD, 8, true>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
+    each<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
   }
 }
 
@@ -268,14 +268,14 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
       float a1[T64][4], a2[T64][4];
       zero(a1);
       zero(a2);
-      gemm<T64, 8>(a1, dOT, view(sAqk, LD6, 1), 64, warp, lane);
-      gemm<T64, 8>(a2, view(dS, LDS, 1), view(sK, 1, LDI), D, warp, lane);
-      each<T64, 8>(a2, warp, lane, [&](int, int j, float& x) { x *= sdec[j]; });
+      gemm<T64, 8, 8, true>(a1, dOT, view(sAqk, LD6, 1), 64, warp, lane);
+      gemm<T64, 8, 8, true>(a2, view(dS, LDS, 1), view(sK, 1, LDI), D, warp, lane);
+      each<T64, 8, 8, true>(a2, warp, lane, [&](int, int j, float& x) { x *= sdec[j]; });
 #pragma unroll
       for (int ti = 0; ti < T64; ++ti)
 #pragma unroll
         for (int e = 0; e < 4; ++e) a1[ti][e] = scale * a1[ti][e] + a2[ti][e];
-      each<T64, 8>(a1, warp, lane, [&](int v, int j, float& x) { dDT[v * LD6 + j] = x; });
+      each<T64, 8, 8, true>(a1, warp, lane, [&](int v, int j, float& x) { dDT[v * LD6 + j] = x; });
     }
     __syncthreads();
     // dS <- e^{gamma_C} dS + scale (dO^T diag(e^gamma)) Q - dDelta^T W
@@ -283,13 +283,13 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
       float a3[TDD][4], a4[TDD][4];
       zero(a3);
       zero(a4);
-      gemm<TDD, D / 8>(a3, cols_scaled(dOT, seg), view(sQ, LDI, 1), 64, warp, lane);
-      gemm<TDD, D / 8>(a4, view(dDT, LD6, 1), view(sW, LDW, 1), 64, warp, lane);
+      gemm<TDD, D / 8, 8, true>(a3, cols_scaled(dOT, seg), view(sQ, LDI, 1), 64, warp, lane);
+      gemm<TDD, D / 8, 8, true>(a4, view(dDT, LD6, 1), view(sW, LDW, 1), 64, warp, lane);
 #pragma unroll
       for (int ti = 0; ti < TDD; ++ti)
 #pragma unroll
         for (int e = 0; e < 4; ++e) a3[ti][e] = scale * a3[ti][e] - a4[ti][e];
-      each<TDD, D / 8>(a3, warp, lane, [&](int v, int c, float& x) {
+      each<TDD, D / 8, 8, true>(a3, warp, lane, [&](int v, int c, float& x) {
         dS[v * LDS + c] = gC * dS[v * LDS + c] + x;
       });
     }
