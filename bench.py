@@ -54,7 +54,7 @@ def fwd_traffic():
     import hashlib
     csrc = os.path.join(ROOT, "chunked_linear_recurrence_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("fwd_split.cu", "fwd_tc.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
+    for f in ("fwd_split.cu", "tmap.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     try:

@@ -10,7 +10,7 @@
 #include "api_internal.cuh"
 #include "common.cuh"
 #include "fwd_split.cuh"
-#include "fwd_tc.cuh"
+#include "tmap.cuh"
 #include "scan.cuh"
 #include "simt_chunk.cuh"
 
@@ -163,7 +163,9 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
 }
 
 size_t sf_gdn_summary_workspace(const sf_gdn_shape* shape, int R) {
-  (void)shape; (void)R;
+  // BF16 with K = V = 128 runs on the split kernel (records pass through a ring)
+  if (shape && shape->dtype == SF_BF16 && shape->K == 128 && shape->V == 128 && R > 0)
+    return sfg::split_summary_workspace(R, shape->H > 0 ? shape->H : 1);
   return kStatusBytes;
 }
 
@@ -191,7 +193,7 @@ sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const
   const bool bf16 = shape->dtype == SF_BF16;
   cudaError_t e;
   if (bf16 && shape->K == 128 && sfg::tc_fwd_available())
-    e = sfg::launch_tc(p, sfg::TC_MODE_SUMMARY, reinterpret_cast<int*>(workspace), cs);
+    e = sfg::launch_split_summary(p, workspace, reinterpret_cast<int*>(workspace), cs);
   else
     e = sfg::launch_simt_chain(p, sfg::MODE_SUMMARY, bf16, shape->K, R, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);

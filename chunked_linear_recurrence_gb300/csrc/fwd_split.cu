@@ -35,6 +35,12 @@
 // (-W)^T = K^T (-T'')^T, U^T = V^T T'^T (all N = 64), T' = T diag(beta),
 // T'' = T diag(beta e^gamma), the 64x64 solve in FP32 with TF32 merges (solve::).
 //
+// Segment summaries (the affine map S_out = S_in P + E of a token range) run on the same
+// kernel: the chain from S0 = 0 with the value term gives E, the chain from S0 = I
+// without it gives P (it multiplies S by e^{gamma_C} I - W^T diag(dec) K per chunk).  Each
+// chunk's record -- (-W)^T, U^T and the decays only -- is prepared once and read by two
+// chain CTAs, j for E and nch + j for P; its ring slot is free when both have copied it.
+//
 // Every wait (mbarrier or global flag) is bounded; a CTA that gives up raises a
 // global abort flag that every other CTA polls, writes SF_ERR_TIMEOUT to the status
 // word, lets its own copies land, frees its TMEM and returns.
@@ -45,7 +51,7 @@
 
 #include "common.cuh"
 #include "fwd_split.cuh"
-#include "fwd_tc.cuh"
+#include "tmap.cuh"
 #include "solve_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -58,7 +64,15 @@ constexpr int D = 128;
 constexpr int NTHR = 512;
 constexpr int NSLOT = 8;          // ring slots per chain CTA
 constexpr int NBUF = 3;           // record buffers in a chain CTA's shared memory
-constexpr int MAX_NCH = 64;       // chain CTAs at most
+constexpr int MAX_NCH = 64;       // chain CTAs that own record streams, at most
+// Stream-owning chain CTAs of a segment-summary launch, at most (each with a P twin).  The
+// summary's chains (two per (range, head), about 2 us per chunk step) and its preparation
+// (about 6 us per record on each of a CTA's two pipelines) balance near 44 + 44 chain CTAs
+// and 64 preparation CTAs on 152 SMs.
+#ifndef SF_SUMMARY_CHAINS
+#define SF_SUMMARY_CHAINS 44
+#endif
+static_assert(SF_SUMMARY_CHAINS >= 1 && SF_SUMMARY_CHAINS <= MAX_NCH, "summary chain CTAs");
 constexpr int FLAG_STRIDE = 32;   // words between chain CTAs' flags: one 128-byte line each
 
 // ---- record (global ring slot, and the chain CTA's shared-memory copy) ----
@@ -128,6 +142,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, false, false);   // both K-major
 constexpr uint32_t ID_AMN = idesc_bf16(128, 64, true, false);    // A MN-major (X^T from a tile)
 constexpr uint32_t ID_MG = idesc_bf16(128, 128, false, true);    // A@tmem, B MN-major, N = 128
+constexpr uint32_t ID_MG64 = idesc_bf16(128, 64, false, true);   // the same, N = 64
 
 // ---- mbarriers ----
 enum {
@@ -181,10 +196,35 @@ struct SplitParams {
   int* sstart;               // packed: [N*H] first stream position of each chain in its CTA
   int* lenj;                 // packed: [nch] stream length of each chain CTA
   int* sortj;                // packed: [nch] chain CTAs by stream length, longest first
+  // segment summaries (twin != 0): chain x = n H + h is token range n of `bounds`; chain
+  // CTA j < nch runs it from S0 = 0 with the value term (-> sumE), chain CTA nch + j runs
+  // the same records from S0 = I without it (-> sumP)
+  const int32_t* bounds;     // [N,2] token ranges, else NULL
+  float* sumP;               // [N,H,K,K]
+  float* sumE;               // [N,H,V,K]
+  int twin;
   int B, T, H, N;
   int nch, nprep;
   float scale;
 };
+
+// Token rows [bos, eos) of chain x = n H + h: sequence n (dense rows or cu_seqlens), or
+// token range n of `bounds`.  A range out of [0, B T], reversed or crossing a batch row is
+// empty here and returns false.
+__device__ __forceinline__ bool chain_span(const SplitParams& p, int x, int64_t& bos,
+                                           int64_t& eos) {
+  const int n = x / p.H;
+  if (!p.bounds) {
+    seq_span(n, p.B, p.T, p.cu, bos, eos);
+    return true;
+  }
+  const int64_t total = (int64_t)p.B * p.T;
+  const int64_t r0 = p.bounds[2 * n], r1 = p.bounds[2 * n + 1];
+  const bool ok = r0 >= 0 && r1 >= r0 && r1 <= total && (r1 == r0 || r0 / p.T == (r1 - 1) / p.T);
+  bos = ok ? r0 : 0;
+  eos = ok ? r1 : 0;
+  return ok;
+}
 
 // About 2 s at the GB300's clocks.
 constexpr long long kWaitLimitCycles = 4000000000ll;
@@ -251,8 +291,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
 // Geometry.  Chain CTA j owns the chains x = j + nch t (t = 0, 1, ...; x = n H + h) and
 // walks their chunks in order: its stream position s is chunk c of one of them.  Records
 // are produced in the order (s, j): every chain CTA's position s before any s + 1, the
-// CTAs with the longer streams first.  Dense inputs have closed forms; packed inputs use
-// the per-chain stream starts and per-CTA stream lengths built by split_setup_kernel.
+// CTAs with the longer streams first.  Dense inputs have closed forms; packed inputs and
+// token ranges use the per-chain stream starts and per-CTA stream lengths built by
+// split_setup_kernel.
 struct Geo {
   const SplitParams* p;
   int H, NH, nch, ncd, q, r;
@@ -270,7 +311,7 @@ struct Geo {
     H = pr.H;
     NH = pr.N * pr.H;
     nch = pr.nch;
-    packed = pr.cu != nullptr;
+    packed = pr.cu != nullptr || pr.bounds != nullptr;
     ncd = (pr.T + CHUNK - 1) / CHUNK;
     q = NH / nch;
     r = NH % nch;
@@ -285,9 +326,7 @@ struct Geo {
     }
   }
   __device__ int chains_of(int j) const { return (NH - j + nch - 1) / nch; }
-  __device__ void span(int x, int64_t& bos, int64_t& eos) const {
-    seq_span(x / H, p->B, p->T, p->cu, bos, eos);
-  }
+  __device__ bool span(int x, int64_t& bos, int64_t& eos) const { return chain_span(*p, x, bos, eos); }
   __device__ int len_of(int j) const { return packed ? lenj[j] : chains_of(j) * ncd; }
   // w-th record in production order -> (chain CTA, stream position)
   __device__ void item(long long w, int& j, int& s) const {
@@ -353,11 +392,16 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
                                           const Geo& geo, uint8_t* sm, uint32_t sb,
                                           uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.x, H = p.H;
+  const int H = p.H;
+  // segment summaries: chain CTA nch + j is the P twin of chain CTA j (same chains, same
+  // records and ring); it reads (-W)^T and the decays only and has no output
+  const bool summ = p.twin != 0, ptwin = summ && (int)blockIdx.x >= geo.nch;
+  const int j = ptwin ? (int)blockIdx.x - geo.nch : (int)blockIdx.x;   // the stream's owner
   const int cnt = geo.chains_of(j);
   const int len = geo.len_of(j);
   const uint8_t* ringj = p.ring + (size_t)j * NSLOT * REC_BYTES;
   const uint32_t* readyj = p.ready + (size_t)j * FLAG_STRIDE;
+  uint32_t* const consumed_me = p.consumed + (size_t)blockIdx.x * FLAG_STRIDE;
 
   if (warp < 4) {
     reg_dealloc<RC_CTL>();
@@ -373,7 +417,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         bool ok = true;
         auto release_to = [&](int n) {
           fence_proxy_async_global();
-          st_release_u32(p.consumed + (size_t)j * FLAG_STRIDE, (uint32_t)n);
+          st_release_u32(consumed_me, (uint32_t)n);
           rel = n;
         };
         int s = 0, t = 0, c = 0, ncx = 0;
@@ -393,10 +437,19 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           uint8_t* buf = sm + b * C_BUF;
           const int row0 = (int)(bos + (int64_t)c * CHUNK), h = (j + geo.nch * (t - 1)) % H;
           const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
-          mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
+          if (!summ) {
+            mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, &bars[C_RECFULL + b]);
+            for (int q4 = 0; q4 < 4; ++q4)
+              bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, &bars[C_RECFULL + b]);
+          } else {
+            // (-W)^T, U^T (not for the P twin) and the decays
+            mbar_arrive_expect_tx(&bars[C_RECFULL + b], (ptwin ? 16384 : 32768) + (REC_BYTES - R_VEC) +
+                                                            2 * C_K_PANEL);
+            bulk_g2s(buf + R_WQ, src + R_WQ, R_WQ_PANEL, &bars[C_RECFULL + b]);
+            if (!ptwin) bulk_g2s(buf + R_U, src + R_U, R_AH - R_U, &bars[C_RECFULL + b]);
+            bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, &bars[C_RECFULL + b]);
+          }
           tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, h, row0);
           tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, h, row0);
           issued = s + 1;
@@ -430,7 +483,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           // [-S W^T | S Qg^T] = S [(-W)^T | Qg^T]
           if (!wait_bar(&bars[C_SREADY], s & 1, cx) ||
               !wait_bar(&bars[C_RECFULL + rb], (s / NBUF) & 1, cx) ||
-              (s >= 2 && !wait_bar(&bars[C_OFREE + b], ((s - 2) >> 1) & 1, cx))) {
+              (!summ && s >= 2 && !wait_bar(&bars[C_OFREE + b], ((s - 2) >> 1) & 1, cx))) {
             raise_abort(cx);
             break;
           }
@@ -439,7 +492,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ta(tm + TM_BUF + 128 * b, tm + TM_SB + kk * 8, bw + (uint64_t)(kk * 2048 >> 4),
-                        ID_MG, kk > 0 ? 1u : 0u);
+                        summ ? ID_MG64 : ID_MG, kk > 0 ? 1u : 0u);
           mma_commit(&bars[C_MERGED]);
           // S <- e^{gamma_C} S + (Delta^T diag(dec)) K, then O += Delta^T Ahat^T
           if (!wait_bar(&bars[C_DREADY], s & 1, cx) || !wait_bar(&bars[C_SSCALED], s & 1, cx)) {
@@ -452,12 +505,14 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_MG, 1u);
           mma_commit(&bars[C_SUDONE]);
-          const uint64_t ba = sdesc_sw128(buf + R_AH, 0, 1024);
+          if (!summ) {
+            const uint64_t ba = sdesc_sw128(buf + R_AH, 0, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ta(tm + TM_BUF + 128 * b + 64, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2),
-                        ID_N64, 1u);
-          mma_commit(&bars[C_ODONE + b]);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ta(tm + TM_BUF + 128 * b + 64, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2),
+                          ID_N64, 1u);
+            mma_commit(&bars[C_ODONE + b]);
+          }
           mma_commit(&bars[C_RECFREE + rb]);
         }
       }
@@ -476,8 +531,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       const int x = j + geo.nch * t;
       const size_t soff = ((size_t)x * D + v) * D + 64 * w;   // states [N*H, V, K]
       int64_t bos, eos;
-      geo.span(x, bos, eos);
+      const bool okr = geo.span(x, bos, eos);
       const int nc = (int)n_chunks(eos - bos);
+      float* const fdst = summ ? (ptwin ? p.sumP : p.sumE) : p.final_state;
+      // entry state element (v, 64 w + e) without S0: zero, or the identity for the P twin
+      auto s_init = [&](int e) -> float { return (ptwin && 64 * w + e == v) ? 1.f : 0.f; };
       // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c]
       // (checkpoint blocks in the threads' order: float4 e of thread st_t at 256 e + st_t)
       float* ck = p.ckpt ? p.ckpt + ((size_t)chunk_slot_base(x / H, p.B, p.T, p.cu) * H + x % H) * D * D +
@@ -485,12 +543,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
                          : nullptr;
       const size_t ck_stride = (size_t)H * D * D;
       if (nc == 0) {
-        // an empty sequence passes its initial state through
-        if (p.final_state) {
-          float4* dst = reinterpret_cast<float4*>(p.final_state + soff);
+        // an empty sequence passes its initial state through (an empty range: the identity
+        // map; an invalid range: NaN)
+        if (fdst) {
+          float4* dst = reinterpret_cast<float4*>(fdst + soff);
           const float4* src = reinterpret_cast<const float4*>(p.s0 + soff);
+          const float nanv = __int_as_float(0x7fc00000);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dst[e] = p.s0 ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int e = 0; e < 16; ++e)
+            dst[e] = p.s0 ? src[e]
+                   : !okr ? make_float4(nanv, nanv, nanv, nanv)
+                          : make_float4(s_init(4 * e), s_init(4 * e + 1), s_init(4 * e + 2), s_init(4 * e + 3));
         }
         continue;
       }
@@ -509,7 +572,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) xv[e] = 0.f;
+          for (int e = 0; e < 64; ++e) xv[e] = s_init(e);
         }
         if (ck) {
           float4* dst = reinterpret_cast<float4*>(ck);
@@ -544,23 +607,27 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         if (!(ok = group_wait(&bars[C_MERGED], s & 1, BAR_STATE, 256, cx))) break;
         tc_fence_after();
         {
-          // Delta^T = U^T - S W^T for columns [32w, 32w + 32)
+          // Delta^T = U^T - S W^T for columns [32w, 32w + 32) (the P twin: -S W^T)
           float a[32];
           tmem_ld32(tl + TM_BUF + 128 * b + 32 * w, a);
           const uint4* urow = reinterpret_cast<const uint4*>(buf + R_U + v * 128);
           uint4 uu[4];
+          if (!ptwin) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) uu[e] = urow[(4 * w + e) ^ (v & 7)];
+            for (int e = 0; e < 4; ++e) uu[e] = urow[(4 * w + e) ^ (v & 7)];
+          }
           const float* dec = reinterpret_cast<const float*>(buf + R_VEC) + 32 * w;
           tmem_ld_wait();
+          if (!ptwin) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uu[e]);
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uu[e]);
 #pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[q2]));
-              a[8 * e + 2 * q2] += f.x;
-              a[8 * e + 2 * q2 + 1] += f.y;
+              for (int q2 = 0; q2 < 4; ++q2) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[q2]));
+                a[8 * e + 2 * q2] += f.x;
+                a[8 * e + 2 * q2 + 1] += f.y;
+              }
             }
           }
           uint32_t d1[16], d2[16];
@@ -591,8 +658,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         float xv[64];
         tmem_ld64(tl + TM_S + 64 * w, xv);
         if (c + 1 == nc) {
-          if (p.final_state) {
-            float4* dst = reinterpret_cast<float4*>(p.final_state + soff);
+          if (fdst) {
+            float4* dst = reinterpret_cast<float4*>(fdst + soff);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
@@ -640,7 +707,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
     const size_t rs = (size_t)H * D;
     bool ok = true;
     int s = 0;
-    for (int t = 0; t < cnt && ok; ++t) {
+    for (int t = 0; t < (summ ? 0 : cnt) && ok; ++t) {
       const int x = j + geo.nch * t, h = x % H;
       int64_t bos, eos;
       geo.span(x, bos, eos);
@@ -897,6 +964,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
+  // segment summaries: no Q (its map is K's) and no Qg^T or Ahat in the records, whose
+  // ring slots are read by two chain CTAs
+  const bool summ = p.twin != 0;
   // item g -> (chain CTA, stream position, head, first row, length)
   auto item = [&](long long g, int& jj, int& s, int& h, int& row0, int& L) {
     geo.item(g, jj, s);
@@ -945,7 +1015,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
 #pragma unroll
           for (int pnl = 0; pnl < 2; ++pnl) {
             tma_prefetch_l2_3d(tmK, 64 * pnl, n.h, n.row0);
-            tma_prefetch_l2_3d(tmQ, 64 * pnl, n.h, n.row0);
+            if (!summ) tma_prefetch_l2_3d(tmQ, 64 * pnl, n.h, n.row0);
             tma_prefetch_l2_3d(tmV, 64 * pnl, n.h, n.row0);
           }
         }
@@ -1013,7 +1083,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           vi[2] = s;
         }
         __syncwarp();
-        if (!done) {
+        if (!done && !summ) {
           // diag(e^gamma), the B operand of Qg^T, once the previous item's Qg^T is done
           if (use >= 1 && !(ok = warp_wait(&bars[P_QGDONE + pp], (use - 1) & 1, cx))) break;
           for (int e = lane; e < 64; e += 32)
@@ -1068,7 +1138,10 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (done) break;
         // this record's ring slot must have been copied out by its chain CTA
         if (lane == 0) {
-          ok = s < NSLOT || poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx);
+          ok = s < NSLOT ||
+               (poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx) &&
+                (!summ || poll_ge(p.consumed + (size_t)(jj + geo.nch) * FLAG_STRIDE,
+                                  (uint32_t)(s - NSLOT + 1), cx)));
           if (ok) mbar_arrive(&bars[P_SLOTOK + pp]);
         }
         if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) {
@@ -1120,7 +1193,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           // Qg^T: the previous item's Qg^T accumulator read out (TMFREE)
           if (u > 0 && !wait_bar(&bars[P_TMFREE + pp], (u - 1) & 1, cx)) { raise_abort(cx); break; }
           tc_fence_after();
-          {
+          if (!summ) {
             // Qg^T = Q^T diag(e^gamma)
             const uint64_t aq = sdesc_sw128(base + P_KQ + kq_q, P_KQ_PANEL, 1024);
             const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
@@ -1244,7 +1317,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         solve::half(AT, base + P_T1, base + P_T2, vs, (warp & 3) & 1, lane);
       } else {
         ok1 = __all_sync(0xffffffffu, wait_bar(&bars[P_SLOTOK + pp], use & 1, cx)) != 0;
-        if (ok1) store_rows(rec + R_AH, stage_ah, ((warp & 3) * 32) & 63, ah, lane);
+        if (ok1 && !summ) store_rows(rec + R_AH, stage_ah, ((warp & 3) * 32) & 63, ah, lane);
       }
       if (!(ok = named_bar_and(bid, 128, ok1))) {
         if (r == 0) raise_abort(cx);
@@ -1259,9 +1332,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       fence_proxy_async_smem();
       named_bar(bid, 128);
       if (r == 0) mbar_arrive(&bars[P_TT + pp]);
-      if (!(ok = group_wait(&bars[P_QGDONE + pp], use & 1, bid, 128, cx))) break;
-      tc_fence_after();
-      {
+      if (!summ) {
+        if (!(ok = group_wait(&bars[P_QGDONE + pp], use & 1, bid, 128, cx))) break;
+        tc_fence_after();
         float x[64];
         uint32_t u[32];
         tmem_ld64(tl + TP_QG, x);
@@ -1307,7 +1380,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
-  const bool is_chain = (int)blockIdx.x < p.nch;
+  const bool is_chain = (int)blockIdx.x < p.nch * (p.twin ? 2 : 1);
   uint8_t* bar_area = sm + (is_chain ? C_BAR : P_BAR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 256);
@@ -1317,7 +1390,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   int* sort_s = len_s + 64;
   int* seg_s = sort_s + 64;
   long long* seg_w = reinterpret_cast<long long*>(seg_s + 66);
-  if (p.cu && tid < p.nch) {
+  const bool packed = p.cu || p.bounds;
+  if (packed && tid < p.nch) {
     len_s[tid] = p.lenj[tid];
     sort_s[tid] = p.sortj[tid];
   }
@@ -1329,7 +1403,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
       // a record buffer is free once its chunk's products are done (MMA commit) and its
       // output tile, staged in it, has been read out (output warps)
-      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], 2);
+      // (summaries have no output)
+      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], p.twin ? 1 : 2);
     } else {
       for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
       mbar_init(&bars[P_FULL], 33);
@@ -1344,7 +1419,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     prefetch_tmap(&tmK);
     if (is_chain && p.out) prefetch_tmap(&tmO);
     if (!is_chain) {
-      prefetch_tmap(&tmQ);
+      if (!p.twin) prefetch_tmap(&tmQ);
       prefetch_tmap(&tmV);
     }
   }
@@ -1355,7 +1430,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (p.cu) {
+  if (packed) {
     if (tid == 0) Geo::build_table(p.nch, len_s, sort_s, seg_s, seg_w);
     __syncthreads();
   }
@@ -1375,14 +1450,14 @@ __global__ void __launch_bounds__(NTHR, 1)
   }
 }
 
-// Packed inputs: each chain's first stream position in its chain CTA, each chain CTA's
+// Packed inputs and token ranges: each chain's first stream position in its chain CTA, each chain CTA's
 // stream length, and the chain CTAs ordered by stream length (longest first).  One CTA.
 __global__ void split_setup_kernel(const SplitParams p) {
   __shared__ int len_s[MAX_NCH];
   const int NH = p.N * p.H, nch = p.nch, tid = threadIdx.x;
   for (int x = tid; x < NH; x += blockDim.x) {
     int64_t b, e;
-    seq_span(x / p.H, p.B, p.T, p.cu, b, e);
+    chain_span(p, x, b, e);
     p.sstart[x] = (int)n_chunks(e - b);
   }
   __syncthreads();
@@ -1406,82 +1481,120 @@ __global__ void split_setup_kernel(const SplitParams p) {
 }
 
 // Workspace: [0, 256) status word; [256, 260) abort flag; [384, 388) the item counter of
-// the preparation CTAs; from 512 consumed, then ready
-// (one 128-byte line per chain CTA each: the flags polled by different CTAs never share
-// a line); the ring from 20480; then (packed inputs) the chain stream starts [N*H],
-// stream lengths [64] and their order [64].
-constexpr size_t WS_ABORT = 256, WS_NEXT = 384, WS_CONSUMED = 512, WS_READY = WS_CONSUMED + MAX_NCH * 128;
+// the preparation CTAs; from 512 consumed (one 128-byte line per chain CTA, P twins
+// included), then ready (one line per stream-owning chain CTA): the flags polled by
+// different CTAs never share a line; the ring from 32768 (one per stream-owning chain
+// CTA); then (packed inputs and token ranges) the chain stream starts [N*H], stream
+// lengths [64] and their order [64].
+constexpr size_t WS_ABORT = 256, WS_NEXT = 384, WS_CONSUMED = 512,
+                 WS_READY = WS_CONSUMED + 2 * MAX_NCH * 128;
 constexpr size_t WS_FLAGS_END = WS_READY + (size_t)MAX_NCH * 128;
-constexpr size_t WS_RING = 20480;
+constexpr size_t WS_RING = 32768;
 static_assert(WS_FLAGS_END <= WS_RING, "workspace flags");
-
-}  // namespace
 
 int chain_ctas(int N, int H) {
   const long long nh = (long long)N * H;
   return (int)(nh < MAX_NCH ? nh : MAX_NCH);
 }
-size_t ws_geo(int N, int H) { return WS_RING + (size_t)chain_ctas(N, H) * NSLOT * REC_BYTES; }
-
-size_t split_fwd_workspace(int N, int H) {
-  return ws_geo(N, H) + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
+// segment summaries: chain CTAs that own streams (each has a P twin)
+int summary_chain_ctas(int R, int H) {
+  const long long nh = (long long)R * H;
+  if (nh <= SF_SUMMARY_CHAINS) return (int)nh;
+  // as few chain CTAs as keep the most chains per CTA at ceil(nh / SF_SUMMARY_CHAINS); the
+  // SMs left over prepare records
+  const long long k = (nh + SF_SUMMARY_CHAINS - 1) / SF_SUMMARY_CHAINS;
+  return (int)((nh + k - 1) / k);
+}
+size_t ws_ring_end(int nch) { return WS_RING + (size_t)nch * NSLOT * REC_BYTES; }
+size_t ws_total(int nch, int N, int H) {
+  return ws_ring_end(nch) + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
 }
 
-cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
-  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1)) return cudaErrorInvalidValue;
+// The launch shared by the forward, the state replay and the segment summaries: flags
+// reset, the packed-geometry setup, tensor maps, then one cooperative launch over every
+// SM (chain CTAs first).  p arrives with its inputs, outputs, mode and nch set.
+cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const void* v, void* out,
+                         int chain_blocks, void* ws, int* status, cudaStream_t st) {
   int dev = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int NH = cp.N * cp.H;
-  const int nch = chain_ctas(cp.N, cp.H);
-  const int nprep = nsm - nch;
+  const int nprep = nsm - chain_blocks;
   if (nprep < 1) return cudaErrorInvalidConfiguration;
-  const int rows = cp.B * cp.T;
+  const int rows = p.B * p.T;
   CUtensorMap mq, mk, mv;
-  if (!make_bf16_map(&mq, cp.q, rows, cp.H) || !make_bf16_map(&mk, cp.k, rows, cp.H) ||
-      !make_bf16_map(&mv, cp.v, rows, cp.H))
-    return cudaErrorInvalidValue;
+  if (!make_bf16_map(&mk, k, rows, p.H) || !make_bf16_map(&mv, v, rows, p.H)) return cudaErrorInvalidValue;
+  mq = mk;   // summaries have no q: K stands in (its products are not used)
+  if (q && !make_bf16_map(&mq, q, rows, p.H)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(gdn_fwd_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   char* w = reinterpret_cast<char*>(ws);
   e = cudaMemsetAsync(w + WS_ABORT, 0, WS_FLAGS_END - WS_ABORT, st);
   if (e != cudaSuccess) return e;
+  const int NH = p.N * p.H;
+  p.status = status;
+  p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
+  p.next_item = reinterpret_cast<uint32_t*>(w + WS_NEXT);
+  p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
+  p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
+  p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
+  p.sstart = reinterpret_cast<int*>(w + ws_ring_end(p.nch));
+  p.lenj = p.sstart + (size_t)NH;
+  p.sortj = p.lenj + MAX_NCH;
+  p.nprep = nprep;
+  if (p.cu || p.bounds) {
+    split_setup_kernel<<<1, 256, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // the output map (the K map stands in when there is no output: it is never used then)
+  CUtensorMap mo = mk;
+  if (out && !make_bf16_map(&mo, out, rows, p.H)) return cudaErrorInvalidValue;
+  void* args[] = {&mq, &mk, &mv, &mo, &p};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
+                                     dim3(chain_blocks + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
+}
+
+}  // namespace
+
+size_t split_fwd_workspace(int N, int H) { return ws_total(chain_ctas(N, H), N, H); }
+size_t split_summary_workspace(int R, int H) { return ws_total(summary_chain_ctas(R, H), R, H); }
+
+cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
+  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1)) return cudaErrorInvalidValue;
   SplitParams p{};
   p.g = cp.g;
   p.beta = cp.beta;
   p.s0 = cp.s0;
   p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
   p.final_state = cp.final_state;
-  p.status = status;
   p.ckpt = cp.ckpt;
-  p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
-  p.next_item = reinterpret_cast<uint32_t*>(w + WS_NEXT);
-  p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
-  p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
-  p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
   p.cu = cp.cu;
-  p.sstart = reinterpret_cast<int*>(w + ws_geo(cp.N, cp.H));
-  p.lenj = p.sstart + (size_t)NH;
-  p.sortj = p.lenj + MAX_NCH;
   p.B = cp.B;
   p.T = cp.T;
   p.H = cp.H;
   p.N = cp.N;
-  p.nch = nch;
-  p.nprep = nprep;
+  p.nch = chain_ctas(cp.N, cp.H);
   p.scale = cp.scale;
-  if (p.cu) {
-    split_setup_kernel<<<1, 256, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  // the output map (the K map stands in when there is no output: it is never used then)
-  CUtensorMap mo = mk;
-  if (cp.out && !make_bf16_map(&mo, cp.out, rows, cp.H)) return cudaErrorInvalidValue;
-  void* args[] = {&mq, &mk, &mv, &mo, &p};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
-                                     dim3(nch + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
+  return launch_split(p, cp.q, cp.k, cp.v, cp.out, p.nch, ws, status, st);
+}
+
+cudaError_t launch_split_summary(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
+  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || !cp.bounds || !cp.P || !cp.E) return cudaErrorInvalidValue;
+  SplitParams p{};
+  p.g = cp.g;
+  p.beta = cp.beta;
+  p.bounds = cp.bounds;
+  p.sumP = cp.P;
+  p.sumE = cp.E;
+  p.twin = 1;
+  p.B = cp.B;
+  p.T = cp.T;
+  p.H = cp.H;
+  p.N = cp.N;
+  p.nch = summary_chain_ctas(cp.N, cp.H);
+  p.scale = 1.f;
+  return launch_split(p, nullptr, cp.k, cp.v, nullptr, 2 * p.nch, ws, status, st);
 }
 
 }  // namespace sfg

@@ -17,4 +17,12 @@ size_t split_fwd_workspace(int N, int H);
 // p.out / p.final_state may be NULL.
 cudaError_t launch_split_fwd(const ChainParams& p, void* ws, int* status, cudaStream_t st);
 
+// Workspace bytes of the segment summaries for R token ranges of H heads.
+size_t split_summary_workspace(int R, int H);
+// Segment summaries of p.N = R token ranges p.bounds ([R,2]) of the dense rows (p.B, p.T > 0)
+// into p.P ([R,H,K,K]) and p.E ([R,H,V,K]) on the split kernel: each chunk's record is
+// prepared once and read by two chain CTAs, one from S0 = 0 with the value term (E), one
+// from S0 = I without it (P).  ws: split_summary_workspace(R, H) bytes, first 256 unused.
+cudaError_t launch_split_summary(const ChainParams& p, void* ws, int* status, cudaStream_t st);
+
 }  // namespace sfg

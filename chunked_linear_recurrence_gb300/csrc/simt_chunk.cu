@@ -3,8 +3,9 @@
 // These kernels carry every matrix product in FP32 on the CUDA cores.  They
 // are the path for FP32 inputs (which need FP32 accuracy end to end) and for
 // head size 64, and they compute the backward for every supported dtype.
-// The BF16, head-size-128 forward runs on the tensor-core kernel instead
-// (fwd_tc.cu); the two never substitute for each other at run time.
+// The BF16, head-size-128 forward and segment summaries run on the split
+// tensor-core kernel instead (fwd_split.cu); the two never substitute for each
+// other at run time.
 //
 // Work decomposition (StateFlow, section 2.2, Eq. 2: Pre / ST / Out per chunk;
 // section 3.4.1, Eq. 16: the state transition is tiled along the value

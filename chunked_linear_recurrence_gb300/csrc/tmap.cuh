@@ -1,0 +1,14 @@
+// tmap.cuh -- TMA tensor maps of the BF16 token-major tensors ([rows, H, 128]).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sfg {
+
+// True when this build can encode TMA descriptors (the tensor-core kernels are usable).
+bool tc_fwd_available();
+// TMA descriptor of a [rows, H, 128] BF16 tensor viewed as (128, H, rows), box 64 x 1 x 64,
+// 128-byte swizzle (one head's 64-token chunk, in two 64-column panels).
+bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int H);
+
+}  // namespace sfg

@@ -38,15 +38,45 @@ def test_summary_matches_oracle(dtype, D):
     assert not E[2].any() and not E[5].any()
 
 
-def test_summary_invalid_bounds_give_nan():
-    inp = small_inputs(2, 100, 1, 64, torch.float32, seed=2, s0=False)
+@pytest.mark.parametrize("dtype,D", [(torch.float32, 64), (torch.bfloat16, 128)])
+def test_summary_invalid_bounds_give_nan(dtype, D):
+    inp = small_inputs(2, 100, 1, D, dtype, seed=2, s0=False)
     bounds = torch.tensor([[0, 50], [90, 110], [-1, 5], [10, 5], [0, 201]], dtype=torch.int32)
     P, E = _sf().sf_gdn_segment_summary(inp["k"], inp["v"], inp["gate"], inp["beta"],
                                         bounds.cuda())
     torch.cuda.synchronize()
-    assert torch.isfinite(P[0]).all()
+    assert torch.isfinite(P[0]).all() and torch.isfinite(E[0]).all()
     for r in (1, 2, 3, 4):      # crosses a batch row / negative / reversed / past the end
         assert torch.isnan(P[r]).all() and torch.isnan(E[r]).all(), r
+
+
+def test_summary_more_ranges_than_chain_ctas():
+    """BF16, K = V = 128: 23 ranges x 2 heads = 46 (range, head) chains, more than the 32
+    chain CTAs that own record streams (each with its P twin), so some walk two chains;
+    range lengths from 0 to 7 chunks, starts not on chunk boundaries, a partial last chunk."""
+    B, T, H, D = 2, 520, 2, 128
+    inp = small_inputs(B, T, H, D, torch.bfloat16, seed=77, s0=False)
+    inp["gate"] *= 0.05
+    g = torch.Generator().manual_seed(5)
+    rows = []
+    for r in range(23):
+        b = r % B
+        n = int(torch.randint(0, 450, (1,), generator=g))
+        st = int(torch.randint(0, T - n + 1, (1,), generator=g))
+        rows.append((b * T + st, b * T + st + n))
+    rows[4] = (600, 600)             # empty
+    rows[9] = (T, 2 * T)             # a whole batch row
+    bounds = torch.tensor(rows, dtype=torch.int32)
+    P, E = _sf().sf_gdn_segment_summary(inp["k"], inp["v"], inp["gate"], inp["beta"],
+                                        bounds.cuda())
+    torch.cuda.synchronize()
+    Pr, Er = oracle.segment_summary(f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                                    f64(inp["beta"]), bounds.numpy())
+    tol = TOL[torch.bfloat16]
+    for r in range(len(rows)):
+        assert rel_err(P[r], Pr[r]) <= tol, r
+        assert rel_err(E[r], Er[r]) <= tol or np.abs(Er[r]).max() == 0, r
+    assert torch.equal(P[4], torch.eye(D, device="cuda").expand(H, D, D)) and not E[4].any()
 
 
 @pytest.mark.parametrize("D", [64, 128])
