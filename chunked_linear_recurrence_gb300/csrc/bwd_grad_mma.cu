@@ -1,5 +1,8 @@
 // bwd_grad_mma.cu -- token gradients of one chunk of the chunked gated delta rule on the
-// warp-level tensor cores (mma.sync m16n8k8, TF32 operands, FP32 accumulation).
+// warp-level tensor cores, FP32 accumulation: for BF16 inputs the ten products with k = D
+// take BF16 operand pairs (mma.sync m16n8k16; the forward's tensor-core operand precision),
+// the rest -- the k = 64 products, among them every product with T -- TF32 (m16n8k8); FP32
+// inputs use TF32 throughout.
 //
 // StateFlow section 3.4.2, Eq. 18 ("OutputGrad" and "PrepGrad"): given the chunk's entry
 // state S (state replay) and the cotangent dSn of its exit state (reverse state chain),
@@ -31,11 +34,14 @@ namespace {
 using namespace mt;
 constexpr int NWG = 16;          // warps
 constexpr int NTG = 32 * NWG;
-// Leading dimensions (floats) of the FP32 tiles: 4 mod 32, so that the mma fragment loads
-// (8 rows x 4 columns per instruction) fall on distinct banks.
+// Leading dimensions (floats) of the FP32 tiles.  4 mod 32 where TF32 fragments are loaded
+// (8 rows x 4 columns per instruction fall on distinct banks); 8 mod 32 for the [64][D]
+// tiles of BF16 inputs, read as BF16 pairs (8-byte loads, 8 rows x 8 columns per half-warp).
 constexpr int G_LD6 = 68;
-template <int D>
-__host__ __device__ constexpr int g_ldf() { return D + 4; }
+template <typename Tin, int D>
+__host__ __device__ constexpr int g_ldf() {
+  return D + (std::is_same<Tin, __nv_bfloat16>::value ? 8 : 4);
+}
 
 struct CtaBarG {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
@@ -49,6 +55,15 @@ struct TiledState {
   __device__ __forceinline__ float operator()(int r, int c) const {
     return TR ? p[ckpt_tiled_off(c, r)] : p[ckpt_tiled_off(r, c)];
   }
+  // BF16 pairs along c and along r (adjacent k of a state row are adjacent in the block)
+  __device__ __forceinline__ uint32_t pc(int r, int c) const {
+    return TR ? mt::pk(p[ckpt_tiled_off(c, r)], p[ckpt_tiled_off(c + 1, r)])
+              : mt::pair_at(p + ckpt_tiled_off(r, c));
+  }
+  __device__ __forceinline__ uint32_t pr(int r, int c) const {
+    return TR ? mt::pair_at(p + ckpt_tiled_off(c, r))
+              : mt::pk(p[ckpt_tiled_off(r, c)], p[ckpt_tiled_off(r + 1, c)]);
+  }
 };
 
 }  // namespace
@@ -57,7 +72,9 @@ template <typename Tin, int D, bool kTiled>
 __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) {
   static_assert(!kTiled || D == 128, "tiled checkpoints have D = 128");
   constexpr int LDI = D + 8;      // input tiles (Tin)
-  constexpr int LDF = g_ldf<D>();  // fp32 [64][D] tiles
+  constexpr int LDF = g_ldf<Tin, D>();  // fp32 [64][D] tiles
+  // products with k = D on BF16 operand pairs for BF16 inputs (TF32 for FP32 inputs)
+  constexpr bool B16 = std::is_same<Tin, __nv_bfloat16>::value;
   constexpr int LD6 = G_LD6;
   constexpr int NTD = D / 8;      // 8-column tiles of a 64 x D output
   constexpr int TD = 4 * NTD / NWG;  // tiles per warp of a 64 x D output
@@ -160,13 +177,11 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   __syncthreads();
   const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), Vv = view(sV, LDI, 1),
              dOv = view(sdO, LDI, 1);
-  const auto KvT = view(sK, 1, LDI), VvT = view(sV, 1, LDI);
-  const auto dSnT = view(dSn, 1, D), dSnv = view(dSn, D, 1);
   const auto Sv = [&] {
-    if constexpr (kTiled) return TiledState<false>{S}; else return view(S, D, 1);
+    if constexpr (kTiled) return TiledState<false>{S}; else return rm(S, D);
   }();
   const auto SvT = [&] {
-    if constexpr (kTiled) return TiledState<true>{S}; else return view(S, 1, D);
+    if constexpr (kTiled) return TiledState<true>{S}; else return cm(S, D);
   }();
 
   // Ak = Gamma o K K^T (strict lower), Aqk = Gamma o Q K^T (lower incl. diagonal)
@@ -174,8 +189,8 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     float a1[T6][4], a2[T6][4];
     zero(a1);
     zero(a2);
-    gemm<T6, 8, NWG, true>(a1, Kv, KvT, D, warp, lane);
-    gemm<T6, 8, NWG, true>(a2, Qv, KvT, D, warp, lane);
+    gemmx<B16, T6, 8, NWG, true>(a1, rm(sK, LDI), cm(sK, LDI), D, warp, lane);
+    gemmx<B16, T6, 8, NWG, true>(a2, rm(sQ, LDI), cm(sK, LDI), D, warp, lane);
     each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) {
       sM[i * LD6 + j] = (j < i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
     });
@@ -209,18 +224,18 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
   }
   __syncthreads();
-  const auto B1v = view(B1, LDF, 1), B2v = view(B2, LDF, 1), B3v = view(B3, LDF, 1);
+  const auto B1v = view(B1, LDF, 1), B3v = view(B3, LDF, 1);
   // Delta = U - W S^T (B2);  dDelta = scale Aqk^T dO + diag(dec) K dSn^T (B3)
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG, true>(acc, B1v, SvT, D, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, rm(B1, LDF), SvT, D, warp, lane);
     float acc2[TD][4];
     zero(acc2);
     gemm<TD, NTD, NWG, true>(acc2, view(sP, 1, LD6), dOv, 64, warp, lane);
     float acc3[TD][4];
     zero(acc3);
-    gemm<TD, NTD, NWG, true>(acc3, Kv, dSnT, D, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc3, rm(sK, LDI), cm(dSn, D), D, warp, lane);
     __syncthreads();   // every warp has read W (B1), U (B2) as operands of its own tiles only
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int r, float& x) { B2[i * LDF + r] -= x; });
     each<TD, NTD, NWG, true>(acc3, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG, true>(a1, dOv, view(B2, 1, LDF), D, warp, lane);
+    gemmx<B16, T6, 8, NWG, true>(a1, rm(sdO, LDI), cm(B2, LDF), D, warp, lane);
     __syncthreads();   // sP (Aqk) fully read as an operand before it is overwritten
     each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) {
       float gval = 0.f;
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG, true>(acc, rows_scaled(dOv, ssc), Sv, D, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, rows_scaled(rm(sdO, LDI), ssc), Sv, D, warp, lane);
     row_dot<TD, NTD, NWG, true>(acc, Qv, sdgam, warp, lane);
 #pragma unroll
     for (int ti = 0; ti < TD; ++ti)
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG, true>(acc, B2v, dSnv, D, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, rm(B2, LDF), rm(dSn, D), D, warp, lane);
     row_dot<TD, NTD, NWG, true>(acc, Kv, sz, warp, lane);
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int, float& x) { x *= sdec[i]; });
 #pragma unroll
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     float acc[TD][4], acc2[TD][4];
     zero(acc);
     zero(acc2);
-    gemm<TD, NTD, NWG, true>(acc, B3v, Sv, D, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, rm(B3, LDF), Sv, D, warp, lane);
     gemm<TD, NTD, NWG, true>(acc2, TvT, B3v, 64, warp, lane);
     __syncthreads();
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = -x; });
@@ -331,8 +346,8 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float a1[T6][4];
     zero(a1);
-    gemm<T6, 8, NWG, true>(a1, B3v, cols_scaled(VvT, sb), D, warp, lane);
-    gemm<T6, 8, NWG, true>(a1, B1v, cols_scaled(KvT, sbeg), D, warp, lane);
+    gemmx<B16, T6, 8, NWG, true>(a1, rm(B3, LDF), cols_scaled(cm(sV, LDI), sb), D, warp, lane);
+    gemmx<B16, T6, 8, NWG, true>(a1, rm(B1, LDF), cols_scaled(cm(sK, LDI), sbeg), D, warp, lane);
     each<T6, 8, NWG, true>(a1, warp, lane, [&](int i, int j, float& x) { sP[i * LD6 + j] = x; });
   }
   __syncthreads();
@@ -434,7 +449,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
 
 template <typename Tin, int D, bool kTiled = false>
 static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
-  const size_t smem = sizeof(float) * (3 * 64 * G_LD6 + 3 * 64 * g_ldf<D>() + 11 * 64) +
+  const size_t smem = sizeof(float) * (3 * 64 * G_LD6 + 3 * 64 * g_ldf<Tin, D>() + 11 * 64) +
                       sizeof(Tin) * 4 * 64 * (D + 8);
   auto kern = mma_bwd_grad_kernel<Tin, D, kTiled>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -1,6 +1,7 @@
-// mma_tiles.cuh -- warp-level tensor-core tiles (mma.sync m16n8k8, TF32 operands, FP32
-// accumulation) for the backward kernels: element views of shared/global operands, a
-// tile GEMM over a warp's fixed set of 16x8 output tiles, and tile epilogues.
+// mma_tiles.cuh -- warp-level tensor-core tiles for the backward kernels: element views
+// of shared/global operands, tile GEMMs over a warp's fixed set of 16x8 output tiles
+// (mma.sync m16n8k8 with TF32 operands, or m16n8k16 with BF16 operand pairs; FP32
+// accumulation, the same accumulator layout), and tile epilogues.
 #pragma once
 
 #include "common.cuh"
@@ -18,12 +19,68 @@ struct View {
 };
 template <typename T>
 __device__ __forceinline__ View<T> view(const T* p, int sr, int sc) { return View<T>{p, sr, sc}; }
+
+// BF16 pairs: the low half holds the first element (the lower k index of an mma operand).
+__device__ __forceinline__ uint32_t pk(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 upk(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+// Two adjacent elements p[0], p[1] as a BF16 pair (p 4-byte aligned for BF16, 8-byte for FP32).
+__device__ __forceinline__ uint32_t pair_at(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+__device__ __forceinline__ uint32_t pair_at(const float* p) {
+  const float2 f = *reinterpret_cast<const float2*>(p);
+  return pk(f.x, f.y);
+}
+
+// Row-major (element (r, c) at p[r ld + c]) and column-major (at p[c ld + r]) views with
+// the BF16 pair accessors of the m16n8k16 operands: pc(r, c) = (x(r, c), x(r, c + 1)),
+// pr(r, c) = (x(r, c), x(r + 1, c)).  The pair along the contiguous index is one load
+// (ld even, the first index of the pair even).
+template <typename T>
+struct RM {
+  const T* p;
+  int ld;
+  __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[r * ld + c]); }
+  __device__ __forceinline__ uint32_t pc(int r, int c) const { return pair_at(p + r * ld + c); }
+  __device__ __forceinline__ uint32_t pr(int r, int c) const {
+    return pk(to_f(p[r * ld + c]), to_f(p[(r + 1) * ld + c]));
+  }
+};
+template <typename T>
+struct CM {
+  const T* p;
+  int ld;
+  __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[c * ld + r]); }
+  __device__ __forceinline__ uint32_t pc(int r, int c) const {
+    return pk(to_f(p[c * ld + r]), to_f(p[(c + 1) * ld + r]));
+  }
+  __device__ __forceinline__ uint32_t pr(int r, int c) const { return pair_at(p + c * ld + r); }
+};
+template <typename T>
+__device__ __forceinline__ RM<T> rm(const T* p, int ld) { return RM<T>{p, ld}; }
+template <typename T>
+__device__ __forceinline__ CM<T> cm(const T* p, int ld) { return CM<T>{p, ld}; }
+
 // rows scaled by s[r]
 template <typename V>
 struct RowScaled {
   V v;
   const float* s;
   __device__ __forceinline__ float operator()(int r, int c) const { return s[r] * v(r, c); }
+  // (pairs: exact for BF16 base views, whose elements the pair carries unrounded)
+  __device__ __forceinline__ uint32_t pc(int r, int c) const {
+    const float2 x = upk(v.pc(r, c));
+    return pk(s[r] * x.x, s[r] * x.y);
+  }
+  __device__ __forceinline__ uint32_t pr(int r, int c) const {
+    const float2 x = upk(v.pr(r, c));
+    return pk(s[r] * x.x, s[r + 1] * x.y);
+  }
 };
 // columns scaled by s[c]
 template <typename V>
@@ -31,6 +88,14 @@ struct ColScaled {
   V v;
   const float* s;
   __device__ __forceinline__ float operator()(int r, int c) const { return s[c] * v(r, c); }
+  __device__ __forceinline__ uint32_t pc(int r, int c) const {
+    const float2 x = upk(v.pc(r, c));
+    return pk(s[c] * x.x, s[c + 1] * x.y);
+  }
+  __device__ __forceinline__ uint32_t pr(int r, int c) const {
+    const float2 x = upk(v.pr(r, c));
+    return pk(s[c] * x.x, s[c] * x.y);
+  }
 };
 template <typename V>
 __device__ __forceinline__ RowScaled<V> rows_scaled(V v, const float* s) { return RowScaled<V>{v, s}; }
@@ -97,6 +162,64 @@ __device__ __forceinline__ void gemm(float (&acc)[NTILE][4], const AV& A, const 
       mma_tf32_16x8x8(acc[ti], a[ia], b[ib]);
     }
   }
+}
+
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (&a)[4],
+                                                 const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// gemm with BF16 operands (m16n8k16, K a multiple of 16): A and B give BF16 pairs along k,
+// A.pc(m, k) = (A(m, k), A(m, k + 1)) and B.pr(k, n) = (B(k, n), B(k + 1, n)).  Lane (g, t)
+// holds rows m0 + g and m0 + g + 8 at k = k0 + 2t and k0 + 2t + 8 of A, column n0 + g at the
+// same k of B; the accumulator layout is that of gemm.
+template <int NTILE, int NTN, int NW = 8, bool BLK = false, typename AV, typename BV>
+__device__ __forceinline__ void gemm16(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
+                                       int warp, int lane) {
+  using M = TileMap<NTILE, NTN, NW, BLK>;
+  constexpr int NA = BLK ? M::WM : NTILE;
+  constexpr bool kShareB = !BLK && (NW % NTN) == 0;
+  constexpr int NB = BLK ? M::WN : (kShareB ? 1 : NTILE);
+  const int g = lane >> 2, t2 = 2 * (lane & 3);
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[NA][4], b[NB][2];
+#pragma unroll
+    for (int ia = 0; ia < NA; ++ia) {
+      int m0, n0;
+      M::at(warp, BLK ? ia * M::WN : ia, m0, n0);
+      a[ia][0] = A.pc(m0 + g, k0 + t2);
+      a[ia][1] = A.pc(m0 + g + 8, k0 + t2);
+      a[ia][2] = A.pc(m0 + g, k0 + t2 + 8);
+      a[ia][3] = A.pc(m0 + g + 8, k0 + t2 + 8);
+    }
+#pragma unroll
+    for (int ib = 0; ib < NB; ++ib) {
+      int m0, n0;
+      M::at(warp, ib, m0, n0);
+      b[ib][0] = B.pr(k0 + t2, n0 + g);
+      b[ib][1] = B.pr(k0 + t2 + 8, n0 + g);
+    }
+#pragma unroll
+    for (int ti = 0; ti < NTILE; ++ti) {
+      const int ia = BLK ? ti / M::WN : ti;
+      const int ib = BLK ? ti % M::WN : (kShareB ? 0 : ti);
+      mma_bf16_16x8x16(acc[ti], a[ia], b[ib]);
+    }
+  }
+}
+
+// gemm16 for BF16 inputs (the forward's operand precision), gemm (TF32) for FP32 inputs.
+template <bool B16, int NTILE, int NTN, int NW = 8, bool BLK = false, typename AV, typename BV>
+__device__ __forceinline__ void gemmx(float (&acc)[NTILE][4], const AV& A, const BV& B, int K,
+                                      int warp, int lane) {
+  if constexpr (B16)
+    gemm16<NTILE, NTN, NW, BLK>(acc, A, B, K, warp, lane);
+  else
+    gemm<NTILE, NTN, NW, BLK>(acc, A, B, K, warp, lane);
 }
 
 template <int NTILE>
