@@ -119,13 +119,14 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
     ovec[tid] = eg;
     ovec[64 + tid] = expf(sgam[63] - sgam[tid]);
   }
-  const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), KvT = view(sK, 1, LDI);
+  const auto Kv = view(sK, LDI, 1);
   {
     float a1[4][4], a2[4][4];
     zero(a1);
     zero(a2);
-    gemm<4, 8, 8, true>(a1, Kv, KvT, D, warp, lane);
-    gemm<4, 8, 8, true>(a2, Qv, KvT, D, warp, lane);
+    // BF16 inputs on BF16 mma: the products are exact, the sums FP32
+    gemm16<4, 8, 8, true>(a1, rm(sK, LDI), cm(sK, LDI), D, warp, lane);
+    gemm16<4, 8, 8, true>(a2, rm(sQ, LDI), cm(sK, LDI), D, warp, lane);
     each<4, 8, 8, true>(a1, warp, lane, [&](int i, int j, float& x) {
       sA[i * LD6 + j] = (j < i) ? sb[i] * expf(sgam[i] - sgam[j]) * x : 0.f;
     });
@@ -175,7 +176,8 @@ struct ChainBuf {
 template <int D, int BV>
 __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p, const float* fac) {
   using B = ChainBuf<D, BV>;
-  constexpr int LDS = c_ldd<D>(), LD6 = C_LD6, LDI = B::LDI, LDO = B::LDO, LDW = c_ldd<D>();
+  // dS rows: 8 mod 32 floats, for the conflict-free 8-byte BF16-pair loads of dS K^T
+  constexpr int LDS = D + 8, LD6 = C_LD6, LDI = B::LDI, LDO = B::LDO, LDW = c_ldd<D>();
   constexpr int MB = BV / 16;                 // 16-row bands of the cotangent tile
   constexpr int T64 = MB * 8 / 8;             // tiles per warp of a BV x 64 output
   constexpr int TDD = MB * (D / 8) / 8;       // tiles per warp of a BV x D output
@@ -269,7 +271,8 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
       zero(a1);
       zero(a2);
       gemm<T64, 8, 8, true>(a1, dOT, view(sAqk, LD6, 1), 64, warp, lane);
-      gemm<T64, 8, 8, true>(a2, view(dS, LDS, 1), view(sK, 1, LDI), D, warp, lane);
+      // (k = D: BF16 operand pairs, the forward's tensor-core precision)
+      gemm16<T64, 8, 8, true>(a2, rm(dS, LDS), cm(sK, LDI), D, warp, lane);
       each<T64, 8, 8, true>(a2, warp, lane, [&](int, int j, float& x) { x *= sdec[j]; });
 #pragma unroll
       for (int ti = 0; ti < T64; ++ti)
@@ -315,7 +318,7 @@ static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slot
     if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTB, smem, st>>>(p, fac);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const size_t smem = sizeof(float) * (BV * c_ldd<D>() + BV * C_LD6) + 2 * ChainBuf<D, BV>::BYTES;
+  const size_t smem = sizeof(float) * (BV * (D + 8) + BV * C_LD6) + 2 * ChainBuf<D, BV>::BYTES;
   auto kern = mma_bwd_chain_kernel<D, BV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -1,8 +1,8 @@
 // bwd_grad_mma.cu -- token gradients of one chunk of the chunked gated delta rule on the
-// warp-level tensor cores, FP32 accumulation: for BF16 inputs the ten products with k = D
-// take BF16 operand pairs (mma.sync m16n8k16; the forward's tensor-core operand precision),
-// the rest -- the k = 64 products, among them every product with T -- TF32 (m16n8k8); FP32
-// inputs use TF32 throughout.
+// warp-level tensor cores, FP32 accumulation: for BF16 inputs every product but the four of
+// the dA path (T^T dDelta, T^T dW, dT T^T, T^T X1) takes BF16 operand pairs (mma.sync
+// m16n8k16; the forward's tensor-core operand precision: W and U from BF16 T'' and T' as
+// there); those four stay TF32 (m16n8k8), and FP32 inputs use TF32 throughout.
 //
 // StateFlow section 3.4.2, Eq. 18 ("OutputGrad" and "PrepGrad"): given the chunk's entry
 // state S (state replay) and the cotangent dSn of its exit state (reverse state chain),
@@ -217,10 +217,10 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     float acc[TD][4];
     zero(acc);
-    gemm<TD, NTD, NWG, true>(acc, cols_scaled(Tv, sbeg), Kv, 64, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, cols_scaled(rm(sT, LD6), sbeg), rm(sK, LDI), 64, warp, lane);
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B1[i * LDF + c] = x; });
     zero(acc);
-    gemm<TD, NTD, NWG, true>(acc, cols_scaled(Tv, sb), Vv, 64, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc, cols_scaled(rm(sT, LD6), sb), rm(sV, LDI), 64, warp, lane);
     each<TD, NTD, NWG, true>(acc, warp, lane, [&](int i, int c, float& x) { B2[i * LDF + c] = x; });
   }
   __syncthreads();
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     gemmx<B16, TD, NTD, NWG, true>(acc, rm(B1, LDF), SvT, D, warp, lane);
     float acc2[TD][4];
     zero(acc2);
-    gemm<TD, NTD, NWG, true>(acc2, view(sP, 1, LD6), dOv, 64, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(acc2, cm(sP, LD6), rm(sdO, LDI), 64, warp, lane);
     float acc3[TD][4];
     zero(acc3);
     gemmx<B16, TD, NTD, NWG, true>(acc3, rm(sK, LDI), cm(dSn, D), D, warp, lane);
@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     for (int ti = 0; ti < TD; ++ti)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dq[ti][e] += acc[ti][e];
-    gemm<TD, NTD, NWG, true>(dq, view(sP, LD6, 1), Kv, 64, warp, lane);
-    gemm<TD, NTD, NWG, true>(dk, view(sP, 1, LD6), Qv, 64, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(dq, rm(sP, LD6), rm(sK, LDI), 64, warp, lane);
+    gemmx<B16, TD, NTD, NWG, true>(dk, cm(sP, LD6), rm(sQ, LDI), 64, warp, lane);
   }
   // exit state: Z = Delta dSn ; dk += dec o Z ; ddec = rowsum(K o Z)
   {
@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   }
   __syncthreads();
   // dk += dKK K + dKK^T K
-  gemm<TD, NTD, NWG, true>(dk, view(sP, LD6, 1), Kv, 64, warp, lane);
-  gemm<TD, NTD, NWG, true>(dk, view(sP, 1, LD6), Kv, 64, warp, lane);
+  gemmx<B16, TD, NTD, NWG, true>(dk, rm(sP, LD6), rm(sK, LDI), 64, warp, lane);
+  gemmx<B16, TD, NTD, NWG, true>(dk, cm(sP, LD6), rm(sK, LDI), 64, warp, lane);
   // write dq, dk
   {
     Tin* dqo = (Tin*)p.dq;

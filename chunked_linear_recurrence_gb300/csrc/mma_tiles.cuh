@@ -36,6 +36,14 @@ __device__ __forceinline__ uint32_t pair_at(const float* p) {
   const float2 f = *reinterpret_cast<const float2*>(p);
   return pk(f.x, f.y);
 }
+// Two separate elements as a BF16 pair (BF16 elements keep their bits).
+__device__ __forceinline__ uint32_t pair_of(const __nv_bfloat16* lo, const __nv_bfloat16* hi) {
+  return (uint32_t)__bfloat16_as_ushort(*lo) | ((uint32_t)__bfloat16_as_ushort(*hi) << 16);
+}
+__device__ __forceinline__ uint32_t pair_of(const float* lo, const float* hi) { return pk(*lo, *hi); }
+// Two adjacent elements as FP32 (for views that scale before rounding).
+__device__ __forceinline__ float2 f2_at(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 f2_at(const __nv_bfloat16* p) { return upk(pair_at(p)); }
 
 // Row-major (element (r, c) at p[r ld + c]) and column-major (at p[c ld + r]) views with
 // the BF16 pair accessors of the m16n8k16 operands: pc(r, c) = (x(r, c), x(r, c + 1)),
@@ -48,7 +56,12 @@ struct RM {
   __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[r * ld + c]); }
   __device__ __forceinline__ uint32_t pc(int r, int c) const { return pair_at(p + r * ld + c); }
   __device__ __forceinline__ uint32_t pr(int r, int c) const {
-    return pk(to_f(p[r * ld + c]), to_f(p[(r + 1) * ld + c]));
+    return pair_of(p + r * ld + c, p + (r + 1) * ld + c);
+  }
+  // the same pairs in FP32
+  __device__ __forceinline__ float2 fc(int r, int c) const { return f2_at(p + r * ld + c); }
+  __device__ __forceinline__ float2 fr(int r, int c) const {
+    return make_float2(to_f(p[r * ld + c]), to_f(p[(r + 1) * ld + c]));
   }
 };
 template <typename T>
@@ -57,9 +70,13 @@ struct CM {
   int ld;
   __device__ __forceinline__ float operator()(int r, int c) const { return to_f(p[c * ld + r]); }
   __device__ __forceinline__ uint32_t pc(int r, int c) const {
-    return pk(to_f(p[c * ld + r]), to_f(p[(c + 1) * ld + r]));
+    return pair_of(p + c * ld + r, p + (c + 1) * ld + r);
   }
   __device__ __forceinline__ uint32_t pr(int r, int c) const { return pair_at(p + c * ld + r); }
+  __device__ __forceinline__ float2 fc(int r, int c) const {
+    return make_float2(to_f(p[c * ld + r]), to_f(p[(c + 1) * ld + r]));
+  }
+  __device__ __forceinline__ float2 fr(int r, int c) const { return f2_at(p + c * ld + r); }
 };
 template <typename T>
 __device__ __forceinline__ RM<T> rm(const T* p, int ld) { return RM<T>{p, ld}; }
@@ -72,13 +89,13 @@ struct RowScaled {
   V v;
   const float* s;
   __device__ __forceinline__ float operator()(int r, int c) const { return s[r] * v(r, c); }
-  // (pairs: exact for BF16 base views, whose elements the pair carries unrounded)
+  // (pairs: scaled in FP32, then rounded once)
   __device__ __forceinline__ uint32_t pc(int r, int c) const {
-    const float2 x = upk(v.pc(r, c));
+    const float2 x = v.fc(r, c);
     return pk(s[r] * x.x, s[r] * x.y);
   }
   __device__ __forceinline__ uint32_t pr(int r, int c) const {
-    const float2 x = upk(v.pr(r, c));
+    const float2 x = v.fr(r, c);
     return pk(s[r] * x.x, s[r + 1] * x.y);
   }
 };
@@ -89,11 +106,11 @@ struct ColScaled {
   const float* s;
   __device__ __forceinline__ float operator()(int r, int c) const { return s[c] * v(r, c); }
   __device__ __forceinline__ uint32_t pc(int r, int c) const {
-    const float2 x = upk(v.pc(r, c));
+    const float2 x = v.fc(r, c);
     return pk(s[c] * x.x, s[c + 1] * x.y);
   }
   __device__ __forceinline__ uint32_t pr(int r, int c) const {
-    const float2 x = upk(v.pr(r, c));
+    const float2 x = v.fr(r, c);
     return pk(s[c] * x.x, s[c] * x.y);
   }
 };
