@@ -9,7 +9,13 @@ code: the oracle is the plain token-by-token definition from the Attention Gym
 
 Functions take and return NumPy float64 arrays in the library's layouts::
 
-    q, k [B,T,H,K]   v, out [B,T,H,V]   g, beta [B,T,H]   state [N,H,V,K]
+    q, k [B,T,HK,K]   v, out [B,T,H,V]   g, beta [B,T,H]   state [N,H,V,K]
+
+HK divides H (grouped heads, the chunk_gdn parameter table of the same page):
+value head h reads query/key head h // (H // HK), i.e. each block of H // HK
+consecutive value heads shares one query/key head.  The oracle takes that
+definition literally: q and k are repeated per block before the per-head
+recurrence, and the gradient of a shared query/key head is the sum over its block.
 
 Pins (see ``tests/test_oracle_pins.py``): closed forms for beta = 0, for the
 delta rule's exact write, for orthonormal keys and for T = 1; an exact
@@ -96,13 +102,31 @@ def _shape(q, v, cu_seqlens):
     return B, T, H, K, V, N
 
 
+def _per_value_head(x, H):
+    """[B,T,HK,K] query/key heads -> [B,T,H,K]: value head h reads head h // (H // HK)."""
+    x = np.asarray(x, np.float64)
+    HK = x.shape[2]
+    if H % HK:
+        raise ValueError(f"query/key heads {HK} do not divide value heads {H}")
+    return np.repeat(x, H // HK, axis=2) if HK != H else x
+
+
+def _per_shared_head(dx, HK):
+    """Gradients per value head [B,T,H,K] -> per shared query/key head [B,T,HK,K] (sum
+    over each block of H // HK consecutive value heads)."""
+    B, T, H, K = dx.shape
+    return dx.reshape(B, T, HK, H // HK, K).sum(axis=3) if HK != H else dx
+
+
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None):
     """Token-by-token forward.  Returns (out [B,T,H,V], final_state [N,H,V,K]).
 
     Rows of ``out`` outside every sequence are NaN.
     """
     lib = _load()
-    q, qp = _d(q); k, kp = _d(k); v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
+    Hv = np.asarray(v).shape[2]
+    q, qp = _d(_per_value_head(q, Hv)); k, kp = _d(_per_value_head(k, Hv))
+    v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
     B, T, H, K, V, N = _shape(q, v, cu_seqlens)
     s0, s0p = _d(initial_state)
     cu, cup = _i(cu_seqlens)
@@ -122,10 +146,14 @@ def gdn_bwd(q, k, v, g, beta, initial_state, d_out, d_final_state=None,
             cu_seqlens=None, scale=None):
     """Reverse-mode gradients of (out, final_state) w.r.t. every input.
 
-    Returns dict with dq, dk, dv, dg, dbeta, d_initial_state (FP64).
+    Returns dict with dq, dk, dv, dg, dbeta, d_initial_state (FP64); dq and dk have the
+    shape of q and k (grouped heads: summed over each head's block of value heads).
     """
     lib = _load()
-    q, qp = _d(q); k, kp = _d(k); v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
+    HK = np.asarray(q).shape[2]
+    Hv = np.asarray(v).shape[2]
+    q, qp = _d(_per_value_head(q, Hv)); k, kp = _d(_per_value_head(k, Hv))
+    v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
     B, T, H, K, V, N = _shape(q, v, cu_seqlens)
     s0, s0p = _d(initial_state)
     do, dop = _d(d_out)
@@ -142,6 +170,8 @@ def gdn_bwd(q, k, v, g, beta, initial_state, d_out, d_final_state=None,
                             ptr["dbeta"], ptr["d_initial_state"])
     if rc != 0:
         raise ValueError("oracle_gdn_bwd: malformed arguments")
+    res["dq"] = _per_shared_head(res["dq"], HK)
+    res["dk"] = _per_shared_head(res["dk"], HK)
     return res
 
 
@@ -151,7 +181,8 @@ def segment_summary(k, v, g, beta, bounds):
     Returns (P [R,H,K,K], E [R,H,V,K]) with S_out = S_in @ P + E.
     """
     lib = _load()
-    k, kp = _d(k); v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
+    k, kp = _d(_per_value_head(k, np.asarray(v).shape[2]))
+    v, vp = _d(v); g, gp = _d(g); beta, bp = _d(beta)
     B, T, H, K = k.shape
     V = v.shape[-1]
     bd, bdp = _i(np.asarray(bounds).reshape(-1, 2))

@@ -329,3 +329,69 @@ def test_backward_adjoint_at_head_dim_64():
     an = sum((grads[n] * d).sum() for n, d in
              zip(["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"], dirs))
     assert abs(fd - an) <= 1e-6 * max(abs(an), 1.0), (fd, an)
+
+
+# ---------------------------------------------------------------- grouped heads
+def test_grouped_heads_are_consecutive_blocks():
+    """H = 4 value heads over HK = 2 query/key heads: heads 0, 1 read query/key head 0 and
+    heads 2, 3 head 1 (consecutive blocks, not h % HK).  Changing query/key head 1 moves
+    value heads 2 and 3 only; each value head equals a one-head run on its own q/k."""
+    B, T, H, HK, K, V = 1, 20, 4, 2, 4, 3
+    rng = np.random.default_rng(7)
+    q, k, v, g, beta, S0 = rand_inputs(B, T, H, K, V, rng)
+    q, k = q[:, :, :HK].copy(), k[:, :, :HK].copy()
+    out, fin = oracle.gdn_fwd(q, k, v, g, beta, S0)
+    q2, k2 = q.copy(), k.copy()
+    q2[:, :, 1] = rng.normal(size=(B, T, K))
+    k2[:, :, 1] = k2[:, :, 1][:, ::-1]
+    out2, fin2 = oracle.gdn_fwd(q2, k2, v, g, beta, S0)
+    assert np.array_equal(out[:, :, :2], out2[:, :, :2]) and np.array_equal(fin[:, :2], fin2[:, :2])
+    assert not np.allclose(out[:, :, 2:], out2[:, :, 2:])
+    for h in range(H):
+        hk = h // (H // HK)
+        o1, f1 = oracle.gdn_fwd(q[:, :, hk:hk + 1], k[:, :, hk:hk + 1], v[:, :, h:h + 1],
+                                g[:, :, h:h + 1], beta[:, :, h:h + 1], S0[:, h:h + 1])
+        assert np.array_equal(o1[:, :, 0], out[:, :, h]) and np.array_equal(f1[:, 0], fin[:, h])
+
+
+def test_grouped_heads_gradients_match_central_differences():
+    """dq and dk of shared query/key heads (H = 4 over HK = 2, and H = 3 over HK = 1)
+    against FP64 central differences: the gradient of a shared head sums its block."""
+    for H, HK in ((4, 2), (3, 1)):
+        B, T, K, V = 1, 12, 4, 3
+        rng = np.random.default_rng(10 * H + HK)
+        q, k, v, g, beta, S0 = rand_inputs(B, T, H, K, V, rng, normalise=False)
+        q, k = 0.4 * q[:, :, :HK], 0.4 * k[:, :, :HK]
+        dO = rng.normal(size=(B, T, H, V))
+        dSf = rng.normal(size=(B, H, V, K))
+        grads = oracle.gdn_bwd(q, k, v, g, beta, S0, dO, dSf)
+        inputs = [q, k, v, g, beta, S0]
+        h = 1e-6
+        for i, name in ((0, "dq"), (1, "dk")):
+            x = inputs[i]
+            assert grads[name].shape == x.shape
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp = [a.copy() for a in inputs]
+                xp[i][idx] += h
+                lp = _loss(xp, dO, dSf)
+                xp[i][idx] -= 2 * h
+                lm = _loss(xp, dO, dSf)
+                fd[idx] = (lp - lm) / (2 * h)
+            err = np.abs(grads[name] - fd).max() / np.abs(fd).max()
+            assert err <= 1e-6, (H, HK, name, err)
+
+
+def test_grouped_heads_summary_is_the_affine_map():
+    """Segment summaries with shared keys: S_out = S_in @ P + S_ext for the forward run of
+    the same range from a random S_in (H = 4 over HK = 2)."""
+    B, T, H, HK, K, V = 1, 40, 4, 2, 5, 3
+    rng = np.random.default_rng(11)
+    q, k, v, g, beta, S0 = rand_inputs(B, T, H, K, V, rng)
+    k = k[:, :, :HK].copy()
+    q = q[:, :, :HK].copy()
+    bounds = np.array([[7, 31]])
+    P, E = oracle.segment_summary(k, v, g, beta, bounds)
+    sl = slice(7, 31)
+    _, fin = oracle.gdn_fwd(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl], S0)
+    assert np.allclose(fin[0], np.einsum("hvk,hkj->hvj", S0[0], P[0]) + E[0], atol=1e-12)
