@@ -37,7 +37,7 @@ class SfError(RuntimeError):
 class sf_gdn_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("K", ctypes.c_int), ("V", ctypes.c_int), ("N", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("HK", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -110,11 +110,12 @@ def _dtype_code(dt):
 
 
 def make_shape(q, v, cu_seqlens=None, scale=None) -> sf_gdn_shape:
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    """Shape of q (or k) [B,T,HK,K] and v [B,T,H,V]: H value heads, HK query/key heads."""
+    B, T, HK, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     return sf_gdn_shape(B, T, H, K, V, N, _dtype_code(q.dtype),
-                        float(scale) if scale is not None else 0.0)
+                        float(scale) if scale is not None else 0.0, HK)
 
 
 def workspace(nbytes: int, device) -> torch.Tensor:
@@ -138,7 +139,7 @@ def sf_gdn_chunk_fwd(q, k, v, gate, beta, initial_state=None, cu_seqlens=None, s
     if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
         raise ValueError("cu_seqlens must be int32")
     if out is None:
-        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)     # [B,T,H,V]
     if output_final_state and final_state is None:
         final_state = torch.empty(shape.N, shape.H, shape.V, shape.K, dtype=torch.float32,
                                   device=q.device)

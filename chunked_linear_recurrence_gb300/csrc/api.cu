@@ -58,6 +58,9 @@ sf_status check_shape(const sf_gdn_shape* s, bool packed, bool need_n, const cha
                 fn, s->B, s->T, s->H, s->K, s->V);
   if (s->dtype != SF_F32 && s->dtype != SF_BF16)
     return fail(SF_ERR_INVALID_ARG, "%s: dtype must be SF_F32 or SF_BF16", fn);
+  if (s->HK < 0 || s->H % (s->HK > 0 ? s->HK : s->H))
+    return fail(SF_ERR_INVALID_ARG, "%s: query/key heads HK = %d must divide H = %d", fn, s->HK,
+                s->H);
   if (s->K != s->V || (s->K != 64 && s->K != 128))
     return fail(SF_ERR_UNSUPPORTED, "%s: head sizes K == V in {64, 128} only (got K=%d V=%d)", fn,
                 s->K, s->V);
@@ -77,6 +80,8 @@ sf_status check_shape(const sf_gdn_shape* s, bool packed, bool need_n, const cha
   return SF_OK;
 }
 
+int eff_hk(const sf_gdn_shape* s) { return s->HK > 0 ? s->HK : s->H; }
+
 float eff_scale(const sf_gdn_shape* s) {
   return s->scale > 0.f ? s->scale : 1.0f / std::sqrt((float)s->K);
 }
@@ -90,13 +95,14 @@ size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Backward workspace: status word | chunk-entry states | exit cotangents (FP32
 // [slots,H,V,K] each) | BF16 only: per-chunk factors [slots,H] and, for head size 128, the
-// split forward's ring (state replay).
+// split forward's ring (state replay) | grouped heads only: the per-value-head parts of dq
+// and dk (FP32 [B,T,H,K] each).
 struct BwdLayout {
-  size_t one, fac, split, total;
+  size_t one, fac, split, gqa, total;
 };
 
 BwdLayout bwd_layout(const sf_gdn_shape* shape) {
-  BwdLayout l{0, 0, 0, kStatusBytes};
+  BwdLayout l{0, 0, 0, 0, kStatusBytes};
   if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0) return l;
   // enough for both layouts: dense needs N*ceil(T/64) slots, packed (B == 1)
   // at most ceil(T/64) + N
@@ -109,7 +115,9 @@ BwdLayout bwd_layout(const sf_gdn_shape* shape) {
     l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));
   if (shape->dtype == SF_BF16 && shape->K == 128 && shape->V == 128)
     l.split = sfg::split_fwd_workspace((int)n, shape->H);
-  l.total = kStatusBytes + 2 * l.one + l.fac + l.split;
+  if (shape->HK > 0 && shape->HK < shape->H)
+    l.gqa = round_up((size_t)shape->B * shape->T * shape->H * shape->K * sizeof(float));
+  l.total = kStatusBytes + 2 * l.one + l.fac + l.split + 2 * l.gqa;
   return l;
 }
 
@@ -152,6 +160,7 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   p.q = q; p.k = k; p.v = v; p.g = gate; p.beta = beta; p.s0 = initial_state;
   p.cu = cu_seqlens; p.out = out; p.final_state = output_final_state ? final_state : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
+  p.HK = eff_hk(shape);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
     e = sfg::launch_split_fwd(p, workspace, reinterpret_cast<int*>(workspace), cs);
@@ -189,6 +198,7 @@ sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const
   sfg::ChainParams p{};
   p.k = k; p.v = v; p.g = gate; p.beta = beta; p.bounds = bounds; p.P = P; p.E = S_ext;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = R; p.scale = 1.f;
+  p.HK = eff_hk(shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const bool bf16 = shape->dtype == SF_BF16;
   cudaError_t e;
@@ -251,6 +261,17 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   p.dbeta = dbeta; p.ds0 = d_initial_state;
   p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + 2 * one) : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
+  p.HK = eff_hk(shape);
+  // grouped heads: the gradient kernels write per-value-head FP32 parts, summed below
+  float* gq = nullptr;
+  float* gk = nullptr;
+  if (lay.gqa) {
+    gq = reinterpret_cast<float*>(ws + kStatusBytes + 2 * one + lay.fac + lay.split);
+    gk = reinterpret_cast<float*>(reinterpret_cast<char*>(gq) + lay.gqa);
+    p.dq = gq;
+    p.dk = gk;
+    p.dqk_f32 = 1;
+  }
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
     p.ckpt_tiled = 1;   // the split kernel writes its checkpoints in its threads' order
@@ -261,6 +282,13 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   if (e != cudaSuccess) return cuda_fail(e, fn);
   e = sfg::launch_simt_bwd(p, bf16, D, slots, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (lay.gqa) {
+    const int64_t rows = (int64_t)shape->B * shape->T;
+    e = sfg::launch_group_sum(gq, dq, bf16, rows, shape->H, p.HK, D, cu_seqlens, shape->N, cs);
+    if (e == cudaSuccess)
+      e = sfg::launch_group_sum(gk, dk, bf16, rows, shape->H, p.HK, D, cu_seqlens, shape->N, cs);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+  }
   return SF_OK;
 }
 

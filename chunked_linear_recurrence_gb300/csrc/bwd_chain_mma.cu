@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
   __nv_bfloat16* sK = sQ + 64 * LDI;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
+  const int hk = qk_head(h, H, p.HK);
   const int64_t slot = blockIdx.x;
   int n;
   int64_t bos, eos, ci;
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
   const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
   for (int idx = tid; idx < 64 * D; idx += NTB) {
     const int i = idx / D, c = idx % D;
-    const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+    const size_t off = ((size_t)(c0 + i) * p.HK + hk) * D + c;
     const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
     sQ[i * LDI + c] = (i < L) ? q[off] : z;
     sK[i * LDI + c] = (i < L) ? k[off] : z;
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, n = blockIdx.z, r0 = blockIdx.x * BV, H = p.H;
+  const int hk = qk_head(h, H, p.HK);
   const float scale = p.scale;
   const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
   const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
     constexpr int QP = D / 8;                 // 16-byte pieces per q/k row
     for (int idx = tid; idx < 64 * QP; idx += NTB) {
       const int i = idx / QP, c = (idx % QP) * 8;
-      const size_t off = ((size_t)(c0 + (i < L ? i : 0)) * H + h) * D + c;
+      const size_t off = ((size_t)(c0 + (i < L ? i : 0)) * p.HK + hk) * D + c;
       const int nb = i < L ? 16 : 0;
       cp_async16(base + B::Q + 2 * (i * LDI + c), q + off, nb);
       cp_async16(base + B::K + 2 * (i * LDI + c), k + off, nb);

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   Tin* sdO = sV + 64 * LDI;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
+  const int HK = p.HK, hk = qk_head(h, H, HK);
   const int64_t slot = blockIdx.x;
   int n = -1;
   int64_t bos = 0, eos = 0, ci = 0;
@@ -141,9 +142,10 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     for (int e = 0; e < NV; ++e) {
       const int idx = (tid + NTG * e) * PV, i = idx / D, c = idx % D;
       const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+      const size_t oqk = ((size_t)(c0 + i) * HK + hk) * D + c;
       const uint4 z = make_uint4(0, 0, 0, 0);
-      vq[e] = (i < L) ? *reinterpret_cast<const uint4*>(q + off) : z;
-      vk[e] = (i < L) ? *reinterpret_cast<const uint4*>(k + off) : z;
+      vq[e] = (i < L) ? *reinterpret_cast<const uint4*>(q + oqk) : z;
+      vk[e] = (i < L) ? *reinterpret_cast<const uint4*>(k + oqk) : z;
       vv[e] = (i < L) ? *reinterpret_cast<const uint4*>(v + off) : z;
       vo[e] = (i < L) ? *reinterpret_cast<const uint4*>(dO + off) : z;
     }
@@ -418,12 +420,24 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
   {
     Tin* dqo = (Tin*)p.dq;
     Tin* dko = (Tin*)p.dk;
-    each<TD, NTD, NWG, true>(dq, warp, lane, [&](int i, int c, float& x) {
-      if (i < L) dqo[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
-    });
-    each<TD, NTD, NWG, true>(dk, warp, lane, [&](int i, int c, float& x) {
-      if (i < L) dko[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
-    });
+    if (p.dqk_f32) {
+      // grouped heads: FP32 per value head, summed over each block afterwards
+      float* dqf = reinterpret_cast<float*>(p.dq);
+      float* dkf = reinterpret_cast<float*>(p.dk);
+      each<TD, NTD, NWG, true>(dq, warp, lane, [&](int i, int c, float& x) {
+        if (i < L) dqf[((size_t)(c0 + i) * H + h) * D + c] = x;
+      });
+      each<TD, NTD, NWG, true>(dk, warp, lane, [&](int i, int c, float& x) {
+        if (i < L) dkf[((size_t)(c0 + i) * H + h) * D + c] = x;
+      });
+    } else {
+      each<TD, NTD, NWG, true>(dq, warp, lane, [&](int i, int c, float& x) {
+        if (i < L) dqo[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
+      });
+      each<TD, NTD, NWG, true>(dk, warp, lane, [&](int i, int c, float& x) {
+        if (i < L) dko[((size_t)(c0 + i) * H + h) * D + c] = from_f<Tin>(x);
+      });
+    }
   }
   __syncthreads();
   // dgate = reverse cumulative sum of dgamma; dbeta

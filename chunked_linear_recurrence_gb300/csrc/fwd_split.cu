@@ -204,9 +204,16 @@ struct SplitParams {
   float* sumE;               // [N,H,V,K]
   int twin;
   int B, T, H, N;
+  int HK;                    // query/key heads: value head h reads head h / (H / HK)
+  int qk_group;              // H / HK
   int nch, nprep;
   float scale;
 };
+
+// Query/key head of value head h (no division in the common case HK = H).
+__device__ __forceinline__ int qk_of(const SplitParams& p, int h) {
+  return p.qk_group == 1 ? h : h / p.qk_group;
+}
 
 // Token rows [bos, eos) of chain x = n H + h: sequence n (dense rows or cu_seqlens), or
 // token range n of `bounds`.  A range out of [0, B T], reversed or crossing a batch row is
@@ -420,13 +427,14 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           st_release_u32(consumed_me, (uint32_t)n);
           rel = n;
         };
-        int s = 0, t = 0, c = 0, ncx = 0;
+        int s = 0, t = 0, c = 0, ncx = 0, hk = 0;
         int64_t bos = 0, eos = 0;
         for (; s < len; ++s, ++c) {
-          while (c >= ncx) {      // next chain with chunks
+          while (c >= ncx) {      // next chain with chunks (and its query/key head)
             const int x = j + geo.nch * (t++);
             geo.span(x, bos, eos);
             ncx = (int)n_chunks(eos - bos);
+            hk = qk_of(p, x % H);
             c = 0;
           }
           const int b = s % NBUF;
@@ -435,7 +443,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           // the producer's plain stores before its release, then our bulk reads
           fence_proxy_async_global();
           uint8_t* buf = sm + b * C_BUF;
-          const int row0 = (int)(bos + (int64_t)c * CHUNK), h = (j + geo.nch * (t - 1)) % H;
+          const int row0 = (int)(bos + (int64_t)c * CHUNK);
           const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
           if (!summ) {
             mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
@@ -450,8 +458,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
             if (!ptwin) bulk_g2s(buf + R_U, src + R_U, R_AH - R_U, &bars[C_RECFULL + b]);
             bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, &bars[C_RECFULL + b]);
           }
-          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, h, row0);
-          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, h, row0);
+          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, hk, row0);
+          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, hk, row0);
           issued = s + 1;
           // records up to s - NBUF have landed (their buffers came back); later ones are
           // tested against their buffers' current phases
@@ -1000,13 +1008,14 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // An item's geometry, its gate/beta values (two tokens per lane, loaded one use
       // ahead so that their latency overlaps the waits), and its tiles warmed in L2.
       struct Next {
-        int g, jj, s, h, row0, L;
+        int g, jj, s, h, hk, row0, L;   // hk: the query/key head of value head h
         float g0, g1, b0, b1;
       };
       auto fetch = [&](int g) {
-        Next n{g, 0, 0, 0, 0, 0, 0.f, 0.f, 0.f, 0.f};
+        Next n{g, 0, 0, 0, 0, 0, 0, 0.f, 0.f, 0.f, 0.f};
         if (g >= geo.total) return n;
         item(g, n.jj, n.s, n.h, n.row0, n.L);
+        n.hk = qk_of(p, n.h);
         const int e0 = 2 * lane, e1 = e0 + 1;
         const size_t o0 = (size_t)(n.row0 + e0) * H + n.h, o1 = (size_t)(n.row0 + e1) * H + n.h;
         if (e0 < n.L) { n.g0 = p.g[o0]; n.b0 = p.beta[o0]; }
@@ -1014,8 +1023,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (lane == 0) {
 #pragma unroll
           for (int pnl = 0; pnl < 2; ++pnl) {
-            tma_prefetch_l2_3d(tmK, 64 * pnl, n.h, n.row0);
-            if (!summ) tma_prefetch_l2_3d(tmQ, 64 * pnl, n.h, n.row0);
+            tma_prefetch_l2_3d(tmK, 64 * pnl, n.hk, n.row0);
+            if (!summ) tma_prefetch_l2_3d(tmQ, 64 * pnl, n.hk, n.row0);
             tma_prefetch_l2_3d(tmV, 64 * pnl, n.h, n.row0);
           }
         }
@@ -1031,7 +1040,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         const bool done = cur.g >= geo.total;
         const Next nxt = fetch(done ? cur.g : gnn);
         if (!done && nxt.g < geo.total) gnn = claim();
-        const int jj = cur.jj, s = cur.s, h = cur.h, row0 = cur.row0, L = cur.L;
+        const int jj = cur.jj, s = cur.s, h = cur.h, hk = cur.hk, row0 = cur.row0, L = cur.L;
         // the vector slot is free once the item two uses back has finished (one barrier
         // per slot, so a phase can never be mistaken for the one two items later)
         if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx)))
@@ -1100,8 +1109,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             mbar_arrive_expect_tx(&bars[P_FULL + pp], 2 * 16384);
 #pragma unroll
             for (int pnl = 0; pnl < 2; ++pnl) {
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + pp], 64 * pnl, h, row0);
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + pp], 64 * pnl, h,
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + pp], 64 * pnl, hk, row0);
+              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + pp], 64 * pnl, hk,
                           row0);
             }
             mbar_arrive_expect_tx(&bars[P_FULLV + pp], 16384);
@@ -1523,9 +1532,9 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   if (nprep < 1) return cudaErrorInvalidConfiguration;
   const int rows = p.B * p.T;
   CUtensorMap mq, mk, mv;
-  if (!make_bf16_map(&mk, k, rows, p.H) || !make_bf16_map(&mv, v, rows, p.H)) return cudaErrorInvalidValue;
+  if (!make_bf16_map(&mk, k, rows, p.HK) || !make_bf16_map(&mv, v, rows, p.H)) return cudaErrorInvalidValue;
   mq = mk;   // summaries have no q: K stands in (its products are not used)
-  if (q && !make_bf16_map(&mq, q, rows, p.H)) return cudaErrorInvalidValue;
+  if (q && !make_bf16_map(&mq, q, rows, p.HK)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(gdn_fwd_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_ALLOC);
   if (e != cudaSuccess) return e;
@@ -1533,6 +1542,7 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   e = cudaMemsetAsync(w + WS_ABORT, 0, WS_FLAGS_END - WS_ABORT, st);
   if (e != cudaSuccess) return e;
   const int NH = p.N * p.H;
+  p.qk_group = p.H / p.HK;
   p.status = status;
   p.abort_g = reinterpret_cast<int*>(w + WS_ABORT);
   p.next_item = reinterpret_cast<uint32_t*>(w + WS_NEXT);
@@ -1561,7 +1571,8 @@ size_t split_fwd_workspace(int N, int H) { return ws_total(chain_ctas(N, H), N, 
 size_t split_summary_workspace(int R, int H) { return ws_total(summary_chain_ctas(R, H), R, H); }
 
 cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
-  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1)) return cudaErrorInvalidValue;
+  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || (cp.cu && cp.B != 1) || (cp.HK > 0 && cp.H % cp.HK))
+    return cudaErrorInvalidValue;
   SplitParams p{};
   p.g = cp.g;
   p.beta = cp.beta;
@@ -1574,13 +1585,15 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaS
   p.T = cp.T;
   p.H = cp.H;
   p.N = cp.N;
+  p.HK = cp.HK > 0 ? cp.HK : cp.H;
   p.nch = chain_ctas(cp.N, cp.H);
   p.scale = cp.scale;
   return launch_split(p, cp.q, cp.k, cp.v, cp.out, p.nch, ws, status, st);
 }
 
 cudaError_t launch_split_summary(const ChainParams& cp, void* ws, int* status, cudaStream_t st) {
-  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || !cp.bounds || !cp.P || !cp.E) return cudaErrorInvalidValue;
+  if (cp.T <= 0 || cp.N < 1 || cp.H < 1 || !cp.bounds || !cp.P || !cp.E || (cp.HK > 0 && cp.H % cp.HK))
+    return cudaErrorInvalidValue;
   SplitParams p{};
   p.g = cp.g;
   p.beta = cp.beta;
@@ -1592,6 +1605,7 @@ cudaError_t launch_split_summary(const ChainParams& cp, void* ws, int* status, c
   p.T = cp.T;
   p.H = cp.H;
   p.N = cp.N;
+  p.HK = cp.HK > 0 ? cp.HK : cp.H;
   p.nch = summary_chain_ctas(cp.N, cp.H);
   p.scale = 1.f;
   return launch_split(p, nullptr, cp.k, cp.v, nullptr, 2 * p.nch, ws, status, st);

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
   const int tid = threadIdx.x;
   const int h = blockIdx.y, item = blockIdx.z;
   const int r0 = blockIdx.x * BV;           // first (augmented) state row of this CTA
-  const int H = p.H;
+  const int H = p.H, HK = p.HK, hk = qk_head(h, H, HK);
   const Tin* q = (const Tin*)p.q;
   const Tin* k = (const Tin*)p.k;
   const Tin* v = (const Tin*)p.v;
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
     }
     for (int idx = tid; idx < 64 * D; idx += NT) {
       const int i = idx / D, c = idx % D;
-      const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+      const size_t off = ((size_t)(c0 + i) * HK + hk) * D + c;
       sK[i * LDK + c] = (i < L) ? ldg_f(k + off) : 0.f;
       if (MODE == MODE_FWD) sQ[i * LDK + c] = (i < L) ? ldg_f(q + off) : 0.f;
     }
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_chain_kernel(const ChainParams p)
 
   const int tid = threadIdx.x;
   const int h = blockIdx.y, n = blockIdx.z, r0 = blockIdx.x * BV;
-  const int H = p.H;
+  const int H = p.H, HK = p.HK, hk = qk_head(h, H, HK);
   const Tin* q = (const Tin*)p.q;
   const Tin* k = (const Tin*)p.k;
   const Tin* dO = (const Tin*)p.dout;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_chain_kernel(const ChainParams p)
     }
     for (int idx = tid; idx < 64 * D; idx += NT) {
       const int i = idx / D, c = idx % D;
-      const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+      const size_t off = ((size_t)(c0 + i) * HK + hk) * D + c;
       sK[i * LDK + c] = (i < L) ? ldg_f(k + off) : 0.f;
       sQ[i * LDK + c] = (i < L) ? ldg_f(q + off) : 0.f;
     }
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) 
   Tin* sV = sK + 64 * LDI;
   Tin* sdO = sV + 64 * LDI;
 
-  const int tid = threadIdx.x, h = blockIdx.y, H = p.H;
+  const int tid = threadIdx.x, h = blockIdx.y, H = p.H, HK = p.HK, hk = qk_head(h, H, HK);
   const int64_t slot = blockIdx.x;
   // locate (sequence, chunk) of this slot
   int n = -1;
@@ -426,9 +426,10 @@ __global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) 
   for (int idx = tid; idx < 64 * D; idx += NT) {
     const int i = idx / D, c = idx % D;
     const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
+    const size_t oqk = ((size_t)(c0 + i) * HK + hk) * D + c;
     const Tin z = from_f<Tin>(0.f);
-    sQ[i * LDI + c] = (i < L) ? q[off] : z;
-    sK[i * LDI + c] = (i < L) ? k[off] : z;
+    sQ[i * LDI + c] = (i < L) ? q[oqk] : z;
+    sK[i * LDI + c] = (i < L) ? k[oqk] : z;
     sV[i * LDI + c] = (i < L) ? v[off] : z;
     sdO[i * LDI + c] = (i < L) ? dO[off] : z;
   }
@@ -661,8 +662,13 @@ __global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) 
       const int idx = tid + e * NT, i = idx / D, c = idx % D;
       if (i < L) {
         const size_t off = ((size_t)(c0 + i) * H + h) * D + c;
-        dqo[off] = from_f<Tin>(dq[e]);
-        dko[off] = from_f<Tin>(dk[e]);
+        if (p.dqk_f32) {         // grouped heads: per value head, summed afterwards
+          reinterpret_cast<float*>(p.dq)[off] = dq[e];
+          reinterpret_cast<float*>(p.dk)[off] = dk[e];
+        } else {
+          dqo[off] = from_f<Tin>(dq[e]);
+          dko[off] = from_f<Tin>(dk[e]);
+        }
       }
     }
   }

@@ -33,9 +33,15 @@ struct ChainParams {
   float* dbeta;
   float* ds0;             // [N,H,V,K] or NULL
   float* fac;             // [slots,H] per-chunk backward factors (BF16 backward)
+  int dqk_f32;            // backward: dq, dk are FP32 [B,T,H,K] per value head (grouped
+                          // heads, summed into the caller's tensors afterwards)
   int B, T, H, N;
+  int HK;                 // query/key heads (divides H): value head h reads h / (H / HK)
   float scale;
 };
+
+// Query/key head of value head h.
+__host__ __device__ inline int qk_head(int h, int H, int HK) { return h / (H / HK); }
 
 // Forward / summary / replay chain kernel: `items` = N (fwd, replay) or R (summary).
 cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, int items,
@@ -51,6 +57,10 @@ __host__ __device__ inline int ckpt_tiled_off(int v, int k) {
 
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
                             cudaStream_t st);
+// Grouped heads: out[r, hk, c] = sum over j < H / HK of acc[r, hk (H / HK) + j, c] for the
+// active rows r (r < cu[N] when cu != NULL, else all B*T), in the q/k/v dtype.
+cudaError_t launch_group_sum(const float* acc, void* out, bool bf16, int64_t rows, int H, int HK,
+                             int D, const int32_t* cu, int N, cudaStream_t st);
 // BF16 backward's reverse cotangent chain on the warp-level tensor cores
 // (bwd_chain_mma.cu): per-chunk factors into p.fac, then the chain (tape, ds0).
 size_t mma_bwd_fac_bytes(int D);

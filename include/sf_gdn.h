@@ -22,10 +22,14 @@
  *    for sf_gdn_chunk_bwd_noalloc only, from a fixed array built into the
  *    library.
  *  * Layouts are contiguous, row-major:
- *        q, k    [B, T, H, K]      v, out, d_out  [B, T, H, V]
+ *        q, k    [B, T, HK, K]     v, out, d_out  [B, T, H, V]
  *        gate, beta, dgate, dbeta  [B, T, H]  (FP32)
  *        states  [N, H, V, K] (FP32; V-major: S @ k is a [V] vector)
  *        cu_seqlens  int32 [N+1] or NULL
+ *  * Grouped query/key heads (Attention Gym chunk_gdn parameter table): HK
+ *    divides H and value head h reads query/key head h / (H / HK), i.e. each
+ *    block of H / HK consecutive value heads shares one query/key head; dq and
+ *    dk of a shared head are the sums over its block.  HK = H is the plain case.
  *  * q/k/v (and out, d_out, dq, dk, dv) share one dtype: SF_BF16 or SF_F32.
  *    gate, beta and every state are FP32; all recurrence math is FP32.
  *  * Supported head sizes: K == V, either 64 or 128 (else SF_ERR_UNSUPPORTED).
@@ -76,11 +80,14 @@ typedef enum {
 typedef enum { SF_F32 = 0, SF_BF16 = 1 } sf_dtype;
 
 /* Problem shape.  N = number of sequences: B when cu_seqlens is NULL, else
- * len(cu_seqlens) - 1 (and then B must be 1).  scale <= 0 selects 1/sqrt(K). */
+ * len(cu_seqlens) - 1 (and then B must be 1).  scale <= 0 selects 1/sqrt(K).
+ * H = value heads (v, gate, beta, states); HK = query/key heads, which must
+ * divide H (0 means HK = H, so a zero-initialised shape keeps every head). */
 typedef struct {
   int B, T, H, K, V, N;
   sf_dtype dtype;
   float scale;
+  int HK;
 } sf_gdn_shape;
 
 /* Description of the calling thread's last error (never NULL). */
@@ -152,7 +159,7 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float *P, const float 
  * with respect to every input:
  *   d_out          [B,T,H,V] q/k/v dtype (rows past cu_seqlens[N] ignored)
  *   d_final_state  [N,H,V,K] FP32 or NULL (zeros)
- *   dq, dk [B,T,H,K], dv [B,T,H,V] in the q/k/v dtype; dgate, dbeta [B,T,H]
+ *   dq, dk [B,T,HK,K], dv [B,T,H,V] in the q/k/v dtype; dgate, dbeta [B,T,H]
  *   FP32; d_initial_state [N,H,V,K] FP32 or NULL (not computed).
  * Inactive rows of the gradients are not written.
  * Supported: BF16 with K=V in {64,128}; F32 with K=V=64.

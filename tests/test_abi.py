@@ -58,7 +58,8 @@ def _fwd(lib, shape, out_final=0, ws_bytes=4096, ptr=FAKE, cu=None, fin=None):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(K=96, V=96), 2), (dict(K=128, V=64), 2), (dict(T=-1), 1), (dict(H=0), 1),
-    (dict(dtype=7), 1), (dict(N=2), 1), (dict(B=40000, T=40000), 2)])
+    (dict(dtype=7), 1), (dict(N=2), 1), (dict(B=40000, T=40000), 2),
+    (dict(H=4, HK=3), 1), (dict(H=4, HK=-1), 1), (dict(H=2, HK=4), 1)])
 def test_forward_rejects_bad_shapes(lib, kw, status):
     assert _fwd(lib, _shape(**kw)) == status
     assert len(lib.sf_last_error()) > 0
@@ -88,3 +89,14 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert need >= 256 + 2 * 128 * 128 * 4      # one chunk: checkpoint + cotangent tape
     assert lib.sf_gdn_chunk_bwd(ctypes.byref(s), *([FAKE] * 5), None, None, FAKE, None,
                                 *([FAKE] * 5), None, FAKE, need - 1, None) == 3
+
+
+def test_grouped_heads_workspace(lib):
+    """HK = 0 means HK = H; the backward of grouped heads adds two FP32 [B,T,H,K] areas for
+    the per-value-head parts of dq and dk, and nothing else changes."""
+    plain = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(H=4, T=256)))
+    assert lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(H=4, HK=4, T=256))) == plain
+    grouped = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(H=4, HK=2, T=256)))
+    assert grouped == plain + 2 * 256 * 4 * 128 * 4
+    assert (lib.sf_gdn_fwd_workspace(ctypes.byref(_shape(H=4, HK=1, T=256))) ==
+            lib.sf_gdn_fwd_workspace(ctypes.byref(_shape(H=4, T=256))))
