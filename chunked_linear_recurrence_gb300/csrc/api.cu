@@ -104,12 +104,12 @@ struct BwdLayout {
 BwdLayout bwd_layout(const sf_gdn_shape* shape) {
   BwdLayout l{0, 0, 0, 0, kStatusBytes};
   if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0) return l;
-  // enough for both layouts: dense needs N*ceil(T/64) slots, packed (B == 1)
-  // at most ceil(T/64) + N
+  // dense inputs need N * ceil(T/64) slots with N == B; packed ones (B == 1) at most
+  // ceil(T/64) + N (every sequence's last chunk may be partial), which also covers the
+  // dense B == N == 1
   const int64_t per = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK;
   const int64_t n = shape->N > 0 ? shape->N : shape->B;
-  int64_t slots = n * per;
-  if (shape->B == 1 && slots < per + n) slots = per + n;
+  const int64_t slots = shape->B == 1 ? per + n : (int64_t)shape->B * per;
   l.one = round_up((size_t)slots * shape->H * shape->K * shape->V * sizeof(float));
   if (shape->dtype == SF_BF16 && (shape->K == 64 || shape->K == 128))
     l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));

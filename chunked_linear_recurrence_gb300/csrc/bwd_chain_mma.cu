@@ -36,34 +36,6 @@ struct CtaBarB {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
 
-// Locates chunk `slot` (dense: n * ceil(T/64) + c; packed: running sum over sequences).
-__device__ __forceinline__ bool locate_slot(const ChainParams& p, int64_t slot, int& n,
-                                            int64_t& bos, int64_t& eos, int64_t& ci) {
-  if (!p.cu) {
-    const int64_t nc = n_chunks(p.T);
-    n = (int)(slot / nc);
-    ci = slot % nc;
-    if (n >= p.N) return false;
-    seq_span(n, p.B, p.T, nullptr, bos, eos);
-    return true;
-  }
-  int64_t s = 0;
-  for (int m = 0; m < p.N; ++m) {
-    int64_t b, e;
-    seq_span(m, p.B, p.T, p.cu, b, e);
-    const int64_t c = n_chunks(e - b);
-    if (slot < s + c) {
-      n = m;
-      ci = slot - s;
-      bos = b;
-      eos = e;
-      return true;
-    }
-    s += c;
-  }
-  return false;
-}
-
 }  // namespace
 
 // Per-chunk factors of the backward chain: fac[(slot * H + h)] = { Aqk [64][64], W [64][D],
@@ -71,8 +43,9 @@ __device__ __forceinline__ bool locate_slot(const ChainParams& p, int64_t slot, 
 template <int D>
 __host__ __device__ constexpr size_t fac_bytes() { return 4 * (64 * 64 + 64 * D + 128); }
 
+// One chunk (backward slot `slot`); false when the slot holds no chunk.
 template <int D>
-__global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p, float* fac) {
+__device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, int64_t slot) {
   constexpr int LDI = D + 8, LD6 = C_LD6, NTD = D / 8, TD = 4 * NTD / 8;
   extern __shared__ float sm[];
   float* sA = sm;                 // A = diag(beta) Ak, then scratch of the solve
@@ -87,10 +60,9 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
   const int hk = qk_head(h, H, p.HK);
-  const int64_t slot = blockIdx.x;
   int n;
   int64_t bos, eos, ci;
-  if (!locate_slot(p, slot, n, bos, eos, ci)) return;
+  if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) return false;
   const int64_t c0 = bos + ci * CHUNK;
   const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
   const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
@@ -143,6 +115,17 @@ __global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p
     zero(acc);
     gemm<TD, NTD, 8, true>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
     each<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
+  }
+  return true;
+}
+
+// Slots blockIdx.x, blockIdx.x + gridDim.x, ... until the first empty one.
+template <int D>
+__global__ void __launch_bounds__(NTB) mma_bwd_factor_kernel(const ChainParams p, float* fac,
+                                                             int64_t slots) {
+  for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
+    if (!factor_chunk<D>(p, fac, slot)) break;
+    __syncthreads();   // shared memory is rewritten by the next chunk
   }
 }
 
@@ -317,7 +300,7 @@ static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slot
     auto kern = mma_bwd_factor_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTB, smem, st>>>(p, fac);
+    if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTB, smem, st>>>(p, fac, slots);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t smem = sizeof(float) * (BV * (D + 8) + BV * C_LD6) + 2 * ChainBuf<D, BV>::BYTES;

@@ -68,8 +68,9 @@ struct TiledState {
 
 }  // namespace
 
+// One chunk (backward slot `slot`); false when the slot holds no chunk.
 template <typename Tin, int D, bool kTiled>
-__global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) {
+__device__ __forceinline__ bool grad_chunk(const ChainParams& p, int64_t slot) {
   static_assert(!kTiled || D == 128, "tiled checkpoints have D = 128");
   constexpr int LDI = D + 8;      // input tiles (Tin)
   constexpr int LDF = g_ldf<Tin, D>();  // fp32 [64][D] tiles
@@ -103,26 +104,9 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
   const int HK = p.HK, hk = qk_head(h, H, HK);
-  const int64_t slot = blockIdx.x;
   int n = -1;
   int64_t bos = 0, eos = 0, ci = 0;
-  if (!p.cu) {
-    const int64_t nc = n_chunks(p.T);
-    n = (int)(slot / nc);
-    ci = slot % nc;
-    if (n >= p.N) return;
-    seq_span(n, p.B, p.T, nullptr, bos, eos);
-  } else {
-    int64_t s = 0;
-    for (int m = 0; m < p.N; ++m) {
-      int64_t b, e;
-      seq_span(m, p.B, p.T, p.cu, b, e);
-      const int64_t c = n_chunks(e - b);
-      if (slot < s + c) { n = m; ci = slot - s; bos = b; eos = e; break; }
-      s += c;
-    }
-    if (n < 0) return;
-  }
+  if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) return false;
   const int64_t c0 = bos + ci * CHUNK;
   const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
   const float* S = p.ckpt + ((size_t)slot * H + h) * D * D;
@@ -459,6 +443,17 @@ __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p) 
     p.dg[off] = sgam[tid];
     p.dbeta[off] = sred[tid];
   }
+  return true;
+}
+
+// Slots blockIdx.x, blockIdx.x + gridDim.x, ... until the first empty one (the grid may be
+// smaller than the slot count: packed inputs whose offsets end early leave slots empty).
+template <typename Tin, int D, bool kTiled>
+__global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p, int64_t slots) {
+  for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
+    if (!grad_chunk<Tin, D, kTiled>(p, slot)) break;
+    __syncthreads();   // shared memory is rewritten by the next chunk
+  }
 }
 
 template <typename Tin, int D, bool kTiled = false>
@@ -468,7 +463,7 @@ static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream
   auto kern = mma_bwd_grad_kernel<Tin, D, kTiled>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (slots > 0) kern<<<dim3((unsigned)slots, p.H), NTG, smem, st>>>(p);
+  if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTG, smem, st>>>(p, slots);
   return cudaGetLastError();
 }
 

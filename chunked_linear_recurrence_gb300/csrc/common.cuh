@@ -65,6 +65,38 @@ __device__ __forceinline__ int64_t chunk_slot_base(int n, int B, int T, const in
   return s;
 }
 
+// Chunk `slot` of the backward's chunk numbering (dense: n * ceil(T/64) + c; packed: the
+// chunks of sequences 0 .. n-1 come first) -> sequence n, its rows [bos, eos) and the chunk
+// index ci within it.  False when the slot holds no chunk; every later slot is then empty
+// too, so a loop over slots may stop there.
+__device__ __forceinline__ bool locate_chunk(int64_t slot, int B, int T, const int32_t* cu, int N,
+                                             int& n, int64_t& bos, int64_t& eos, int64_t& ci) {
+  if (!cu) {
+    const int64_t nc = n_chunks(T);
+    if (nc == 0) return false;
+    n = (int)(slot / nc);
+    ci = slot % nc;
+    if (n >= N) return false;
+    seq_span(n, B, T, nullptr, bos, eos);
+    return true;
+  }
+  int64_t s = 0;
+  for (int m = 0; m < N; ++m) {
+    int64_t b, e;
+    seq_span(m, B, T, cu, b, e);
+    const int64_t c = n_chunks(e - b);
+    if (slot < s + c) {
+      n = m;
+      ci = slot - s;
+      bos = b;
+      eos = e;
+      return true;
+    }
+    s += c;
+  }
+  return false;
+}
+
 // Inclusive prefix sum of 64 values held in smem, by one warp (2 per lane).
 __device__ __forceinline__ void warp_cumsum64(const float* in, float* out, int lane) {
   const float a = in[2 * lane], b = in[2 * lane + 1];

@@ -366,8 +366,9 @@ __global__ void __launch_bounds__(NT) simt_bwd_chain_kernel(const ChainParams p)
 // grid = (slots, H), block = 256.  Q/K/V/dO are staged in smem in the input
 // dtype; the per-thread dq/dk accumulators live in registers.
 // ---------------------------------------------------------------------------
+// One chunk (backward slot `slot`); false when the slot holds no chunk.
 template <typename Tin, int D>
-__global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) {
+__device__ __forceinline__ bool simt_grad_chunk(const ChainParams& p, int64_t slot) {
   constexpr int LDI = D + 8;      // input tiles (Tin)
   constexpr int LDF = D + 1;      // fp32 [64][D] tiles
   constexpr int LD6 = 65;
@@ -392,27 +393,10 @@ __global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) 
   Tin* sdO = sV + 64 * LDI;
 
   const int tid = threadIdx.x, h = blockIdx.y, H = p.H, HK = p.HK, hk = qk_head(h, H, HK);
-  const int64_t slot = blockIdx.x;
   // locate (sequence, chunk) of this slot
   int n = -1;
   int64_t bos = 0, eos = 0, ci = 0;
-  if (!p.cu) {
-    const int64_t nc = n_chunks(p.T);
-    n = (int)(slot / nc);
-    ci = slot % nc;
-    if (n >= p.N) return;
-    seq_span(n, p.B, p.T, nullptr, bos, eos);
-  } else {
-    int64_t s = 0;
-    for (int m = 0; m < p.N; ++m) {
-      int64_t b, e;
-      seq_span(m, p.B, p.T, p.cu, b, e);
-      const int64_t c = n_chunks(e - b);
-      if (slot < s + c) { n = m; ci = slot - s; bos = b; eos = e; break; }
-      s += c;
-    }
-    if (n < 0) return;
-  }
+  if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) return false;
   const int64_t c0 = bos + ci * CHUNK;
   const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
   const float* S = p.ckpt + ((size_t)slot * H + h) * D * D;
@@ -698,6 +682,16 @@ __global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p) 
 #undef KF
 #undef VF
 #undef DOF
+  return true;
+}
+
+// Slots blockIdx.x, blockIdx.x + gridDim.x, ... until the first empty one.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(NT) simt_bwd_grad_kernel(const ChainParams p, int64_t slots) {
+  for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
+    if (!simt_grad_chunk<Tin, D>(p, slot)) break;
+    __syncthreads();   // shared memory is rewritten by the next chunk
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -766,7 +760,7 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
   auto kern2 = simt_bwd_grad_kernel<Tin, D>;
   e = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
   if (e != cudaSuccess) return e;
-  if (slots > 0) kern2<<<dim3((unsigned)slots, p.H), NT, smem2, st>>>(p);
+  if (slots > 0) kern2<<<dim3((unsigned)slot_grid(p, slots), p.H), NT, smem2, st>>>(p, slots);
   return cudaGetLastError();
 }
 

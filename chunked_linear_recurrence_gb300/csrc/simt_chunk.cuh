@@ -43,6 +43,20 @@ struct ChainParams {
 // Query/key head of value head h.
 __host__ __device__ inline int qk_head(int h, int H, int HK) { return h / (H / HK); }
 
+// CTAs along the slot axis of the per-chunk backward kernels (which walk slots with a
+// grid stride and stop at the first empty one): one per slot for dense inputs, where every
+// slot holds a chunk; for packed inputs, whose offsets may end long before T, about eight
+// waves of (slot, head) CTAs at most, so that empty slots cost no launches.
+inline int64_t slot_grid(const ChainParams& p, int64_t slots) {
+  if (!p.cu) return slots;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
+    nsm = 1;
+  const int64_t cap = (8LL * nsm + p.H - 1) / p.H;
+  return slots < cap ? slots : cap;
+}
+
 // Forward / summary / replay chain kernel: `items` = N (fwd, replay) or R (summary).
 cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, int items,
                               cudaStream_t st);
