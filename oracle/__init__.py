@@ -213,3 +213,45 @@ def state_scan(P, E, initial_state=None):
                           entry.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                           fin.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return entry, fin
+
+
+def segment_reverse_summary(q, k, g, beta, d_out, seg_offsets):
+    """Reverse (cotangent) map of each segment by probing, the backward counterpart of
+    ``segment_summary`` (Attention Gym "Linear Attention", section "Context Parallelism":
+    the backward carries the state cotangent from the end of the sequence to its start,
+    and every token step's adjoint is affine in it).
+
+    Segments are consecutive token ranges of one batch row, given as offsets [R+1] with the
+    cu_seqlens convention (q, k, d_out [1,T,...]).  The cotangent at a segment's start is
+    dS_entry = dS_exit @ P^T + C, with P the segment's forward transition; C is the
+    cotangent that the segment's own output gradients produce at its start when nothing
+    flows in at its end.  It is probed here by the backward of each segment run as its own
+    sequence with a zero exit cotangent (zero values and entry state: the cotangent chain
+    reads neither).  Returns C [R,H,V,K].
+    """
+    q = np.asarray(q, np.float64)
+    d_out = np.asarray(d_out, np.float64)
+    B, T, H, V = d_out.shape
+    K = np.asarray(k).shape[-1]
+    R = len(seg_offsets) - 1
+    v0 = np.zeros((B, T, H, V))
+    s0 = np.zeros((R, H, V, K))
+    res = gdn_bwd(q, k, v0, g, beta, s0, d_out, np.zeros((R, H, V, K)), cu_seqlens=seg_offsets)
+    return res["d_initial_state"]
+
+
+def state_scan_reverse(P, C, d_final_state=None):
+    """Exclusive scan of the cotangent maps from the last segment to the first:
+    exit_{R-1} = dS_final, exit_{j-1} = exit_j @ P_j^T + C_j; the cotangent at the start of
+    segment 0 is exit_0 @ P_0^T + C_0.  Returns (exit cotangents [R,H,V,K], d_initial [H,V,K]).
+    """
+    P = np.asarray(P, np.float64)
+    C = np.asarray(C, np.float64)
+    R, H, K, _ = P.shape
+    V = C.shape[2]
+    cur = np.zeros((H, V, K)) if d_final_state is None else np.array(d_final_state, np.float64)
+    exits = np.zeros((R, H, V, K))
+    for j in range(R - 1, -1, -1):
+        exits[j] = cur
+        cur = np.einsum("hvk,hjk->hvj", cur, P[j]) + C[j]
+    return exits, cur

@@ -395,3 +395,51 @@ def test_grouped_heads_summary_is_the_affine_map():
     sl = slice(7, 31)
     _, fin = oracle.gdn_fwd(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl], S0)
     assert np.allclose(fin[0], np.einsum("hvk,hkj->hvj", S0[0], P[0]) + E[0], atol=1e-12)
+
+
+# ---------------------------------------------------------------- reverse (cotangent) maps
+def test_reverse_map_is_affine_with_the_transposed_forward_transition():
+    """For a segment, the backward's cotangent at its start equals dS_exit @ P^T + C for
+    any exit cotangent, entry state and values: P from the forward summary (identity
+    probing), C from the reverse summary (zero probing), the left side from the plain
+    backward -- three oracle routines that share nothing but the token rule."""
+    B, T, H, K, V = 1, 45, 2, 5, 3
+    rng = np.random.default_rng(21)
+    q, k, v, g, beta, S0 = rand_inputs(B, T, H, K, V, rng)
+    g *= 0.3
+    dO = rng.normal(size=(B, T, H, V))
+    offs = [0, 19, 19, 45]
+    P, _ = oracle.segment_summary(k, v, g, beta, np.array([[0, 19], [19, 19], [19, 45]]))
+    C = oracle.segment_reverse_summary(q, k, g, beta, dO, offs)
+    dSf = rng.normal(size=(3, H, V, K))
+    S0r = rng.normal(size=(3, H, V, K))
+    got = oracle.gdn_bwd(q, k, v, g, beta, S0r, dO, dSf, cu_seqlens=offs)["d_initial_state"]
+    want = np.einsum("rhvk,rhjk->rhvj", dSf, P) + C
+    assert np.allclose(got, want, rtol=1e-11, atol=1e-12)
+    assert np.array_equal(C[1], np.zeros_like(C[1]))          # an empty segment adds nothing
+
+
+def test_reverse_scan_equals_the_single_pass_backward():
+    """Segment maps composed from the end reproduce the single-pass cotangents: the exit
+    cotangent of each segment is the d_initial_state of the backward of everything after
+    it, and the scan's last value is the whole sequence's d_initial_state."""
+    B, T, H, K, V = 1, 60, 1, 4, 4
+    rng = np.random.default_rng(22)
+    q, k, v, g, beta, S0 = rand_inputs(B, T, H, K, V, rng)
+    g *= 0.2
+    dO = rng.normal(size=(B, T, H, V))
+    dSf = rng.normal(size=(1, H, V, K))
+    offs = [0, 17, 40, 60]
+    bounds = np.array([[offs[i], offs[i + 1]] for i in range(3)])
+    P, _ = oracle.segment_summary(k, v, g, beta, bounds)
+    C = oracle.segment_reverse_summary(q, k, g, beta, dO, offs)
+    exits, d0 = oracle.state_scan_reverse(P, C, dSf[0])
+    full = oracle.gdn_bwd(q, k, v, g, beta, S0, dO, dSf)
+    assert np.allclose(d0, full["d_initial_state"][0], rtol=1e-10, atol=1e-12)
+    for j in range(3):
+        sl = slice(offs[j + 1], T)
+        tail = oracle.gdn_bwd(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl],
+                              S0, dO[:, sl], dSf)["d_initial_state"][0]
+        if offs[j + 1] == T:
+            tail = dSf[0]
+        assert np.allclose(exits[j], tail, rtol=1e-10, atol=1e-12), j
