@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "SF_OK", 1: "SF_ERR_INVALID_ARG", 2: "SF_ERR_UNSUPPORTED",
 EXPORTS = ("sf_last_error", "sf_version", "sf_gdn_fwd_workspace", "sf_gdn_chunk_fwd",
            "sf_gdn_summary_workspace", "sf_gdn_segment_summary", "sf_state_scan",
            "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc",
-           "sf_validate_cu_seqlens", "sf_workspace_status")
+           "sf_gdn_reverse_summary_workspace", "sf_gdn_segment_reverse_summary",
+           "sf_state_scan_reverse", "sf_validate_cu_seqlens", "sf_workspace_status")
 
 
 class SfError(RuntimeError):
@@ -71,11 +72,16 @@ def load(path: str = LIB_PATH):
                                          vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.sf_gdn_chunk_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  vp, vp, vp, vp, vp, vp, vp]
+        lib.sf_gdn_reverse_summary_workspace.argtypes = [sp]
+        lib.sf_gdn_reverse_summary_workspace.restype = sz
+        lib.sf_gdn_segment_reverse_summary.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.sf_state_scan_reverse.argtypes = [I, I, I, I, vp, vp, vp, vp, vp, vp]
         lib.sf_validate_cu_seqlens.argtypes = [vp, I, I, vp]
         lib.sf_workspace_status.argtypes = [vp, vp]
         for f in ("sf_gdn_chunk_fwd", "sf_gdn_segment_summary", "sf_state_scan",
                   "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc", "sf_validate_cu_seqlens",
-                  "sf_workspace_status"):
+                  "sf_workspace_status", "sf_gdn_segment_reverse_summary",
+                  "sf_state_scan_reverse"):
             getattr(lib, f).restype = st
         _lib = lib
         return lib
@@ -187,6 +193,46 @@ def sf_state_scan(P, S_ext, S0=None, entry_states=None, final_state=None, stream
     _check(lib.sf_state_scan(R, H, K, V, _ptr(_f32(P)), _ptr(_f32(S_ext)), _ptr(_f32(S0)),
                              _ptr(entry_states), _ptr(final_state), _stream(stream)))
     return entry_states, final_state
+
+
+def sf_gdn_segment_reverse_summary(q, k, gate, beta, d_out, seg_offsets, scale=None, C=None,
+                                   ws=None, stream=None):
+    """Cotangent map of consecutive segments (offsets [R+1], cu_seqlens convention) of one
+    token stream (B = 1): returns C [R,H,V,K], the cotangent each segment's own output
+    gradients leave at its start (dS_entry = dS_exit @ P^T + C)."""
+    lib = load()
+    shape = make_shape(q, d_out, seg_offsets, scale)
+    if seg_offsets.dtype != torch.int32:
+        raise ValueError("seg_offsets must be int32 [R+1]")
+    if C is None:
+        C = torch.empty(shape.N, shape.H, shape.V, shape.K, dtype=torch.float32, device=q.device)
+    need = lib.sf_gdn_reverse_summary_workspace(ctypes.byref(shape))
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib.sf_gdn_segment_reverse_summary(ctypes.byref(shape), _ptr(q), _ptr(k),
+                                              _ptr(_f32(gate)), _ptr(_f32(beta)), _ptr(d_out),
+                                              _ptr(seg_offsets), _ptr(C), _ptr(ws), ws.numel(),
+                                              _stream(stream)))
+    return C
+
+
+def sf_state_scan_reverse(P, C, dS_final=None, exit_cotangents=None, d_initial=None,
+                          stream=None, want_initial=True):
+    """Reverse scan of cotangent maps: returns (exit cotangents [R,H,V,K], d_initial [H,V,K])."""
+    lib = load()
+    R, H, K, _ = P.shape
+    V = C.shape[2]
+    if exit_cotangents is None:
+        exit_cotangents = torch.empty(R, H, V, K, dtype=torch.float32, device=P.device)
+    if want_initial and d_initial is None:
+        d_initial = torch.empty(H, V, K, dtype=torch.float32, device=P.device)
+    _check(lib.sf_state_scan_reverse(R, H, K, V, _ptr(_f32(P)), _ptr(_f32(C)), _ptr(_f32(dS_final)),
+                                     _ptr(exit_cotangents), _ptr(d_initial), _stream(stream)))
+    return exit_cotangents, d_initial
+
+
+def reverse_summary_workspace_bytes(shape: sf_gdn_shape) -> int:
+    return int(load().sf_gdn_reverse_summary_workspace(ctypes.byref(shape)))
 
 
 def sf_gdn_chunk_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state=None,

@@ -228,6 +228,78 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float* P, const float*
 
 size_t sf_gdn_bwd_workspace(const sf_gdn_shape* shape) { return bwd_layout(shape).total; }
 
+// Reverse summary workspace: status word | exit cotangents of every chunk (the reverse
+// chain's tape, FP32 [slots,H,V,K]) | BF16 only: per-chunk factors [slots,H].  Slots as the
+// packed backward: ceil(T/64) + R.
+struct RevLayout {
+  size_t tape, fac, total;
+};
+
+RevLayout rev_layout(const sf_gdn_shape* shape) {
+  RevLayout l{0, 0, kStatusBytes};
+  if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0 || shape->N < 0) return l;
+  const int64_t slots = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK + shape->N;
+  l.tape = round_up((size_t)slots * shape->H * shape->K * shape->V * sizeof(float));
+  if (shape->dtype == SF_BF16 && (shape->K == 64 || shape->K == 128))
+    l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));
+  l.total = kStatusBytes + l.tape + l.fac;
+  return l;
+}
+
+size_t sf_gdn_reverse_summary_workspace(const sf_gdn_shape* shape) {
+  return rev_layout(shape).total;
+}
+
+sf_status sf_gdn_segment_reverse_summary(const sf_gdn_shape* shape, const void* q, const void* k,
+                                         const float* gate, const float* beta, const void* d_out,
+                                         const int32_t* seg_offsets, float* C, void* workspace,
+                                         size_t ws_bytes, sf_stream_t stream) {
+  const char* fn = "sf_gdn_segment_reverse_summary";
+  sf_status st = check_shape(shape, true, true, fn);
+  if (st != SF_OK) return st;
+  const bool bf16 = shape->dtype == SF_BF16;
+  const int D = shape->K;
+  if (!bf16 && D != 64)
+    return fail(SF_ERR_UNSUPPORTED, "%s: FP32 inputs support K = V = 64 only", fn);
+  if (!seg_offsets || !C)
+    return fail(SF_ERR_INVALID_ARG, "%s: seg_offsets and C must be non-NULL", fn);
+  if (shape->T > 0 && (!q || !k || !gate || !beta || !d_out))
+    return fail(SF_ERR_INVALID_ARG, "%s: q, k, gate, beta and d_out must be non-NULL", fn);
+  const RevLayout lay = rev_layout(shape);
+  if (!workspace || ws_bytes < lay.total)
+    return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn, lay.total);
+  char* ws = reinterpret_cast<char*>(workspace);
+  sfg::ChainParams p{};
+  p.q = q; p.k = k; p.g = gate; p.beta = beta; p.cu = seg_offsets; p.dout = d_out;
+  p.dsf = nullptr;        // nothing flows in at a segment's end
+  p.ds0 = C;              // the cotangent the chain leaves at the segment's start
+  p.tape = reinterpret_cast<float*>(ws + kStatusBytes);
+  p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + lay.tape) : nullptr;
+  p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
+  p.HK = eff_hk(shape);
+  const int64_t slots = bwd_slots(shape, true);
+  cudaError_t e = sfg::launch_simt_bwd(p, bf16, D, slots, reinterpret_cast<cudaStream_t>(stream),
+                                       /*chain_only=*/true);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
+sf_status sf_state_scan_reverse(int R, int H, int K, int V, const float* P, const float* C,
+                                const float* dS_final, float* exit_cotangents, float* d_initial,
+                                sf_stream_t stream) {
+  const char* fn = "sf_state_scan_reverse";
+  if (R < 0 || H < 1) return fail(SF_ERR_INVALID_ARG, "%s: need R>=0 and H>=1", fn);
+  if (K != V || (K != 64 && K != 128))
+    return fail(SF_ERR_UNSUPPORTED, "%s: K == V in {64, 128} only", fn);
+  if (R > 0 && (!P || !C || !exit_cotangents))
+    return fail(SF_ERR_INVALID_ARG, "%s: P, C and exit_cotangents must be non-NULL", fn);
+  if (R == 0 && !d_initial) return SF_OK;
+  cudaError_t e = sfg::launch_state_scan_reverse(R, H, K, P, C, dS_final, exit_cotangents,
+                                                 d_initial, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return SF_OK;
+}
+
 sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
                            const float* gate, const float* beta, const float* initial_state,
                            const int32_t* cu_seqlens, const void* d_out, const float* d_final_state,

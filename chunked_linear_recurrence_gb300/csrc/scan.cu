@@ -5,6 +5,10 @@
 //
 //   entry_0 = S0,  entry_{j+1} = entry_j P_j + S_ext_j,  final = entry_R
 //
+// and its reverse, for the state cotangents of the backward (whose per-segment map is
+// dS_entry = dS_exit P^T + C): the segments are walked from the last one and P enters
+// transposed, exit_{R-1} = dS_final, exit_{j-1} = exit_j P_j^T + C_j.
+//
 // Rows of the state are independent under right-multiplication by P, so the
 // scan is split over (head, block of RB rows); each CTA keeps its rows in
 // shared memory and walks the R segments in order.  FP32 throughout.
@@ -13,7 +17,7 @@
 
 namespace sfg {
 
-template <int D, int RB>
+template <int D, int RB, bool REV>
 __global__ void __launch_bounds__(D) state_scan_kernel(int R, int H, const float* __restrict__ P,
                                                        const float* __restrict__ E,
                                                        const float* __restrict__ S0,
@@ -27,7 +31,8 @@ __global__ void __launch_bounds__(D) state_scan_kernel(int R, int H, const float
   for (int r = 0; r < RB; ++r)
     cur[r][c] = S0 ? S0[(size_t)h * SZ + (size_t)(r0 + r) * D + c] : 0.f;
   __syncthreads();
-  for (int j = 0; j < R; ++j) {
+  for (int jj = 0; jj < R; ++jj) {
+    const int j = REV ? R - 1 - jj : jj;
     const size_t base = ((size_t)j * H + h) * SZ;
     float acc[RB];
 #pragma unroll
@@ -38,7 +43,7 @@ __global__ void __launch_bounds__(D) state_scan_kernel(int R, int H, const float
     const float* Pj = P + base;
 #pragma unroll 4
     for (int m = 0; m < D; ++m) {
-      const float pm = Pj[(size_t)m * D + c];
+      const float pm = REV ? Pj[(size_t)c * D + m] : Pj[(size_t)m * D + c];
 #pragma unroll
       for (int r = 0; r < RB; ++r) acc[r] += cur[r][m] * pm;
     }
@@ -52,17 +57,31 @@ __global__ void __launch_bounds__(D) state_scan_kernel(int R, int H, const float
     for (int r = 0; r < RB; ++r) final_state[(size_t)h * SZ + (size_t)(r0 + r) * D + c] = cur[r][c];
 }
 
-cudaError_t launch_state_scan(int R, int H, int D, const float* P, const float* E,
-                              const float* S0, float* entry, float* final_state, cudaStream_t st) {
+template <bool REV>
+static cudaError_t launch_scan_t(int R, int H, int D, const float* P, const float* E,
+                                 const float* S0, float* entry, float* final_state,
+                                 cudaStream_t st) {
   constexpr int RB = 8;
   if (D == 64)
-    state_scan_kernel<64, RB><<<dim3(64 / RB, H), 64, 0, st>>>(R, H, P, E, S0, entry, final_state);
+    state_scan_kernel<64, RB, REV><<<dim3(64 / RB, H), 64, 0, st>>>(R, H, P, E, S0, entry,
+                                                                    final_state);
   else if (D == 128)
-    state_scan_kernel<128, RB><<<dim3(128 / RB, H), 128, 0, st>>>(R, H, P, E, S0, entry,
-                                                                  final_state);
+    state_scan_kernel<128, RB, REV><<<dim3(128 / RB, H), 128, 0, st>>>(R, H, P, E, S0, entry,
+                                                                       final_state);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
+}
+
+cudaError_t launch_state_scan(int R, int H, int D, const float* P, const float* E,
+                              const float* S0, float* entry, float* final_state, cudaStream_t st) {
+  return launch_scan_t<false>(R, H, D, P, E, S0, entry, final_state, st);
+}
+
+cudaError_t launch_state_scan_reverse(int R, int H, int D, const float* P, const float* C,
+                                      const float* dSf, float* exits, float* d_initial,
+                                      cudaStream_t st) {
+  return launch_scan_t<true>(R, H, D, P, C, dSf, exits, d_initial, st);
 }
 
 }  // namespace sfg

@@ -739,12 +739,13 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 }
 
 template <typename Tin, int D>
-static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
+static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_t st,
+                                bool chain_only) {
   cudaError_t e;
   if (std::is_same<Tin, __nv_bfloat16>::value) {
     // BF16: reverse chain and token gradients on the warp-level tensor cores
     if ((e = launch_mma_bwd_chain(p, p.fac, D, slots, st)) != cudaSuccess) return e;
-    return launch_mma_bwd_grad(p, true, D, slots, st);
+    return chain_only ? cudaSuccess : launch_mma_bwd_grad(p, true, D, slots, st);
   }
   // FP32 inputs keep FP32 products on the CUDA cores (1e-4 parity)
   constexpr int BV = 32;
@@ -754,7 +755,7 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(D / BV, p.H, p.N), NT, smem, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess || chain_only) return e;
   const size_t smem2 = sizeof(float) * (3 * 64 * 65 + 3 * 64 * (D + 1) + 7 * 64) +
                        sizeof(Tin) * 4 * 64 * (D + 8);
   auto kern2 = simt_bwd_grad_kernel<Tin, D>;
@@ -765,10 +766,10 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
 }
 
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
-                            cudaStream_t st) {
-  if (bf16 && D == 64) return launch_bwd_t<__nv_bfloat16, 64>(p, slots, st);
-  if (bf16 && D == 128) return launch_bwd_t<__nv_bfloat16, 128>(p, slots, st);
-  if (!bf16 && D == 64) return launch_bwd_t<float, 64>(p, slots, st);
+                            cudaStream_t st, bool chain_only) {
+  if (bf16 && D == 64) return launch_bwd_t<__nv_bfloat16, 64>(p, slots, st, chain_only);
+  if (bf16 && D == 128) return launch_bwd_t<__nv_bfloat16, 128>(p, slots, st, chain_only);
+  if (!bf16 && D == 64) return launch_bwd_t<float, 64>(p, slots, st, chain_only);
   return cudaErrorInvalidValue;
 }
 

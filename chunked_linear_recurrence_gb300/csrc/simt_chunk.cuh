@@ -69,8 +69,10 @@ __host__ __device__ inline int ckpt_tiled_off(int v, int k) {
   return ((((k & 63) >> 2) << 8) + ((k >> 6) << 7) + v) * 4 + (k & 3);
 }
 
+// chain_only: only the reverse cotangent chain (and, for BF16, its per-chunk factors) --
+// the segments' cotangent maps need p.ds0 alone, no state replay and no token gradients.
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
-                            cudaStream_t st);
+                            cudaStream_t st, bool chain_only = false);
 // Grouped heads: out[r, hk, c] = sum over j < H / HK of acc[r, hk (H / HK) + j, c] for the
 // active rows r (r < cu[N] when cu != NULL, else all B*T), in the q/k/v dtype.
 cudaError_t launch_group_sum(const float* acc, void* out, bool bf16, int64_t rows, int H, int HK,

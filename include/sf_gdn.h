@@ -151,6 +151,49 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float *P, const float 
                         sf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Reverse segment summary: the backward counterpart of the segment summary
+ * (same section: the backward carries the state cotangent from the end of
+ * the sequence to its start, and each token's adjoint is affine in it).  For
+ * consecutive segments of one token stream, the cotangent at a segment's
+ * start is
+ *     dS_entry = dS_exit @ P^T + C
+ * with P the segment's forward transition (sf_gdn_segment_summary) and C the
+ * cotangent its own output gradients produce at its start when nothing flows
+ * in at its end.  This entry point computes C.
+ *
+ *   shape          B = 1 (rows flattened), T = rows, N = R segments,
+ *                  HK query/key heads as everywhere
+ *   seg_offsets    int32 [R+1] device, the cu_seqlens convention: segment r
+ *                  owns rows [seg_offsets[r], seg_offsets[r+1])
+ *   q, k [1,T,HK,K]; gate, beta [1,T,H]; d_out [1,T,H,V] (q/k dtype)
+ *   C              [R,H,V,K] FP32
+ * C depends on neither the values nor the forward states.  Supported: BF16
+ * with K = V in {64,128}; F32 with K = V = 64.
+ * ---------------------------------------------------------------------- */
+size_t sf_gdn_reverse_summary_workspace(const sf_gdn_shape *shape);
+sf_status sf_gdn_segment_reverse_summary(const sf_gdn_shape *shape, const void *q,
+                                         const void *k, const float *gate, const float *beta,
+                                         const void *d_out, const int32_t *seg_offsets,
+                                         float *C, void *workspace, size_t ws_bytes,
+                                         sf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Reverse exclusive scan of the cotangent maps, from the last segment to the
+ * first:
+ *     exit_{R-1} = dS_final,   exit_{j-1} = exit_j @ P_j^T + C_j,
+ *     d_initial  = exit_0 @ P_0^T + C_0
+ *   P [R,H,K,K], C [R,H,V,K], dS_final [H,V,K] or NULL (zeros),
+ *   exit_cotangents [R,H,V,K] (the cotangent at each segment's end),
+ *   d_initial [H,V,K] or NULL.  All FP32.  K == V in {64,128}.  No workspace.
+ * With the entry states of sf_state_scan and these exit cotangents, the
+ * packed backward over the segments (initial_state = entry states,
+ * d_final_state = exit cotangents) gives every gradient of the single pass.
+ * ---------------------------------------------------------------------- */
+sf_status sf_state_scan_reverse(int R, int H, int K, int V, const float *P, const float *C,
+                                const float *dS_final, float *exit_cotangents,
+                                float *d_initial, sf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Backward of sf_gdn_chunk_fwd (StateFlow section 3.1, Eq. 6-7: the
  * input-state gradient of chunk i+1 is the output-state gradient of chunk i;
  * section 3.4.2, Eq. 18: state replay, output gradient, backward state

@@ -112,3 +112,24 @@ def test_packed_backward_workspace_scales_with_tokens_not_sequences(lib):
     assert eight - one == 7 * 2 * 180736 + 7 * 2 * 462848
     dense = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(B=8, N=8, T=4096, H=2)))
     assert dense - eight == (8 * 64 - (64 + 8)) * 2 * 180736
+
+
+def test_reverse_maps_reject_bad_arguments(lib):
+    """The reverse summary wants packed offsets (B = 1), C and a large enough workspace;
+    the reverse scan the same sizes as the forward scan."""
+    s = _shape(T=256, N=2)
+    need = lib.sf_gdn_reverse_summary_workspace(ctypes.byref(s))
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert lib.sf_gdn_segment_reverse_summary(ctypes.byref(s), *args, None, FAKE, FAKE, need,
+                                              None) == 1          # no offsets
+    assert lib.sf_gdn_segment_reverse_summary(ctypes.byref(s), *args, FAKE, None, FAKE, need,
+                                              None) == 1          # no C
+    assert lib.sf_gdn_segment_reverse_summary(ctypes.byref(s), *args, FAKE, FAKE, FAKE, need - 1,
+                                              None) == 3          # workspace too small
+    assert lib.sf_gdn_segment_reverse_summary(ctypes.byref(_shape(B=2, T=256, N=2)), *args, FAKE,
+                                              FAKE, FAKE, need, None) == 1   # offsets need B = 1
+    assert lib.sf_gdn_segment_reverse_summary(ctypes.byref(_shape(T=256, N=2, dtype=0)), *args,
+                                              FAKE, FAKE, FAKE, need, None) == 2   # FP32 at K = 128
+    assert lib.sf_state_scan_reverse(2, 1, 128, 64, FAKE, FAKE, None, FAKE, None, None) == 2
+    assert lib.sf_state_scan_reverse(-1, 1, 128, 128, FAKE, FAKE, None, FAKE, None, None) == 1
+    assert lib.sf_state_scan_reverse(2, 1, 128, 128, None, FAKE, None, FAKE, None, None) == 1
