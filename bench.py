@@ -40,7 +40,9 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# Algorithmic traffic / work per token-head at d = 128, chunk 64:
+# Algorithmic traffic / work per token-head at d = 128, chunk 64: the bytes the method must
+# move (inputs read once, outputs written once) and its FLOPs with the causal C x C products
+# counted as triangles:
 FWD_BYTES_PER_TH = 1032          # q,k,v 768 + gate,beta 8 + out 256 (BF16)
 FWD_FLOP_PER_TH = 139264         # 6 d^2 + 5 C d
 BWD_BYTES_PER_TH = 1808          # read q,k,v,g,beta,dO + write dq,dk,dv,dg,dbeta
