@@ -255,3 +255,32 @@ def state_scan_reverse(P, C, d_final_state=None):
         exits[j] = cur
         cur = np.einsum("hvk,hjk->hvj", cur, P[j]) + C[j]
     return exits, cur
+
+
+def paged_chunk_fwd(q, k, v, g, beta, state_cache, state_indices, has_initial_state=None,
+                    cu_seqlens=None, scale=None):
+    """The forward advancing a paged state cache (Attention Gym "Linear Attention",
+    paged_chunk_gdn): sequence n starts from slot state_indices[n] (from zero when
+    has_initial_state[n] is False) and leaves its final state there; an index outside
+    [1, num_slots) is padding -- zero output rows, the cache untouched.
+
+    Returns (out [B,T,H,V], the advanced cache)."""
+    cache = np.array(state_cache, np.float64)
+    idx = np.asarray(state_indices).astype(np.int64)
+    N = len(idx)
+    num_slots = cache.shape[0]
+    live = (idx > 0) & (idx < num_slots)
+    load_ = live if has_initial_state is None else live & np.asarray(has_initial_state, bool)
+    S0 = np.zeros((N,) + cache.shape[1:])
+    for n in range(N):
+        if load_[n]:
+            S0[n] = cache[idx[n]]
+    out, fin = gdn_fwd(q, k, v, g, beta, S0, cu_seqlens=cu_seqlens, scale=scale)
+    for n in range(N):
+        if live[n]:
+            cache[idx[n]] = fin[n]
+        elif cu_seqlens is None:
+            out[n] = 0.0
+        else:
+            out[:, int(cu_seqlens[n]):int(cu_seqlens[n + 1])] = 0.0
+    return out, cache

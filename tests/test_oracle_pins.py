@@ -443,3 +443,45 @@ def test_reverse_scan_equals_the_single_pass_backward():
         if offs[j + 1] == T:
             tail = dSf[0]
         assert np.allclose(exits[j], tail, rtol=1e-10, atol=1e-12), j
+
+
+# ---------------------------------------------------------------- paged state cache
+def test_paged_cache_advances_like_one_pass():
+    """Prefill through the cache in two calls (the first from fresh slots full of NaN,
+    has_initial_state False) equals one forward over the whole sequences; padding rows are
+    zero and every slot not selected keeps its bits."""
+    B, T, H, K, V = 1, 40, 2, 4, 3
+    rng = np.random.default_rng(31)
+    q, k, v, g, beta, _ = rand_inputs(B, T, H, K, V, rng)
+    lengths = [(9, 6), (0, 11), (7, 7)]                       # (first call, second call) per sequence
+    whole_cu = np.cumsum([0] + [a + b for a, b in lengths])
+    slots = np.array([3, -1, 1], np.int32)                    # sequence 1 is padding
+    cache = rng.normal(size=(5, H, V, K))
+    cache[3] = np.nan                                         # garbage: must never be read
+    cache[1] = np.nan
+
+    def part(which):
+        rows = np.concatenate([np.arange(whole_cu[n] + (0 if which == 0 else lengths[n][0]),
+                                         whole_cu[n] + lengths[n][0] + (0 if which == 0 else lengths[n][1]))
+                               for n in range(3)]).astype(int)
+        cu = np.cumsum([0] + [lengths[n][which] for n in range(3)])
+        sl = lambda a: a[:, rows]
+        return sl(q), sl(k), sl(v), sl(g), sl(beta), cu, rows
+
+    q1, k1, v1, g1, b1, cu1, r1 = part(0)
+    out1, c1 = oracle.paged_chunk_fwd(q1, k1, v1, g1, b1, cache, slots,
+                                      has_initial_state=[False, True, False], cu_seqlens=cu1)
+    q2, k2, v2, g2, b2, cu2, r2 = part(1)
+    out2, c2 = oracle.paged_chunk_fwd(q2, k2, v2, g2, b2, c1, slots, cu_seqlens=cu2)
+    ref_out, ref_fin = oracle.gdn_fwd(q, k, v, g, beta, None, cu_seqlens=whole_cu)
+    for n, s in ((0, 3), (2, 1)):
+        assert np.allclose(c2[s], ref_fin[n], rtol=1e-12, atol=1e-12)
+    full = np.full_like(ref_out, np.nan)
+    full[:, r1] = out1
+    full[:, r2] = out2
+    for n in (0, 2):
+        rows = slice(whole_cu[n], whole_cu[n + 1])
+        assert np.allclose(full[:, rows], ref_out[:, rows], rtol=1e-12, atol=1e-12)
+    assert not full[:, whole_cu[1]:whole_cu[2]].any()         # padding: zero output
+    for s in (0, 2, 4):
+        assert np.array_equal(c2[s], cache[s])                # unselected slots keep their bits
