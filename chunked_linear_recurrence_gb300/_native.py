@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "SF_OK", 1: "SF_ERR_INVALID_ARG", 2: "SF_ERR_UNSUPPORTED",
 
 # Every symbol include/sf_gdn.h declares.
 EXPORTS = ("sf_last_error", "sf_version", "sf_gdn_fwd_workspace", "sf_gdn_chunk_fwd",
+           "sf_gdn_paged_chunk_fwd",
            "sf_gdn_summary_workspace", "sf_gdn_segment_summary", "sf_state_scan",
            "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc",
            "sf_gdn_reverse_summary_workspace", "sf_gdn_segment_reverse_summary",
@@ -62,6 +63,8 @@ def load(path: str = LIB_PATH):
         lib.sf_gdn_fwd_workspace.argtypes = [sp]
         lib.sf_gdn_fwd_workspace.restype = sz
         lib.sf_gdn_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, I, vp, vp, vp, sz, vp]
+        lib.sf_gdn_paged_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, I, vp, vp, vp, vp, vp,
+                                               sz, vp]
         lib.sf_gdn_summary_workspace.argtypes = [sp, I]
         lib.sf_gdn_summary_workspace.restype = sz
         lib.sf_gdn_segment_summary.argtypes = [sp, vp, vp, vp, vp, vp, I, vp, vp, vp, sz, vp]
@@ -78,7 +81,8 @@ def load(path: str = LIB_PATH):
         lib.sf_state_scan_reverse.argtypes = [I, I, I, I, vp, vp, vp, vp, vp, vp]
         lib.sf_validate_cu_seqlens.argtypes = [vp, I, I, vp]
         lib.sf_workspace_status.argtypes = [vp, vp]
-        for f in ("sf_gdn_chunk_fwd", "sf_gdn_segment_summary", "sf_state_scan",
+        for f in ("sf_gdn_chunk_fwd", "sf_gdn_paged_chunk_fwd", "sf_gdn_segment_summary",
+                  "sf_state_scan",
                   "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc", "sf_validate_cu_seqlens",
                   "sf_workspace_status", "sf_gdn_segment_reverse_summary",
                   "sf_state_scan_reverse"):
@@ -158,6 +162,31 @@ def sf_gdn_chunk_fwd(q, k, v, gate, beta, initial_state=None, cu_seqlens=None, s
                                 _ptr(final_state) if output_final_state else None,
                                 _ptr(ws), ws.numel(), _stream(stream)))
     return out, (final_state if output_final_state else None)
+
+
+def sf_gdn_paged_chunk_fwd(q, k, v, gate, beta, state_cache, state_indices, cu_seqlens=None,
+                           has_initial_state=None, scale=None, out=None, ws=None, stream=None):
+    """paged_chunk_gdn: the forward advancing state_cache [num_slots,H,V,K] in place at the
+    slots state_indices (int32 [N]; <= 0: padding, zero output); has_initial_state (bool
+    [N]) False starts from zero.  Returns out [B,T,H,V]."""
+    lib = load()
+    shape = make_shape(q, v, cu_seqlens, scale)
+    if state_indices.dtype != torch.int32 or state_indices.numel() != shape.N:
+        raise ValueError("state_indices must be int32 [N]")
+    if has_initial_state is not None and (has_initial_state.dtype != torch.bool or
+                                          has_initial_state.numel() != shape.N):
+        raise ValueError("has_initial_state must be bool [N]")
+    if out is None:
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    need = lib.sf_gdn_fwd_workspace(ctypes.byref(shape))
+    if ws is None:
+        ws = workspace(need, q.device)
+    _check(lib.sf_gdn_paged_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(_f32(gate)), _ptr(_f32(beta)), _ptr(_f32(state_cache)),
+                                      state_cache.shape[0], _ptr(state_indices),
+                                      _ptr(has_initial_state), _ptr(cu_seqlens), _ptr(out),
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def sf_gdn_segment_summary(k, v, gate, beta, bounds, P=None, S_ext=None, ws=None, stream=None):

@@ -137,20 +137,24 @@ size_t sf_gdn_fwd_workspace(const sf_gdn_shape* shape) {
   return kStatusBytes;
 }
 
-sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
-                           const float* gate, const float* beta, const float* initial_state,
-                           const int32_t* cu_seqlens, int output_final_state, void* out,
-                           float* final_state, void* workspace, size_t ws_bytes,
-                           sf_stream_t stream) {
-  const char* fn = "sf_gdn_chunk_fwd";
+}  // extern "C"
+
+namespace {
+
+// The forward shared by sf_gdn_chunk_fwd and sf_gdn_paged_chunk_fwd (pool != NULL: the
+// entry and final states are slots of the paged cache).
+sf_status chunk_fwd(const char* fn, const sf_gdn_shape* shape, const void* q, const void* k,
+                    const void* v, const float* gate, const float* beta,
+                    const float* initial_state, const int32_t* cu_seqlens, float* final_state,
+                    void* out, float* pool, int num_slots, const int32_t* state_indices,
+                    const uint8_t* has_initial_state, void* workspace, size_t ws_bytes,
+                    sf_stream_t stream) {
   sf_status st = check_shape(shape, cu_seqlens != nullptr, true, fn);
   if (st != SF_OK) return st;
   if (shape->T > 0 && (!q || !k || !v || !gate || !beta || !out))
     return fail(SF_ERR_INVALID_ARG, "%s: q, k, v, gate, beta and out must be non-NULL", fn);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(SF_ERR_INVALID_ARG, "%s: q, k, v and out must be 16-byte aligned", fn);
-  if (output_final_state && !final_state)
-    return fail(SF_ERR_INVALID_ARG, "%s: output_final_state requires final_state", fn);
   if (!workspace || ws_bytes < sf_gdn_fwd_workspace(shape))
     return fail(SF_ERR_WORKSPACE, "%s: workspace needs %zu bytes", fn, sf_gdn_fwd_workspace(shape));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -158,7 +162,9 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   const int D = shape->K;
   sfg::ChainParams p{};
   p.q = q; p.k = k; p.v = v; p.g = gate; p.beta = beta; p.s0 = initial_state;
-  p.cu = cu_seqlens; p.out = out; p.final_state = output_final_state ? final_state : nullptr;
+  p.cu = cu_seqlens; p.out = out; p.final_state = final_state;
+  p.pool = pool; p.num_slots = num_slots; p.state_idx = state_indices;
+  p.has_init = has_initial_state;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   p.HK = eff_hk(shape);
   cudaError_t e;
@@ -169,6 +175,37 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void*
   }
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return SF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sf_status sf_gdn_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void* k, const void* v,
+                           const float* gate, const float* beta, const float* initial_state,
+                           const int32_t* cu_seqlens, int output_final_state, void* out,
+                           float* final_state, void* workspace, size_t ws_bytes,
+                           sf_stream_t stream) {
+  const char* fn = "sf_gdn_chunk_fwd";
+  if (output_final_state && !final_state)
+    return fail(SF_ERR_INVALID_ARG, "%s: output_final_state requires final_state", fn);
+  return chunk_fwd(fn, shape, q, k, v, gate, beta, initial_state, cu_seqlens,
+                   output_final_state ? final_state : nullptr, out, nullptr, 0, nullptr, nullptr,
+                   workspace, ws_bytes, stream);
+}
+
+sf_status sf_gdn_paged_chunk_fwd(const sf_gdn_shape* shape, const void* q, const void* k,
+                                 const void* v, const float* gate, const float* beta,
+                                 float* state_cache, int num_slots, const int32_t* state_indices,
+                                 const uint8_t* has_initial_state, const int32_t* cu_seqlens,
+                                 void* out, void* workspace, size_t ws_bytes, sf_stream_t stream) {
+  const char* fn = "sf_gdn_paged_chunk_fwd";
+  if (!state_cache || !state_indices || num_slots < 1)
+    return fail(SF_ERR_INVALID_ARG, "%s: state_cache, state_indices and num_slots >= 1 needed", fn);
+  if (!aligned16(state_cache))
+    return fail(SF_ERR_INVALID_ARG, "%s: state_cache must be 16-byte aligned", fn);
+  return chunk_fwd(fn, shape, q, k, v, gate, beta, nullptr, cu_seqlens, nullptr, out, state_cache,
+                   num_slots, state_indices, has_initial_state, workspace, ws_bytes, stream);
 }
 
 size_t sf_gdn_summary_workspace(const sf_gdn_shape* shape, int R) {

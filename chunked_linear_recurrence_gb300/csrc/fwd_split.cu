@@ -200,6 +200,12 @@ struct SplitParams {
   // CTA j < nch runs it from S0 = 0 with the value term (-> sumE), chain CTA nch + j runs
   // the same records from S0 = I without it (-> sumP)
   const int32_t* bounds;     // [N,2] token ranges, else NULL
+  // paged state cache: sequence n reads and advances slot state_idx[n] of pool (zeros in
+  // when has_init[n] == 0); state_idx[n] <= 0: zero output, the pool untouched
+  float* pool;               // [num_slots,H,V,K] or NULL
+  const int32_t* state_idx;
+  const uint8_t* has_init;   // or NULL
+  int num_slots;             // indices >= num_slots: padding as well
   float* sumP;               // [N,H,K,K]
   float* sumE;               // [N,H,V,K]
   int twin;
@@ -542,6 +548,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       const bool okr = geo.span(x, bos, eos);
       const int nc = (int)n_chunks(eos - bos);
       float* const fdst = summ ? (ptwin ? p.sumP : p.sumE) : p.final_state;
+      // this thread's 64 entry values and final values: the [N,H,V,K] arguments, or the
+      // chain's slot of the paged cache (padding: zeros in, nothing out)
+      const float* s0p = p.s0 ? p.s0 + soff : nullptr;
+      float* fp = fdst ? fdst + soff : nullptr;
+      if (p.pool) {
+        const int n = x / H, ps = p.state_idx[n];
+        const bool live = ps > 0 && ps < p.num_slots;
+        const size_t off = (((size_t)(live ? ps : 0) * H + x % H) * D + v) * D + 64 * w;
+        s0p = (live && (!p.has_init || p.has_init[n])) ? p.pool + off : nullptr;
+        fp = live ? p.pool + off : nullptr;
+      }
       // entry state element (v, 64 w + e) without S0: zero, or the identity for the P twin
       auto s_init = [&](int e) -> float { return (ptwin && 64 * w + e == v) ? 1.f : 0.f; };
       // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c]
@@ -553,13 +570,13 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       if (nc == 0) {
         // an empty sequence passes its initial state through (an empty range: the identity
         // map; an invalid range: NaN)
-        if (fdst) {
-          float4* dst = reinterpret_cast<float4*>(fdst + soff);
-          const float4* src = reinterpret_cast<const float4*>(p.s0 + soff);
+        if (fp) {
+          float4* dst = reinterpret_cast<float4*>(fp);
+          const float4* src = reinterpret_cast<const float4*>(s0p);
           const float nanv = __int_as_float(0x7fc00000);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            dst[e] = p.s0 ? src[e]
+            dst[e] = s0p ? src[e]
                    : !okr ? make_float4(nanv, nanv, nanv, nanv)
                           : make_float4(s_init(4 * e), s_init(4 * e + 1), s_init(4 * e + 2), s_init(4 * e + 3));
         }
@@ -571,8 +588,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       {
         const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NBUF) * C_BUF + R_VEC + 256);
         float xv[64];
-        if (p.s0) {
-          const float4* src = reinterpret_cast<const float4*>(p.s0 + soff);
+        if (s0p) {
+          const float4* src = reinterpret_cast<const float4*>(s0p);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float4 f = src[e];
@@ -666,8 +683,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         float xv[64];
         tmem_ld64(tl + TM_S + 64 * w, xv);
         if (c + 1 == nc) {
-          if (fdst) {
-            float4* dst = reinterpret_cast<float4*>(fdst + soff);
+          if (fp) {
+            float4* dst = reinterpret_cast<float4*>(fp);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
@@ -720,6 +737,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       int64_t bos, eos;
       geo.span(x, bos, eos);
       const int nc = (int)n_chunks(eos - bos);
+      // paged cache: padding (a slot index outside [1, num_slots)) gives zero output
+      const bool padded = p.pool && (p.state_idx[x / H] <= 0 || p.state_idx[x / H] >= p.num_slots);
       for (int c = 0; c < nc; ++c, ++s) {
         const int b = s & 1;
         if (!(ok = group_wait(&bars[C_ODONE + b], (s >> 1) & 1, BAR_OUT, 128, cx))) break;
@@ -739,7 +758,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
 #pragma unroll
           for (int i = 0; i < 64; ++i)
             *reinterpret_cast<__nv_bfloat16*>(st + sw128_off(i, v, 8192)) =
-                __float2bfloat16_rn(p.scale * o[i]);
+                __float2bfloat16_rn(padded ? 0.f : p.scale * o[i]);
           fence_proxy_async_smem();
           named_bar(BAR_OUT, 128);
           if (v == 0) {
@@ -753,7 +772,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (i < L) orow[i * rs] = __float2bfloat16_rn(p.scale * o[i]);
+            if (i < L) orow[i * rs] = __float2bfloat16_rn(padded ? 0.f : p.scale * o[i]);
         }
         if (v == 0) mbar_arrive(&bars[C_RECFREE + rb]);
       }
@@ -1580,6 +1599,10 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaS
   p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
   p.final_state = cp.final_state;
   p.ckpt = cp.ckpt;
+  p.pool = cp.pool;
+  p.state_idx = cp.state_idx;
+  p.has_init = cp.has_init;
+  p.num_slots = cp.num_slots;
   p.cu = cp.cu;
   p.B = cp.B;
   p.T = cp.T;

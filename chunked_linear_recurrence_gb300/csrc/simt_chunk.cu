@@ -86,6 +86,18 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
   }
   const bool value_on = (MODE != MODE_SUMMARY) || (r0 < D);
 
+  // where this chain's entry state comes from and its final state goes: the [N,H,V,K]
+  // arguments, or a slot of the paged cache (padding: zeros in, nothing out, zero output)
+  const size_t HDD = (size_t)H * D * D;
+  const float* s0src = p.s0 ? p.s0 + (size_t)item * HDD : nullptr;
+  float* fdst = p.final_state ? p.final_state + (size_t)item * HDD : nullptr;
+  bool padded = false;
+  if (MODE == MODE_FWD && p.pool) {
+    const int ps = p.state_idx[item];
+    padded = ps <= 0 || ps >= p.num_slots;
+    s0src = (!padded && (!p.has_init || p.has_init[item])) ? p.pool + (size_t)ps * HDD : nullptr;
+    fdst = padded ? nullptr : p.pool + (size_t)ps * HDD;
+  }
   for (int idx = tid; idx < BV * D; idx += NT) {
     const int r = idx / D, c = idx % D;
     float s;
@@ -93,7 +105,7 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
       const int ar = r0 + r;
       s = (ar >= D && c == ar - D) ? 1.f : 0.f;
     } else {
-      s = p.s0 ? p.s0[(((size_t)item * H + h) * D + r0 + r) * D + c] : 0.f;
+      s = s0src ? s0src[((size_t)h * D + r0 + r) * D + c] : 0.f;
     }
     sS[r * LDK + c] = s;
   }
@@ -186,7 +198,8 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
         float s1 = 0.f, s2 = 0.f;
         for (int c = 0; c < D; ++c) s1 += sQ[i * LDK + c] * sS[r * LDK + c];
         for (int j = 0; j <= i; ++j) s2 += sQK[i * LD6 + j] * sU[j * LDV + r];
-        out[((size_t)(c0 + i) * H + h) * D + r0 + r] = from_f<Tin>(p.scale * (seg[i] * s1 + s2));
+        out[((size_t)(c0 + i) * H + h) * D + r0 + r] =
+            from_f<Tin>(padded ? 0.f : p.scale * (seg[i] * s1 + s2));
       }
       bar();
     }
@@ -201,10 +214,10 @@ __global__ void __launch_bounds__(NT) simt_chain_kernel(const ChainParams p) {
   }
   bar();
   if (MODE == MODE_FWD) {
-    if (p.final_state)
+    if (fdst)
       for (int idx = tid; idx < BV * D; idx += NT) {
         const int r = idx / D, c = idx % D;
-        p.final_state[(((size_t)item * H + h) * D + r0 + r) * D + c] = sS[r * LDK + c];
+        fdst[((size_t)h * D + r0 + r) * D + c] = sS[r * LDK + c];
       }
   } else if (MODE == MODE_SUMMARY) {
     const float nan = __int_as_float(0x7fc00000);

@@ -33,6 +33,13 @@ struct ChainParams {
   float* dbeta;
   float* ds0;             // [N,H,V,K] or NULL
   float* fac;             // [slots,H] per-chunk backward factors (BF16 backward)
+  // paged state cache (forward): sequence n starts from pool[state_idx[n]] (zeros when
+  // has_init[n] == 0) and leaves its final state there; state_idx[n] <= 0 marks padding:
+  // zero output, the pool untouched.  p.s0 / p.final_state are then unused.
+  float* pool;            // [num_slots,H,V,K] or NULL
+  const int32_t* state_idx;
+  const uint8_t* has_init;  // or NULL (every slot is loaded)
+  int num_slots;          // slot indices >= num_slots are treated as padding as well
   int dqk_f32;            // backward: dq, dk are FP32 [B,T,H,K] per value head (grouped
                           // heads, summed into the caller's tensors afterwards)
   int B, T, H, N;

@@ -118,6 +118,30 @@ sf_status sf_gdn_chunk_fwd(const sf_gdn_shape *shape, const void *q, const void 
                            void *workspace, size_t ws_bytes, sf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Paged-cache prefill (Attention Gym "Linear Attention", paged_chunk_gdn): the
+ * forward, advancing a pool of recurrent states in place.
+ *   state_cache    [num_slots,H,V,K] FP32, read and written in place
+ *   state_indices  int32 [N] device: sequence n starts from slot
+ *                  state_indices[n] and leaves its final state there.  Indices
+ *                  must be unique among the positive ones (caller's
+ *                  responsibility); an index <= 0 (or >= num_slots) marks
+ *                  padding: zero output rows, the cache untouched.
+ *   has_initial_state  uint8 [N] device or NULL (all 1): 0 starts the
+ *                  sequence from zero without reading the slot, and the slot
+ *                  is overwritten (also for an empty sequence)
+ *   out            [B,T,H,V]; rows past cu_seqlens[N] untouched
+ * Shapes, dtypes, workspace (sf_gdn_fwd_workspace) and errors as
+ * sf_gdn_chunk_fwd, whose initial/final state arguments the cache replaces.
+ * ---------------------------------------------------------------------- */
+sf_status sf_gdn_paged_chunk_fwd(const sf_gdn_shape *shape, const void *q, const void *k,
+                                 const void *v, const float *gate, const float *beta,
+                                 float *state_cache, int num_slots,
+                                 const int32_t *state_indices,
+                                 const uint8_t *has_initial_state,
+                                 const int32_t *cu_seqlens, void *out, void *workspace,
+                                 size_t ws_bytes, sf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Segment summary.  Attention Gym "Linear Attention", section "Context
  * Parallelism": every token step is affine in the V-major state, so a token
  * range maps its entry state to S_out = S_in @ P + S_ext; Megatron-LM PR
