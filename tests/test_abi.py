@@ -133,3 +133,18 @@ def test_reverse_maps_reject_bad_arguments(lib):
     assert lib.sf_state_scan_reverse(2, 1, 128, 64, FAKE, FAKE, None, FAKE, None, None) == 2
     assert lib.sf_state_scan_reverse(-1, 1, 128, 128, FAKE, FAKE, None, FAKE, None, None) == 1
     assert lib.sf_state_scan_reverse(2, 1, 128, 128, None, FAKE, None, FAKE, None, None) == 1
+
+
+def test_paged_forward_rejects_bad_arguments(lib):
+    """The paged forward wants a cache, slot indices, num_slots >= 1 and an aligned cache;
+    otherwise it checks exactly what the plain forward checks."""
+    s = _shape(T=64, N=1)
+    def call(cache=FAKE, nslots=4, idx=FAKE, ws=4 << 20, shape=s):
+        return lib.sf_gdn_paged_chunk_fwd(ctypes.byref(shape), FAKE, FAKE, FAKE, FAKE, FAKE, cache,
+                                          nslots, idx, None, None, FAKE, FAKE, ws, None)
+    assert call(cache=None) == 1
+    assert call(idx=None) == 1
+    assert call(nslots=0) == 1
+    assert call(cache=ctypes.c_void_p((1 << 20) + 4)) == 1    # misaligned cache
+    assert call(ws=8) == 3
+    assert call(shape=_shape(K=96, V=96)) == 2
