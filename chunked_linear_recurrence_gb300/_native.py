@@ -128,6 +128,39 @@ def make_shape(q, v, cu_seqlens=None, scale=None) -> sf_gdn_shape:
                         float(scale) if scale is not None else 0.0, HK)
 
 
+def _validate(q, v, k=None, gate=None, beta=None, cu_seqlens=None, tensors=(), states=()):
+    """The tensor shapes and dtypes that the C ABI takes on trust from the shape struct:
+    q, k [B,T,HK,K] of one dtype, v [B,T,H,V] in q's dtype, gate and beta [B,T,H],
+    cu_seqlens int32 [N+1] (then B == 1), `tensors` (name, tensor, shape, dtype) entries
+    (None tensors are skipped), `states` (name, tensor) pairs [N,H,V,K].  Raises
+    ValueError before anything reaches the library (a mismatch there would be read or
+    written past its end)."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k and v must be 4-D: [B,T,HK,K] and [B,T,H,V]")
+    B, T, HK, K = q.shape
+    H, V = v.shape[2], v.shape[3]
+    if tuple(v.shape[:2]) != (B, T):
+        raise ValueError(f"v {tuple(v.shape)} does not match q {tuple(q.shape)} in [B,T]")
+    if v.dtype != q.dtype:
+        raise ValueError("q, k and v must share one dtype")
+    if k is not None and (k.shape != q.shape or k.dtype != q.dtype):
+        raise ValueError(f"k {tuple(k.shape)} must match q {tuple(q.shape)} in shape and dtype")
+    for name, t in (("gate", gate), ("beta", beta)):
+        if t is not None and tuple(t.shape) != (B, T, H):
+            raise ValueError(f"{name} must be [B,T,H] = {(B, T, H)}, got {tuple(t.shape)}")
+    N = B
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or cu_seqlens.dtype != torch.int32:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor")
+        N = cu_seqlens.numel() - 1
+    for name, t, shp, dt in tensors:
+        if t is not None and (tuple(t.shape) != tuple(shp) or t.dtype != dt):
+            raise ValueError(f"{name} must be {tuple(shp)} {dt}, got {tuple(t.shape)} {t.dtype}")
+    for name, t in states:
+        if t is not None and tuple(t.shape) != (N, H, V, K):
+            raise ValueError(f"{name} must be [N,H,V,K] = {(N, H, V, K)}, got {tuple(t.shape)}")
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     """Zero-initialised byte buffer (the status word must start at zero)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
@@ -145,6 +178,9 @@ def sf_gdn_chunk_fwd(q, k, v, gate, beta, initial_state=None, cu_seqlens=None, s
                      output_final_state=False, out=None, final_state=None, ws=None, stream=None):
     """chunk_gdn forward.  Returns (out [B,T,H,V], final_state [N,H,V,K] or None)."""
     lib = load()
+    _validate(q, v, k, gate, beta, cu_seqlens,
+              tensors=[("out", out, v.shape, q.dtype)],
+              states=[("initial_state", initial_state), ("final_state", final_state)])
     shape = make_shape(q, v, cu_seqlens, scale)
     if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
         raise ValueError("cu_seqlens must be int32")
@@ -170,6 +206,11 @@ def sf_gdn_paged_chunk_fwd(q, k, v, gate, beta, state_cache, state_indices, cu_s
     slots state_indices (int32 [N]; <= 0: padding, zero output); has_initial_state (bool
     [N]) False starts from zero.  Returns out [B,T,H,V]."""
     lib = load()
+    _validate(q, v, k, gate, beta, cu_seqlens,
+              tensors=[("out", out, v.shape, q.dtype)])
+    if state_cache.dim() != 4 or tuple(state_cache.shape[1:]) != (v.shape[2], v.shape[3],
+                                                                   q.shape[3]):
+        raise ValueError("state_cache must be [num_slots,H,V,K]")
     shape = make_shape(q, v, cu_seqlens, scale)
     if state_indices.dtype != torch.int32 or state_indices.numel() != shape.N:
         raise ValueError("state_indices must be int32 [N]")
@@ -192,6 +233,9 @@ def sf_gdn_paged_chunk_fwd(q, k, v, gate, beta, state_cache, state_indices, cu_s
 def sf_gdn_segment_summary(k, v, gate, beta, bounds, P=None, S_ext=None, ws=None, stream=None):
     """Affine map of each token range: returns (P [R,H,K,K], S_ext [R,H,V,K])."""
     lib = load()
+    _validate(k, v, None, gate, beta)
+    if bounds.dim() != 2 or bounds.shape[1] != 2:
+        raise ValueError("bounds must be int32 [R,2]")
     shape = make_shape(k, v)
     R = bounds.shape[0]
     if bounds.dtype != torch.int32:
@@ -230,6 +274,7 @@ def sf_gdn_segment_reverse_summary(q, k, gate, beta, d_out, seg_offsets, scale=N
     token stream (B = 1): returns C [R,H,V,K], the cotangent each segment's own output
     gradients leave at its start (dS_entry = dS_exit @ P^T + C)."""
     lib = load()
+    _validate(q, d_out, k, gate, beta, seg_offsets)
     shape = make_shape(q, d_out, seg_offsets, scale)
     if seg_offsets.dtype != torch.int32:
         raise ValueError("seg_offsets must be int32 [R+1]")
@@ -264,11 +309,23 @@ def reverse_summary_workspace_bytes(shape: sf_gdn_shape) -> int:
     return int(load().sf_gdn_reverse_summary_workspace(ctypes.byref(shape)))
 
 
+def _validate_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state, cu_seqlens, grads):
+    g = grads or {}
+    _validate(q, v, k, gate, beta, cu_seqlens,
+              tensors=[("d_out", d_out, v.shape, v.dtype), ("dq", g.get("dq"), q.shape, q.dtype),
+                       ("dk", g.get("dk"), k.shape, k.dtype), ("dv", g.get("dv"), v.shape, v.dtype),
+                       ("dgate", g.get("dgate"), gate.shape, gate.dtype),
+                       ("dbeta", g.get("dbeta"), beta.shape, beta.dtype)],
+              states=[("initial_state", initial_state), ("d_final_state", d_final_state),
+                      ("d_initial_state", g.get("d_initial_state"))])
+
+
 def sf_gdn_chunk_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state=None,
                      cu_seqlens=None, scale=None, want_d_initial_state=True, grads=None, ws=None,
                      stream=None):
     """Backward of sf_gdn_chunk_fwd.  Returns dict dq, dk, dv, dgate, dbeta, d_initial_state."""
     lib = load()
+    _validate_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state, cu_seqlens, grads)
     shape = make_shape(q, v, cu_seqlens, scale)
     dev = q.device
     if grads is None:
@@ -296,6 +353,7 @@ def sf_gdn_chunk_bwd_noalloc(q, k, v, gate, beta, initial_state, d_out, d_final_
     (for callers that cannot allocate device memory at this point; see
     include/sf_gdn.h for the size limit and the sharing rules)."""
     lib = load()
+    _validate_bwd(q, k, v, gate, beta, initial_state, d_out, d_final_state, cu_seqlens, grads)
     shape = make_shape(q, v, cu_seqlens, scale)
     if grads is None:
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
