@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             list(ex.map(run, jobs))
     if jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-ldl"])   # -ldl: NVTX on older glibc
         os.replace(tmp, LIB)
     return LIB
 

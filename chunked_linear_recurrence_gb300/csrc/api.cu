@@ -1,6 +1,8 @@
 // api.cu -- the C ABI (include/sf_gdn.h): argument checks, workspace layout and
 // kernel dispatch.  No entry point allocates memory or synchronises the host
 // (except the two documented synchronous helpers at the end).
+#include <nvtx3/nvToolsExt.h>
+
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -41,6 +43,15 @@ sf_status sfg::report(sf_status s, const char* fmt, ...) {
 }
 
 namespace {
+
+// An NVTX range around each compute entry point, so that timelines (Nsight Systems, ncu's
+// range filters) show the library's calls; without a tool attached it does nothing.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 
 sf_status cuda_fail(cudaError_t e, const char* where) {
   return fail(SF_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
@@ -149,6 +160,7 @@ sf_status chunk_fwd(const char* fn, const sf_gdn_shape* shape, const void* q, co
                     void* out, float* pool, int num_slots, const int32_t* state_indices,
                     const uint8_t* has_initial_state, void* workspace, size_t ws_bytes,
                     sf_stream_t stream) {
+  const Range range(fn);
   sf_status st = check_shape(shape, cu_seqlens != nullptr, true, fn);
   if (st != SF_OK) return st;
   if (shape->T > 0 && (!q || !k || !v || !gate || !beta || !out))
@@ -220,6 +232,7 @@ sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const
                                  int R, float* P, float* S_ext, void* workspace, size_t ws_bytes,
                                  sf_stream_t stream) {
   const char* fn = "sf_gdn_segment_summary";
+  const Range range(fn);
   sf_status st = check_shape(shape, false, false, fn);
   if (st != SF_OK) return st;
   if (R < 0) return fail(SF_ERR_INVALID_ARG, "%s: R must be >= 0", fn);
@@ -251,6 +264,7 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float* P, const float*
                         const float* S0, float* entry_states, float* final_state,
                         sf_stream_t stream) {
   const char* fn = "sf_state_scan";
+  const Range range(fn);
   if (R < 0 || H < 1) return fail(SF_ERR_INVALID_ARG, "%s: need R>=0 and H>=1", fn);
   if (K != V || (K != 64 && K != 128))
     return fail(SF_ERR_UNSUPPORTED, "%s: K == V in {64, 128} only", fn);
@@ -292,6 +306,7 @@ sf_status sf_gdn_segment_reverse_summary(const sf_gdn_shape* shape, const void* 
                                          const int32_t* seg_offsets, float* C, void* workspace,
                                          size_t ws_bytes, sf_stream_t stream) {
   const char* fn = "sf_gdn_segment_reverse_summary";
+  const Range range(fn);
   sf_status st = check_shape(shape, true, true, fn);
   if (st != SF_OK) return st;
   const bool bf16 = shape->dtype == SF_BF16;
@@ -325,6 +340,7 @@ sf_status sf_state_scan_reverse(int R, int H, int K, int V, const float* P, cons
                                 const float* dS_final, float* exit_cotangents, float* d_initial,
                                 sf_stream_t stream) {
   const char* fn = "sf_state_scan_reverse";
+  const Range range(fn);
   if (R < 0 || H < 1) return fail(SF_ERR_INVALID_ARG, "%s: need R>=0 and H>=1", fn);
   if (K != V || (K != 64 && K != 128))
     return fail(SF_ERR_UNSUPPORTED, "%s: K == V in {64, 128} only", fn);
@@ -344,6 +360,7 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
                            float* d_initial_state, void* workspace, size_t ws_bytes,
                            sf_stream_t stream) {
   const char* fn = "sf_gdn_chunk_bwd";
+  const Range range(fn);
   const bool packed = cu_seqlens != nullptr;
   sf_status st = check_shape(shape, packed, true, fn);
   if (st != SF_OK) return st;
