@@ -1,7 +1,10 @@
 // api.cu -- the C ABI (include/sf_gdn.h): argument checks, workspace layout and
 // kernel dispatch.  No entry point allocates memory or synchronises the host
 // (except the two documented synchronous helpers at the end).
+#if __has_include(<nvtx3/nvToolsExt.h>)
 #include <nvtx3/nvToolsExt.h>
+#define SF_HAVE_NVTX 1
+#endif
 
 #include <cmath>
 #include <cstdarg>
@@ -46,9 +49,14 @@ namespace {
 
 // An NVTX range around each compute entry point, so that timelines (Nsight Systems, ncu's
 // range filters) show the library's calls; without a tool attached it does nothing.
+// (Without the NVTX headers it compiles to nothing.)
 struct Range {
+#ifdef SF_HAVE_NVTX
   explicit Range(const char* name) { nvtxRangePushA(name); }
   ~Range() { nvtxRangePop(); }
+#else
+  explicit Range(const char*) {}
+#endif
   Range(const Range&) = delete;
   Range& operator=(const Range&) = delete;
 };
