@@ -107,8 +107,9 @@ const char *sf_version(void);
  *   final_state    [N,H,V,K] FP32; required iff output_final_state != 0
  *
  * Returns SF_ERR_INVALID_ARG for NULL/misaligned pointers or inconsistent
- * shapes, SF_ERR_UNSUPPORTED for head sizes other than 64/128, K != V or
- * int32 overflow, SF_ERR_WORKSPACE when ws_bytes < sf_gdn_fwd_workspace().
+ * shapes (HK not dividing H among them), SF_ERR_UNSUPPORTED for head sizes
+ * other than 64/128, K != V or int32 overflow, SF_ERR_WORKSPACE when
+ * ws_bytes < sf_gdn_fwd_workspace().
  * ---------------------------------------------------------------------- */
 size_t sf_gdn_fwd_workspace(const sf_gdn_shape *shape);
 sf_status sf_gdn_chunk_fwd(const sf_gdn_shape *shape, const void *q, const void *k,
