@@ -1,0 +1,71 @@
+"""FP64 NumPy statement of the chunk-parallel form of Kimi Delta Attention (KDA).
+
+Test-only design aid (never imported by the library), the KDA counterpart of
+chunk_form.py: it writes out per 64-token chunk the algebra a chunked KDA kernel would
+implement, so that the algebra is checked against the token-by-token oracle
+(oracle/kda.py) before any kernel exists.  The pages give the per-token rule only; the
+derivation is this library's reading of it.
+
+Within a chunk with entry state S [V,K] and per-channel cumulative gates
+gamma_i = sum_{m<=i} g_m (vectors over K), write the state in decay-normalised
+coordinates S~_i = S_i diag(e^{-gamma_i}).  The token rule then becomes an ungated delta
+rule that reads with K o e^{gamma} and writes with K o e^{-gamma}, which gives (all
+exponents below are gamma_i - gamma_j <= 0 for j <= i, since gates are non-positive):
+
+    Akk_ij = sum_c k_i[c] k_j[c] e^{gamma_i[c] - gamma_j[c]}      (j < i)
+    Aqk_ij = sum_c q_i[c] k_j[c] e^{gamma_i[c] - gamma_j[c]}      (j <= i)
+    T      = (I + diag(beta) Akk)^{-1}
+    U      = T diag(beta) V,       W = T diag(beta) (K o e^{gamma})
+    Delta  = U - W S^T
+    O      = scale ((Q o e^{gamma}) S^T + Aqk Delta)
+    S_next = S diag(e^{gamma_C}) + Delta^T (K o e^{gamma_C - gamma})
+
+and the chunk's affine map S_next = S P_c + E_c:
+
+    P_c = diag(e^{gamma_C}) - W^T (K o e^{gamma_C - gamma}),   E_c = U^T (K o e^{gamma_C - gamma}).
+"""
+import numpy as np
+
+CHUNK = 64
+
+
+def chunk_terms(q, k, v, g, beta):
+    """Per-chunk factors for one (sequence, head): q, k, g [L,K], v [L,V], beta [L]."""
+    L = k.shape[0]
+    gam = np.cumsum(g, axis=0)                                       # [L, K]
+    diff = np.minimum(gam[:, None, :] - gam[None, :, :], 0.0)        # [L, L, K], <= 0
+    E = np.exp(diff)
+    Akk = np.tril(np.einsum("ic,jc,ijc->ij", k, k, E), -1)
+    Aqk = np.tril(np.einsum("ic,jc,ijc->ij", q, k, E))
+    T = np.linalg.inv(np.eye(L) + beta[:, None] * Akk)
+    U = T @ (beta[:, None] * v)
+    W = T @ (beta[:, None] * (k * np.exp(gam)))
+    kdec = k * np.exp(gam[-1][None, :] - gam)                        # K o e^{gamma_C - gamma}
+    return gam, Aqk, U, W, kdec
+
+
+def fwd_seq(q, k, v, g, beta, S, scale, C=CHUNK):
+    """Chunked forward of one sequence/head.  Returns (out [L,V], S_final)."""
+    L = q.shape[0]
+    out = np.zeros((L, v.shape[1]))
+    for c0 in range(0, L, C):
+        sl = slice(c0, min(c0 + C, L))
+        gam, Aqk, U, W, kdec = chunk_terms(q[sl], k[sl], v[sl], g[sl], beta[sl])
+        Delta = U - W @ S.T
+        out[sl] = scale * ((q[sl] * np.exp(gam)) @ S.T + Aqk @ Delta)
+        S = S * np.exp(gam[-1])[None, :] + Delta.T @ kdec
+    return out, S
+
+
+def summary_seq(q, k, v, g, beta, C=CHUNK):
+    """Chunk-composed affine map (P [K,K], E [V,K]) of one token range."""
+    Kd = k.shape[1]
+    P = np.eye(Kd)
+    E = np.zeros((v.shape[1], Kd))
+    for c0 in range(0, k.shape[0], C):
+        sl = slice(c0, min(c0 + C, k.shape[0]))
+        gam, _, U, W, kdec = chunk_terms(q[sl], k[sl], v[sl], g[sl], beta[sl])
+        Pc = np.diag(np.exp(gam[-1])) - W.T @ kdec
+        Ec = U.T @ kdec
+        P, E = P @ Pc, E @ Pc + Ec
+    return P, E

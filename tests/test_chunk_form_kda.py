@@ -1,0 +1,43 @@
+"""The KDA chunk-form algebra (chunk_form_kda.py) equals the token-by-token KDA oracle:
+forward over several chunks with a ragged tail, and the chunk-composed affine map equals
+the probing construction (run from S0 = I without values, and from S0 = 0)."""
+import numpy as np
+
+import chunk_form_kda as cf
+from oracle import kda
+
+
+def _inputs(T, K, V, rng):
+    q = rng.normal(size=(T, K))
+    k = rng.normal(size=(T, K))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.normal(size=(T, V))
+    g = -np.log1p(np.exp(rng.normal(size=(T, K)))) * 0.3
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(size=T)))
+    return q, k, v, g, beta
+
+
+def test_chunk_form_forward_equals_oracle():
+    rng = np.random.default_rng(51)
+    T, K, V = 150, 8, 6                      # three chunks, the last one partial
+    q, k, v, g, beta = _inputs(T, K, V, rng)
+    S0 = rng.normal(size=(V, K)) * 0.3
+    out, S = cf.fwd_seq(q, k, v, g, beta, S0.copy(), 1.0 / np.sqrt(K))
+    ref_out, ref_fin = kda.kda_fwd(q[None, :, None], k[None, :, None], v[None, :, None],
+                                   g[None, :, None], beta[None, :, None], S0[None, None])
+    assert np.allclose(out, ref_out[0, :, 0], rtol=1e-10, atol=1e-12)
+    assert np.allclose(S, ref_fin[0, 0], rtol=1e-10, atol=1e-12)
+
+
+def test_chunk_form_summary_equals_probing():
+    rng = np.random.default_rng(52)
+    T, K, V = 130, 6, 5
+    q, k, v, g, beta = _inputs(T, K, V, rng)
+    P, E = cf.summary_seq(q, k, v, g, beta)
+    _, fP = kda.kda_fwd(q[None, :, None], k[None, :, None], np.zeros((1, T, 1, K)),
+                        g[None, :, None], beta[None, :, None], np.eye(K)[None, None])
+    _, fE = kda.kda_fwd(q[None, :, None], k[None, :, None], v[None, :, None],
+                        g[None, :, None], beta[None, :, None], None)
+    assert np.allclose(P, fP[0, 0], rtol=1e-10, atol=1e-12)
+    assert np.allclose(E, fE[0, 0], rtol=1e-10, atol=1e-12)
