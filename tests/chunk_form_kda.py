@@ -69,3 +69,85 @@ def summary_seq(q, k, v, g, beta, C=CHUNK):
         Ec = U.T @ kdec
         P, E = P @ Pc, E @ Pc + Ec
     return P, E
+
+
+def bwd_chunk(q, k, v, g, beta, S, dO, dSn, scale):
+    """Chunk-form backward of one chunk (L <= 64 rows) from its entry state S and the
+    cotangent dSn of its exit state.  Returns (dq, dk, dv, dg [L,K], dbeta, dS_entry).
+
+    The chunk algebra above, with read keys Kh = K o e^{gamma}, Qh = Q o e^{gamma}, write
+    keys Kv = K o e^{-gamma} (Akk = tril(Kh Kv^T, -1), Aqk = tril(Qh Kv^T)) and end keys
+    Kt = K o e^{gamma_C - gamma}, differentiated term by term; the gate gradient is the
+    per-channel reverse cumulative sum of dgamma.  FP64 design aid: e^{-gamma} is formed
+    directly, so keep gates moderate."""
+    L, Kd = k.shape
+    gam = np.cumsum(g, axis=0)
+    Eh = np.exp(gam)
+    Ev = np.exp(-gam)
+    EC = np.exp(gam[-1])
+    Kh, Qh, Kv = k * Eh, q * Eh, k * Ev
+    Kt = Kv * EC[None, :]
+    Akk = np.tril(Kh @ Kv.T, -1)
+    A = beta[:, None] * Akk
+    T = np.linalg.inv(np.eye(L) + A)
+    U = T @ (beta[:, None] * v)
+    W = T @ (beta[:, None] * Kh)
+    Delta = U - W @ S.T
+    Aqk = np.tril(Qh @ Kv.T)
+    # S_next = S diag(EC) + Delta^T Kt
+    dS = dSn * EC[None, :]
+    dDelta = Kt @ dSn.T
+    dKt = Delta @ dSn
+    dEC = (dSn * S).sum(axis=0)
+    # O = scale (Qh S^T + Aqk Delta)
+    dQh = scale * dO @ S
+    dS += scale * dO.T @ Qh
+    dAqk = np.tril(scale * dO @ Delta.T)
+    dDelta += scale * Aqk.T @ dO
+    dQh += dAqk @ Kv
+    dKv = dAqk.T @ Qh
+    # Delta = U - W S^T
+    dU = dDelta
+    dW = -dDelta @ S
+    dS += -dDelta.T @ W
+    # U = T diag(beta) V ;  W = T diag(beta) Kh
+    dT = dU @ (beta[:, None] * v).T + dW @ (beta[:, None] * Kh).T
+    TU, TW = T.T @ dU, T.T @ dW
+    dv = beta[:, None] * TU
+    dbeta = (v * TU).sum(axis=1) + (Kh * TW).sum(axis=1)
+    dKh = beta[:, None] * TW
+    # T = (I + A)^{-1};  A = diag(beta) tril(Kh Kv^T, -1)
+    dA = np.tril(-T.T @ dT @ T.T, -1)
+    dbeta += (dA * Akk).sum(axis=1)
+    dM = beta[:, None] * dA
+    dKh += dM @ Kv
+    dKv += dM.T @ Kh
+    # back to Q, K and gamma
+    dq = dQh * Eh
+    dk = dKh * Eh + dKv * Ev + dKt * np.exp(gam[-1][None, :] - gam)
+    dgam = dQh * q * Eh + dKh * k * Eh - dKv * Kv - dKt * Kt
+    dgamC = (dKt * Kt).sum(axis=0) + dEC * EC
+    dgam[-1] += dgamC
+    dg = np.cumsum(dgam[::-1], axis=0)[::-1]
+    return dq, dk, dv, dg, dbeta, dS
+
+
+def bwd_seq(q, k, v, g, beta, S0, dO, dSf, scale, C=CHUNK):
+    """Chunk-form backward of one sequence/head: the forward's chunk-entry states, then the
+    chunks in reverse with the cotangent carried from each chunk's start to the one before."""
+    L = q.shape[0]
+    starts = list(range(0, L, C))
+    entries, S = [], S0
+    for c0 in starts:
+        sl = slice(c0, min(c0 + C, L))
+        entries.append(S)
+        _, S = fwd_seq(q[sl], k[sl], v[sl], g[sl], beta[sl], S, scale, C)
+    grads = [np.zeros_like(x) for x in (q, k, v, g, beta)]
+    dS = dSf
+    for ci in range(len(starts) - 1, -1, -1):
+        sl = slice(starts[ci], min(starts[ci] + C, L))
+        r = bwd_chunk(q[sl], k[sl], v[sl], g[sl], beta[sl], entries[ci], dO[sl], dS, scale)
+        for gr, part in zip(grads, r[:5]):
+            gr[sl] = part
+        dS = r[5]
+    return (*grads, dS)

@@ -41,3 +41,23 @@ def test_chunk_form_summary_equals_probing():
                         g[None, :, None], beta[None, :, None], None)
     assert np.allclose(P, fP[0, 0], rtol=1e-10, atol=1e-12)
     assert np.allclose(E, fE[0, 0], rtol=1e-10, atol=1e-12)
+
+
+def test_chunk_form_backward_equals_oracle():
+    rng = np.random.default_rng(53)
+    T, K, V = 150, 6, 5
+    q, k, v, g, beta = _inputs(T, K, V, rng)
+    g *= 0.5                                     # e^{-gamma} is formed directly here
+    S0 = rng.normal(size=(V, K)) * 0.3
+    dO = rng.normal(size=(T, V))
+    dSf = rng.normal(size=(V, K))
+    scale = 1.0 / np.sqrt(K)
+    dq, dk, dv, dg, dbeta, dS0 = cf.bwd_seq(q, k, v, g, beta, S0, dO, dSf, scale)
+    ref = kda.kda_bwd(q[None, :, None], k[None, :, None], v[None, :, None], g[None, :, None],
+                      beta[None, :, None], S0[None, None], dO[None, :, None], dSf[None, None])
+    for name, got, want in (("dq", dq, ref["dq"][0, :, 0]), ("dk", dk, ref["dk"][0, :, 0]),
+                            ("dv", dv, ref["dv"][0, :, 0]), ("dg", dg, ref["dg"][0, :, 0]),
+                            ("dbeta", dbeta, ref["dbeta"][0, :, 0]),
+                            ("dS0", dS0, ref["d_initial_state"][0, 0])):
+        err = np.abs(got - want).max() / np.abs(want).max()
+        assert err <= 1e-9, (name, err)
