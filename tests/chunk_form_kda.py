@@ -151,3 +151,27 @@ def bwd_seq(q, k, v, g, beta, S0, dO, dSf, scale, C=CHUNK):
             gr[sl] = part
         dS = r[5]
     return (*grads, dS)
+
+
+def decay_products_stable(x, k, g, sub=16, dtype=np.float32):
+    """Aq_ij = sum_c x_i[c] k_j[c] e^{gamma_i[c] - gamma_j[c]} for j <= i (x = q or k), in a
+    form whose exponentials stay bounded: the chunk is cut into `sub`-token blocks with the
+    reference point r_I at the start of block I.  For j in an earlier block J,
+    e^{gamma_i - gamma_j} = e^{gamma_i - gamma_rI} e^{gamma_rI - gamma_j}, both exponents <= 0,
+    so block (I, J) is one product of two bounded factors; within a block the per-entry
+    exponentials e^{gamma_i - gamma_j} <= 1 are formed directly.  Computed in `dtype`."""
+    x, k, g = (np.asarray(a, dtype) for a in (x, k, g))
+    L, Kd = k.shape
+    gam = np.cumsum(g, axis=0, dtype=dtype)
+    out = np.zeros((L, L), dtype)
+    for I0 in range(0, L, sub):
+        I = slice(I0, min(I0 + sub, L))
+        ref = gam[I0]
+        xa = x[I] * np.exp(np.minimum(gam[I] - ref, 0))             # rows of block I, <= 1
+        if I0 > 0:
+            J = slice(0, I0)
+            kb = k[J] * np.exp(np.minimum(ref - gam[J], 0))          # earlier columns, <= 1
+            out[I, J] = xa @ kb.T
+        d = np.minimum(gam[I][:, None, :] - gam[I][None, :, :], 0)  # within the block
+        out[I, I] = np.tril(np.einsum("ic,jc,ijc->ij", x[I], k[I], np.exp(d)))
+    return out

@@ -61,3 +61,29 @@ def test_chunk_form_backward_equals_oracle():
                             ("dS0", dS0, ref["d_initial_state"][0, 0])):
         err = np.abs(got - want).max() / np.abs(want).max()
         assert err <= 1e-9, (name, err)
+
+
+def test_stable_decay_products_match_and_survive_extreme_gates():
+    """The sub-blocked form of Aqk / Akk equals the direct one, and with gates at the pages'
+    bound (about -5.9 per token: gamma falls to about -380 over 64 tokens) it stays finite in
+    FP32 where the read/write-key factorisation Kh Kv^T overflows."""
+    rng = np.random.default_rng(54)
+    L, K, V = 64, 8, 4
+    q, k, v, g, beta = _inputs(L, K, V, rng)
+    _, Aqk, _, _, _ = cf.chunk_terms(q, k, v, g, beta)
+    got = cf.decay_products_stable(q, k, g, dtype=np.float64)
+    assert np.allclose(got, Aqk, rtol=1e-12, atol=1e-14)
+    gx = -5.9 * np.ones((L, K))                           # every 16-token sum is -94.4
+    gx[:, ::2] = -5.4                                     # (-86.4 on half the channels)
+    s32 = cf.decay_products_stable(q, k, gx, dtype=np.float32)
+    assert np.isfinite(s32).all()
+    gam = np.cumsum(gx, axis=0)
+    with np.errstate(over="ignore", invalid="ignore"):
+        naive = (q.astype(np.float32) * np.exp(gam).astype(np.float32)) @ \
+                (k.astype(np.float32) * np.exp(-gam).astype(np.float32)).T
+    assert not np.isfinite(naive).all()
+    ref = np.tril(np.einsum("ic,jc,ijc->ij", q, k,
+                            np.exp(np.minimum(gam[:, None, :] - gam[None, :, :], 0))))
+    # error relative to the largest entry (the parity tests' metric): FP32 rounding of the
+    # cumulative gates moves a few tiny cancelling entries by ~1e-4 of themselves only
+    assert np.abs(s32 - ref).max() <= 1e-6 * np.abs(ref).max()
