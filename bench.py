@@ -145,6 +145,83 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's libnvidia-ml,
+    via ctypes) every few milliseconds in a background thread, so that a timed region of
+    a few milliseconds still gets samples.  Read-only: it changes no setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None, index: int, period_s: float = 0.002):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        self.period = period_s
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = 1
+            if uuid:
+                rc = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.ct = nv, h, ctypes
+            self.ok = True
+        except Exception:
+            self.ok = False
+        self.run = False
+
+    def start(self):
+        if not self.ok:
+            return
+        self.run = True
+        self.th = threading.Thread(target=self._loop, daemon=True)
+        self.th.start()
+
+    def _loop(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while self.run:
+            t = time.time()
+            if self.nv.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(mhz)) == 0 and \
+                    self.get_reasons(self.h, ct.byref(rs)) == 0:
+                self.samples.append((t, float(mhz.value), int(rs.value)))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.run = False
+        if self.ok:
+            self.th.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [(m, r) for (t, m, r) in self.samples if t0 <= t <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for (_, r) in inside for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "window": "timed",
+                "source": "nvml"}
+
+
+def device_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
 def dist_init(backend=None):
     """One process per GPU under torchrun (NCCL); gloo when no GPU is visible (the host-side
     rank logic, which CPU tests drive with world size 2)."""
@@ -237,11 +314,32 @@ def run_ours(args):
                             final_state=fin, ws=wsb)
 
     sampler = ClockSampler(local) if rank == 0 else None
+    nvml = NvmlSampler(device_uuid(dev), local) if rank == 0 else None
+    # about a second of the same step before the timed region, so that it starts at the
+    # clocks the GPU holds under this load (these steps are warm-up: not timed)
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    t_load = time.time()
+    n_load = 0
+    while time.time() - t_load < args.load_s:
+        for _ in range(50):
+            fwd()
+        n_load += 50
+        torch.cuda.synchronize()
+    if nvml:
+        nvml.start()
     t0 = time.time()
-    ms = time_loop(fwd, args.steps, args.warmup, ws_n, stream=stream)
+    ms = time_loop(fwd, args.steps, 0, ws_n, stream=stream)
     t1 = time.time()
+    if nvml:
+        nvml.stop()
     _native.sf_workspace_status(wsb)     # raises if a kernel reported a timeout
-    clocks = sampler.summary(t0, t1) if sampler else None
+    clocks = (nvml.summary(t0, t1) if nvml else None) or \
+        (sampler.summary(t0, t1) if sampler else None)
+    if clocks is not None and sampler:
+        smi = sampler.summary(t_load, t1)          # the load phase plus the timed region
+        clocks["nvidia_smi_load_window"] = {k: smi.get(k) for k in ("sm_mhz", "reasons", "samples")}
     if sampler:
         sampler.stop()
     tokens = w1.B * w1.T
@@ -284,6 +382,8 @@ def run_ours(args):
     if not args.fwd_only:
         extra["fwd_bwd"] = bench_fwd_bwd(args, W, dev, ws_n, hbm, peak_src)
         extra["state_passing"] = bench_state_passing(args, W, dev, ws_n, hbm, peak_src)
+        extra["varlen"] = bench_varlen(args, W, dev, ws_n, hbm, peak_src)
+        extra["tiny_f32"] = bench_tiny(args, W, dev, ws_n)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -394,6 +494,66 @@ def bench_state_passing(args, W, dev, ws_n, hbm, peak_src):
                          "frac": bytes_ / (ms * 1e-3) / 1e9 / hbm}}
 
 
+def bench_varlen(args, W, dev, ws_n, hbm, peak_src):
+    """Packed varlen forward: H = 32, 8 sequences (one empty, one ragged) in a
+    T_phys = 65536 stream with an inactive tail; the fraction is on the active tokens."""
+    import torch
+
+    import chunked_linear_recurrence_gb300 as sf
+    from chunked_linear_recurrence_gb300 import _native
+    from chunked_linear_recurrence_gb300.workloads import make_inputs
+
+    w = W["varlen_bf16_h32"]
+    inp = make_inputs(w, dev)
+    cu = inp["cu_seqlens"]
+    out = torch.empty_like(inp["v"])
+    fin = torch.empty(w.N, w.H, w.V, w.K, dtype=torch.float32, device=dev)
+    wsv = _native.workspace(_native.fwd_workspace_bytes(_native.make_shape(inp["q"], inp["v"], cu)),
+                            dev)
+
+    def fwd():
+        sf.sf_gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["gate"], inp["beta"],
+                            inp["initial_state"], cu_seqlens=cu, output_final_state=True,
+                            out=out, final_state=fin, ws=wsv)
+
+    steps = max(3, min(args.steps, 20))
+    ms = time_loop(fwd, steps, args.warmup, ws_n)
+    _native.sf_workspace_status(wsv)
+    tokens = w.tokens
+    bytes_ = tokens * w.H * FWD_BYTES_PER_TH + 2 * w.N * w.H * STATE_BYTES
+    ach = bytes_ / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "lengths": w.lengths, "active_tokens": tokens, "T_phys": w.T,
+            "value": tokens * ws_n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "peak_source": peak_src, "frac": ach / hbm,
+                         "algorithmic_bytes": bytes_}}
+
+
+def bench_tiny(args, W, dev, ws_n):
+    """The small FP32 workload (B=1, T=256, H=2, K=V=64): launch-bound, timed for the
+    record (its roofline time is well under a microsecond)."""
+    import torch
+
+    import chunked_linear_recurrence_gb300 as sf
+    from chunked_linear_recurrence_gb300.workloads import make_inputs
+
+    w = W["tiny_f32"]
+    inp = make_inputs(w, dev)
+    out = torch.empty_like(inp["v"])
+    fin = torch.empty(w.N, w.H, w.V, w.K, dtype=torch.float32, device=dev)
+
+    def fwd():
+        sf.sf_gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["gate"], inp["beta"], None,
+                            output_final_state=True, out=out, final_state=fin)
+
+    steps = max(3, min(args.steps, 20))
+    ms = time_loop(fwd, steps, args.warmup, ws_n)
+    return {"workload": w.name, "tokens_per_step": w.B * w.T, "dtype": "f32",
+            "value": w.B * w.T * ws_n / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "note": "launch-bound (one small kernel launch per step)"}
+
+
 def oracle_baseline(inp, w, target_s=10.0):
     """The FP64 oracle on a bounded sample of the workload: the whole workload
     (every batch row, head and token) repeated until about `target_s` seconds
@@ -468,6 +628,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--fwd-only", action="store_true", help="skip the fwd+bwd and state-passing lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--load-s", type=float, default=1.0,
+                    help="seconds of untimed steps right before the timed region (clock settling)")
     ap.add_argument("--ref-tokens", type=int, default=4096,
                     help="tokens of one batch row the reference arm runs per step")
     args = ap.parse_args(argv)

@@ -7,7 +7,6 @@ library is missing or fails to load, every call raises -- nothing falls back.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -26,8 +25,10 @@ EXPORTS = ("sf_last_error", "sf_version", "sf_gdn_fwd_workspace", "sf_gdn_chunk_
            "sf_gdn_paged_chunk_fwd",
            "sf_gdn_summary_workspace", "sf_gdn_segment_summary", "sf_state_scan",
            "sf_gdn_bwd_workspace", "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc",
+           "sf_gdn_chunk_bwd_noalloc_status",
            "sf_gdn_reverse_summary_workspace", "sf_gdn_segment_reverse_summary",
-           "sf_state_scan_reverse", "sf_validate_cu_seqlens", "sf_workspace_status")
+           "sf_state_scan_reverse", "sf_validate_cu_seqlens", "sf_workspace_status",
+           "sf_testing_inject_timeout")
 
 
 class SfError(RuntimeError):
@@ -81,9 +82,13 @@ def load(path: str = LIB_PATH):
         lib.sf_state_scan_reverse.argtypes = [I, I, I, I, vp, vp, vp, vp, vp, vp]
         lib.sf_validate_cu_seqlens.argtypes = [vp, I, I, vp]
         lib.sf_workspace_status.argtypes = [vp, vp]
+        lib.sf_gdn_chunk_bwd_noalloc_status.argtypes = [vp]
+        lib.sf_testing_inject_timeout.argtypes = [ctypes.c_longlong, ctypes.c_longlong]
         for f in ("sf_gdn_chunk_fwd", "sf_gdn_paged_chunk_fwd", "sf_gdn_segment_summary",
                   "sf_state_scan",
-                  "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc", "sf_validate_cu_seqlens",
+                  "sf_gdn_chunk_bwd", "sf_gdn_chunk_bwd_noalloc",
+                  "sf_gdn_chunk_bwd_noalloc_status", "sf_testing_inject_timeout",
+                  "sf_validate_cu_seqlens",
                   "sf_workspace_status", "sf_gdn_segment_reverse_summary",
                   "sf_state_scan_reverse"):
             getattr(lib, f).restype = st
@@ -375,6 +380,12 @@ def sf_validate_cu_seqlens(cu_seqlens, T, stream=None):
                                       _stream(stream)))
 
 
+def sf_gdn_chunk_bwd_noalloc_status(stream=None):
+    """Reads and clears the status word of sf_gdn_chunk_bwd_noalloc's built-in scratch on
+    the current device; raises SfError (SF_ERR_TIMEOUT) if a kernel reported a timeout."""
+    _check(load().sf_gdn_chunk_bwd_noalloc_status(_stream(stream)))
+
+
 def sf_workspace_status(ws, stream=None):
     _check(load().sf_workspace_status(_ptr(ws), _stream(stream)))
 
@@ -389,7 +400,3 @@ def summary_workspace_bytes(shape: sf_gdn_shape, R: int) -> int:
 
 def bwd_workspace_bytes(shape: sf_gdn_shape) -> int:
     return int(load().sf_gdn_bwd_workspace(ctypes.byref(shape)))
-
-
-def default_scale(K: int) -> float:
-    return 1.0 / math.sqrt(K)

@@ -67,6 +67,12 @@ sf_status cuda_fail(cudaError_t e, const char* where) {
 
 constexpr size_t kStatusBytes = 256;
 
+// BF16 with K = V = 128 runs only on the tensor-core kernels, which need TMA descriptors;
+// without the driver's encoder that request is unsupported (nothing else serves it).
+constexpr const char* kNoTmaEncoder =
+    "BF16 with K = V = 128 needs the tensor-core kernels, but the driver entry point "
+    "cuTensorMapEncodeTiled is unavailable (or disabled by SF_GDN_DISABLE_TMA_ENCODER)";
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Host-visible checks shared by every token-stream entry point.
@@ -187,12 +193,13 @@ sf_status chunk_fwd(const char* fn, const sf_gdn_shape* shape, const void* q, co
   p.has_init = has_initial_state;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   p.HK = eff_hk(shape);
+  if (bf16 && D == 128 && shape->T > 0 && !sfg::tc_fwd_available())
+    return fail(SF_ERR_UNSUPPORTED, "%s: %s", fn, kNoTmaEncoder);
   cudaError_t e;
-  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
+  if (bf16 && D == 128 && shape->T > 0)
     e = sfg::launch_split_fwd(p, workspace, reinterpret_cast<int*>(workspace), cs);
-  } else {
-    e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16, D, shape->N, cs);
-  }
+  else  // (T = 0: no token is read or written, only the states move; any dtype's kernel does)
+    e = sfg::launch_simt_chain(p, sfg::MODE_FWD, bf16 && shape->T > 0, D, shape->N, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return SF_OK;
 }
@@ -259,8 +266,10 @@ sf_status sf_gdn_segment_summary(const sf_gdn_shape* shape, const void* k, const
   p.HK = eff_hk(shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const bool bf16 = shape->dtype == SF_BF16;
+  if (bf16 && shape->K == 128 && !sfg::tc_fwd_available())
+    return fail(SF_ERR_UNSUPPORTED, "%s: %s", fn, kNoTmaEncoder);
   cudaError_t e;
-  if (bf16 && shape->K == 128 && sfg::tc_fwd_available())
+  if (bf16 && shape->K == 128)
     e = sfg::launch_split_summary(p, workspace, reinterpret_cast<int*>(workspace), cs);
   else
     e = sfg::launch_simt_chain(p, sfg::MODE_SUMMARY, bf16, shape->K, R, cs);
@@ -406,13 +415,18 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
     p.dk = gk;
     p.dqk_f32 = 1;
   }
+  if (bf16 && D == 128 && shape->T > 0 && !sfg::tc_fwd_available())
+    return fail(SF_ERR_UNSUPPORTED, "%s: %s", fn, kNoTmaEncoder);
   cudaError_t e;
-  if (bf16 && D == 128 && shape->T > 0 && sfg::tc_fwd_available()) {
+  if (bf16 && D == 128 && shape->T > 0) {
     p.ckpt_tiled = 1;   // the split kernel writes its checkpoints in its threads' order
     e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
                               reinterpret_cast<int*>(workspace), cs);
-  } else
+  } else if (shape->T > 0) {
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
+  } else {
+    e = cudaSuccess;   // no chunk: nothing to replay
+  }
   if (e != cudaSuccess) return cuda_fail(e, fn);
   e = sfg::launch_simt_bwd(p, bf16, D, slots, cs);
   if (e != cudaSuccess) return cuda_fail(e, fn);
@@ -441,6 +455,14 @@ sf_status sf_validate_cu_seqlens(const int32_t* cu_seqlens, int N, int T, sf_str
       return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens decreases at %d (%d -> %d)", fn, i, c[i],
                   c[i + 1]);
   if (c[N] > T) return fail(SF_ERR_INVALID_ARG, "%s: cu_seqlens[N] = %d exceeds T = %d", fn, c[N], T);
+  return SF_OK;
+}
+
+sf_status sf_testing_inject_timeout(long long record, long long wait_limit_cycles) {
+  if (record < 0 || wait_limit_cycles < 1000000)
+    return fail(SF_ERR_INVALID_ARG,
+                "sf_testing_inject_timeout: need record >= 0 and wait_limit_cycles >= 1e6");
+  sfg::inject_split_timeout(record, wait_limit_cycles);
   return SF_OK;
 }
 

@@ -2,15 +2,17 @@
 //
 // sf_gdn_chunk_bwd needs scratch (the chunk-entry state checkpoints and the
 // state-cotangent tape) that the caller allocates.  Some callers cannot
-// allocate at the point where they need gradients: code recording a CUDA
-// graph (a cudaMalloc there is not captured and would have to be redone
-// outside the graph), host runtimes whose allocator is frozen after warm-up,
-// and embedders that own every byte of device memory and have no allocator to
-// hand to a library.  This entry point serves them: its scratch is a fixed
-// array compiled into the library (SF_BWD_NOALLOC_SCRATCH_BYTES on every GPU
-// that loads it, held until the process exits), and it calls no allocating
-// routine of CUDA, of the library or of anyone else.
+// allocate at the point where they need gradients: host runtimes whose
+// allocator is frozen after warm-up (a new device allocation there would be
+// refused or would break their memory accounting), and embedders that own
+// every byte of device memory and have no allocator to hand to a library.
+// This entry point serves them: its scratch is a fixed array compiled into the
+// library (SF_BWD_NOALLOC_SCRATCH_BYTES on every GPU that loads it, held until
+// the process exits), and it calls no allocating routine of CUDA, of the
+// library or of anyone else.
 #include <mutex>
+
+#include <cuda_runtime.h>
 
 #include "../../include/sf_gdn.h"
 #include "api_internal.cuh"
@@ -67,4 +69,22 @@ extern "C" sf_status sf_gdn_chunk_bwd_noalloc(
   return sf_gdn_chunk_bwd(shape, q, k, v, gate, beta, initial_state, cu_seqlens, d_out,
                           d_final_state, dq, dk, dv, dgate, dbeta, d_initial_state, scratch,
                           (size_t)SF_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// The array's first word is the status word of the kernels that ran on it (a bounded wait
+// that ran out writes SF_ERR_TIMEOUT there).  Read it back on `stream` and clear it.
+extern "C" sf_status sf_gdn_chunk_bwd_noalloc_status(sf_stream_t stream) {
+  const char* fn = "sf_gdn_chunk_bwd_noalloc_status";
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess)
+    return sfg::report(SF_ERR_CUDA, "%s: scratch address: %s", fn, cudaGetErrorString(e));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  e = cudaMemcpyAsync(&word, scratch, sizeof(int), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(int), cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return sfg::report(SF_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  if (word != 0) return sfg::report((sf_status)word, "%s: a kernel reported status %d", fn, word);
+  return SF_OK;
 }

@@ -156,7 +156,8 @@ enum {
   C_SSCALED = 10,  // state: TMEM S scaled by e^{gamma_C} of the chunk
   C_ODONE = 11,    // [2] MMA: O of a TMEM buffer complete
   C_OFREE = 13,    // [2] out: O of a TMEM buffer read
-  C_COUNT = 15,
+  C_DRAIN = 15,    // MMA issuer, abort path only: every product it issued has completed
+  C_COUNT = 16,
   // preparation CTA
   P_FULL = 0,      // [2] K and Q tiles landed, diag(e^gamma) written (33 arrivals + tx)
   P_HEAD = 2,      // [2] loader: decay vectors, diag(e^gamma), padding rows zeroed
@@ -171,7 +172,8 @@ enum {
   P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
   P_VECFREE = 22,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
   P_FULLV = 26,    // [2] V tile landed (tx)
-  P_COUNT = 28
+  P_DRAIN = 28,    // [2] MMA issuer, abort path only: every product it issued has completed
+  P_COUNT = 30
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
 
@@ -214,6 +216,8 @@ struct SplitParams {
   int qk_group;              // H / HK
   int nch, nprep;
   float scale;
+  long long wait_limit;      // clock cycles a bounded wait may take before it gives up
+  long long drop_item;       // failure-detection tests only: this record is never published
 };
 
 // Query/key head of value head h (no division in the common case HK = H).
@@ -242,6 +246,14 @@ __device__ __forceinline__ bool chain_span(const SplitParams& p, int x, int64_t&
 // About 2 s at the GB300's clocks.
 constexpr long long kWaitLimitCycles = 4000000000ll;
 
+// Failure-detection tests: the next split launch on this host thread never publishes one
+// record and uses a short wait limit, so that a bounded wait runs out (one shot).
+struct InjectedTimeout {
+  long long item = -1;
+  long long wait_limit = 0;
+};
+thread_local InjectedTimeout g_inject;
+
 struct Ctx {
   volatile int* abort_l;     // CTA-local abort flag (shared memory)
   const SplitParams* p;
@@ -265,7 +277,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*cx.abort_l) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > cx.p->wait_limit) return false;
   }
 }
 
@@ -291,7 +303,7 @@ __device__ __forceinline__ bool poll_ge(const uint32_t* f, uint32_t target, cons
     __nanosleep(32);
     if (ld_acquire_u32(f) >= target) return true;
     if (aborted(cx, n)) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > cx.p->wait_limit) return false;
   }
 }
 
@@ -528,6 +540,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
             mma_commit(&bars[C_ODONE + b]);
           }
           mma_commit(&bars[C_RECFREE + rb]);
+        }
+        if (*cx.abort_l) {
+          // leave no product running into the TMEM that the CTA frees on its way out
+          mma_commit(&bars[C_DRAIN]);
+          mbar_wait(&bars[C_DRAIN], 0, 100000000ull);
         }
       }
       __syncwarp();
@@ -1051,6 +1068,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       };
       int last = -1;                 // last use with a tile copy
       int pj = -1, ps = 0;           // the previous use's record (chain CTA, position)
+      long long pg = -1;             // and its item
       bool ok = true;
       // items are claimed two uses ahead: `cur` is this use's, `nxt` the next one's
       Next cur = fetch(claim());
@@ -1160,7 +1178,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         // record that its own chain is waiting for must never sit behind that check)
         if (pj >= 0) {
           if (!(ok = warp_wait(&bars[P_PUB + pp], (use - 1) & 1, cx))) break;
-          if (lane == 0) st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
+          if (lane == 0 && pg != p.drop_item)
+            st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
           pj = -1;
         }
         if (done) break;
@@ -1178,6 +1197,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         }
         pj = jj;
         ps = s;
+        pg = cur.g;
         cur = nxt;
       }
       // never leave with a tile copy in flight
@@ -1254,6 +1274,11 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             mma_commit(&bars[P_WUDONE + pp]);
             mma_commit(&bars[P_ITEMFREE + pp]);
           }
+        }
+        if (*cx.abort_l) {
+          // leave no product running into the TMEM that the CTA frees on its way out
+          mma_commit(&bars[P_DRAIN + pp]);
+          mbar_wait(&bars[P_DRAIN + pp], 0, 100000000ull);
         }
       }
       __syncwarp();
@@ -1572,6 +1597,13 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   p.lenj = p.sstart + (size_t)NH;
   p.sortj = p.lenj + MAX_NCH;
   p.nprep = nprep;
+  p.wait_limit = kWaitLimitCycles;
+  p.drop_item = -1;
+  if (g_inject.item >= 0) {
+    p.drop_item = g_inject.item;
+    p.wait_limit = g_inject.wait_limit;
+    g_inject = InjectedTimeout{};
+  }
   if (p.cu || p.bounds) {
     split_setup_kernel<<<1, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1585,6 +1617,11 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
 }
 
 }  // namespace
+
+void inject_split_timeout(long long item, long long wait_limit_cycles) {
+  g_inject.item = item;
+  g_inject.wait_limit = wait_limit_cycles;
+}
 
 size_t split_fwd_workspace(int N, int H) { return ws_total(chain_ctas(N, H), N, H); }
 size_t split_summary_workspace(int R, int H) { return ws_total(summary_chain_ctas(R, H), R, H); }

@@ -25,4 +25,9 @@ size_t split_summary_workspace(int R, int H);
 // from S0 = I without it (P).  ws: split_summary_workspace(R, H) bytes, first 256 unused.
 cudaError_t launch_split_summary(const ChainParams& p, void* ws, int* status, cudaStream_t st);
 
+// Failure-detection tests: the next split launch on the calling host thread never publishes
+// record `item` (production order) and gives every bounded wait `wait_limit_cycles` clock
+// cycles, so that a wait runs out and the kernel takes its abort path (one shot).
+void inject_split_timeout(long long item, long long wait_limit_cycles);
+
 }  // namespace sfg

@@ -733,12 +733,10 @@ cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, 
 #define SF_CHAIN(T_, D_, M_)                                                   \
   if (D == D_ && mode == M_) return launch_chain_t<T_, D_, 32, M_>(p, items, st);
   if (bf16) {
+    // (BF16 with K = 128 runs on the tensor-core split kernel only)
     SF_CHAIN(__nv_bfloat16, 64, MODE_FWD)
-    SF_CHAIN(__nv_bfloat16, 128, MODE_FWD)
     SF_CHAIN(__nv_bfloat16, 64, MODE_SUMMARY)
-    SF_CHAIN(__nv_bfloat16, 128, MODE_SUMMARY)
     SF_CHAIN(__nv_bfloat16, 64, MODE_REPLAY)
-    SF_CHAIN(__nv_bfloat16, 128, MODE_REPLAY)
   } else {
     SF_CHAIN(float, 64, MODE_FWD)
     SF_CHAIN(float, 128, MODE_FWD)
@@ -755,11 +753,11 @@ template <typename Tin, int D>
 static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_t st,
                                 bool chain_only) {
   cudaError_t e;
-  if (std::is_same<Tin, __nv_bfloat16>::value) {
+  if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
     // BF16: reverse chain and token gradients on the warp-level tensor cores
     if ((e = launch_mma_bwd_chain(p, p.fac, D, slots, st)) != cudaSuccess) return e;
     return chain_only ? cudaSuccess : launch_mma_bwd_grad(p, true, D, slots, st);
-  }
+  } else {
   // FP32 inputs keep FP32 products on the CUDA cores (1e-4 parity)
   constexpr int BV = 32;
   const size_t smem = sizeof(float) * (3 * 64 * (D + 1) + 2 * 64 * (BV + 1) + BV * (D + 1) +
@@ -776,6 +774,7 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
   if (e != cudaSuccess) return e;
   if (slots > 0) kern2<<<dim3((unsigned)slot_grid(p, slots), p.H), NT, smem2, st>>>(p, slots);
   return cudaGetLastError();
+  }
 }
 
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,

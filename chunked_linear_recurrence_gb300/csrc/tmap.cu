@@ -2,6 +2,7 @@
 // entry point that the runtime hands out (no link-time dependency on libcuda).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "tmap.cuh"
@@ -15,6 +16,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
+    // A host-side switch to report the encoder as absent, so that the status a caller gets
+    // without it (SF_ERR_UNSUPPORTED, nothing launched) can be checked on any machine.
+    const char* off = std::getenv("SF_GDN_DISABLE_TMA_ENCODER");
+    if (off && off[0] && off[0] != '0') return;
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,

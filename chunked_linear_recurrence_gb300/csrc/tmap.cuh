@@ -6,7 +6,8 @@
 namespace sfg {
 
 // True when the driver entry point that encodes TMA descriptors is available (the tensor-core
-// kernels are usable).
+// kernels are usable).  The environment variable SF_GDN_DISABLE_TMA_ENCODER (set to anything
+// but "0" before the first call) makes it report false.
 bool tc_fwd_available();
 // TMA descriptor of a [rows, H, 128] BF16 tensor viewed as (128, H, rows), box 64 x 1 x 64,
 // 128-byte swizzle (one head's 64-token chunk, in two 64-column panels).

@@ -244,9 +244,9 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape *shape, const void *q, const void 
 /* ------------------------------------------------------------------------
  * Backward without a workspace.  The pages have no counterpart of this entry
  * point; it exists for callers that cannot allocate device memory where they
- * need gradients -- code recording a CUDA graph (an allocation is not part of
- * the captured work), host runtimes that freeze their allocator after
- * warm-up, embedders that own all device memory themselves.  Same arguments
+ * need gradients -- host runtimes that freeze their allocator after warm-up
+ * (a late allocation is refused or breaks their accounting), embedders that
+ * own all device memory themselves and hand none to libraries.  Same arguments
  * and results as sf_gdn_chunk_bwd, minus the workspace: the scratch (chunk
  * checkpoints and cotangent tape) is a fixed device array of
  * SF_BWD_NOALLOC_SCRATCH_BYTES built into the library, present on every GPU
@@ -264,6 +264,10 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape *shape, const void *q, const void 
  *  * Every call shares the one array: calls whose work overlaps on the GPU
  *    (other streams, other host threads) race on it.  Nothing in it has to
  *    start at zero; each call writes every scratch value before reading it.
+ *  * The array's first word is the call's device status word (the workspace
+ *    status word of the other entry points): a bounded internal wait that ran
+ *    out leaves SF_ERR_TIMEOUT there.  sf_gdn_chunk_bwd_noalloc_status reads
+ *    it for the current device, clears it and returns it.
  * ---------------------------------------------------------------------- */
 #define SF_BWD_NOALLOC_SCRATCH_BYTES (32ull << 20)
 sf_status sf_gdn_chunk_bwd_noalloc(const sf_gdn_shape *shape, const void *q, const void *k,
@@ -272,6 +276,12 @@ sf_status sf_gdn_chunk_bwd_noalloc(const sf_gdn_shape *shape, const void *q, con
                                    const void *d_out, const float *d_final_state, void *dq,
                                    void *dk, void *dv, float *dgate, float *dbeta,
                                    float *d_initial_state, sf_stream_t stream);
+
+/* Synchronises `stream`, reads the status word of sf_gdn_chunk_bwd_noalloc's
+ * built-in scratch on the current device, clears it and returns it (SF_OK when
+ * no kernel reported a timeout since the last read).  Like the entry point it
+ * allocates nothing; the pages have no counterpart of it either. */
+sf_status sf_gdn_chunk_bwd_noalloc_status(sf_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Helpers (not on the hot path).
@@ -283,6 +293,19 @@ sf_status sf_validate_cu_seqlens(const int32_t *cu_seqlens, int N, int T, sf_str
 /* Synchronises `stream`, reads the workspace status word, clears it and returns
  * it (SF_OK when no kernel reported a timeout). */
 sf_status sf_workspace_status(void *workspace, sf_stream_t stream);
+
+/* Failure-detection testing only (not for production use; the pages have no
+ * counterpart).  The next call on the calling host thread that runs the BF16
+ * K = V = 128 tensor-core kernel (forward, paged forward, segment summary or
+ * the backward's state replay) never publishes the chunk record with index
+ * `record` in the kernel's production order, and every bounded internal wait
+ * of that launch gives up after `wait_limit_cycles` SM clock cycles (>= 1e6)
+ * instead of about 2 s.  The waiting CTA raises the kernel's abort flag, every
+ * CTA leaves after its own copies and products have completed, and the status
+ * word reads SF_ERR_TIMEOUT; the call itself still returns SF_OK (the failure
+ * is on the device).  Later launches are normal.  One shot; returns
+ * SF_ERR_INVALID_ARG for a negative record or a limit below 1e6. */
+sf_status sf_testing_inject_timeout(long long record, long long wait_limit_cycles);
 
 #ifdef __cplusplus
 }

@@ -148,3 +148,43 @@ def test_paged_forward_rejects_bad_arguments(lib):
     assert call(cache=ctypes.c_void_p((1 << 20) + 4)) == 1    # misaligned cache
     assert call(ws=8) == 3
     assert call(shape=_shape(K=96, V=96)) == 2
+
+
+_NO_ENCODER_SCRIPT = r'''
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from chunked_linear_recurrence_gb300 import _native
+lib = _native.load()
+F = ctypes.c_void_p(1 << 20)
+sh = _native.sf_gdn_shape(B=1, T=64, H=1, K=128, V=128, N=1, dtype=1, scale=0.0, HK=0)
+r = []
+ws = lib.sf_gdn_fwd_workspace(ctypes.byref(sh))
+r.append(lib.sf_gdn_chunk_fwd(ctypes.byref(sh), F, F, F, F, F, None, None, 0, F, None, F, ws, None))
+r.append(lib.sf_last_error())
+ws = lib.sf_gdn_summary_workspace(ctypes.byref(sh), 1)
+r.append(lib.sf_gdn_segment_summary(ctypes.byref(sh), F, F, F, F, F, 1, F, F, F, ws, None))
+r.append(lib.sf_last_error())
+ws = lib.sf_gdn_bwd_workspace(ctypes.byref(sh))
+r.append(lib.sf_gdn_chunk_bwd(ctypes.byref(sh), F, F, F, F, F, None, None, F, None, F, F, F, F,
+                              F, None, F, ws, None))
+r.append(lib.sf_last_error())
+print(repr(r))
+'''
+
+
+def test_bf16_128_without_tensor_map_encoder_is_unsupported(lib):
+    """BF16 with K = V = 128 runs only on the tensor-core kernels: with the driver's TMA
+    descriptor encoder reported absent (a host-side switch, set here in a child process),
+    the forward, the summary and the backward return SF_ERR_UNSUPPORTED with a message and
+    launch nothing -- no CUDA-core kernel stands in for them."""
+    import ast
+    import subprocess
+    import sys
+    env = dict(os.environ, SF_GDN_DISABLE_TMA_ENCODER="1")
+    res = subprocess.run([sys.executable, "-c", _NO_ENCODER_SCRIPT, ROOT], env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    r = ast.literal_eval(res.stdout.strip().splitlines()[-1])
+    for status, msg in zip(r[0::2], r[1::2]):
+        assert status == 2, (status, msg)               # SF_ERR_UNSUPPORTED
+        assert b"cuTensorMapEncodeTiled" in msg, msg
