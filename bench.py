@@ -153,7 +153,7 @@ class NvmlSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, uuid: str | None, index: int, period_s: float = 0.002):
+    def __init__(self, uuid: str | None, index: int, period_s: float = 0.0005):
         import ctypes
         self.samples = []
         self.ok = False

@@ -5,9 +5,9 @@
 // two parts with very different shapes:
 //   Pre  (fully parallel over chunks): the decays, [K;Q] K^T, the triangular solve
 //        T = (I + A)^{-1}, and the factors W = T diag(beta e^gamma) K,
-//        U = T diag(beta) V, Qg = diag(e^gamma) Q, Ahat = M o Gamma o Q K^T;
-//   ST + Out (serial along a chain): Delta = U - W S^T, O = Qg S^T + Ahat Delta,
-//        S <- e^{gamma_C} S + Delta^T diag(dec) K.
+//        T' = T diag(beta), Ahat = M o Gamma o Q K^T;
+//   ST + Out (serial along a chain): Delta = U - W S^T with U = T' V,
+//        O = diag(e^gamma) Q S^T + Ahat Delta, S <- e^{gamma_C} S + Delta^T diag(dec) K.
 // One cooperative persistent launch gives each kind its own SMs.  The first `nch`
 // CTAs are state-chain CTAs, each owning a fixed list of (sequence, head) chains and
 // walking their chunks in order; the other CTAs are preparation CTAs that turn
@@ -21,24 +21,27 @@
 // serial chain no longer waits on the preparation of its own chunks.
 //
 // Record of one chunk (BF16 tiles in the 128-byte-swizzled panel layout of tc_ptx.cuh):
-//   WQ   [128 k][128 n]: n < 64: (-W)^T, n >= 64: Qg^T      (B of the merged product)
-//   U^T  [128 v][64 i]                                      (added to -S W^T)
-//   Ahat [64 i][64 j]                                       (B of O += Delta^T Ahat^T)
-//   dec[64] = e^{gamma_C - gamma_j}, e^{gamma_C}            (FP32)
-// Chain products per chunk (all M = 128; S, Delta as BF16 A operands in TMEM):
-//   [-(S W^T) | S Qg^T] = S [(-W)^T | Qg^T]         N = 128, K = 128  (one product)
-//   Delta^T = U^T - S W^T                           (CUDA cores, while O is pending)
-//   S <- e^{gamma_C} S + (Delta^T diag(dec)) K      N = 128, K = 64
-//   O += Delta^T Ahat^T                             N = 64,  K = 64
-//   out[i][v] = scale O[v][i]
-// Preparation products per chunk: KQ = [K;Q] K^T, Qg^T = Q^T diag(e^gamma),
-// (-W)^T = K^T (-T'')^T, U^T = V^T T'^T (all N = 64), T' = T diag(beta),
-// T'' = T diag(beta e^gamma), the 64x64 solve in FP32 with TF32 merges (solve::).
+//   (-W)^T [128 k][64 i]                        (B of D += S (-W)^T)
+//   T'     [64 i][64 j]                         (B of U^T = V^T T'^T)
+//   Ahat   [64 i][64 j]                         (B of O2 = Delta^T Ahat^T)
+//   e^{gamma_C - gamma_j}, e^{gamma_i}, e^{gamma_C}  (FP32)
+// The chain CTA loads the chunk's K, Q and V tiles itself (TMA; the preparation warmed
+// them in L2) and forms the value and query terms on its own tensor pipe, off the serial
+// path.  Chain products per chunk (all M = 128; S, Delta as BF16 A operands in TMEM):
+//   D  = V^T T'^T (= U^T), then D += S (-W)^T    N = 64, K = 64 / 128   -> Delta^T
+//   O1 = S Q^T                                    N = 64, K = 128  (while Delta is formed)
+//   S <- e^{gamma_C} S + (Delta^T diag(dec)) K    N = 128, K = 64
+//   O2 = Delta^T Ahat^T                           N = 64,  K = 64
+//   out[i][v] = scale (e^{gamma_i} O1[v][i] + O2[v][i])
+// Preparation products per chunk: KQ = [K;Q] K^T and (-W)^T = K^T (-T'')^T (N = 64),
+// T' = T diag(beta), T'' = T diag(beta e^gamma), the 64x64 solve in FP32 with TF32 merges
+// (solve::); the K/Q tiles are double-buffered so that the next chunk's KQ runs during
+// the current chunk's solve.
 //
 // Segment summaries (the affine map S_out = S_in P + E of a token range) run on the same
 // kernel: the chain from S0 = 0 with the value term gives E, the chain from S0 = I
 // without it gives P (it multiplies S by e^{gamma_C} I - W^T diag(dec) K per chunk).  Each
-// chunk's record -- (-W)^T, U^T and the decays only -- is prepared once and read by two
+// chunk's record -- (-W)^T, T' and the decays only -- is prepared once and read by two
 // chain CTAs, j for E and nch + j for P; its ring slot is free when both have copied it.
 //
 // Every wait (mbarrier or global flag) is bounded; a CTA that gives up raises a
@@ -63,7 +66,7 @@ using namespace tc;
 constexpr int D = 128;
 constexpr int NTHR = 512;
 constexpr int NSLOT = 8;          // ring slots per chain CTA
-constexpr int NBUF = 3;           // record buffers in a chain CTA's shared memory
+constexpr int NBUF = 2;           // chunk buffers (record + K, Q, V tiles) of a chain CTA
 constexpr int MAX_NCH = 64;       // chain CTAs that own record streams, at most
 // Stream-owning chain CTAs of a segment-summary launch, at most (each with a P twin).  The
 // summary's chains (two per (range, head), about 2 us per chunk step) and its preparation
@@ -76,36 +79,42 @@ static_assert(SF_SUMMARY_CHAINS >= 1 && SF_SUMMARY_CHAINS <= MAX_NCH, "summary c
 constexpr int FLAG_STRIDE = 32;   // words between chain CTAs' flags: one 128-byte line each
 
 // ---- record (global ring slot, and the chain CTA's shared-memory copy) ----
-constexpr uint32_t R_WQ = 0;          // 2 panels x 16 KB
-constexpr uint32_t R_WQ_PANEL = 16384;
-constexpr uint32_t R_U = 32768;       // 16 KB
-constexpr uint32_t R_AH = 49152;      // 8 KB
-constexpr uint32_t R_VEC = 57344;     // dec[64], then e^{gamma_C} at +256
-constexpr uint32_t REC_BYTES = 57856;
+constexpr uint32_t R_W = 0;           // (-W)^T [128 k][64 i], one panel, 16 KB
+constexpr uint32_t R_T1 = 16384;      // T' [64 i][64 j], 8 KB
+constexpr uint32_t R_AH = 24576;      // Ahat [64 i][64 j], 8 KB
+constexpr uint32_t R_VEC = 32768;     // the decay vectors (FP32), at these offsets:
+constexpr uint32_t V_DEC = 0;         //   e^{gamma_C - gamma_j}, j < 64
+constexpr uint32_t V_EG = 256;        //   e^{gamma_i}, i < 64
+constexpr uint32_t V_GC = 512;        //   e^{gamma_C}
+constexpr uint32_t REC_BYTES = 33792;
 constexpr uint32_t REC_PART = REC_BYTES / 4;   // the slot is fetched in 4 bulk copies
-static_assert(REC_PART % 16 == 0, "bulk copy granularity");
+static_assert(REC_PART % 16 == 0 && V_GC + 4 <= REC_BYTES - R_VEC, "record layout");
 
-// ---- chain CTA shared memory: NBUF record buffers, each followed by its K tile ----
-constexpr uint32_t C_K = 58368;       // K tile [64 tok][128 k]: 2 panels x 8 KB
-constexpr uint32_t C_K_PANEL = 8192;
-constexpr uint32_t C_BUF = 74752;     // buffer stride (1024-aligned)
+// ---- chain CTA shared memory: NBUF buffers, each the record then the K, Q, V tiles ----
+constexpr uint32_t C_K = 34816;       // K tile [64 tok][128 k]: 2 panels x 8 KB
+constexpr uint32_t C_Q = 51200;       // Q tile, same layout
+constexpr uint32_t C_V = 67584;       // V tile [64 tok][128 v]
+constexpr uint32_t C_T_PANEL = 8192;
+constexpr uint32_t C_BUF = 83968;     // buffer stride (1024-aligned)
 constexpr uint32_t C_BAR = NBUF * C_BUF;
 static_assert(C_K >= REC_BYTES && C_K % 1024 == 0 && C_BUF % 1024 == 0, "chain smem");
+static_assert(C_Q == C_K + 2 * C_T_PANEL && C_V == C_Q + 2 * C_T_PANEL &&
+              C_BUF == C_V + 2 * C_T_PANEL, "chain tiles");
 
 // ---- preparation CTA shared memory, per pipeline (two pipelines) ----
-constexpr uint32_t P_KQ = 0;          // [K;Q]: 2 panels x 16 KB (rows 0-63 K, 64-127 Q)
-constexpr uint32_t P_KQ_PANEL = 16384;
-constexpr uint32_t P_V = 32768;       // V: 2 panels x 8 KB
-constexpr uint32_t P_V_PANEL = 8192;
-constexpr uint32_t P_T1 = 49152;      // T'  [64 i][64 j]
-constexpr uint32_t P_T2 = 57344;      // -T'' [64 i][64 j]
-constexpr uint32_t P_DG = 65536;      // diag(e^gamma) [64][64]
-constexpr uint32_t P_AT = 73728;      // FP32 [64][SOLVE_LD]: A, then T
-constexpr uint32_t P_X = 91136;       // staging of the Ahat rows (2 warps x 4 KB)
-constexpr uint32_t P_VEC = 99840;     // 2 slots x 512 floats (items alternate)
+constexpr uint32_t P_KQ = 0;          // two [K;Q] tile buffers: 2 panels x 16 KB each
+constexpr uint32_t P_KQ_PANEL = 16384;  // (rows 0-63 K, 64-127 Q; pipeline 1: [Q;K])
+constexpr uint32_t P_KQ_BUF = 32768;
+constexpr uint32_t P_T1 = 65536;      // T'  [64 i][64 j]
+constexpr uint32_t P_T2 = 73728;      // -T'' [64 i][64 j]
+constexpr uint32_t P_AT = 81920;      // FP32 [64][SOLVE_LD]: A, then T
+constexpr uint32_t P_X = 99328;       // staging of the Ahat rows (2 warps x 4 KB)
+constexpr uint32_t P_VEC = 107520;    // 2 slots x 512 floats (items alternate)
 constexpr uint32_t P_VEC_SLOT = 2048;
-constexpr uint32_t P_STRIDE = 104448;
+constexpr uint32_t P_STRIDE = 111616;
 constexpr uint32_t P_BAR = 2 * P_STRIDE;
+static_assert(P_T1 == P_KQ + 2 * P_KQ_BUF && P_T2 == P_T1 + 8192 && P_AT == P_T2 + 8192,
+              "prep smem");
 static_assert(P_AT + 64 * SOLVE_LD * 4 <= P_X && P_X + 2 * 4096 <= P_VEC, "prep smem");
 static_assert(P_VEC + 2 * P_VEC_SLOT <= P_STRIDE && P_STRIDE % 1024 == 0, "prep smem");
 static_assert(64 * SOLVE_LD * 4 >= 4 * 4096, "the A/T area doubles as the store staging area");
@@ -132,11 +141,12 @@ constexpr int VEC_BETA = 64, VEC_GAM = 128, VEC_EG = 192, VEC_DEC = 256,
                                 // stream position (ints)
 
 // ---- TMEM columns ----
-// chain: S FP32, S BF16 pairs, Delta^T BF16 pairs, Delta^T diag(dec) BF16 pairs, two
-// buffers of [ -S W^T (64) | O (64) ].
-constexpr uint32_t TM_S = 0, TM_SB = 128, TM_DB = 192, TM_DDB = 224, TM_BUF = 256;
-// preparation, per pipeline p at 256 p: KQ, Qg^T, (-W)^T, U^T
-constexpr uint32_t TP_KQ = 0, TP_QG = 64, TP_WT = 128, TP_UT = 192;
+// chain: S FP32, S BF16 pairs, Delta^T BF16 pairs, Delta^T diag(dec) BF16 pairs, the
+// Delta accumulator (U^T - S W^T), O1 = S Q^T and O2 = Delta^T Ahat^T.
+constexpr uint32_t TM_S = 0, TM_SB = 128, TM_DB = 192, TM_DDB = 224, TM_D = 256,
+                   TM_O1 = 320, TM_O2 = 384;
+// preparation, per pipeline p at 256 p: [K;Q] K^T and (-W)^T
+constexpr uint32_t TP_KQ = 0, TP_WT = 64;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, false, false);   // both K-major
@@ -147,35 +157,36 @@ constexpr uint32_t ID_MG64 = idesc_bf16(128, 64, false, true);   // the same, N 
 // ---- mbarriers ----
 enum {
   // chain CTA
-  C_RECFULL = 0,   // [NBUF] record + K tile landed (tx)
-  C_RECFREE = 3,   // [NBUF] the chunk's last product done (MMA commit) + its output tile out
-  C_MERGED = 6,    // MMA: [-S W^T | S Qg^T] complete
-  C_DREADY = 7,    // state: Delta BF16 operands in TMEM (and K padding zeroed)
-  C_SUDONE = 8,    // MMA: state update complete
+  C_RECFULL = 0,   // [NBUF] the chunk's record and tiles in shared memory (tx, or the
+                   //        loader's arrival once a partial chunk's rows are zeroed)
+  C_RECFREE = 2,   // [NBUF] the chunk's last product done (MMA commit) + its output tile out
+  C_LANDED = 4,    // [NBUF] a partial chunk's copies landed (tx)
+  C_MERGED = 6,    // MMA: Delta accumulator U^T - S W^T complete
+  C_DREADY = 7,    // state: Delta BF16 operands in TMEM
+  C_SUDONE = 8,    // MMA: state update complete (and O1 of the chunk)
   C_SREADY = 9,    // state: S BF16 operand in TMEM
   C_SSCALED = 10,  // state: TMEM S scaled by e^{gamma_C} of the chunk
-  C_ODONE = 11,    // [2] MMA: O of a TMEM buffer complete
-  C_OFREE = 13,    // [2] out: O of a TMEM buffer read
-  C_DRAIN = 15,    // MMA issuer, abort path only: every product it issued has completed
-  C_COUNT = 16,
+  C_ODONE = 11,    // MMA: O1 and O2 of the chunk complete
+  C_OFREE = 12,    // out: O1 and O2 read
+  C_DRAIN = 13,    // MMA issuer, abort path only: every product it issued has completed
+  C_COUNT = 14,
   // preparation CTA
-  P_FULL = 0,      // [2] K and Q tiles landed, diag(e^gamma) written (33 arrivals + tx)
-  P_HEAD = 2,      // [2] loader: decay vectors, diag(e^gamma), padding rows zeroed
-  P_KQDONE = 4,    // [2]
-  P_QGDONE = 6,    // [2]
-  P_TT = 8,        // [2] T', -T'' written
-  P_WUDONE = 10,   // [2]
-  P_ITEMFREE = 12, // [2] MMA commit after the item's last product (tiles free)
-  P_TMFREE = 14,   // [2] item finished: TMEM region read out, vector slot free
-  P_PUB = 16,      // [2] item's record landed (one arrival per warp): it may be released
-  P_SLOTOK = 18,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
-  P_KQFREE = 20,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
-  P_VECFREE = 22,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
-  P_FULLV = 26,    // [2] V tile landed (tx)
+  P_FULL = 0,      // [2 pipelines][2 buffers] K and Q tiles landed (tx)
+  P_HEAD = 4,      // [2][2 slots] controller: item slot, decay vectors, padding rows zeroed
+  P_KQDONE = 8,    // [2]
+  P_TT = 10,       // [2] T', -T'' written
+  P_WDONE = 12,    // [2] (-W)^T complete
+  P_ITEMFREE = 14, // [2][2 buffers] the tile buffer's last product, (-W)^T, done
+  P_PUB = 18,      // [2] item's record landed (one arrival per warp): it may be released
+  P_SLOTOK = 20,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
+  P_KQFREE = 22,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
+  P_VECFREE = 24,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
   P_DRAIN = 28,    // [2] MMA issuer, abort path only: every product it issued has completed
   P_COUNT = 30
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
+static_assert(C_RECFREE == C_RECFULL + NBUF && C_LANDED == C_RECFREE + NBUF &&
+              C_MERGED == C_LANDED + NBUF, "chain barriers");
 
 // named barriers
 constexpr int BAR_STATE = 1, BAR_OUT = 2;       // chain: 256, 128 threads
@@ -409,18 +420,27 @@ struct Geo {
 };
 
 // --------------------------------------------------------------------------
-// State-chain CTA.  warp 0: record / K-tile loader; warp 1: MMA issuer; warps 4-11:
-// the state (two warpgroups, one column half each); warps 12-15: output stores.
+// State-chain CTA.  warp 0: record / tile loader; warp 1: MMA issuer; warps 4-11: the
+// state (two warpgroups, one column half each); warps 12-15: output stores.
+// Per chunk the products are issued in this order (all M = 128, v rows):
+//   U^T = V^T T'^T                      into D      (as soon as the chunk has landed)
+//   D  += S (-W)^T                      -> Delta^T  (the critical path: N = 64 only)
+//   O1  = S Q^T                         (while the state warps turn D into Delta)
+//   S   = e^{gamma_C} S + (Delta^T diag(dec)) K
+//   O2  = Delta^T Ahat^T                out = scale (e^{gamma_i} O1 + O2)
 // --------------------------------------------------------------------------
-__device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensorMap* tmO,
-                                          const SplitParams& p,
-                                          const Geo& geo, uint8_t* sm, uint32_t sb,
-                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
+__device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                          const CUtensorMap* tmV, const CUtensorMap* tmO,
+                                          const SplitParams& p, const Geo& geo, uint8_t* sm,
+                                          uint32_t sb, uint64_t* bars, uint32_t tm,
+                                          const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   // segment summaries: chain CTA nch + j is the P twin of chain CTA j (same chains, same
   // records and ring); it reads (-W)^T and the decays only and has no output
   const bool summ = p.twin != 0, ptwin = summ && (int)blockIdx.x >= geo.nch;
+  const bool has_out = !summ && p.out != nullptr;   // the output products and stores
+  const bool need_v = !ptwin;                        // the value term U^T = V^T T'^T
   const int j = ptwin ? (int)blockIdx.x - geo.nch : (int)blockIdx.x;   // the stream's owner
   const int cnt = geo.chains_of(j);
   const int len = geo.len_of(j);
@@ -432,53 +452,91 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
     reg_dealloc<RC_CTL>();
     if (warp == 0) {
       // ------------------------------------------------------------ loader
-      if (lane == 0) {
-        // Up to NBUF copies in flight.  A ring slot is handed back (consumed) once its
-        // record has landed in shared memory: at the latest when the buffer is needed
-        // again (then the chunk that used it is done), earlier if the copy is seen landed;
-        // the slots landed by then go back with one release.  The loader's own path per
-        // record is: ready flag, buffer free, proxy fence, copies.
-        int issued = 0, rel = 0;
-        bool ok = true;
-        auto release_to = [&](int n) {
-          fence_proxy_async_global();
-          st_release_u32(consumed_me, (uint32_t)n);
-          rel = n;
-        };
-        int s = 0, t = 0, c = 0, ncx = 0, hk = 0;
-        int64_t bos = 0, eos = 0;
-        for (; s < len; ++s, ++c) {
-          while (c >= ncx) {      // next chain with chunks (and its query/key head)
-            const int x = j + geo.nch * (t++);
-            geo.span(x, bos, eos);
-            ncx = (int)n_chunks(eos - bos);
-            hk = qk_of(p, x % H);
-            c = 0;
-          }
-          const int b = s % NBUF;
-          if (!(ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx))) break;
-          if (s >= NBUF && !(ok = wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx))) break;
+      // Up to NBUF chunks in flight.  A ring slot is handed back (consumed) once its
+      // record has landed in shared memory: at the latest when the buffer is needed
+      // again (then the chunk that used it is done), earlier if the copy is seen landed;
+      // the slots landed by then go back with one release.  A chunk cut short by its
+      // sequence end lands on its own barrier first: the warp zeroes its K and V rows
+      // past the end (so that they add nothing to U or the state update, whatever the
+      // rows beyond the sequence hold) and only then marks the buffer full.
+      int issued = 0, rel = 0;
+      bool ok = true;
+      uint32_t landed_uses = 0;          // bit b: parity of buffer b's next LANDED phase
+      uint32_t part_of = 0;              // bit b: buffer b holds a partial chunk
+      auto release_to = [&](int n) {
+        fence_proxy_async_global();
+        st_release_u32(consumed_me, (uint32_t)n);
+        rel = n;
+      };
+      const uint32_t rec_tx = summ ? (ptwin ? 16384u : 24576u) + (REC_BYTES - R_VEC) : REC_BYTES;
+      const uint32_t tx = rec_tx + 2 * C_T_PANEL * (1u + (need_v ? 1u : 0u) + (has_out ? 1u : 0u));
+      int s = 0, t = 0, c = 0, ncx = 0, hk = 0, h = 0;
+      int64_t bos = 0, eos = 0;
+      for (; s < len; ++s, ++c) {
+        while (c >= ncx) {      // next chain with chunks (and its query/key head)
+          const int x = j + geo.nch * (t++);
+          geo.span(x, bos, eos);
+          ncx = (int)n_chunks(eos - bos);
+          h = x % H;
+          hk = qk_of(p, h);
+          c = 0;
+        }
+        const int b = s % NBUF;
+        const int row0 = (int)(bos + (int64_t)c * CHUNK);
+        const int64_t rem = eos - (bos + (int64_t)c * CHUNK);
+        const int L = rem < CHUNK ? (int)rem : CHUNK;
+        if (lane == 0) {
+          ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx) &&
+               (s < NBUF || wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx));
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) break;
+        const bool part = L < CHUNK;
+        part_of = (part_of & ~(1u << b)) | ((part ? 1u : 0u) << b);
+        uint64_t* txbar = part ? &bars[C_LANDED + b] : &bars[C_RECFULL + b];
+        uint8_t* buf = sm + b * C_BUF;
+        if (lane == 0) {
           // the producer's plain stores before its release, then our bulk reads
           fence_proxy_async_global();
-          uint8_t* buf = sm + b * C_BUF;
-          const int row0 = (int)(bos + (int64_t)c * CHUNK);
           const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
+          mbar_arrive_expect_tx(txbar, tx);
           if (!summ) {
-            mbar_arrive_expect_tx(&bars[C_RECFULL + b], REC_BYTES + 2 * C_K_PANEL);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-              bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, &bars[C_RECFULL + b]);
+              bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, txbar);
           } else {
-            // (-W)^T, U^T (not for the P twin) and the decays
-            mbar_arrive_expect_tx(&bars[C_RECFULL + b], (ptwin ? 16384 : 32768) + (REC_BYTES - R_VEC) +
-                                                            2 * C_K_PANEL);
-            bulk_g2s(buf + R_WQ, src + R_WQ, R_WQ_PANEL, &bars[C_RECFULL + b]);
-            if (!ptwin) bulk_g2s(buf + R_U, src + R_U, R_AH - R_U, &bars[C_RECFULL + b]);
-            bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, &bars[C_RECFULL + b]);
+            // (-W)^T and, for the E chain, T' (contiguous), then the decays
+            bulk_g2s(buf + R_W, src + R_W, ptwin ? 16384u : 24576u, txbar);
+            bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, txbar);
           }
-          tma_load_3d(buf + C_K, tmK, &bars[C_RECFULL + b], 0, hk, row0);
-          tma_load_3d(buf + C_K + C_K_PANEL, tmK, &bars[C_RECFULL + b], 64, hk, row0);
-          issued = s + 1;
+#pragma unroll
+          for (int pnl = 0; pnl < 2; ++pnl) {
+            tma_load_3d(buf + C_K + pnl * C_T_PANEL, tmK, txbar, 64 * pnl, hk, row0);
+            if (has_out) tma_load_3d(buf + C_Q + pnl * C_T_PANEL, tmQ, txbar, 64 * pnl, hk, row0);
+            if (need_v) tma_load_3d(buf + C_V + pnl * C_T_PANEL, tmV, txbar, 64 * pnl, h, row0);
+          }
+        }
+        issued = s + 1;
+        if (part) {
+          const uint32_t ph = (landed_uses >> b) & 1u;
+          landed_uses ^= 1u << b;
+          bool okl = true;
+          if (lane == 0) okl = wait_bar(txbar, ph, cx);
+          if (!(ok = __shfl_sync(0xffffffffu, okl, 0) != 0)) break;
+          // rows L..63 of K and V (two 64-column panels each): zero
+          const int rows = CHUNK - L;
+          const int per = rows * 8;               // 16-byte chunks per panel
+          const int ntile = need_v ? 4 : 2;
+          for (int idx = lane; idx < ntile * per; idx += 32) {
+            const int tile = idx / per, rr = idx % per;
+            uint8_t* base_t = buf + ((tile >> 1) ? C_V : C_K) + (tile & 1) * C_T_PANEL;
+            *reinterpret_cast<uint4*>(base_t + (L + rr / 8) * 128 + (rr % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C_RECFULL + b]);
+        }
+        if (lane == 0) {
           // records up to s - NBUF have landed (their buffers came back); later ones are
           // tested against their buffers' current phases
           int n = rel;
@@ -486,6 +544,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           while (n < s && mbar_test(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1)) ++n;
           if (n > rel) release_to(n);
         }
+      }
+      if (lane == 0) {
         while (ok && rel < len) {
           if (!(ok = wait_bar(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1, cx))) break;
           release_to(rel + 1);
@@ -493,8 +553,13 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         if (!ok) {
           raise_abort(cx);
           // let every copy still in flight land before leaving
-          for (int q = issued > NBUF ? issued - NBUF : 0; q < issued; ++q)
-            mbar_wait(&bars[C_RECFULL + q % NBUF], (q / NBUF) & 1, 100000000ull);
+          for (int q = issued > NBUF ? issued - NBUF : 0; q < issued; ++q) {
+            const int b = q % NBUF;
+            if ((part_of >> b) & 1u)
+              mbar_wait(&bars[C_LANDED + b], ((landed_uses >> b) & 1u) ^ 1u, 100000000ull);
+            else
+              mbar_wait(&bars[C_RECFULL + b], (q / NBUF) & 1, 100000000ull);
+          }
         }
       }
       __syncwarp();
@@ -504,40 +569,69 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       // condition in turn (a suspended wait leaves the issue slots to the other warps).
       if (lane == 0) {
         for (int s = 0; s < len; ++s) {
-          const int b = s & 1, rb = s % NBUF;
+          const int rb = s % NBUF;
           const uint32_t buf = sb + rb * C_BUF;
-          // [-S W^T | S Qg^T] = S [(-W)^T | Qg^T]
-          if (!wait_bar(&bars[C_SREADY], s & 1, cx) ||
-              !wait_bar(&bars[C_RECFULL + rb], (s / NBUF) & 1, cx) ||
-              (!summ && s >= 2 && !wait_bar(&bars[C_OFREE + b], ((s - 2) >> 1) & 1, cx))) {
+          if (!wait_bar(&bars[C_RECFULL + rb], (s / NBUF) & 1, cx)) {
             raise_abort(cx);
             break;
           }
           tc_fence_after();
-          const uint64_t bw = sdesc_sw128(buf + R_WQ, R_WQ_PANEL, 1024);
+          if (need_v) {
+            // U^T = V^T T'^T (the accumulator's previous contents were read before the
+            // previous chunk's DREADY, which this thread waited for)
+            const uint64_t av = sdesc_sw128(buf + C_V, C_T_PANEL, 1024);
+            const uint64_t bt = sdesc_sw128(buf + R_T1, 0, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ta(tm + TM_BUF + 128 * b, tm + TM_SB + kk * 8, bw + (uint64_t)(kk * 2048 >> 4),
-                        summ ? ID_MG64 : ID_MG, kk > 0 ? 1u : 0u);
-          mma_commit(&bars[C_MERGED]);
-          // S <- e^{gamma_C} S + (Delta^T diag(dec)) K, then O += Delta^T Ahat^T
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tm + TM_D, av + (uint64_t)(kk * 2048 >> 4), bt + (uint64_t)(kk * 2), ID_AMN,
+                       kk > 0 ? 1u : 0u);
+          }
+          // Delta^T = U^T - S W^T: the products on the chain's critical path
+          if (!wait_bar(&bars[C_SREADY], s & 1, cx)) {
+            raise_abort(cx);
+            break;
+          }
+          tc_fence_after();
+          {
+            const uint64_t bw = sdesc_sw128(buf + R_W, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ta(tm + TM_D, tm + TM_SB + kk * 8, bw + (uint64_t)(kk * 2048 >> 4), ID_MG64,
+                          (need_v || kk > 0) ? 1u : 0u);
+            mma_commit(&bars[C_MERGED]);
+          }
+          if (has_out) {
+            // O1 = S Q^T, while the state warps form Delta (O1 of the previous chunk read)
+            if (s >= 1 && !wait_bar(&bars[C_OFREE], (s - 1) & 1, cx)) {
+              raise_abort(cx);
+              break;
+            }
+            tc_fence_after();
+            const uint64_t bq = sdesc_sw128(buf + C_Q, 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t o = (uint64_t)(((kk >> 2) * C_T_PANEL + (kk & 3) * 32) >> 4);
+              mma_bf16_ta(tm + TM_O1, tm + TM_SB + kk * 8, bq + o, ID_N64, kk > 0 ? 1u : 0u);
+            }
+          }
+          // S <- e^{gamma_C} S + (Delta^T diag(dec)) K, then O2 = Delta^T Ahat^T
           if (!wait_bar(&bars[C_DREADY], s & 1, cx) || !wait_bar(&bars[C_SSCALED], s & 1, cx)) {
             raise_abort(cx);
             break;
           }
           tc_fence_after();
-          const uint64_t bk = sdesc_sw128(buf + C_K, C_K_PANEL, 1024);
+          const uint64_t bk = sdesc_sw128(buf + C_K, C_T_PANEL, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_MG, 1u);
           mma_commit(&bars[C_SUDONE]);
-          if (!summ) {
+          if (has_out) {
             const uint64_t ba = sdesc_sw128(buf + R_AH, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ta(tm + TM_BUF + 128 * b + 64, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2),
-                          ID_N64, 1u);
-            mma_commit(&bars[C_ODONE + b]);
+              mma_bf16_ta(tm + TM_O2, tm + TM_DB + kk * 8, ba + (uint64_t)(kk * 2), ID_N64,
+                          kk > 0 ? 1u : 0u);
+            mma_commit(&bars[C_ODONE]);
           }
           mma_commit(&bars[C_RECFREE + rb]);
         }
@@ -603,7 +697,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
                             cx)))
         break;
       {
-        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NBUF) * C_BUF + R_VEC + 256);
+        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NBUF) * C_BUF + R_VEC + V_GC);
         float xv[64];
         if (s0p) {
           const float4* src = reinterpret_cast<const float4*>(s0p);
@@ -642,36 +736,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
         }
       }
       for (int c = 0; c < nc && ok; ++c) {
-        const int s = sbase + c, b = s & 1;
+        const int s = sbase + c;
         uint8_t* buf = sm + (s % NBUF) * C_BUF;
-        const int64_t rem = eos - (bos + (int64_t)c * CHUNK);
-        const int L = rem < CHUNK ? (int)rem : CHUNK;
         if (!(ok = group_wait(&bars[C_MERGED], s & 1, BAR_STATE, 256, cx))) break;
         tc_fence_after();
         {
-          // Delta^T = U^T - S W^T for columns [32w, 32w + 32) (the P twin: -S W^T)
+          // Delta^T for columns [32w, 32w + 32): the accumulator holds U^T - S W^T (the P
+          // twin: -S W^T)
           float a[32];
-          tmem_ld32(tl + TM_BUF + 128 * b + 32 * w, a);
-          const uint4* urow = reinterpret_cast<const uint4*>(buf + R_U + v * 128);
-          uint4 uu[4];
-          if (!ptwin) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) uu[e] = urow[(4 * w + e) ^ (v & 7)];
-          }
-          const float* dec = reinterpret_cast<const float*>(buf + R_VEC) + 32 * w;
+          tmem_ld32(tl + TM_D + 32 * w, a);
+          const float* dec = reinterpret_cast<const float*>(buf + R_VEC + V_DEC) + 32 * w;
           tmem_ld_wait();
-          if (!ptwin) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uu[e]);
-#pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[q2]));
-                a[8 * e + 2 * q2] += f.x;
-                a[8 * e + 2 * q2 + 1] += f.y;
-              }
-            }
-          }
           uint32_t d1[16], d2[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -680,16 +755,6 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           }
           tmem_st16(tl + TM_DB + 16 * w, d1);
           tmem_st16(tl + TM_DDB + 16 * w, d2);
-        }
-        if (L < CHUNK) {
-          // K rows past the sequence end: zero, so they add nothing to the state update
-          const int rows = CHUNK - L;
-          for (int idx = st_t; idx < 2 * rows * 8; idx += 256) {
-            const int pnl = idx / (rows * 8), rem = idx % (rows * 8);
-            *reinterpret_cast<uint4*>(buf + C_K + pnl * C_K_PANEL + (L + rem / 8) * 128 +
-                                      (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
         }
         tmem_st_wait();
         tc_fence_before();
@@ -728,7 +793,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
           const int s1 = s + 1;
           if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))
             break;
-          const float gn = *reinterpret_cast<const float*>(sm + (s1 % NBUF) * C_BUF + R_VEC + 256);
+          const float gn = *reinterpret_cast<const float*>(sm + (s1 % NBUF) * C_BUF + R_VEC + V_GC);
 #pragma unroll
           for (int e = 0; e < 64; ++e) xv[e] *= gn;
           tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -749,7 +814,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
     const size_t rs = (size_t)H * D;
     bool ok = true;
     int s = 0;
-    for (int t = 0; t < (summ ? 0 : cnt) && ok; ++t) {
+    for (int t = 0; t < (has_out ? cnt : 0) && ok; ++t) {
       const int x = j + geo.nch * t, h = x % H;
       int64_t bos, eos;
       geo.span(x, bos, eos);
@@ -757,25 +822,38 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
       // paged cache: padding (a slot index outside [1, num_slots)) gives zero output
       const bool padded = p.pool && (p.state_idx[x / H] <= 0 || p.state_idx[x / H] >= p.num_slots);
       for (int c = 0; c < nc; ++c, ++s) {
-        const int b = s & 1;
-        if (!(ok = group_wait(&bars[C_ODONE + b], (s >> 1) & 1, BAR_OUT, 128, cx))) break;
+        if (!(ok = group_wait(&bars[C_ODONE], s & 1, BAR_OUT, 128, cx))) break;
         tc_fence_after();
-        float o[64];
-        tmem_ld64(tl + TM_BUF + 128 * b + 64, o);
+        const int rb = s % NBUF;
+        const float* eg = reinterpret_cast<const float*>(sm + rb * C_BUF + R_VEC + V_EG);
+        const float sc = padded ? 0.f : p.scale;
+        uint32_t ob[32];     // BF16 pairs: out rows 2e and 2e + 1 of this thread's column v
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float a1[32], a2[32];
+          tmem_ld32(tl + TM_O1 + 32 * hh, a1);
+          tmem_ld32(tl + TM_O2 + 32 * hh, a2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 32 * hh + 2 * e;
+            ob[16 * hh + e] = pack_bf16x2(sc * fmaf(eg[i], a1[2 * e], a2[2 * e]),
+                                          sc * fmaf(eg[i + 1], a1[2 * e + 1], a2[2 * e + 1]));
+          }
+        }
+        auto out_at = [&](int i) -> uint16_t { return (uint16_t)(ob[i >> 1] >> (16 * (i & 1))); };
         tc_fence_before();
         named_bar(BAR_OUT, 128);
-        if (v == 0) mbar_arrive(&bars[C_OFREE + b]);
-        const int rb = s % NBUF;
+        if (v == 0) mbar_arrive(&bars[C_OFREE]);
         const int64_t row0 = bos + (int64_t)c * CHUNK;
         const int L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
-        if (p.out && L == CHUNK) {
-          // the record's U^T area (read by the Delta step, long done) stages the [64 token]
-          // [128 v] tile in the panel layout; one TMA store sends it out
-          uint8_t* st = sm + rb * C_BUF + R_U;
+        if (L == CHUNK) {
+          // the record's (-W)^T area (read by the chunk's first product, long done) stages
+          // the [64 token][128 v] tile in the panel layout; one TMA store sends it out
+          uint8_t* st = sm + rb * C_BUF + R_W;
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            *reinterpret_cast<__nv_bfloat16*>(st + sw128_off(i, v, 8192)) =
-                __float2bfloat16_rn(padded ? 0.f : p.scale * o[i]);
+            *reinterpret_cast<uint16_t*>(st + sw128_off(i, v, 8192)) = out_at(i);
           fence_proxy_async_smem();
           named_bar(BAR_OUT, 128);
           if (v == 0) {
@@ -784,12 +862,12 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmK, const CUtensor
             bulk_commit();
             bulk_wait_read_all();   // the buffer may take the next record
           }
-        } else if (p.out) {
+        } else {
           // a chunk cut short by the sequence end: only its own rows are written
-          __nv_bfloat16* orow = p.out + ((size_t)row0 * H + h) * D + v;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.out + ((size_t)row0 * H + h) * D + v);
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (i < L) orow[i * rs] = __float2bfloat16_rn(padded ? 0.f : p.scale * o[i]);
+            if (i < L) orow[i * rs] = out_at(i);
         }
         if (v == 0) mbar_arrive(&bars[C_RECFREE + rb]);
       }
@@ -998,9 +1076,12 @@ __device__ __forceinline__ void lower(const float* AT, uint8_t* t1, uint8_t* t2,
 // Preparation CTA.  Items (chunk records) are claimed one at a time, in stream order,
 // from a grid-wide counter, so that a pipeline waiting for a full ring slot holds up
 // only the chain that slot belongs to.  warps 0 and 2: controllers of pipelines 0 and 1
-// (claim, gate/beta and the chunk's decay vectors, the K/Q/V tiles by TMA, the ring-slot
-// check, the release of the finished record); warps 1 and 3: MMA issuers of pipelines 0
-// and 1; warps 4-7 and 8-11: the two pipelines; warps 12-15 idle.
+// (claim, gate/beta and the chunk's decay vectors, the K/Q tiles by TMA into one of two
+// buffers, the ring-slot check, the release of the finished record); warps 1 and 3: MMA
+// issuers of pipelines 0 and 1; warps 4-7 and 8-11: the two pipelines; warps 12-15 idle.
+// A pipeline's item u: [K;Q] K^T (issued while item u-1 is still in its solve), the
+// decayed A and Ahat, the solve to T' and -T'', (-W)^T = K^T (-T'')^T; the record it
+// writes holds (-W)^T, T', Ahat and the decay vectors.
 // --------------------------------------------------------------------------
 __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                          const CUtensorMap* tmV, const SplitParams& p,
@@ -1008,8 +1089,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
-  // segment summaries: no Q (its map is K's) and no Qg^T or Ahat in the records, whose
-  // ring slots are read by two chain CTAs
+  // segment summaries: no Q (its map is K's) and no Ahat in the records, whose ring slots
+  // are read by two chain CTAs
   const bool summ = p.twin != 0;
   // item g -> (chain CTA, stream position, head, first row, length)
   auto item = [&](long long g, int& jj, int& s, int& h, int& row0, int& L) {
@@ -1034,15 +1115,14 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       uint8_t* base = sm + pp * P_STRIDE;
       // pipeline 0 keeps [K;Q] in its tile rows, pipeline 1 [Q;K] (see the pipelines)
       const uint32_t kq_k = pp ? 8192u : 0u, kq_q = pp ? 0u : 8192u;
-      for (int idx = lane; idx < 512; idx += 32)
-        reinterpret_cast<uint4*>(base + P_DG)[idx] = make_uint4(0, 0, 0, 0);
       auto claim = [&]() -> int {
         int g = 0;
         if (lane == 0) g = (int)atomicAdd(p.next_item, 1u);
         return __shfl_sync(0xffffffffu, g, 0);
       };
       // An item's geometry, its gate/beta values (two tokens per lane, loaded one use
-      // ahead so that their latency overlaps the waits), and its tiles warmed in L2.
+      // ahead so that their latency overlaps the waits), and its tiles warmed in L2 (V
+      // for the chain CTA that will load it).
       struct Next {
         int g, jj, s, h, hk, row0, L;   // hk: the query/key head of value head h
         float g0, g1, b0, b1;
@@ -1077,10 +1157,11 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         const bool done = cur.g >= geo.total;
         const Next nxt = fetch(done ? cur.g : gnn);
         if (!done && nxt.g < geo.total) gnn = claim();
-        const int jj = cur.jj, s = cur.s, h = cur.h, hk = cur.hk, row0 = cur.row0, L = cur.L;
-        // the vector slot is free once the item two uses back has finished (one barrier
-        // per slot, so a phase can never be mistaken for the one two items later)
-        if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + (use & 1)], ((use - 2) >> 1) & 1, cx)))
+        const int jj = cur.jj, s = cur.s, hk = cur.hk, row0 = cur.row0, L = cur.L;
+        const int ub = use & 1;        // vector slot and tile buffer of this use
+        // the slot and the buffer are free once the item two uses back has finished (one
+        // barrier per slot, so a phase can never be mistaken for the one two items later)
+        if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + ub], ((use - 2) >> 1) & 1, cx)))
           break;
         float* vs = vec_of(pp, use);
         if (!done) {
@@ -1129,51 +1210,38 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           vi[2] = s;
         }
         __syncwarp();
-        if (!done && !summ) {
-          // diag(e^gamma), the B operand of Qg^T, once the previous item's Qg^T is done
-          if (use >= 1 && !(ok = warp_wait(&bars[P_QGDONE + pp], (use - 1) & 1, cx))) break;
-          for (int e = lane; e < 64; e += 32)
-            *reinterpret_cast<__nv_bfloat16*>(base + P_DG + sw128_off(e, e, 8192)) =
-                __float2bfloat16_rn(vs[VEC_EG + e]);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        // the pipeline's previous item has had its last product (its tiles are free)
-        if (use >= 1 && !(ok = warp_wait(&bars[P_ITEMFREE + pp], (use - 1) & 1, cx))) break;
         if (!done) {
+          // tile buffer ub: the product that read it last, (-W)^T of item use - 2, is done
+          if (use >= 2 &&
+              !(ok = warp_wait(&bars[P_ITEMFREE + 2 * pp + ub], ((use - 2) >> 1) & 1, cx)))
+            break;
+          uint8_t* kq = base + P_KQ + ub * P_KQ_BUF;
           if (lane == 0) {
-            // K and Q first (the first product needs only them), V on its own barrier
-            mbar_arrive_expect_tx(&bars[P_FULL + pp], 2 * 16384);
+            mbar_arrive_expect_tx(&bars[P_FULL + 2 * pp + ub], 2 * 16384);
 #pragma unroll
             for (int pnl = 0; pnl < 2; ++pnl) {
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + pp], 64 * pnl, hk, row0);
-              tma_load_3d(base + P_KQ + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + pp], 64 * pnl, hk,
+              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
+                          row0);
+              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
                           row0);
             }
-            mbar_arrive_expect_tx(&bars[P_FULLV + pp], 16384);
-#pragma unroll
-            for (int pnl = 0; pnl < 2; ++pnl)
-              tma_load_3d(base + P_V + pnl * P_V_PANEL, tmV, &bars[P_FULLV + pp], 64 * pnl, h, row0);
           }
-          mbar_arrive(&bars[P_FULL + pp]);
           last = use;
           if (L < CHUNK) {
-            // rows past the sequence end: zero K, Q and V so they add nothing to any product
-            if (!(ok = warp_wait(&bars[P_FULL + pp], use & 1, cx) && warp_wait(&bars[P_FULLV + pp], use & 1, cx)))
-              break;
+            // rows past the sequence end: zero K and Q so they add nothing to any product
+            if (!(ok = warp_wait(&bars[P_FULL + 2 * pp + ub], (use >> 1) & 1, cx))) break;
             const int rows = CHUNK - L;
-            for (int idx = lane; idx < 6 * rows * 8; idx += 32) {
-              const int t6 = idx / (rows * 8), rem = idx % (rows * 8);
-              const int row = L + rem / 8, ch = rem % 8, pnl = t6 & 1, which = t6 >> 1;
-              uint8_t* tb = (which == 2) ? base + P_V + pnl * P_V_PANEL
-                                         : base + P_KQ + pnl * P_KQ_PANEL + (which == 1 ? kq_q : kq_k);
+            for (int idx = lane; idx < 4 * rows * 8; idx += 32) {
+              const int t4 = idx / (rows * 8), rem = idx % (rows * 8);
+              const int row = L + rem / 8, ch = rem % 8, pnl = t4 & 1, which = t4 >> 1;
+              uint8_t* tb = kq + pnl * P_KQ_PANEL + (which == 1 ? kq_q : kq_k);
               *reinterpret_cast<uint4*>(tb + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[P_HEAD + pp]);
+        if (lane == 0) mbar_arrive(&bars[P_HEAD + 2 * pp + ub]);
         // release the previous record once written (before this item's slot check: a
         // record that its own chain is waiting for must never sit behind that check)
         if (pj >= 0) {
@@ -1200,37 +1268,37 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         pg = cur.g;
         cur = nxt;
       }
-      // never leave with a tile copy in flight
-      if (last >= 0) {
-        mbar_wait(&bars[P_FULL + pp], last & 1, 100000000ull);
-        mbar_wait(&bars[P_FULLV + pp], last & 1, 100000000ull);
-      }
+      // never leave with a tile copy in flight (the last two uses may each have one)
+      for (int u = last - 1; u <= last; ++u)
+        if (u >= 0) mbar_wait(&bars[P_FULL + 2 * pp + (u & 1)], (u >> 1) & 1, 100000000ull);
       __syncwarp();
     } else {
-      // ------------------------------------------------------------ MMA issuers
+      // ------------------------------------------------------------ MMA issuer
       // warp 1 issues pipeline 0's products, warp 3 pipeline 1's (an issue waits for the
       // tensor pipe, so one thread serving both pipelines would hold each up behind the
-      // other).  Per item, in order: KQ, Qg^T, then (-W)^T and U^T; each waits (suspended)
-      // for exactly what it needs.  A pipeline ends at the use whose item slot says -1.
+      // other).  Iteration u issues item u's [K;Q] K^T -- as soon as the pipeline has
+      // read out item u-1's, i.e. while item u-1 is in its solve -- and then item u-1's
+      // (-W)^T once its T'' is written.  Each waits (suspended) for exactly what it needs.
       const int pp = warp >> 1;
       if (lane == 0) {
         const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
-        const uint32_t kq_k = pp ? 8192u : 0u, kq_q = pp ? 0u : 8192u;
+        const uint32_t kq_k = pp ? 8192u : 0u;
         for (int u = 0;; ++u) {
-          // KQ: the item slot and vectors (HEAD), the K and Q tiles (FULL), the previous
-          // item's KQ accumulator read out (KQFREE)
-          if (!wait_bar(&bars[P_HEAD + pp], u & 1, cx)) { raise_abort(cx); break; }
-          if (reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0) break;
-          if (!wait_bar(&bars[P_FULL + pp], u & 1, cx) ||
-              (u > 0 && !wait_bar(&bars[P_KQFREE + pp], (u - 1) & 1, cx))) {
-            raise_abort(cx);
-            break;
-          }
-          tc_fence_after();
-          {
+          // the item slot and vectors (HEAD), the K and Q tiles (FULL), the previous item's
+          // KQ accumulator read out (KQFREE)
+          if (!wait_bar(&bars[P_HEAD + 2 * pp + (u & 1)], (u >> 1) & 1, cx)) { raise_abort(cx); break; }
+          const bool done = reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0;
+          if (!done) {
+            if (!wait_bar(&bars[P_FULL + 2 * pp + (u & 1)], (u >> 1) & 1, cx) ||
+                (u > 0 && !wait_bar(&bars[P_KQFREE + pp], (u - 1) & 1, cx))) {
+              raise_abort(cx);
+              break;
+            }
+            tc_fence_after();
             // KQ = [K; Q] K^T
-            const uint64_t aq = sdesc_sw128(base + P_KQ, 0, 1024);
-            const uint64_t bk = sdesc_sw128(base + P_KQ + kq_k, 0, 1024);
+            const uint32_t kq = base + P_KQ + (u & 1) * P_KQ_BUF;
+            const uint64_t aq = sdesc_sw128(kq, 0, 1024);
+            const uint64_t bk = sdesc_sw128(kq + kq_k, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t o = (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
@@ -1238,42 +1306,24 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
             }
             mma_commit(&bars[P_KQDONE + pp]);
           }
-          // Qg^T: the previous item's Qg^T accumulator read out (TMFREE)
-          if (u > 0 && !wait_bar(&bars[P_TMFREE + pp], (u - 1) & 1, cx)) { raise_abort(cx); break; }
-          tc_fence_after();
-          if (!summ) {
-            // Qg^T = Q^T diag(e^gamma)
-            const uint64_t aq = sdesc_sw128(base + P_KQ + kq_q, P_KQ_PANEL, 1024);
-            const uint64_t bd = sdesc_sw128(base + P_DG, 0, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tp + TP_QG, aq + (uint64_t)(kk * 2048 >> 4), bd + (uint64_t)(kk * 2), ID_AMN,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(&bars[P_QGDONE + pp]);
-          }
-          // (-W)^T, U^T: T' and -T'' (TT), the V tile (FULLV)
-          if (!wait_bar(&bars[P_TT + pp], u & 1, cx) || !wait_bar(&bars[P_FULLV + pp], u & 1, cx)) {
-            raise_abort(cx);
-            break;
-          }
-          tc_fence_after();
-          {
-            // (-W)^T = K^T (-T'')^T ; U^T = V^T T'^T
-            const uint64_t ak = sdesc_sw128(base + P_KQ + kq_k, P_KQ_PANEL, 1024);
+          if (u > 0) {
+            // (-W)^T = K^T (-T'')^T of item u - 1, once its -T'' is written (TT)
+            if (!wait_bar(&bars[P_TT + pp], (u - 1) & 1, cx)) {
+              raise_abort(cx);
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kq = base + P_KQ + ((u - 1) & 1) * P_KQ_BUF;
+            const uint64_t ak = sdesc_sw128(kq + kq_k, P_KQ_PANEL, 1024);
             const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16(tp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_AMN,
                        kk > 0 ? 1u : 0u);
-            const uint64_t av = sdesc_sw128(base + P_V, P_V_PANEL, 1024);
-            const uint64_t b1 = sdesc_sw128(base + P_T1, 0, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tp + TP_UT, av + (uint64_t)(kk * 2048 >> 4), b1 + (uint64_t)(kk * 2), ID_AMN,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(&bars[P_WUDONE + pp]);
-            mma_commit(&bars[P_ITEMFREE + pp]);
+            mma_commit(&bars[P_WDONE + pp]);
+            mma_commit(&bars[P_ITEMFREE + 2 * pp + ((u - 1) & 1)]);
           }
+          if (done) break;
         }
         if (*cx.abort_l) {
           // leave no product running into the TMEM that the CTA frees on its way out
@@ -1310,7 +1360,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       const float* vs = vec_of(pp, use);
       // the controller's item slot and vectors for this use (HEAD), then the chunk's
       // [K;Q] K^T; meanwhile the previous record's stores land (then it may be released)
-      if (!(ok = group_wait(&bars[P_HEAD + pp], use & 1, bid, 128, cx))) break;
+      if (!(ok = group_wait(&bars[P_HEAD + 2 * pp + (use & 1)], (use >> 1) & 1, bid, 128, cx))) break;
       if (pend) record_landed(lane, &bars[P_PUB + pp]);
       pend = false;
       const int gi = reinterpret_cast<const int*>(vs)[VEC_ITEM];
@@ -1357,7 +1407,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           pack64(x, ah);
         }
       }
-      // this warp's part of the KQ accumulator is read out (four arrivals)
+      // this warp's part of the KQ accumulator is read out (four arrivals): the issuer
+      // may start the next item's [K;Q] K^T
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[P_KQFREE + pp]);
@@ -1384,38 +1435,30 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         solve::lower<1>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
       fence_proxy_async_smem();
       named_bar(bid, 128);
-      if (r == 0) mbar_arrive(&bars[P_TT + pp]);
-      if (!summ) {
-        if (!(ok = group_wait(&bars[P_QGDONE + pp], use & 1, bid, 128, cx))) break;
-        tc_fence_after();
-        float x[64];
-        uint32_t u[32];
-        tmem_ld64(tl + TP_QG, x);
-        pack64(x, u);
-        store_rows(rec + R_WQ + R_WQ_PANEL, stage, (warp & 3) * 32, u, lane);
+      if (r == 0) {
+        mbar_arrive(&bars[P_TT + pp]);
+        // T' goes to the record as it is: the chain CTA's B operand of U^T = V^T T'^T
+        bulk_s2g(rec + R_T1, base + P_T1, 8192);
+        bulk_commit();
       }
-      if (!(ok = group_wait(&bars[P_WUDONE + pp], use & 1, bid, 128, cx))) break;
+      if (!(ok = group_wait(&bars[P_WDONE + pp], use & 1, bid, 128, cx))) break;
       tc_fence_after();
       {
         float x[64];
         uint32_t u[32];
         tmem_ld64(tl + TP_WT, x);
         pack64(x, u);
-        store_rows(rec + R_WQ, stage, (warp & 3) * 32, u, lane);
-        tmem_ld64(tl + TP_UT, x);
-        pack64(x, u);
-        store_rows(rec + R_U, stage, (warp & 3) * 32, u, lane);
+        store_rows(rec + R_W, stage, (warp & 3) * 32, u, lane);
       }
-      if (r < 64) reinterpret_cast<float*>(rec + R_VEC)[r] = vs[VEC_DEC + r];
-      if (r == 0) reinterpret_cast<float*>(rec + R_VEC)[64] = vs[VEC_EG + 63];
-      record_read(lane);     // the A/T and X areas are written again by the next item
+      // the decays e^{gamma_C - gamma_j}, e^{gamma_i} and e^{gamma_C}
+      if (r < 64) reinterpret_cast<float*>(rec + R_VEC + V_DEC)[r] = vs[VEC_DEC + r];
+      else reinterpret_cast<float*>(rec + R_VEC + V_EG)[r - 64] = vs[VEC_EG + r - 64];
+      if (r == 0) reinterpret_cast<float*>(rec + R_VEC + V_GC)[0] = vs[VEC_EG + 63];
+      record_read(lane);     // the A/T and X areas, and T', are written again by the next item
       pend = true;
       tc_fence_before();
       named_bar(bid, 128);
-      if (r == 0) {
-        mbar_arrive(&bars[P_TMFREE + pp]);
-        mbar_arrive(&bars[P_VECFREE + 2 * pp + (use & 1)]);
-      }
+      if (r == 0) mbar_arrive(&bars[P_VECFREE + 2 * pp + (use & 1)]);
     }
     // the last record (and, on the abort path, every bulk store) lands before leaving
     if (pend) record_landed(lane, &bars[P_PUB + pp]);
@@ -1457,11 +1500,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       // a record buffer is free once its chunk's products are done (MMA commit) and its
       // output tile, staged in it, has been read out (output warps)
       // (summaries have no output)
-      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], p.twin ? 1 : 2);
+      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], (p.twin || !p.out) ? 1 : 2);
     } else {
       for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
-      mbar_init(&bars[P_FULL], 33);
-      mbar_init(&bars[P_FULL + 1], 33);
       mbar_init(&bars[P_KQFREE], 4);
       mbar_init(&bars[P_KQFREE + 1], 4);
       mbar_init(&bars[P_PUB], 4);
@@ -1470,11 +1511,9 @@ __global__ void __launch_bounds__(NTHR, 1)
     *abort_l = 0;
     fence_mbar_init();
     prefetch_tmap(&tmK);
+    if (!p.twin) prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmV);
     if (is_chain && p.out) prefetch_tmap(&tmO);
-    if (!is_chain) {
-      if (!p.twin) prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmV);
-    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TM_COLS);
@@ -1491,7 +1530,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   geo.init(p, len_s, sort_s);
 
   if (is_chain)
-    chain_cta(&tmK, &tmO, p, geo, sm, sb, bars, tm, cx);
+    chain_cta(&tmQ, &tmK, &tmV, &tmO, p, geo, sm, sb, bars, tm, cx);
   else
     prep_cta(&tmQ, &tmK, &tmV, p, geo, sm, sb, bars, tm, cx);
 
