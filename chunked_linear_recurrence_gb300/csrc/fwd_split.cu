@@ -87,8 +87,7 @@ constexpr uint32_t V_DEC = 0;         //   e^{gamma_C - gamma_j}, j < 64
 constexpr uint32_t V_EG = 256;        //   e^{gamma_i}, i < 64
 constexpr uint32_t V_GC = 512;        //   e^{gamma_C}
 constexpr uint32_t REC_BYTES = 33792;
-constexpr uint32_t REC_PART = REC_BYTES / 4;   // the slot is fetched in 4 bulk copies
-static_assert(REC_PART % 16 == 0 && V_GC + 4 <= REC_BYTES - R_VEC, "record layout");
+static_assert(REC_BYTES % 16 == 0 && V_GC + 4 <= REC_BYTES - R_VEC, "record layout");
 
 // ---- chain CTA shared memory: NBUF buffers, each the record then the K, Q, V tiles ----
 constexpr uint32_t C_K = 34816;       // K tile [64 tok][128 k]: 2 panels x 8 KB
@@ -96,7 +95,8 @@ constexpr uint32_t C_Q = 51200;       // Q tile, same layout
 constexpr uint32_t C_V = 67584;       // V tile [64 tok][128 v]
 constexpr uint32_t C_T_PANEL = 8192;
 constexpr uint32_t C_BUF = 83968;     // buffer stride (1024-aligned)
-constexpr uint32_t C_BAR = NBUF * C_BUF;
+constexpr uint32_t C_OST = NBUF * C_BUF;   // two staging tiles of the output [64 tok][128 v]
+constexpr uint32_t C_BAR = C_OST + 2 * 16384;
 static_assert(C_K >= REC_BYTES && C_K % 1024 == 0 && C_BUF % 1024 == 0, "chain smem");
 static_assert(C_Q == C_K + 2 * C_T_PANEL && C_V == C_Q + 2 * C_T_PANEL &&
               C_BUF == C_V + 2 * C_T_PANEL, "chain tiles");
@@ -122,9 +122,9 @@ static_assert(64 * SOLVE_LD * 4 >= 4 * 4096, "the A/T area doubles as the store 
 // Registers per thread after setmaxnreg, by role.  Each CTA is launched with 128 per
 // thread (512 threads, the SM's 64K), and the roles' shares must add up to no more.
 constexpr int RC_CTL = 56, RC_STATE = 168, RC_OUT = 120;        // chain: 4, 8, 4 warps
-constexpr int RP_CTL = 96, RP_PIPE = 192, RP_IDLE = 24;         // preparation: 4, 8, 4 warps
+constexpr int RP_CTL = 96, RP_PIPE = 192, RP_AUX = 32;          // preparation: 4, 8, 4 warps
 static_assert(4 * RC_CTL + 8 * RC_STATE + 4 * RC_OUT <= 16 * 128, "chain register split");
-static_assert(4 * RP_CTL + 8 * RP_PIPE + 4 * RP_IDLE <= 16 * 128, "preparation register split");
+static_assert(4 * RP_CTL + 8 * RP_PIPE + 4 * RP_AUX <= 16 * 128, "preparation register split");
 
 constexpr uint32_t BAR_BYTES = 512;
 // packed inputs: stream lengths and their order (2 x 64 ints), then the production-order
@@ -181,8 +181,8 @@ enum {
   P_SLOTOK = 20,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
   P_KQFREE = 22,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
   P_VECFREE = 24,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
-  P_DRAIN = 28,    // [2] MMA issuer, abort path only: every product it issued has completed
-  P_COUNT = 30
+  P_DRAIN = 28,    // [2][2] MMA issuers (KQ, W), abort path only: their products completed
+  P_COUNT = 32
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
 static_assert(C_RECFREE == C_RECFULL + NBUF && C_LANDED == C_RECFREE + NBUF &&
@@ -282,13 +282,25 @@ __device__ __forceinline__ bool aborted(const Ctx& cx, uint32_t n) {
   return *cx.abort_l || ((n & 63) == 0 && ld_volatile_s32(cx.p->abort_g));
 }
 
+// The first wait that runs out records where it was in the word after the status word
+// (kept, like the status, until the caller clears it): bit 30 set, the CTA in bits 12-29,
+// the warp in bits 6-11, and what it waited on in bits 0-5 (an mbarrier's index in its
+// CTA, or 63 for a flag in global memory).
+__device__ __forceinline__ void note_timeout(const Ctx& cx, uint32_t what) {
+  atomicCAS(cx.p->status + 1, 0,
+            (int)(0x40000000u | (blockIdx.x << 12) | ((threadIdx.x >> 5) << 6) | (what & 63u)));
+}
+
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*cx.abort_l) return false;
-    if (clock64() - t0 > cx.p->wait_limit) return false;
+    if (clock64() - t0 > cx.p->wait_limit) {
+      note_timeout(cx, (smem_u32(bar) & 255u) >> 3);
+      return false;
+    }
   }
 }
 
@@ -314,7 +326,10 @@ __device__ __forceinline__ bool poll_ge(const uint32_t* f, uint32_t target, cons
     __nanosleep(32);
     if (ld_acquire_u32(f) >= target) return true;
     if (aborted(cx, n)) return false;
-    if (clock64() - t0 > cx.p->wait_limit) return false;
+    if (clock64() - t0 > cx.p->wait_limit) {
+      note_timeout(cx, 63);
+      return false;
+    }
   }
 }
 
@@ -461,6 +476,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       // rows beyond the sequence hold) and only then marks the buffer full.
       int issued = 0, rel = 0;
       bool ok = true;
+      uint32_t flag_next = 0;            // the next record's ready flag, read one chunk ahead
       uint32_t landed_uses = 0;          // bit b: parity of buffer b's next LANDED phase
       uint32_t part_of = 0;              // bit b: buffer b holds a partial chunk
       auto release_to = [&](int n) {
@@ -485,37 +501,37 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         const int row0 = (int)(bos + (int64_t)c * CHUNK);
         const int64_t rem = eos - (bos + (int64_t)c * CHUNK);
         const int L = rem < CHUNK ? (int)rem : CHUNK;
-        if (lane == 0) {
-          ok = poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx) &&
-               (s < NBUF || wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx));
-        }
-        if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) break;
         const bool part = L < CHUNK;
-        part_of = (part_of & ~(1u << b)) | ((part ? 1u : 0u) << b);
         uint64_t* txbar = part ? &bars[C_LANDED + b] : &bars[C_RECFULL + b];
         uint8_t* buf = sm + b * C_BUF;
+        // the record's flag first (usually set long before: its latency hides behind the
+        // wait for the buffer), then the buffer, free once the chunk that used it has had
+        // its products and its output read
         if (lane == 0) {
+          ok = flag_next >= (uint32_t)s + 1 || poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx);
           // the producer's plain stores before its release, then our bulk reads
-          fence_proxy_async_global();
-          const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
+          if (ok) fence_proxy_async_global();
+          ok = ok && (s < NBUF || wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx));
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) break;
+        part_of = (part_of & ~(1u << b)) | ((part ? 1u : 0u) << b);
+        if (lane == 0) {
           mbar_arrive_expect_tx(txbar, tx);
+          const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
           if (!summ) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              bulk_g2s(buf + q4 * REC_PART, src + q4 * REC_PART, REC_PART, txbar);
+            bulk_g2s(buf, src, REC_BYTES, txbar);
           } else {
             // (-W)^T and, for the E chain, T' (contiguous), then the decays
             bulk_g2s(buf + R_W, src + R_W, ptwin ? 16384u : 24576u, txbar);
             bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, txbar);
           }
-#pragma unroll
-          for (int pnl = 0; pnl < 2; ++pnl) {
-            tma_load_3d(buf + C_K + pnl * C_T_PANEL, tmK, txbar, 64 * pnl, hk, row0);
-            if (has_out) tma_load_3d(buf + C_Q + pnl * C_T_PANEL, tmQ, txbar, 64 * pnl, hk, row0);
-            if (need_v) tma_load_3d(buf + C_V + pnl * C_T_PANEL, tmV, txbar, 64 * pnl, h, row0);
-          }
+          tma_load_4d(buf + C_K, tmK, txbar, 0, row0, 0, hk);
+          if (has_out) tma_load_4d(buf + C_Q, tmQ, txbar, 0, row0, 0, hk);
+          if (need_v) tma_load_4d(buf + C_V, tmV, txbar, 0, row0, 0, h);
         }
         issued = s + 1;
+        // the next record's flag, read now and looked at next time round
+        if (lane == 0 && s + 1 < len) flag_next = ld_acquire_u32(readyj + (s + 1) % NSLOT);
         if (part) {
           const uint32_t ph = (landed_uses >> b) & 1u;
           landed_uses ^= 1u << b;
@@ -542,13 +558,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           int n = rel;
           if (s >= NBUF && n < s - NBUF + 1) n = s - NBUF + 1;
           while (n < s && mbar_test(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1)) ++n;
-          if (n > rel) release_to(n);
+          if (n >= rel + 2) release_to(n);   // two slots at a time (the ring has NSLOT)
         }
       }
       if (lane == 0) {
-        while (ok && rel < len) {
-          if (!(ok = wait_bar(&bars[C_RECFULL + rel % NBUF], (rel / NBUF) & 1, cx))) break;
-          release_to(rel + 1);
+        if (ok && rel < len) {
+          // records before len - NBUF landed before their buffers were taken again (and a
+          // parity wait on a buffer's older phase could be mistaken for its newer one), so
+          // only the last NBUF are waited for
+          for (int n = rel > len - NBUF ? rel : (len > NBUF ? len - NBUF : 0); n < len && ok; ++n)
+            ok = wait_bar(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1, cx);
+          if (ok) release_to(len);
         }
         if (!ok) {
           raise_abort(cx);
@@ -842,25 +862,29 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           }
         }
         auto out_at = [&](int i) -> uint16_t { return (uint16_t)(ob[i >> 1] >> (16 * (i & 1))); };
+        // O1, O2 and the chunk's buffer (e^gamma read) are free for the next products and
+        // records; the staging tile of two chunks back must have been read by its store
         tc_fence_before();
+        if (v == 0) bulk_wait_read<1>();
         named_bar(BAR_OUT, 128);
-        if (v == 0) mbar_arrive(&bars[C_OFREE]);
+        if (v == 0) {
+          mbar_arrive(&bars[C_OFREE]);
+          mbar_arrive(&bars[C_RECFREE + rb]);
+        }
         const int64_t row0 = bos + (int64_t)c * CHUNK;
         const int L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
         if (L == CHUNK) {
-          // the record's (-W)^T area (read by the chunk's first product, long done) stages
-          // the [64 token][128 v] tile in the panel layout; one TMA store sends it out
-          uint8_t* st = sm + rb * C_BUF + R_W;
+          // a staging tile of its own takes the [64 token][128 v] tile in the panel layout;
+          // one TMA store sends it out
+          uint8_t* st = sm + C_OST + (s & 1) * 16384;
 #pragma unroll
           for (int i = 0; i < 64; ++i)
             *reinterpret_cast<uint16_t*>(st + sw128_off(i, v, 8192)) = out_at(i);
           fence_proxy_async_smem();
           named_bar(BAR_OUT, 128);
           if (v == 0) {
-            tma_store_3d(tmO, st, 0, h, (int)row0);
-            tma_store_3d(tmO, st + 8192, 64, h, (int)row0);
+            tma_store_4d(tmO, st, 0, (int)row0, 0, h);
             bulk_commit();
-            bulk_wait_read_all();   // the buffer may take the next record
           }
         } else {
           // a chunk cut short by the sequence end: only its own rows are written
@@ -869,7 +893,6 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           for (int i = 0; i < 64; ++i)
             if (i < L) orow[i * rs] = out_at(i);
         }
-        if (v == 0) mbar_arrive(&bars[C_RECFREE + rb]);
       }
     }
     if (v == 0) bulk_wait_all();   // every output store has landed before the CTA leaves
@@ -1075,16 +1098,23 @@ __device__ __forceinline__ void lower(const float* AT, uint8_t* t1, uint8_t* t2,
 // --------------------------------------------------------------------------
 // Preparation CTA.  Items (chunk records) are claimed one at a time, in stream order,
 // from a grid-wide counter, so that a pipeline waiting for a full ring slot holds up
-// only the chain that slot belongs to.  warps 0 and 2: controllers of pipelines 0 and 1
-// (claim, gate/beta and the chunk's decay vectors, the K/Q tiles by TMA into one of two
-// buffers, the ring-slot check, the release of the finished record); warps 1 and 3: MMA
-// issuers of pipelines 0 and 1; warps 4-7 and 8-11: the two pipelines; warps 12-15 idle.
+// only the chain that slot belongs to.  Per pipeline p (p = 0, 1) one warp each:
+//   feeder (warp 2p): claim, gate/beta and the chunk's decay vectors, the K/Q tiles by TMA
+//     into one of two buffers;
+//   KQ issuer (warp 2p + 1): [K;Q] K^T of each item once its tiles have landed and the
+//     previous item's accumulator was read out -- typically during the previous solve;
+//   W issuer (warp 12 + p): (-W)^T of each item once its -T'' is written;
+//   publisher (warp 14 + p): the release of each finished record and the ring-slot check
+//     of the next;
+// and four warps (4-7, 8-11) that turn the products into the record.  Every role waits
+// (suspended) only on what it needs, so none of them holds up another.
 // A pipeline's item u: [K;Q] K^T (issued while item u-1 is still in its solve), the
 // decayed A and Ahat, the solve to T' and -T'', (-W)^T = K^T (-T'')^T; the record it
 // writes holds (-W)^T, T', Ahat and the decay vectors.
 // --------------------------------------------------------------------------
 __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                         const CUtensorMap* tmV, const SplitParams& p,
+                                         const CUtensorMap* tmQ4, const CUtensorMap* tmK4,
+                                         const CUtensorMap* tmV4, const SplitParams& p,
                                          const Geo& geo, uint8_t* sm, uint32_t sb,
                                          uint64_t* bars, uint32_t tm, const Ctx& cx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1110,7 +1140,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
   if (warp < 4) {
     reg_dealloc<RP_CTL>();
     if (warp == 0 || warp == 2) {
-      // ------------------------------------------------------------ controller
+      // ------------------------------------------------------------ feeder
       const int pp = warp >> 1;
       uint8_t* base = sm + pp * P_STRIDE;
       // pipeline 0 keeps [K;Q] in its tile rows, pipeline 1 [Q;K] (see the pipelines)
@@ -1120,6 +1150,10 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (lane == 0) g = (int)atomicAdd(p.next_item, 1u);
         return __shfl_sync(0xffffffffu, g, 0);
       };
+      // lane 0's claim in flight (its result is read one use later, so that the atomic's
+      // round trip overlaps a whole use)
+      auto claim_start = [&]() -> uint32_t { return lane == 0 ? atomicAdd(p.next_item, 1u) : 0u; };
+      auto claim_end = [&](uint32_t c) -> int { return __shfl_sync(0xffffffffu, (int)c, 0); };
       // An item's geometry, its gate/beta values (two tokens per lane, loaded one use
       // ahead so that their latency overlaps the waits), and its tiles warmed in L2 (V
       // for the chain CTA that will load it).
@@ -1137,27 +1171,30 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (e0 < n.L) { n.g0 = p.g[o0]; n.b0 = p.beta[o0]; }
         if (e1 < n.L) { n.g1 = p.g[o1]; n.b1 = p.beta[o1]; }
         if (lane == 0) {
-#pragma unroll
-          for (int pnl = 0; pnl < 2; ++pnl) {
-            tma_prefetch_l2_3d(tmK, 64 * pnl, n.hk, n.row0);
-            if (!summ) tma_prefetch_l2_3d(tmQ, 64 * pnl, n.hk, n.row0);
-            tma_prefetch_l2_3d(tmV, 64 * pnl, n.h, n.row0);
-          }
+          tma_prefetch_l2_4d(tmK4, 0, n.row0, 0, n.hk);
+          if (!summ) tma_prefetch_l2_4d(tmQ4, 0, n.row0, 0, n.hk);
+          tma_prefetch_l2_4d(tmV4, 0, n.row0, 0, n.h);
         }
         return n;
       };
       int last = -1;                 // last use with a tile copy
-      int pj = -1, ps = 0;           // the previous use's record (chain CTA, position)
-      long long pg = -1;             // and its item
       bool ok = true;
-      // items are claimed two uses ahead: `cur` is this use's, `nxt` the next one's
+      // items are claimed three uses ahead: `cur` is this use's, `nxt` the next one's,
+      // and the claim in flight the one after (every claimed item below geo.total is
+      // processed: a pipeline's claims only grow, so once one is past the end, so are the
+      // ones after it)
       Next cur = fetch(claim());
       int gnn = claim();
+      uint32_t inflight = claim_start();
       for (int use = 0; ok; ++use) {
         const bool done = cur.g >= geo.total;
         const Next nxt = fetch(done ? cur.g : gnn);
-        if (!done && nxt.g < geo.total) gnn = claim();
+        if (!done && nxt.g < geo.total) {
+          gnn = claim_end(inflight);
+          inflight = claim_start();
+        }
         const int jj = cur.jj, s = cur.s, hk = cur.hk, row0 = cur.row0, L = cur.L;
+        const long long gitem = cur.g;
         const int ub = use & 1;        // vector slot and tile buffer of this use
         // the slot and the buffer are free once the item two uses back has finished (one
         // barrier per slot, so a phase can never be mistaken for the one two items later)
@@ -1205,7 +1242,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         }
         if (lane == 0) {
           int* vi = reinterpret_cast<int*>(vs) + VEC_ITEM;
-          vi[0] = done ? -1 : cur.g;
+          vi[0] = done ? -1 : (int)gitem;
           vi[1] = jj;
           vi[2] = s;
         }
@@ -1242,30 +1279,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[P_HEAD + 2 * pp + ub]);
-        // release the previous record once written (before this item's slot check: a
-        // record that its own chain is waiting for must never sit behind that check)
-        if (pj >= 0) {
-          if (!(ok = warp_wait(&bars[P_PUB + pp], (use - 1) & 1, cx))) break;
-          if (lane == 0 && pg != p.drop_item)
-            st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
-          pj = -1;
-        }
         if (done) break;
-        // this record's ring slot must have been copied out by its chain CTA
-        if (lane == 0) {
-          ok = s < NSLOT ||
-               (poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx) &&
-                (!summ || poll_ge(p.consumed + (size_t)(jj + geo.nch) * FLAG_STRIDE,
-                                  (uint32_t)(s - NSLOT + 1), cx)));
-          if (ok) mbar_arrive(&bars[P_SLOTOK + pp]);
-        }
-        if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) {
-          if (lane == 0) raise_abort(cx);
-          break;
-        }
-        pj = jj;
-        ps = s;
-        pg = cur.g;
         cur = nxt;
       }
       // never leave with a tile copy in flight (the last two uses may each have one)
@@ -1273,62 +1287,36 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         if (u >= 0) mbar_wait(&bars[P_FULL + 2 * pp + (u & 1)], (u >> 1) & 1, 100000000ull);
       __syncwarp();
     } else {
-      // ------------------------------------------------------------ MMA issuer
-      // warp 1 issues pipeline 0's products, warp 3 pipeline 1's (an issue waits for the
-      // tensor pipe, so one thread serving both pipelines would hold each up behind the
-      // other).  Iteration u issues item u's [K;Q] K^T -- as soon as the pipeline has
-      // read out item u-1's, i.e. while item u-1 is in its solve -- and then item u-1's
-      // (-W)^T once its T'' is written.  Each waits (suspended) for exactly what it needs.
+      // ------------------------------------------------------------ KQ issuer
+      // warp 1 issues pipeline 0's [K;Q] K^T, warp 3 pipeline 1's: item u's as soon as its
+      // tiles have landed (FULL) and the pipeline has read out item u-1's (KQFREE).
       const int pp = warp >> 1;
       if (lane == 0) {
         const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
         const uint32_t kq_k = pp ? 8192u : 0u;
         for (int u = 0;; ++u) {
-          // the item slot and vectors (HEAD), the K and Q tiles (FULL), the previous item's
-          // KQ accumulator read out (KQFREE)
           if (!wait_bar(&bars[P_HEAD + 2 * pp + (u & 1)], (u >> 1) & 1, cx)) { raise_abort(cx); break; }
-          const bool done = reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0;
-          if (!done) {
-            if (!wait_bar(&bars[P_FULL + 2 * pp + (u & 1)], (u >> 1) & 1, cx) ||
-                (u > 0 && !wait_bar(&bars[P_KQFREE + pp], (u - 1) & 1, cx))) {
-              raise_abort(cx);
-              break;
-            }
-            tc_fence_after();
-            // KQ = [K; Q] K^T
-            const uint32_t kq = base + P_KQ + (u & 1) * P_KQ_BUF;
-            const uint64_t aq = sdesc_sw128(kq, 0, 1024);
-            const uint64_t bk = sdesc_sw128(kq + kq_k, 0, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t o = (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
-              mma_bf16(tp + TP_KQ, aq + o, bk + o, ID_N64, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars[P_KQDONE + pp]);
+          if (reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0) break;
+          if (!wait_bar(&bars[P_FULL + 2 * pp + (u & 1)], (u >> 1) & 1, cx) ||
+              (u > 0 && !wait_bar(&bars[P_KQFREE + pp], (u - 1) & 1, cx))) {
+            raise_abort(cx);
+            break;
           }
-          if (u > 0) {
-            // (-W)^T = K^T (-T'')^T of item u - 1, once its -T'' is written (TT)
-            if (!wait_bar(&bars[P_TT + pp], (u - 1) & 1, cx)) {
-              raise_abort(cx);
-              break;
-            }
-            tc_fence_after();
-            const uint32_t kq = base + P_KQ + ((u - 1) & 1) * P_KQ_BUF;
-            const uint64_t ak = sdesc_sw128(kq + kq_k, P_KQ_PANEL, 1024);
-            const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
+          tc_fence_after();
+          const uint32_t kq = base + P_KQ + (u & 1) * P_KQ_BUF;
+          const uint64_t aq = sdesc_sw128(kq, 0, 1024);
+          const uint64_t bk = sdesc_sw128(kq + kq_k, 0, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_AMN,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(&bars[P_WDONE + pp]);
-            mma_commit(&bars[P_ITEMFREE + 2 * pp + ((u - 1) & 1)]);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t o = (uint64_t)(((kk >> 2) * P_KQ_PANEL + (kk & 3) * 32) >> 4);
+            mma_bf16(tp + TP_KQ, aq + o, bk + o, ID_N64, kk > 0 ? 1u : 0u);
           }
-          if (done) break;
+          mma_commit(&bars[P_KQDONE + pp]);
         }
         if (*cx.abort_l) {
           // leave no product running into the TMEM that the CTA frees on its way out
-          mma_commit(&bars[P_DRAIN + pp]);
-          mbar_wait(&bars[P_DRAIN + pp], 0, 100000000ull);
+          mma_commit(&bars[P_DRAIN + 2 * pp]);
+          mbar_wait(&bars[P_DRAIN + 2 * pp], 0, 100000000ull);
         }
       }
       __syncwarp();
@@ -1464,14 +1452,79 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     if (pend) record_landed(lane, &bars[P_PUB + pp]);
     else if (lane == 0) bulk_wait_all();
   } else {
-    reg_dealloc<RP_IDLE>();
+    reg_dealloc<RP_AUX>();
+    const int pp = warp & 1;
+    if (warp < 14) {
+      // ------------------------------------------------------------ W issuer
+      // (-W)^T = K^T (-T'')^T of item u once its -T'' is written (TT)
+      if (lane == 0) {
+        const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
+        const uint32_t kq_k = pp ? 8192u : 0u;
+        for (int u = 0;; ++u) {
+          if (!wait_bar(&bars[P_HEAD + 2 * pp + (u & 1)], (u >> 1) & 1, cx)) { raise_abort(cx); break; }
+          if (reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0) break;
+          if (!wait_bar(&bars[P_TT + pp], u & 1, cx)) { raise_abort(cx); break; }
+          tc_fence_after();
+          const uint32_t kq = base + P_KQ + (u & 1) * P_KQ_BUF;
+          const uint64_t ak = sdesc_sw128(kq + kq_k, P_KQ_PANEL, 1024);
+          const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_AMN,
+                     kk > 0 ? 1u : 0u);
+          mma_commit(&bars[P_WDONE + pp]);
+          mma_commit(&bars[P_ITEMFREE + 2 * pp + (u & 1)]);
+        }
+        if (*cx.abort_l) {
+          mma_commit(&bars[P_DRAIN + 2 * pp + 1]);
+          mbar_wait(&bars[P_DRAIN + 2 * pp + 1], 0, 100000000ull);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ publisher
+      // Record u-1 is released once its stores have landed (PUB: the pipeline's warps
+      // arrive when they start item u), and item u's ring slot must have been copied out
+      // by its chain CTA before the pipeline writes to it (SLOTOK).
+      if (lane == 0) {
+        int pj = -1, ps = 0;
+        long long pg = -1;
+        for (int u = 0;; ++u) {
+          if (!wait_bar(&bars[P_HEAD + 2 * pp + (u & 1)], (u >> 1) & 1, cx)) { raise_abort(cx); break; }
+          const int* vi = reinterpret_cast<const int*>(vec_of(pp, u)) + VEC_ITEM;
+          const int g = vi[0], jj = vi[1], s = vi[2];
+          if (pj >= 0) {
+            if (!wait_bar(&bars[P_PUB + pp], (u - 1) & 1, cx)) { raise_abort(cx); break; }
+            if (pg != p.drop_item)
+              st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
+            pj = -1;
+          }
+          if (g < 0) break;
+          const bool ok = s < NSLOT ||
+                          (poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx) &&
+                           (!summ || poll_ge(p.consumed + (size_t)(jj + geo.nch) * FLAG_STRIDE,
+                                             (uint32_t)(s - NSLOT + 1), cx)));
+          if (!ok) {
+            raise_abort(cx);
+            break;
+          }
+          mbar_arrive(&bars[P_SLOTOK + pp]);
+          pj = jj;
+          ps = s;
+          pg = g;
+        }
+      }
+      __syncwarp();
+    }
   }
 }
 
 __global__ void __launch_bounds__(NTHR, 1)
     gdn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ4,
+                         const __grid_constant__ CUtensorMap tmK4,
+                         const __grid_constant__ CUtensorMap tmV4,
                          const __grid_constant__ CUtensorMap tmO, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1510,10 +1563,15 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
     *abort_l = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmK);
-    if (!p.twin) prefetch_tmap(&tmQ);
-    prefetch_tmap(&tmV);
-    if (is_chain && p.out) prefetch_tmap(&tmO);
+    if (is_chain) {
+      prefetch_tmap(&tmK4);
+      if (!p.twin) prefetch_tmap(&tmQ4);
+      prefetch_tmap(&tmV4);
+      if (p.out) prefetch_tmap(&tmO);
+    } else {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmQ);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TM_COLS);
@@ -1530,9 +1588,9 @@ __global__ void __launch_bounds__(NTHR, 1)
   geo.init(p, len_s, sort_s);
 
   if (is_chain)
-    chain_cta(&tmQ, &tmK, &tmV, &tmO, p, geo, sm, sb, bars, tm, cx);
+    chain_cta(&tmQ4, &tmK4, &tmV4, &tmO, p, geo, sm, sb, bars, tm, cx);
   else
-    prep_cta(&tmQ, &tmK, &tmV, p, geo, sm, sb, bars, tm, cx);
+    prep_cta(&tmQ, &tmK, &tmQ4, &tmK4, &tmV4, p, geo, sm, sb, bars, tm, cx);
 
   tc_fence_before();
   __syncthreads();
@@ -1614,10 +1672,16 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   const int nprep = nsm - chain_blocks;
   if (nprep < 1) return cudaErrorInvalidConfiguration;
   const int rows = p.B * p.T;
-  CUtensorMap mq, mk, mv;
-  if (!make_bf16_map(&mk, k, rows, p.HK) || !make_bf16_map(&mv, v, rows, p.H)) return cudaErrorInvalidValue;
+  // the preparation loads [K;Q] panel by panel (3-D maps); the state chains load whole
+  // tiles, prefetch and store through the 4-D views
+  CUtensorMap mq, mk, mq4, mk4, mv4;
+  if (!make_bf16_map(&mk, k, rows, p.HK) || !make_bf16_map_4d(&mk4, k, rows, p.HK) ||
+      !make_bf16_map_4d(&mv4, v, rows, p.H))
+    return cudaErrorInvalidValue;
   mq = mk;   // summaries have no q: K stands in (its products are not used)
-  if (q && !make_bf16_map(&mq, q, rows, p.HK)) return cudaErrorInvalidValue;
+  mq4 = mk4;
+  if (q && (!make_bf16_map(&mq, q, rows, p.HK) || !make_bf16_map_4d(&mq4, q, rows, p.HK)))
+    return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(gdn_fwd_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_ALLOC);
   if (e != cudaSuccess) return e;
@@ -1648,9 +1712,9 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // the output map (the K map stands in when there is no output: it is never used then)
-  CUtensorMap mo = mk;
-  if (out && !make_bf16_map(&mo, out, rows, p.H)) return cudaErrorInvalidValue;
-  void* args[] = {&mq, &mk, &mv, &mo, &p};
+  CUtensorMap mo = mk4;
+  if (out && !make_bf16_map_4d(&mo, out, rows, p.H)) return cudaErrorInvalidValue;
+  void* args[] = {&mq, &mk, &mq4, &mk4, &mv4, &mo, &p};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
                                      dim3(chain_blocks + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
 }

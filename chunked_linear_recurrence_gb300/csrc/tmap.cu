@@ -46,4 +46,18 @@ bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int H) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_bf16_map_4d(CUtensorMap* m, const void* base, int rows, int H) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  // (64 columns, rows, 2 column panels, heads): the panel dimension sits between the rows
+  // and the heads in memory, so one box of 64 x 64 x 2 x 1 lands as two 64-row panels
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)H};
+  cuuint64_t strides[3] = {(cuuint64_t)H * D * 2, 128, (cuuint64_t)D * 2};
+  cuuint32_t box[4] = {64, 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace sfg

@@ -51,7 +51,10 @@
  *    implementation: an unsupported request returns SF_ERR_UNSUPPORTED.
  *  * The workspace's first 256 bytes hold a device status word.  A kernel
  *    whose internal wait exceeds its time limit writes SF_ERR_TIMEOUT there
- *    and returns; sf_workspace_status reads (and clears) it.
+ *    and returns; sf_workspace_status reads (and clears) it.  The next word
+ *    records where the first expired wait was (a diagnostic: bit 30 set, the
+ *    block index in bits 12-29, the warp in bits 6-11, the awaited barrier in
+ *    bits 0-5); it is left for the caller to read and clear.
  *  * sf_last_error() describes the last non-SF_OK status of the calling host
  *    thread.
  */
