@@ -402,6 +402,7 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   p.tape = reinterpret_cast<float*>(ws + kStatusBytes + one);
   p.dout = d_out; p.dsf = d_final_state; p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dgate;
   p.dbeta = dbeta; p.ds0 = d_initial_state;
+  p.status = reinterpret_cast<int*>(workspace);
   p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + 2 * one) : nullptr;
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   p.HK = eff_hk(shape);

@@ -45,6 +45,7 @@ struct ChainParams {
   int B, T, H, N;
   int HK;                 // query/key heads (divides H): value head h reads h / (H / HK)
   float scale;
+  int* status;            // the workspace's status words (kernels with bounded waits), or NULL
 };
 
 // Query/key head of value head h.
@@ -92,5 +93,8 @@ cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_
 // Per-chunk token gradients on the warp-level tensor cores (bwd_grad_mma.cu).
 cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
                                 cudaStream_t st);
+// Per-chunk token gradients on tcgen05 (bwd_grad_tc.cu): BF16, K = V = 128, checkpoints in
+// the split kernel's order (ckpt_tiled_off).
+cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t st);
 
 }  // namespace sfg
