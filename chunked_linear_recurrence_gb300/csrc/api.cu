@@ -118,8 +118,16 @@ int64_t bwd_slots(const sf_gdn_shape* s, bool packed) {
 
 size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Backward workspace: status word | chunk-entry states | exit cotangents (FP32
-// [slots,H,V,K] each) | BF16 only: per-chunk factors [slots,H] and, for head size 128, the
+// Bytes of one chunk-head's entry state (replay checkpoint) or exit cotangent (tape): BF16
+// with K = V = 128 keeps them as the BF16 swizzled tiles the tensor-core gradient kernel reads
+// (32 KB), the other kernels as FP32 [V,K].
+size_t state_tile_bytes(const sf_gdn_shape* s) {
+  if (s->dtype == SF_BF16 && s->K == 128 && s->V == 128) return 128 * 128 * 2;
+  return (size_t)s->K * s->V * sizeof(float);
+}
+
+// Backward workspace: status word | chunk-entry states | exit cotangents ([slots,H] of
+// state_tile_bytes each) | BF16 only: per-chunk factors [slots,H] and, for head size 128, the
 // split forward's ring (state replay) | grouped heads only: the per-value-head parts of dq
 // and dk (FP32 [B,T,H,K] each).
 struct BwdLayout {
@@ -135,7 +143,7 @@ BwdLayout bwd_layout(const sf_gdn_shape* shape) {
   const int64_t per = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK;
   const int64_t n = shape->N > 0 ? shape->N : shape->B;
   const int64_t slots = shape->B == 1 ? per + n : (int64_t)shape->B * per;
-  l.one = round_up((size_t)slots * shape->H * shape->K * shape->V * sizeof(float));
+  l.one = round_up((size_t)slots * shape->H * state_tile_bytes(shape));
   if (shape->dtype == SF_BF16 && (shape->K == 64 || shape->K == 128))
     l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));
   if (shape->dtype == SF_BF16 && shape->K == 128 && shape->V == 128)
@@ -297,8 +305,8 @@ sf_status sf_state_scan(int R, int H, int K, int V, const float* P, const float*
 size_t sf_gdn_bwd_workspace(const sf_gdn_shape* shape) { return bwd_layout(shape).total; }
 
 // Reverse summary workspace: status word | exit cotangents of every chunk (the reverse
-// chain's tape, FP32 [slots,H,V,K]) | BF16 only: per-chunk factors [slots,H].  Slots as the
-// packed backward: ceil(T/64) + R.
+// chain's tape, [slots,H] of state_tile_bytes) | BF16 only: per-chunk factors [slots,H].
+// Slots as the packed backward: ceil(T/64) + R.
 struct RevLayout {
   size_t tape, fac, total;
 };
@@ -307,7 +315,7 @@ RevLayout rev_layout(const sf_gdn_shape* shape) {
   RevLayout l{0, 0, kStatusBytes};
   if (!shape || shape->K < 1 || shape->H < 1 || shape->T < 0 || shape->N < 0) return l;
   const int64_t slots = (shape->T + sfg::CHUNK - 1) / sfg::CHUNK + shape->N;
-  l.tape = round_up((size_t)slots * shape->H * shape->K * shape->V * sizeof(float));
+  l.tape = round_up((size_t)slots * shape->H * state_tile_bytes(shape));
   if (shape->dtype == SF_BF16 && (shape->K == 64 || shape->K == 128))
     l.fac = round_up((size_t)slots * shape->H * sfg::mma_bwd_fac_bytes(shape->K));
   l.total = kStatusBytes + l.tape + l.fac;
@@ -420,7 +428,6 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
     return fail(SF_ERR_UNSUPPORTED, "%s: %s", fn, kNoTmaEncoder);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0) {
-    p.ckpt_tiled = 1;   // the split kernel writes its checkpoints in its threads' order
     e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
                               reinterpret_cast<int*>(workspace), cs);
   } else if (shape->T > 0) {

@@ -12,8 +12,9 @@
 //   * mma_bwd_chain_kernel walks each (sequence, head) chain backwards, tiled along V
 //     (StateFlow section 3.4.1, Eq. 16: rows of the cotangent evolve independently given
 //     the chunk factors), with the cotangent rows FP32 in shared memory.  Each chunk's
-//     exit cotangent goes to the tape for the token-gradient kernel; the cotangent at the
-//     sequence start is d_initial_state.
+//     exit cotangent goes to the tape for the token-gradient kernel (head size 128: as the
+//     BF16 swizzled tile that kernel's tensor cores read; 64: FP32 [V,K]); the cotangent
+//     at the sequence start is d_initial_state.
 #include <type_traits>
 
 #include "common.cuh"
@@ -31,6 +32,12 @@ constexpr int NTB = 256;   // 8 warps
 constexpr int C_LD6 = 68;
 template <int D>
 __host__ __device__ constexpr int c_ldd() { return D + 4; }
+
+// Two floats as a BF16 pair (the lower index in the low half).
+__device__ __forceinline__ uint32_t tc_pack(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 
 struct CtaBarB {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
@@ -241,7 +248,19 @@ __global__ void __launch_bounds__(NTB) mma_bwd_chain_kernel(const ChainParams p,
     const float* seg = reinterpret_cast<const float*>(base + B::VEC);
     const float* sdec = seg + 64;
     const auto dOT = view(sdO, 1, LDO);       // dO^T (v, i)
-    {
+    if constexpr (D == 128) {
+      // the tensor-core gradient kernel's operand: rows r0 .. r0 + BV - 1 of a BF16
+      // [128 v][128 k] tile in the 128-byte-swizzled panel layout (16-byte chunk c of row v
+      // of panel k / 64 at ((c ^ (v mod 8)) << 4))
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.tape) + (slot * H + h) * (size_t)(D * D * 2);
+      for (int idx = tid; idx < BV * 16; idx += NTB) {
+        const int r = idx >> 4, pc = idx & 15, v = r0 + r, c = pc & 7;
+        const float* x = dS + r * LDS + 8 * pc;
+        const uint4 val = make_uint4(tc_pack(x[0], x[1]), tc_pack(x[2], x[3]), tc_pack(x[4], x[5]),
+                                     tc_pack(x[6], x[7]));
+        *reinterpret_cast<uint4*>(dst + (pc >> 3) * 16384 + v * 128 + ((c ^ (v & 7)) << 4)) = val;
+      }
+    } else {
       float4* dst = reinterpret_cast<float4*>(p.tape + (slot * H + h) * D * D + (size_t)r0 * D);
       for (int idx = tid; idx < BV * D / 4; idx += NTB) {
         const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;

@@ -47,31 +47,11 @@ struct CtaBarG {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
 
-// Element (r, c) of a D = 128 checkpoint block in the split kernel's thread order (TR:
-// the transpose).
-template <bool TR>
-struct TiledState {
-  const float* p;
-  __device__ __forceinline__ float operator()(int r, int c) const {
-    return TR ? p[ckpt_tiled_off(c, r)] : p[ckpt_tiled_off(r, c)];
-  }
-  // BF16 pairs along c and along r (adjacent k of a state row are adjacent in the block)
-  __device__ __forceinline__ uint32_t pc(int r, int c) const {
-    return TR ? mt::pk(p[ckpt_tiled_off(c, r)], p[ckpt_tiled_off(c + 1, r)])
-              : mt::pair_at(p + ckpt_tiled_off(r, c));
-  }
-  __device__ __forceinline__ uint32_t pr(int r, int c) const {
-    return TR ? mt::pair_at(p + ckpt_tiled_off(c, r))
-              : mt::pk(p[ckpt_tiled_off(r, c)], p[ckpt_tiled_off(r + 1, c)]);
-  }
-};
-
 }  // namespace
 
 // One chunk (backward slot `slot`); false when the slot holds no chunk.
-template <typename Tin, int D, bool kTiled>
+template <typename Tin, int D>
 __device__ __forceinline__ bool grad_chunk(const ChainParams& p, int64_t slot) {
-  static_assert(!kTiled || D == 128, "tiled checkpoints have D = 128");
   constexpr int LDI = D + 8;      // input tiles (Tin)
   constexpr int LDF = g_ldf<Tin, D>();  // fp32 [64][D] tiles
   // products with k = D on BF16 operand pairs for BF16 inputs (TF32 for FP32 inputs)
@@ -163,12 +143,8 @@ __device__ __forceinline__ bool grad_chunk(const ChainParams& p, int64_t slot) {
   __syncthreads();
   const auto Qv = view(sQ, LDI, 1), Kv = view(sK, LDI, 1), Vv = view(sV, LDI, 1),
              dOv = view(sdO, LDI, 1);
-  const auto Sv = [&] {
-    if constexpr (kTiled) return TiledState<false>{S}; else return rm(S, D);
-  }();
-  const auto SvT = [&] {
-    if constexpr (kTiled) return TiledState<true>{S}; else return cm(S, D);
-  }();
+  const auto Sv = rm(S, D);
+  const auto SvT = cm(S, D);
 
   // Ak = Gamma o K K^T (strict lower), Aqk = Gamma o Q K^T (lower incl. diagonal)
   {
@@ -286,10 +262,7 @@ __device__ __forceinline__ bool grad_chunk(const ChainParams& p, int64_t slot) {
     const float4* b4 = reinterpret_cast<const float4*>(S);
 #pragma unroll 8
     for (int idx = tid; idx < D * D / 4; idx += NTG) {
-      // S's float4 idx holds (v, k0 .. k0 + 3) of the tiled order, or the row-major ones
-      const int v = kTiled ? (idx & 127) : 0;
-      const int k0 = kTiled ? ((idx >> 7) & 1) * 64 + (idx >> 8) * 4 : 0;
-      const float4 x = a4[kTiled ? (v * D + k0) / 4 : idx], y = b4[idx];
+      const float4 x = a4[idx], y = b4[idx];
       part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
     }
 #pragma unroll
@@ -448,19 +421,19 @@ __device__ __forceinline__ bool grad_chunk(const ChainParams& p, int64_t slot) {
 
 // Slots blockIdx.x, blockIdx.x + gridDim.x, ... until the first empty one (the grid may be
 // smaller than the slot count: packed inputs whose offsets end early leave slots empty).
-template <typename Tin, int D, bool kTiled>
+template <typename Tin, int D>
 __global__ void __launch_bounds__(NTG) mma_bwd_grad_kernel(const ChainParams p, int64_t slots) {
   for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
-    if (!grad_chunk<Tin, D, kTiled>(p, slot)) break;
+    if (!grad_chunk<Tin, D>(p, slot)) break;
     __syncthreads();   // shared memory is rewritten by the next chunk
   }
 }
 
-template <typename Tin, int D, bool kTiled = false>
+template <typename Tin, int D>
 static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream_t st) {
   const size_t smem = sizeof(float) * (3 * 64 * G_LD6 + 3 * 64 * g_ldf<Tin, D>() + 11 * 64) +
                       sizeof(Tin) * 4 * 64 * (D + 8);
-  auto kern = mma_bwd_grad_kernel<Tin, D, kTiled>;
+  auto kern = mma_bwd_grad_kernel<Tin, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTG, smem, st>>>(p, slots);
@@ -470,9 +443,6 @@ static cudaError_t launch_grad_t(const ChainParams& p, int64_t slots, cudaStream
 cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
                                 cudaStream_t st) {
   if (bf16 && D == 64) return launch_grad_t<__nv_bfloat16, 64>(p, slots, st);
-  if (bf16 && D == 128)
-    return p.ckpt_tiled ? launch_grad_t<__nv_bfloat16, 128, true>(p, slots, st)
-                        : launch_grad_t<__nv_bfloat16, 128>(p, slots, st);
   if (!bf16 && D == 64) return launch_grad_t<float, 64>(p, slots, st);
   return cudaErrorInvalidValue;
 }

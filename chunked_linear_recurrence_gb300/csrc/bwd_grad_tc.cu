@@ -30,10 +30,16 @@
 // (solve_tc.cuh).  Row sums over the feature axis (q . dq-part, k . Z, k . Y, v . X) are
 // warp-shuffle reductions over the lanes that hold the features.
 //
+// S and dSn arrive as BF16 tiles in that same layout (the state replay and the reverse
+// chain write them so), one bulk copy each.  The CTAs are persistent: the next chunk's S,
+// dSn and dO are fetched as soon as the current chunk's last product reading them has
+// completed, and its Q one step later, so that only K and V (read until the last step)
+// load in the open.
+//
 // Each step is: one thread issues the products and commits them to an mbarrier; all
 // threads wait for it, read the accumulators, write the next operand tiles; a CTA
 // barrier hands the tiles to the next step.  Every wait is bounded; a CTA that gives up
-// writes SF_ERR_TIMEOUT to the status word, drains its products and returns.
+// writes SF_ERR_TIMEOUT to the status word, drains its products and copies and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -62,8 +68,8 @@ constexpr uint32_t O_V = 32768;       // V [64 tok][128 v]
 constexpr uint32_t O_DO = 49152;      // dO [64 tok][128 v]
 constexpr uint32_t O_S = 65536;       // S [128 v][128 k]
 constexpr uint32_t O_DSN = 98304;     // dSn [128 v][128 k]
-constexpr uint32_t O_TT = 131072;     // T [64 i][64 j]
-constexpr uint32_t O_DDT = 139264;    // dDelta^T [128 v][64 i]
+constexpr uint32_t O_DDT = 131072;    // dDelta^T [128 v][64 i]
+constexpr uint32_t O_TT = 147456;     // T [64 i][64 j]
 constexpr uint32_t O_DWT = 155648;    // dW^T [128 k][64 j]
 constexpr uint32_t O_NWT = 172032;    // -W^T [128 k][64 i], then Delta^T [128 v][64 i]
 constexpr uint32_t O_UN = 188416;     // area shared by steps that do not overlap in time:
@@ -89,8 +95,10 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory");
 // products whose M = 128 operand reads 64 rows past a 64-row tile read these neighbours:
 static_assert(O_DO + 2 * X_PANEL == O_S, "dO Delta^T: the rows past dO's second panel");
 static_assert(O_UN + U_DT + X_PANEL == O_UN + U_X1, "dT T^T: the rows past dT");
-static_assert(O_DDT + F_PANEL == O_DWT && O_DWT + F_PANEL == O_NWT, "MN-major padding groups");
-static_assert(O_TT - X_PANEL >= O_DSN, "T^T X1 on the upper lanes: the group before T");
+static_assert(O_DDT + F_PANEL == O_TT && O_DWT + F_PANEL == O_NWT, "MN-major padding groups");
+static_assert(O_TT - X_PANEL == O_DDT + X_PANEL, "T^T X1 on the upper lanes: the group before T");
+// (the next chunk's S, dSn, dO and Q land while the last steps run: no product of those
+// steps reads them, padding groups included)
 
 // TMEM columns (512 allocated): accumulators of 64 FP32 columns each
 constexpr uint32_t TM_KQ = 0;     // [Q;K] K^T (lanes 0-63: Q K^T, 64-127: K K^T)
@@ -164,14 +172,46 @@ __device__ __forceinline__ int colsum_col(int lane) {
   return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
+// mbarriers
+enum { B_SDO = 0, B_MMA, B_DRAIN, B_Q, B_KV, B_COUNT };
+constexpr uint32_t TILE_BYTES = 32768;   // one BF16 [128][128] S or dSn tile
+
+// One chunk-head: backward slot, value head, query/key head, first row, length.
+struct Item {
+  int64_t slot, c0;
+  int h, hk, L;
+  bool valid;
+};
+
+__device__ __forceinline__ Item locate_item(const ChainParams& p, int64_t item) {
+  Item it{};
+  it.valid = false;
+  const int64_t slot = item / p.H;
+  int n = -1;
+  int64_t bos = 0, eos = 0, ci = 0;
+  if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) return it;
+  it.slot = slot;
+  it.h = (int)(item % p.H);
+  it.hk = qk_head(it.h, p.H, p.HK);
+  it.c0 = bos + ci * CHUNK;
+  it.L = (int)((eos - it.c0) < CHUNK ? (eos - it.c0) : CHUNK);
+  it.valid = true;
+  return it;
+}
+
+struct Maps {
+  const CUtensorMap *q, *k, *v, *dout;
+};
+
 struct Ctx {
   uint8_t* sm;
   uint32_t sb;       // shared address of sm
   uint32_t tm;       // TMEM base
-  uint64_t* bars;    // [0] loads, [1] products, [2] drain
+  uint64_t* bars;
   float* vec;
   int tid, warp, lane, q4, wg;
-  uint32_t lph, mph;
+  uint32_t lph, mph;   // completed phases of the per-chunk load barriers / of B_MMA
+  uint32_t pend;       // thread 0: copies issued and not yet waited for (1 << B_SDO | ...)
   int* status;
   __device__ float* v(int which) const { return vec + which * 64; }
   // TMEM address of this warp's lane quarter at column `col`
@@ -188,7 +228,7 @@ __device__ __forceinline__ void note_timeout(const Ctx& c, uint32_t what) {
 // Products committed by thread 0 -> every thread waits (bounded), then orders its TMEM
 // reads after them.
 __device__ __forceinline__ bool wait_products(Ctx& c) {
-  const bool ok = mbar_wait(&c.bars[1], c.mph & 1, WAIT_NS);
+  const bool ok = mbar_wait(&c.bars[B_MMA], c.mph & 1, WAIT_NS);
   if (!ok) note_timeout(c, 1);
   ++c.mph;
   tc_fence_after();
@@ -211,14 +251,49 @@ __device__ __forceinline__ void st_row16(uint8_t* tile, int row, int c0, const f
   st_row8_bf16(tile, row, c0 + 8, X_PANEL, x + 8);
 }
 
-// One chunk.  False when a wait expired (the status word then says where).
-__device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
-                           const CUtensorMap* mk, const CUtensorMap* mv, const CUtensorMap* mdo,
-                           int64_t slot, int n, int64_t c0, int L) {
+// Thread 0: the chunk's S and dSn tiles (bulk copies) and its dO tile (TMA).
+__device__ __forceinline__ void fetch_sdo(Ctx& c, const ChainParams& p, const Maps& m,
+                                          const Item& it) {
+  const uint8_t* ck = reinterpret_cast<const uint8_t*>(p.ckpt);
+  const uint8_t* tp = reinterpret_cast<const uint8_t*>(p.tape);
+  const size_t off = ((size_t)it.slot * p.H + it.h) * TILE_BYTES;
+  c.pend |= 1u << B_SDO;
+  mbar_arrive_expect_tx(&c.bars[B_SDO], 2 * TILE_BYTES + 2 * X_PANEL);
+  bulk_g2s(c.sm + O_S, ck + off, TILE_BYTES, &c.bars[B_SDO]);
+  bulk_g2s(c.sm + O_DSN, tp + off, TILE_BYTES, &c.bars[B_SDO]);
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp)
+    tma_load_3d(c.sm + O_DO + pp * X_PANEL, m.dout, &c.bars[B_SDO], 64 * pp, it.h, (int)it.c0);
+}
+// Thread 0: the chunk's Q tile.
+__device__ __forceinline__ void fetch_q(Ctx& c, const Maps& m, const Item& it) {
+  c.pend |= 1u << B_Q;
+  mbar_arrive_expect_tx(&c.bars[B_Q], 2 * X_PANEL);
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp)
+    tma_load_3d(c.sm + O_QK + pp * QK_PANEL, m.q, &c.bars[B_Q], 64 * pp, it.hk, (int)it.c0);
+}
+// Thread 0: the chunk's K and V tiles.
+__device__ __forceinline__ void fetch_kv(Ctx& c, const Maps& m, const Item& it) {
+  c.pend |= 1u << B_KV;
+  mbar_arrive_expect_tx(&c.bars[B_KV], 4 * X_PANEL);
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    tma_load_3d(c.sm + O_K + pp * QK_PANEL, m.k, &c.bars[B_KV], 64 * pp, it.hk, (int)it.c0);
+    tma_load_3d(c.sm + O_V + pp * X_PANEL, m.v, &c.bars[B_KV], 64 * pp, it.h, (int)it.c0);
+  }
+}
+
+// One chunk.  Its S, dSn, dO and Q copies were issued before (for the next chunk `nx`
+// this chunk issues them); its K and V copies are issued here.  False when a wait
+// expired (the status word then says where).
+__device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const Item& it,
+                           const Item& nx) {
   uint8_t* sm = c.sm;
   const uint32_t sb = c.sb;
   const int tid = c.tid, lane = c.lane, q4 = c.q4, wg = c.wg;
-  const int h = blockIdx.y, H = p.H, hk = qk_head(h, H, p.HK);
+  const int h = it.h, H = p.H, L = it.L;
+  const int64_t c0 = it.c0;
   const float scale = p.scale;
   float* vg = c.v(V_G);
   float* vb = c.v(V_B);
@@ -231,20 +306,11 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
   float* vdb = c.v(V_DB);
   float* vz = c.v(V_Z);
   float* vkt = c.v(V_KT);
-  (void)n;
 
-  // ---- inputs: q, k, v, dO tiles by TMA; S and dSn converted to BF16 by all threads ----
+  // ---- inputs: K and V now; gate and beta; S, dSn, dO and Q are in flight already ----
   if (tid == 0) {
-    fence_proxy_async_smem();   // the previous chunk's generic reads of these tiles
-    mbar_arrive_expect_tx(&c.bars[0], 8 * 8192);
-    const int row = (int)c0;
-#pragma unroll
-    for (int pp = 0; pp < 2; ++pp) {
-      tma_load_3d(sm + O_QK + pp * QK_PANEL, mq, &c.bars[0], 64 * pp, hk, row);
-      tma_load_3d(sm + O_K + pp * QK_PANEL, mk, &c.bars[0], 64 * pp, hk, row);
-      tma_load_3d(sm + O_V + pp * X_PANEL, mv, &c.bars[0], 64 * pp, h, row);
-      tma_load_3d(sm + O_DO + pp * X_PANEL, mdo, &c.bars[0], 64 * pp, h, row);
-    }
+    fence_proxy_async_smem();   // the previous chunk's generic reads of the K and V tiles
+    fetch_kv(c, m, it);
   }
   if (tid < 64) {
     const size_t off = (size_t)(c0 + tid) * H + h;
@@ -254,30 +320,6 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
     vdb[tid] = 0.f;
     vz[tid] = 0.f;
     vkt[tid] = 0.f;
-  }
-  float sdot = 0.f;   // <dSn, S> (FP32)
-  {
-    // S: float4 f of the tiled block holds (v, k0 .. k0 + 3), v = f mod 128,
-    // k0 = 64 ((f / 128) mod 2) + 4 (f / 256); dSn is row-major [v][k]
-    const float4* S4 = reinterpret_cast<const float4*>(p.ckpt + ((size_t)slot * H + h) * D * D);
-    const float4* N4 = reinterpret_cast<const float4*>(p.tape + ((size_t)slot * H + h) * D * D);
-    float4 s[8], d[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int f = tid + NT * m, v = f & 127, k0 = 64 * ((f >> 7) & 1) + 4 * (f >> 8);
-      s[m] = S4[f];
-      d[m] = N4[(v * D + k0) >> 2];
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int f = tid + NT * m, v = f & 127, k0 = 64 * ((f >> 7) & 1) + 4 * (f >> 8);
-      sdot += s[m].x * d[m].x + s[m].y * d[m].y + s[m].z * d[m].z + s[m].w * d[m].w;
-      const uint32_t o = sw128_off(v, k0, F_PANEL);
-      *reinterpret_cast<uint2*>(sm + O_S + o) =
-          make_uint2(pack_bf16x2(s[m].x, s[m].y), pack_bf16x2(s[m].z, s[m].w));
-      *reinterpret_cast<uint2*>(sm + O_DSN + o) =
-          make_uint2(pack_bf16x2(d[m].x, d[m].y), pack_bf16x2(d[m].z, d[m].w));
-    }
   }
   __syncthreads();
   if (tid < 32) warp_cumsum64(vg, vgam, lane);
@@ -289,11 +331,33 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
     vbeg[tid] = vb[tid] * eg;
     vsc[tid] = scale * eg;
   }
+  const uint32_t par = c.lph & 1;
+  bool ok = mbar_wait(&c.bars[B_SDO], par, WAIT_NS);
+  if (!ok) note_timeout(c, 0);
+  float sdot = 0.f;   // <dSn, S>: both tiles share one layout, so position by position
+  {
+    const uint4* a4 = reinterpret_cast<const uint4*>(sm + O_S);
+    const uint4* b4 = reinterpret_cast<const uint4*>(sm + O_DSN);
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+      const uint4 x = a4[tid + NT * mm], y = b4[tid + NT * mm];
+      const uint32_t xa[4] = {x.x, x.y, x.z, x.w}, ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xa[e]));
+        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ya[e]));
+        sdot += fx.x * fy.x + fx.y * fy.y;
+      }
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
-  bool ok = mbar_wait(&c.bars[0], c.lph & 1, WAIT_NS);
-  if (!ok) note_timeout(c, 0);
-  ++c.lph;
+  if (ok && !(ok = mbar_wait(&c.bars[B_Q], par, WAIT_NS))) note_timeout(c, 3);
+  if (ok && !(ok = mbar_wait(&c.bars[B_KV], par, WAIT_NS))) note_timeout(c, 4);
+  if (ok) {
+    c.pend = 0;
+    ++c.lph;
+  }
   if (L < 64) {
     // rows past the chunk's end read other tokens (or the fill): zero them in every tile
     for (int idx = tid; idx < (64 - L) * 8 * 8; idx += NT) {
@@ -323,7 +387,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_bf16(c.tm + TM_B, ad + kstep_k(kk, F_PANEL), bk + kstep_k(kk, QK_PANEL), ID_KK, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
   {
@@ -380,7 +444,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_A, a + kstep_mn(kk), b + kstep_mn(kk), ID_MM, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   float* AT = reinterpret_cast<float*>(sm + O_UN + U_AT);
   solve64_tc_inplace(AT, reinterpret_cast<float*>(sm + O_UN + U_X), tid, NT,
@@ -436,7 +500,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_X, add + kstep_k(kk, F_PANEL), btt + kstep_mn(kk), ID_KM, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
   {
@@ -480,7 +544,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_bf16(c.tm + TM_B, addm + kstep_mn(kk), bv + kstep_k(kk, X_PANEL), ID_MK, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
   {
@@ -519,9 +583,14 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_B, adt + kstep_k(kk, X_PANEL), bt + kstep_k(kk, X_PANEL), ID_KK, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
+  if (tid == 0 && nx.valid) {
+    // the next chunk's S, dSn and dO (the last products reading this chunk's have completed)
+    fence_proxy_async_smem();
+    fetch_sdo(c, p, m, nx);
+  }
   if (q4 < 2) {
     // dAqk = scale dO Delta^T: G = dAqk o Gamma (lower incl. diagonal) -> tile; rho =
     // G o (Q K^T) -> dgamma_i += row sum, dgamma_j -= column sum.  X1 -> tile.
@@ -568,9 +637,14 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_A, att + kstep_mn(kk), bx1 + kstep_mn(kk), ID_MM, kk > 0);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
+  if (tid == 0 && nx.valid) {
+    // the next chunk's Q (the last product reading this chunk's Q has completed)
+    fence_proxy_async_smem();
+    fetch_q(c, m, nx);
+  }
   if (q4 >= 2) {
     // dA = -(T^T X1) strictly lower (rows i on lanes 64-127, beside K K^T): dbeta_i +=
     // sum_j dA Ak; rho = dA beta_i Ak -> dgamma; dKK = dA beta_i Gamma -> tile
@@ -613,7 +687,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_DK, akt + kstep_mn(kk), bkk + kstep_mn(kk), ID_MM, 1u);
-    mma_commit(&c.bars[1]);
+    mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
 
@@ -715,7 +789,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const CUtensorMap* mq,
 __global__ void __launch_bounds__(NT, 1)
     tc_bwd_grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv,
-                       const __grid_constant__ CUtensorMap mdo, const ChainParams p, int64_t slots) {
+                       const __grid_constant__ CUtensorMap mdo, const ChainParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
   c.sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -729,12 +803,12 @@ __global__ void __launch_bounds__(NT, 1)
   c.wg = c.warp >> 2;
   c.lph = 0;
   c.mph = 0;
+  c.pend = 0;
   c.status = p.status;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(c.sm + O_BAR + 32);
+  const Maps m{&mq, &mk, &mv, &mdo};
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(c.sm + O_BAR + 8 * B_COUNT);
   if (c.tid == 0) {
-    mbar_init(&c.bars[0], 1);
-    mbar_init(&c.bars[1], 1);
-    mbar_init(&c.bars[2], 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&c.bars[b], 1);
     fence_mbar_init();
     prefetch_tmap(&mq);
     prefetch_tmap(&mk);
@@ -746,21 +820,27 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   c.tm = *tslot;
+  // chunk-heads blockIdx.x, blockIdx.x + gridDim.x, ... in the order (slot, head), until the
+  // first empty slot
+  Item it = locate_item(p, blockIdx.x);
+  if (c.tid == 0 && it.valid) {
+    fetch_sdo(c, p, m, it);
+    fetch_q(c, m, it);
+  }
   bool ok = true;
-  for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
-    int n = -1;
-    int64_t bos = 0, eos = 0, ci = 0;
-    if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) break;
-    const int64_t c0 = bos + ci * CHUNK;
-    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
-    ok = grad_chunk(c, p, &mq, &mk, &mv, &mdo, slot, n, c0, L);
+  for (int64_t item = blockIdx.x; it.valid; item += gridDim.x) {
+    const Item nx = locate_item(p, item + gridDim.x);
+    ok = grad_chunk(c, p, m, it, nx);
     if (!ok) break;
-    __syncthreads();   // the next chunk's loads overwrite the tiles read above
+    __syncthreads();   // the next chunk's K and V overwrite tiles read above
+    it = nx;
   }
   if (!ok && c.tid == 0) {
-    // leave no product running into the TMEM freed below
-    mma_commit(&c.bars[2]);
-    mbar_wait(&c.bars[2], 0, WAIT_NS);
+    // leave no product running into the TMEM freed below, and no copy landing after exit
+    mma_commit(&c.bars[B_DRAIN]);
+    mbar_wait(&c.bars[B_DRAIN], 0, WAIT_NS);
+    for (int b = 0; b < B_COUNT; ++b)
+      if (c.pend & (1u << b)) mbar_wait(&c.bars[b], c.lph & 1, WAIT_NS);
   }
   tc_fence_before();
   __syncthreads();
@@ -773,6 +853,7 @@ __global__ void __launch_bounds__(NT, 1)
 size_t tc_bwd_grad_smem() { return SMEM_ALLOC; }
 
 cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t st) {
+  if (slots <= 0 || (int64_t)p.B * p.T == 0) return cudaSuccess;   // no chunk
   CUtensorMap mq, mk, mv, mdo;
   const int rows = p.B * p.T;
   if (!make_bf16_map(&mq, p.q, rows, p.HK) || !make_bf16_map(&mk, p.k, rows, p.HK) ||
@@ -782,9 +863,14 @@ cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  if (slots > 0)
-    kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NT, SMEM_ALLOC, st>>>(mq, mk, mv, mdo, p,
-                                                                          slots);
+  int dev = 0, nsm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  // one persistent CTA per SM (the shared memory allows no second), at most one per item
+  const int64_t items = slots * p.H;
+  const int grid = (int)(items < nsm ? items : nsm);
+  if (grid > 0) kern<<<grid, NT, SMEM_ALLOC, st>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 

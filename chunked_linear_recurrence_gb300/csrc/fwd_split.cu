@@ -89,6 +89,19 @@ constexpr uint32_t V_GC = 512;        //   e^{gamma_C}
 constexpr uint32_t REC_BYTES = 33792;
 static_assert(REC_BYTES % 16 == 0 && V_GC + 4 <= REC_BYTES - R_VEC, "record layout");
 
+// ---- state replay checkpoints: one BF16 [128 v][128 k] tile per chunk-head, two 64-column
+// panels of 128 rows x 128 bytes, 16-byte chunk c of row v at ((c ^ (v mod 8)) << 4) (the
+// layout the tensor-core gradient kernel reads as an operand) ----
+constexpr uint32_t CKPT_TILE_BYTES = 32768;
+
+// Row v of one panel of a checkpoint tile from the 64 values' BF16 pairs u.
+__device__ __forceinline__ void store_ckpt_row(uint8_t* row, int v, const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ (v & 7)) << 4)) =
+        make_uint4(u[4 * c], u[4 * c + 1], u[4 * c + 2], u[4 * c + 3]);
+}
+
 // ---- chain CTA shared memory: NBUF buffers, each the record then the K, Q, V tiles ----
 constexpr uint32_t C_K = 34816;       // K tile [64 tok][128 k]: 2 panels x 8 KB
 constexpr uint32_t C_Q = 51200;       // Q tile, same layout
@@ -198,7 +211,7 @@ struct SplitParams {
   const float* s0;           // [N,H,V,K] or NULL
   __nv_bfloat16* out;        // or NULL (state replay: no output)
   float* final_state;        // or NULL
-  float* ckpt;               // state replay: [slots,H,V,K] chunk-entry states, else NULL
+  float* ckpt;               // state replay: [slots,H] BF16 chunk-entry state tiles, else NULL
   int* status;               // workspace status word
   int* abort_g;              // global abort flag
   uint32_t* next_item;       // items claimed so far by the preparation CTAs
@@ -692,12 +705,15 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       }
       // entry state element (v, 64 w + e) without S0: zero, or the identity for the P twin
       auto s_init = [&](int e) -> float { return (ptwin && 64 * w + e == v) ? 1.f : 0.f; };
-      // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c]
-      // (checkpoint blocks in the threads' order: float4 e of thread st_t at 256 e + st_t)
-      float* ck = p.ckpt ? p.ckpt + ((size_t)chunk_slot_base(x / H, p.B, p.T, p.cu) * H + x % H) * D * D +
-                               (size_t)4 * st_t
-                         : nullptr;
-      const size_t ck_stride = (size_t)H * D * D;
+      // state replay: chunk c's entry state goes to ckpt[first slot of the sequence + c], a
+      // BF16 [128 v][128 k] tile in the 128-byte-swizzled panel layout (this thread: row v of
+      // panel w)
+      uint8_t* ck = p.ckpt ? reinterpret_cast<uint8_t*>(p.ckpt) +
+                                 ((size_t)chunk_slot_base(x / H, p.B, p.T, p.cu) * H + x % H) *
+                                     CKPT_TILE_BYTES +
+                                 (size_t)w * 16384 + (size_t)v * 128
+                           : nullptr;
+      const size_t ck_stride = (size_t)H * CKPT_TILE_BYTES;
       if (nc == 0) {
         // an empty sequence passes its initial state through (an empty range: the identity
         // map; an invalid range: NaN)
@@ -730,19 +746,12 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
 #pragma unroll
           for (int e = 0; e < 64; ++e) xv[e] = s_init(e);
         }
-        if (ck) {
-          float4* dst = reinterpret_cast<float4*>(ck);
+        uint32_t u[32];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            dst[256 * e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
-        }
-        uint32_t u[16];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
-          tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
-        }
+        for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
+        tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
+        tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
+        if (ck) store_ckpt_row(ck, v, u);
 #pragma unroll
         for (int e = 0; e < 64; ++e) xv[e] *= g0;
         tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -792,24 +801,17 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
               dst[e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
           }
         } else {
-          uint32_t u[16];
+          uint32_t u[32];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) u[e] = pack_bf16x2(xv[32 * hh + 2 * e], xv[32 * hh + 2 * e + 1]);
-            tmem_st16(tl + TM_SB + 32 * w + 16 * hh, u);
-          }
+          for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
+          tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
+          tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
           tmem_st_wait();
           tc_fence_before();
           named_bar(BAR_STATE, 256);
           if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
-          if (ck) {
-            // state replay: the next chunk's entry state, written while its first product runs
-            float4* dst = reinterpret_cast<float4*>(ck + (size_t)(c + 1) * ck_stride);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              dst[256 * e] = make_float4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]);
-          }
+          // state replay: the next chunk's entry state, written while its first product runs
+          if (ck) store_ckpt_row(ck + (size_t)(c + 1) * ck_stride, v, u);
           const int s1 = s + 1;
           if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))
             break;

@@ -13,8 +13,9 @@ size_t split_fwd_workspace(int N, int H);
 // Dense (p.cu == NULL) or packed (p.cu != NULL, p.B == 1) inputs, p.T > 0.  ws: workspace
 // of split_fwd_workspace(p.N, p.H) bytes whose first 256 bytes are not used; status: the
 // device status word.  With p.ckpt != NULL the launch is the backward's state replay: every
-// chunk's entry state is written to p.ckpt ([slots,H,V,K], slots as chunk_slot_base) and
-// p.out / p.final_state may be NULL.
+// chunk's entry state is written to p.ckpt ([slots,H] tiles of 32 KB, slots as
+// chunk_slot_base: BF16 [128 v][128 k] in the 128-byte-swizzled panel layout of tc_ptx.cuh)
+// and p.out / p.final_state may be NULL.
 cudaError_t launch_split_fwd(const ChainParams& p, void* ws, int* status, cudaStream_t st);
 
 // Workspace bytes of the segment summaries for R token ranges of H heads.

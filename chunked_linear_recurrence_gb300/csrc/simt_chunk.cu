@@ -757,8 +757,8 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
     // BF16: reverse chain and token gradients on the warp-level tensor cores
     if ((e = launch_mma_bwd_chain(p, p.fac, D, slots, st)) != cudaSuccess) return e;
     if (chain_only) return cudaSuccess;
-    // K = V = 128 after the split kernel's replay: token gradients on tcgen05
-    if (D == 128 && p.ckpt_tiled) return launch_tc_bwd_grad(p, slots, st);
+    // K = V = 128 (after the split kernel's replay): token gradients on tcgen05
+    if (D == 128) return launch_tc_bwd_grad(p, slots, st);
     return launch_mma_bwd_grad(p, true, D, slots, st);
   } else {
   // FP32 inputs keep FP32 products on the CUDA cores (1e-4 parity)

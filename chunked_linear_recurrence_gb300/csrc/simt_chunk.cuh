@@ -21,9 +21,9 @@ struct ChainParams {
   float* final_state;     // [N,H,V,K] or NULL
   float* P;               // [R,H,K,K] (summary)
   float* E;               // [R,H,V,K] (summary)
-  float* ckpt;            // [slots,H,V,K] chunk-entry states (replay / backward)
-  int ckpt_tiled;         // ckpt blocks in the state-thread order of ckpt_tiled_off (D = 128)
-  float* tape;            // [slots,H,V,K] chunk-exit cotangents (backward)
+  float* ckpt;            // [slots,H] chunk-entry states (replay / backward): FP32 [V,K], or
+                          // for BF16 with K = V = 128 BF16 swizzled [128][128] tiles (32 KB)
+  float* tape;            // [slots,H] chunk-exit cotangents (backward), laid out as ckpt
   const void* dout;       // [B,T,H,V] (backward)
   const float* dsf;       // [N,H,V,K] or NULL (backward)
   void* dq;
@@ -69,14 +69,6 @@ inline int64_t slot_grid(const ChainParams& p, int64_t slots) {
 cudaError_t launch_simt_chain(const ChainParams& p, int mode, bool bf16, int D, int items,
                               cudaStream_t st);
 // Backward after a replay: reverse cotangent chain then per-chunk token gradients.
-// Offset (floats) of state element (v, k) in a D = 128 checkpoint block written by the
-// split kernel's state threads: thread t = 128 (k / 64) + v stores its 64 values as 16
-// float4 at float4 index 256 e + t (e = (k mod 64) / 4), so that every store instruction
-// of a warp covers 512 contiguous bytes.
-__host__ __device__ inline int ckpt_tiled_off(int v, int k) {
-  return ((((k & 63) >> 2) << 8) + ((k >> 6) << 7) + v) * 4 + (k & 3);
-}
-
 // chain_only: only the reverse cotangent chain (and, for BF16, its per-chunk factors) --
 // the segments' cotangent maps need p.ds0 alone, no state replay and no token gradients.
 cudaError_t launch_simt_bwd(const ChainParams& p, bool bf16, int D, int64_t slots,
@@ -90,11 +82,12 @@ cudaError_t launch_group_sum(const float* acc, void* out, bool bf16, int64_t row
 size_t mma_bwd_fac_bytes(int D);
 cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_t slots,
                                  cudaStream_t st);
-// Per-chunk token gradients on the warp-level tensor cores (bwd_grad_mma.cu).
+// Per-chunk token gradients on the warp-level tensor cores (bwd_grad_mma.cu): BF16 or FP32
+// inputs with head size 64, FP32 [V,K] checkpoints and tape.
 cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t slots,
                                 cudaStream_t st);
-// Per-chunk token gradients on tcgen05 (bwd_grad_tc.cu): BF16, K = V = 128, checkpoints in
-// the split kernel's order (ckpt_tiled_off).
+// Per-chunk token gradients on tcgen05 (bwd_grad_tc.cu): BF16, K = V = 128, checkpoints and
+// tape as BF16 swizzled tiles.
 cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t st);
 
 }  // namespace sfg
