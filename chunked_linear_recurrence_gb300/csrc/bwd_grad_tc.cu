@@ -173,7 +173,7 @@ __device__ __forceinline__ int colsum_col(int lane) {
 }
 
 // mbarriers
-enum { B_SDO = 0, B_MMA, B_DRAIN, B_Q, B_KV, B_COUNT };
+enum { B_SDO = 0, B_MMA, B_DRAIN, B_Q, B_K, B_V, B_COUNT };
 constexpr uint32_t TILE_BYTES = 32768;   // one BF16 [128][128] S or dSn tile
 
 // One chunk-head: backward slot, value head, query/key head, first row, length.
@@ -212,6 +212,7 @@ struct Ctx {
   int tid, warp, lane, q4, wg;
   uint32_t lph, mph;   // completed phases of the per-chunk load barriers / of B_MMA
   uint32_t pend;       // thread 0: copies issued and not yet waited for (1 << B_SDO | ...)
+  float ng, nb;        // threads 0-63: the next chunk's gate and beta at this thread's row
   int* status;
   __device__ float* v(int which) const { return vec + which * 64; }
   // TMEM address of this warp's lane quarter at column `col`
@@ -273,20 +274,32 @@ __device__ __forceinline__ void fetch_q(Ctx& c, const Maps& m, const Item& it) {
   for (int pp = 0; pp < 2; ++pp)
     tma_load_3d(c.sm + O_QK + pp * QK_PANEL, m.q, &c.bars[B_Q], 64 * pp, it.hk, (int)it.c0);
 }
-// Thread 0: the chunk's K and V tiles.
-__device__ __forceinline__ void fetch_kv(Ctx& c, const Maps& m, const Item& it) {
-  c.pend |= 1u << B_KV;
-  mbar_arrive_expect_tx(&c.bars[B_KV], 4 * X_PANEL);
+// Thread 0: the chunk's K tile.
+__device__ __forceinline__ void fetch_k(Ctx& c, const Maps& m, const Item& it) {
+  c.pend |= 1u << B_K;
+  mbar_arrive_expect_tx(&c.bars[B_K], 2 * X_PANEL);
 #pragma unroll
-  for (int pp = 0; pp < 2; ++pp) {
-    tma_load_3d(c.sm + O_K + pp * QK_PANEL, m.k, &c.bars[B_KV], 64 * pp, it.hk, (int)it.c0);
-    tma_load_3d(c.sm + O_V + pp * X_PANEL, m.v, &c.bars[B_KV], 64 * pp, it.h, (int)it.c0);
-  }
+  for (int pp = 0; pp < 2; ++pp)
+    tma_load_3d(c.sm + O_K + pp * QK_PANEL, m.k, &c.bars[B_K], 64 * pp, it.hk, (int)it.c0);
+}
+// Thread 0: the chunk's V tile.
+__device__ __forceinline__ void fetch_v(Ctx& c, const Maps& m, const Item& it) {
+  c.pend |= 1u << B_V;
+  mbar_arrive_expect_tx(&c.bars[B_V], 2 * X_PANEL);
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp)
+    tma_load_3d(c.sm + O_V + pp * X_PANEL, m.v, &c.bars[B_V], 64 * pp, it.h, (int)it.c0);
+}
+// Threads 0-63: the chunk's gate and beta values (registers, stored at the chunk's start).
+__device__ __forceinline__ void fetch_gb(Ctx& c, const ChainParams& p, const Item& it) {
+  const size_t off = (size_t)(it.c0 + c.tid) * p.H + it.h;
+  c.ng = (c.tid < it.L) ? p.g[off] : 0.f;
+  c.nb = (c.tid < it.L) ? p.beta[off] : 0.f;
 }
 
-// One chunk.  Its S, dSn, dO and Q copies were issued before (for the next chunk `nx`
-// this chunk issues them); its K and V copies are issued here.  False when a wait
-// expired (the status word then says where).
+// One chunk.  Its copies (S, dSn, dO, Q, K, V; gate and beta into registers) were issued
+// before; this chunk issues those of the next chunk `nx` as its own tiles fall free.  False
+// when a wait expired (the status word then says where).
 __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const Item& it,
                            const Item& nx) {
   uint8_t* sm = c.sm;
@@ -307,15 +320,10 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
   float* vz = c.v(V_Z);
   float* vkt = c.v(V_KT);
 
-  // ---- inputs: K and V now; gate and beta; S, dSn, dO and Q are in flight already ----
-  if (tid == 0) {
-    fence_proxy_async_smem();   // the previous chunk's generic reads of the K and V tiles
-    fetch_kv(c, m, it);
-  }
+  // ---- inputs: every copy is in flight already ----
   if (tid < 64) {
-    const size_t off = (size_t)(c0 + tid) * H + h;
-    vg[tid] = (tid < L) ? p.g[off] : 0.f;
-    vb[tid] = (tid < L) ? p.beta[off] : 0.f;
+    vg[tid] = c.ng;
+    vb[tid] = c.nb;
     vdg[tid] = 0.f;
     vdb[tid] = 0.f;
     vz[tid] = 0.f;
@@ -353,7 +361,8 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
   if (ok && !(ok = mbar_wait(&c.bars[B_Q], par, WAIT_NS))) note_timeout(c, 3);
-  if (ok && !(ok = mbar_wait(&c.bars[B_KV], par, WAIT_NS))) note_timeout(c, 4);
+  if (ok && !(ok = mbar_wait(&c.bars[B_K], par, WAIT_NS))) note_timeout(c, 4);
+  if (ok && !(ok = mbar_wait(&c.bars[B_V], par, WAIT_NS))) note_timeout(c, 5);
   if (ok) {
     c.pend = 0;
     ++c.lph;
@@ -415,29 +424,10 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
       }
     }
   }
-  {
-    // S^T dO^T (features k on the lanes): scale column i by scale e^{gamma_i}, add
-    // q_i . (that column) to dgamma_i, and leave the scaled values for G K to accumulate on
-    float x[16], pr[16];
-    tmem_ld16(c.ta(TM_DQ + 16 * wg), x);
-    tmem_ld_wait();
-    const int k = 32 * q4 + lane, i0 = 16 * wg;
-#pragma unroll
-    for (int ii = 0; ii < 16; ++ii) {
-      x[ii] *= vsc[i0 + ii];
-      pr[ii] = x[ii] * bf_at(sm + O_QK, i0 + ii, k, QK_PANEL);
-    }
-    uint32_t u[16];
-#pragma unroll
-    for (int ii = 0; ii < 16; ++ii) u[ii] = __float_as_uint(x[ii]);
-    tmem_st16(c.ta(TM_DQ + 16 * wg), u);
-    const float s = warp_colsum16(pr, lane);
-    if (!(lane & 1)) atomicAdd(&vdg[i0 + colsum_col(lane)], s);
-    tmem_st_wait();
-  }
   if (!step_barrier(ok)) return false;
 
-  // ---- dDelta^T's first part: dO^T (scale Aqk); the solve meanwhile ----
+  // ---- dDelta^T's first part dO^T (scale Aqk); meanwhile warps 0-7 solve for T and warps
+  // 8-15 finish dq's first part and form dDelta^T ----
   if (tid == 0) {
     const uint64_t a = sdesc_sw128(sb + O_DO, X_PANEL, 1024);
     const uint64_t b = sdesc_sw128(sb + O_UN + U_AQK, X_PANEL, 1024);
@@ -446,35 +436,63 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
       mma_bf16(c.tm + TM_A, a + kstep_mn(kk), b + kstep_mn(kk), ID_MM, kk > 0);
     mma_commit(&c.bars[B_MMA]);
   }
-  float* AT = reinterpret_cast<float*>(sm + O_UN + U_AT);
-  solve64_tc_inplace(AT, reinterpret_cast<float*>(sm + O_UN + U_X), tid, NT,
-                     [] { __syncthreads(); });
-  ok = wait_products(c);
-  {
+  if (c.warp < 8) {
+    float* AT = reinterpret_cast<float*>(sm + O_UN + U_AT);
+    solve64_tc_inplace(AT, reinterpret_cast<float*>(sm + O_UN + U_X), tid, 256,
+                       [] { named_bar(1, 256); });
+    ok = wait_products(c);   // T' overwrites the Aqk tile that dO^T (scale Aqk) reads
     // T, T' = T diag(beta), T'' = T diag(beta e^gamma) as BF16 tiles [i][j]
-    const int i = tid >> 3, j0 = 8 * (tid & 7);
-    const float* at = AT + i * SOLVE_LD + j0;
-    float t[8], t1[8], t2[8];
+    for (int idx = tid; idx < 64 * 8; idx += 256) {
+      const int i = idx >> 3, j0 = 8 * (idx & 7);
+      const float* at = AT + i * SOLVE_LD + j0;
+      float t[8], t1[8], t2[8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      t[jj] = at[jj];
-      t1[jj] = t[jj] * vb[j0 + jj];
-      t2[jj] = t[jj] * vbeg[j0 + jj];
+      for (int jj = 0; jj < 8; ++jj) {
+        t[jj] = at[jj];
+        t1[jj] = t[jj] * vb[j0 + jj];
+        t2[jj] = t[jj] * vbeg[j0 + jj];
+      }
+      st_row8_bf16(sm + O_TT, i, j0, X_PANEL, t);
+      st_row8_bf16(sm + O_UN + U_T1, i, j0, X_PANEL, t1);
+      st_row8_bf16(sm + O_UN + U_T2, i, j0, X_PANEL, t2);
     }
-    st_row8_bf16(sm + O_TT, i, j0, X_PANEL, t);
-    st_row8_bf16(sm + O_UN + U_T1, i, j0, X_PANEL, t1);
-    st_row8_bf16(sm + O_UN + U_T2, i, j0, X_PANEL, t2);
-  }
-  {
-    // dDelta^T = dO^T (scale Aqk) + (dSn K^T) diag(dec)
-    float x1[16], x2[16];
-    tmem_ld16(c.ta(TM_A + 16 * wg), x1);
-    tmem_ld16(c.ta(TM_B + 16 * wg), x2);
-    tmem_ld_wait();
-    const int v = 32 * q4 + lane, i0 = 16 * wg;
+  } else {
+    // two warps per lane quarter, 32 columns each
+    const int r = 32 * q4 + lane, cbase = 32 * ((c.warp - 8) >> 2);
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) x1[ii] += vdec[i0 + ii] * x2[ii];
-    st_row16(sm + O_DDT, v, i0, x1);
+    for (int hh = 0; hh < 2; ++hh) {
+      // S^T dO^T (features k on the lanes): scale column i by scale e^{gamma_i}, add
+      // q_i . (that column) to dgamma_i, and leave the scaled values for G K to accumulate on
+      const int i0 = cbase + 16 * hh;
+      float x[16], pr[16];
+      tmem_ld16(c.ta(TM_DQ + i0), x);
+      tmem_ld_wait();
+#pragma unroll
+      for (int ii = 0; ii < 16; ++ii) {
+        x[ii] *= vsc[i0 + ii];
+        pr[ii] = x[ii] * bf_at(sm + O_QK, i0 + ii, r, QK_PANEL);
+      }
+      uint32_t u[16];
+#pragma unroll
+      for (int ii = 0; ii < 16; ++ii) u[ii] = __float_as_uint(x[ii]);
+      tmem_st16(c.ta(TM_DQ + i0), u);
+      const float sum = warp_colsum16(pr, lane);
+      if (!(lane & 1)) atomicAdd(&vdg[i0 + colsum_col(lane)], sum);
+    }
+    tmem_st_wait();
+    ok = wait_products(c);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      // dDelta^T = dO^T (scale Aqk) + (dSn K^T) diag(dec)
+      const int i0 = cbase + 16 * hh;
+      float x1[16], x2[16];
+      tmem_ld16(c.ta(TM_A + i0), x1);
+      tmem_ld16(c.ta(TM_B + i0), x2);
+      tmem_ld_wait();
+#pragma unroll
+      for (int ii = 0; ii < 16; ++ii) x1[ii] += vdec[i0 + ii] * x2[ii];
+      st_row16(sm + O_DDT, r, i0, x1);
+    }
   }
   if (!step_barrier(ok)) return false;
 
@@ -546,7 +564,25 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
       mma_bf16(c.tm + TM_B, addm + kstep_mn(kk), bv + kstep_k(kk, X_PANEL), ID_MK, kk > 0);
     mma_commit(&c.bars[B_MMA]);
   }
-  ok = wait_products(c);
+  {
+    // (while those run) X^T = dDelta^T T, features v on the lanes: dv = diag(beta) X;
+    // dbeta += v . X
+    const int r = 32 * q4 + lane, i0 = 16 * wg;
+    float x[16], pv[16];
+    tmem_ld16(c.ta(TM_X + 16 * wg), x);
+    tmem_ld_wait();
+    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
+    const size_t base = ((size_t)(c0 + i0) * H + h) * D + r;
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+      const int i = i0 + ii;
+      pv[ii] = bf_at(sm + O_V, i, r, X_PANEL) * x[ii];
+      if (i < L) dv[base + (size_t)ii * H * D] = __float2bfloat16_rn(vb[i] * x[ii]);
+    }
+    const float sum = warp_colsum16(pv, lane);
+    if (!(lane & 1)) atomicAdd(&vdb[i0 + colsum_col(lane)], sum);
+  }
+  ok = wait_products(c) && ok;
   {
     // Delta^T -> BF16 tile (over -W^T, whose product has completed)
     float x[16];
@@ -584,13 +620,30 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(c.tm + TM_B, adt + kstep_k(kk, X_PANEL), bt + kstep_k(kk, X_PANEL), ID_KK, kk > 0);
     mma_commit(&c.bars[B_MMA]);
+    if (nx.valid) {
+      // the next chunk's V (every read of this chunk's V is behind the barrier above)
+      fence_proxy_async_smem();
+      fetch_v(c, m, nx);
+    }
   }
-  ok = wait_products(c);
+  {
+    // (while those run) Y^T = dW^T T, features k on the lanes: kt_i = k_i . Y_i
+    const int r = 32 * q4 + lane, i0 = 16 * wg;
+    float x[16];
+    tmem_ld16(c.ta(TM_Y + 16 * wg), x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) x[ii] *= bf_at(sm + O_K, i0 + ii, r, QK_PANEL);
+    const float sum = warp_colsum16(x, lane);
+    if (!(lane & 1)) atomicAdd(&vkt[i0 + colsum_col(lane)], sum);
+  }
+  ok = wait_products(c) && ok;
   if (tid == 0 && nx.valid) {
     // the next chunk's S, dSn and dO (the last products reading this chunk's have completed)
     fence_proxy_async_smem();
     fetch_sdo(c, p, m, nx);
   }
+  if (tid < 64 && nx.valid) fetch_gb(c, p, nx);
   if (q4 < 2) {
     // dAqk = scale dO Delta^T: G = dAqk o Gamma (lower incl. diagonal) -> tile; rho =
     // G o (Q K^T) -> dgamma_i += row sum, dgamma_j -= column sum.  X1 -> tile.
@@ -639,7 +692,18 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
       mma_bf16(c.tm + TM_A, att + kstep_mn(kk), bx1 + kstep_mn(kk), ID_MM, kk > 0);
     mma_commit(&c.bars[B_MMA]);
   }
-  ok = wait_products(c);
+  {
+    // (while those run) Z^T = dSn^T Delta^T, features k on the lanes: z_i = k_i . Z_i
+    const int r = 32 * q4 + lane, i0 = 16 * wg;
+    float x[16];
+    tmem_ld16(c.ta(TM_Z + 16 * wg), x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) x[ii] *= bf_at(sm + O_K, i0 + ii, r, QK_PANEL);
+    const float sum = warp_colsum16(x, lane);
+    if (!(lane & 1)) atomicAdd(&vz[i0 + colsum_col(lane)], sum);
+  }
+  ok = wait_products(c) && ok;
   if (tid == 0 && nx.valid) {
     // the next chunk's Q (the last product reading this chunk's Q has completed)
     fence_proxy_async_smem();
@@ -690,14 +754,52 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
     mma_commit(&c.bars[B_MMA]);
   }
   ok = wait_products(c);
+  if (tid == 0 && nx.valid) {
+    // the next chunk's K (the last product reading this chunk's K has completed)
+    fence_proxy_async_smem();
+    fetch_k(c, m, nx);
+  }
+  if (tid < 32) {
+    // dgate and dbeta (every contribution is in by now): the exit-state decay (dk gained
+    // dec o Z, so dgamma_i -= dec_i z_i and the chunk's last position collects their sum),
+    // Y (dbeta += e^gamma kt, dgamma += beta e^gamma kt); dgate = reverse cumulative sum of
+    // dgamma.  Lane l holds rows 2l and 2l + 1.
+    float d[2], db[2], tz = 0.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = 2 * lane + e;
+      const float t = vdec[i] * vz[i];
+      tz += t;
+      d[e] = vdg[i] - t + vbeg[i] * vkt[i];
+      db[e] = vdb[i] + veg[i] * vkt[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tz += __shfl_xor_sync(0xffffffffu, tz, o);
+    if (lane == 31) d[1] += tz;
+    float suf = d[0] + d[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += t;
+    }
+    const float r[2] = {suf, suf - d[0]};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = 2 * lane + e;
+      if (i < L) {
+        const size_t off = (size_t)(c0 + i) * H + h;
+        p.dg[off] = r[e];
+        p.dbeta[off] = db[e];
+      }
+    }
+  }
 
-  // ---- gradient rows (features on the lanes, tokens on the columns) ----
+  // ---- dq and dk rows (features on the lanes, tokens on the columns) ----
   {
     const int r = 32 * q4 + lane, i0 = 16 * wg;
     const size_t row_stride = (size_t)H * D;
     const size_t base = ((size_t)(c0 + i0) * H + h) * D + r;
-    float x[16], y[16], z[16], pz[16], py[16];
-    // dq
+    float x[16], y[16], z[16];
     tmem_ld16(c.ta(TM_DQ + 16 * wg), x);
     tmem_ld_wait();
     if (p.dqk_f32) {
@@ -717,13 +819,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
     tmem_ld16(c.ta(TM_Y + 16 * wg), y);
     tmem_ld_wait();
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) {
-      const int i = i0 + ii;
-      const float kv = bf_at(sm + O_K, i, r, QK_PANEL);
-      x[ii] += vdec[i] * z[ii] + vbeg[i] * y[ii];
-      pz[ii] = kv * z[ii];
-      py[ii] = kv * y[ii];
-    }
+    for (int ii = 0; ii < 16; ++ii) x[ii] += vdec[i0 + ii] * z[ii] + vbeg[i0 + ii] * y[ii];
     if (p.dqk_f32) {
       float* dk = reinterpret_cast<float*>(p.dk);
 #pragma unroll
@@ -735,54 +831,8 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
       for (int ii = 0; ii < 16; ++ii)
         if (i0 + ii < L) dk[base + ii * row_stride] = __float2bfloat16_rn(x[ii]);
     }
-    float s = warp_colsum16(pz, lane);
-    if (!(lane & 1)) atomicAdd(&vz[i0 + colsum_col(lane)], s);
-    s = warp_colsum16(py, lane);
-    if (!(lane & 1)) atomicAdd(&vkt[i0 + colsum_col(lane)], s);
-    // dv = diag(beta) X; dbeta += v . X
-    tmem_ld16(c.ta(TM_X + 16 * wg), x);
-    tmem_ld_wait();
-    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
-#pragma unroll
-    for (int ii = 0; ii < 16; ++ii) {
-      const int i = i0 + ii;
-      pz[ii] = bf_at(sm + O_V, i, r, X_PANEL) * x[ii];
-      if (i < L) dv[base + ii * row_stride] = __float2bfloat16_rn(vb[i] * x[ii]);
-    }
-    s = warp_colsum16(pz, lane);
-    if (!(lane & 1)) atomicAdd(&vdb[i0 + colsum_col(lane)], s);
   }
   tc_fence_before();
-  __syncthreads();
-  if (tid < 64) {
-    // exit-state decay: dk gained dec o Z, so dgamma_i -= dec_i (k_i . Z_i) and the chunk's
-    // last position collects the sum; Y: dbeta += e^gamma kt, dgamma += beta e^gamma kt
-    const float t = vdec[tid] * vz[tid];
-    atomicAdd(&vdg[tid], -t);
-    atomicAdd(&vdg[63], t);
-    vdb[tid] += veg[tid] * vkt[tid];
-    atomicAdd(&vdg[tid], vbeg[tid] * vkt[tid]);
-  }
-  __syncthreads();
-  if (tid < 32) {
-    // dgate = reverse cumulative sum of dgamma
-    const float a = vdg[63 - 2 * lane], b = vdg[62 - 2 * lane];
-    float s = a + b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += t;
-    }
-    const float excl = s - (a + b);
-    vgam[63 - 2 * lane] = excl + a;
-    vgam[62 - 2 * lane] = excl + a + b;
-  }
-  __syncthreads();
-  if (tid < L) {
-    const size_t off = (size_t)(c0 + tid) * H + h;
-    p.dg[off] = vgam[tid];
-    p.dbeta[off] = vdb[tid];
-  }
   return ok;
 }
 
@@ -804,6 +854,7 @@ __global__ void __launch_bounds__(NT, 1)
   c.lph = 0;
   c.mph = 0;
   c.pend = 0;
+  c.ng = c.nb = 0.f;
   c.status = p.status;
   const Maps m{&mq, &mk, &mv, &mdo};
   uint32_t* tslot = reinterpret_cast<uint32_t*>(c.sm + O_BAR + 8 * B_COUNT);
@@ -826,13 +877,16 @@ __global__ void __launch_bounds__(NT, 1)
   if (c.tid == 0 && it.valid) {
     fetch_sdo(c, p, m, it);
     fetch_q(c, m, it);
+    fetch_k(c, m, it);
+    fetch_v(c, m, it);
   }
+  if (c.tid < 64 && it.valid) fetch_gb(c, p, it);
   bool ok = true;
   for (int64_t item = blockIdx.x; it.valid; item += gridDim.x) {
     const Item nx = locate_item(p, item + gridDim.x);
     ok = grad_chunk(c, p, m, it, nx);
     if (!ok) break;
-    __syncthreads();   // the next chunk's K and V overwrite tiles read above
+    __syncthreads();   // the next chunk's vectors overwrite those read above
     it = nx;
   }
   if (!ok && c.tid == 0) {
