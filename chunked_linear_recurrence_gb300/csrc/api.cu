@@ -352,6 +352,7 @@ sf_status sf_gdn_segment_reverse_summary(const sf_gdn_shape* shape, const void* 
   p.ds0 = C;              // the cotangent the chain leaves at the segment's start
   p.tape = reinterpret_cast<float*>(ws + kStatusBytes);
   p.fac = lay.fac ? reinterpret_cast<float*>(ws + kStatusBytes + lay.tape) : nullptr;
+  p.status = reinterpret_cast<int*>(workspace);
   p.B = shape->B; p.T = shape->T; p.H = shape->H; p.N = shape->N; p.scale = eff_scale(shape);
   p.HK = eff_hk(shape);
   const int64_t slots = bwd_slots(shape, true);

@@ -17,10 +17,12 @@
 //     at the sequence start is d_initial_state.
 #include <type_traits>
 
+#include "bwd_chain_tc.cuh"
 #include "common.cuh"
 #include "mma_tiles.cuh"
 #include "simt_chunk.cuh"
 #include "solve_tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace sfg {
 namespace {
@@ -45,10 +47,26 @@ struct CtaBarB {
 
 }  // namespace
 
-// Per-chunk factors of the backward chain: fac[(slot * H + h)] = { Aqk [64][64], W [64][D],
-// e^gamma [64], dec [64] } (FP32; rows past the sequence end are zero).
+// Per-chunk factors of the backward chain, rows past the sequence end zero: head size 64:
+// fac[(slot * H + h)] = { Aqk [64][64], W [64][D], e^gamma [64], dec [64] } (FP32); head
+// size 128: the BF16 tiles and decays of bwd_chain_tc.cuh (FB_BYTES).
 template <int D>
-__host__ __device__ constexpr size_t fac_bytes() { return 4 * (64 * 64 + 64 * D + 128); }
+__host__ __device__ constexpr size_t fac_bytes() {
+  return D == 128 ? (size_t)FB_BYTES : 4 * (64 * 64 + 64 * D + 128);
+}
+
+// As mt::each, two adjacent columns at a time: f(row, col, x[col], x[col + 1]).
+template <int NTILE, int NTN, int NW, bool BLK, typename F>
+__device__ __forceinline__ void each_pair(float (&acc)[NTILE][4], int warp, int lane, F&& f) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ti = 0; ti < NTILE; ++ti) {
+    int m0, n0;
+    TileMap<NTILE, NTN, NW, BLK>::at(warp, ti, m0, n0);
+    f(m0 + g, n0 + 2 * t, acc[ti][0], acc[ti][1]);
+    f(m0 + g + 8, n0 + 2 * t, acc[ti][2], acc[ti][3]);
+  }
+}
 
 // One chunk (backward slot `slot`); false when the slot holds no chunk.
 template <int D>
@@ -93,11 +111,19 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
   float* oAqk = out;
   float* oW = out + 64 * 64;
   float* ovec = oW + 64 * D;
+  uint8_t* ob = reinterpret_cast<uint8_t*>(out);   // head size 128: the BF16 tile layout
+  const float scale = p.scale;
   if (tid < 64) {
     const float eg = expf(sgam[tid]);
     sbeg[tid] = sb[tid] * eg;
-    ovec[tid] = eg;
-    ovec[64 + tid] = expf(sgam[63] - sgam[tid]);
+    if constexpr (D == 128) {
+      float* fv = reinterpret_cast<float*>(ob + FB_VEC);
+      fv[tid] = expf(sgam[63] - sgam[tid]);
+      if (tid == 0) fv[64] = expf(sgam[63]);
+    } else {
+      ovec[tid] = eg;
+      ovec[64 + tid] = expf(sgam[63] - sgam[tid]);
+    }
   }
   const auto Kv = view(sK, LDI, 1);
   {
@@ -110,18 +136,45 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
     each<4, 8, 8, true>(a1, warp, lane, [&](int i, int j, float& x) {
       sA[i * LD6 + j] = (j < i) ? sb[i] * expf(sgam[i] - sgam[j]) * x : 0.f;
     });
-    each<4, 8, 8, true>(a2, warp, lane, [&](int i, int j, float& x) {
-      oAqk[i * 64 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
-    });
+    if constexpr (D == 128) {
+      each_pair<4, 8, 8, true>(a2, warp, lane, [&](int i, int j, float x0, float x1) {
+        const float y0 = (j <= i) ? scale * expf(sgam[i] - sgam[j]) * x0 : 0.f;
+        const float y1 = (j + 1 <= i) ? scale * expf(sgam[i] - sgam[j + 1]) * x1 : 0.f;
+        *reinterpret_cast<uint32_t*>(ob + FB_AQK + tc::sw128_off(i, j, 8192)) =
+            tc::pack_bf16x2(y0, y1);
+      });
+    } else {
+      each<4, 8, 8, true>(a2, warp, lane, [&](int i, int j, float& x) {
+        oAqk[i * 64 + j] = (j <= i) ? expf(sgam[i] - sgam[j]) * x : 0.f;
+      });
+    }
   }
   __syncthreads();
+  if constexpr (D == 128) {
+    // Qg = scale diag(e^gamma) Q, eight columns (16 bytes) per store
+    for (int idx = tid; idx < 64 * 16; idx += NTB) {
+      const int i = idx >> 4, c = (idx & 15) * 8;
+      const float f = scale * expf(sgam[i]);
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(sQ[i * LDI + c + e]);
+      tc::st_row8_bf16(ob + FB_QG, i, c, 8192, x);
+    }
+  }
   static_assert(LD6 == SOLVE_LD, "solve layout");
   solve64_tc(sA, sT, sX, tid, NTB, CtaBarB());   // merges on TF32 mma, as in the forward
   {
     float acc[TD][4];
     zero(acc);
     gemm<TD, NTD, 8, true>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
-    each<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
+    if constexpr (D == 128) {
+      each_pair<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float x0, float x1) {
+        *reinterpret_cast<uint32_t*>(ob + FB_NW + tc::sw128_off(i, c, 8192)) =
+            tc::pack_bf16x2(-x0, -x1);
+      });
+    } else {
+      each<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
+    }
   }
   return true;
 }
@@ -332,7 +385,16 @@ static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slot
 
 cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_t slots,
                                  cudaStream_t st) {
-  if (D == 128) return launch_chain_d<128>(p, fac, slots, st);
+  if (D == 128) {
+    // factors (BF16 tiles) here, then the reverse chain on tcgen05 (bwd_chain_tc.cu)
+    const size_t smem = sizeof(float) * (3 * 64 * C_LD6 + 4 * 64) + 2 * 2 * 64 * (128 + 8);
+    auto kern = mma_bwd_factor_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTB, smem, st>>>(p, fac, slots);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_tc_bwd_chain(p, fac, st);
+  }
   if (D == 64) return launch_chain_d<64>(p, fac, slots, st);
   return cudaErrorInvalidValue;
 }
