@@ -56,7 +56,8 @@ def fwd_traffic():
     import hashlib
     csrc = os.path.join(ROOT, "chunked_linear_recurrence_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("fwd_split.cu", "tmap.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh"):
+    for f in ("fwd_split.cu", "tmap.cu", "tc_ptx.cuh", "solve_tc.cuh", "common.cuh",
+              "chunk_record.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     try:

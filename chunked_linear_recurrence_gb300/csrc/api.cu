@@ -431,6 +431,7 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
   if (bf16 && D == 128 && shape->T > 0) {
     e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
                               reinterpret_cast<int*>(workspace), cs);
+    p.fac_ready = 1;    // the replay kept every chunk's record in p.fac
   } else if (shape->T > 0) {
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
   } else {

@@ -18,6 +18,7 @@
 #include <type_traits>
 
 #include "bwd_chain_tc.cuh"
+#include "chunk_record.cuh"
 #include "common.cuh"
 #include "mma_tiles.cuh"
 #include "simt_chunk.cuh"
@@ -49,10 +50,11 @@ struct CtaBarB {
 
 // Per-chunk factors of the backward chain, rows past the sequence end zero: head size 64:
 // fac[(slot * H + h)] = { Aqk [64][64], W [64][D], e^gamma [64], dec [64] } (FP32); head
-// size 128: the BF16 tiles and decays of bwd_chain_tc.cuh (FB_BYTES).
+// size 128: the backward's chunk record of chunk_record.cuh (Ahat, (-W)^T, the decays and
+// Qg; T' unused).
 template <int D>
 __host__ __device__ constexpr size_t fac_bytes() {
-  return D == 128 ? (size_t)FB_BYTES : 4 * (64 * 64 + 64 * D + 128);
+  return D == 128 ? (size_t)REC2_BYTES : 4 * (64 * 64 + 64 * D + 128);
 }
 
 // As mt::each, two adjacent columns at a time: f(row, col, x[col], x[col + 1]).
@@ -85,6 +87,7 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = p.H;
   const int hk = qk_head(h, H, p.HK);
+  const float scale = p.scale;
   int n;
   int64_t bos, eos, ci;
   if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) return false;
@@ -112,14 +115,14 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
   float* oW = out + 64 * 64;
   float* ovec = oW + 64 * D;
   uint8_t* ob = reinterpret_cast<uint8_t*>(out);   // head size 128: the BF16 tile layout
-  const float scale = p.scale;
   if (tid < 64) {
     const float eg = expf(sgam[tid]);
     sbeg[tid] = sb[tid] * eg;
     if constexpr (D == 128) {
-      float* fv = reinterpret_cast<float*>(ob + FB_VEC);
-      fv[tid] = expf(sgam[63] - sgam[tid]);
-      if (tid == 0) fv[64] = expf(sgam[63]);
+      float* fv = reinterpret_cast<float*>(ob + R_VEC);
+      fv[V_DEC / 4 + tid] = expf(sgam[63] - sgam[tid]);
+      fv[V_EG / 4 + tid] = eg;
+      if (tid == 0) fv[V_GC / 4] = expf(sgam[63]);
     } else {
       ovec[tid] = eg;
       ovec[64 + tid] = expf(sgam[63] - sgam[tid]);
@@ -138,9 +141,9 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
     });
     if constexpr (D == 128) {
       each_pair<4, 8, 8, true>(a2, warp, lane, [&](int i, int j, float x0, float x1) {
-        const float y0 = (j <= i) ? scale * expf(sgam[i] - sgam[j]) * x0 : 0.f;
-        const float y1 = (j + 1 <= i) ? scale * expf(sgam[i] - sgam[j + 1]) * x1 : 0.f;
-        *reinterpret_cast<uint32_t*>(ob + FB_AQK + tc::sw128_off(i, j, 8192)) =
+        const float y0 = (j <= i) ? expf(sgam[i] - sgam[j]) * x0 : 0.f;
+        const float y1 = (j + 1 <= i) ? expf(sgam[i] - sgam[j + 1]) * x1 : 0.f;
+        *reinterpret_cast<uint32_t*>(ob + R_AH + tc::sw128_off(i, j, 8192)) =
             tc::pack_bf16x2(y0, y1);
       });
     } else {
@@ -158,7 +161,7 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
       float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(sQ[i * LDI + c + e]);
-      tc::st_row8_bf16(ob + FB_QG, i, c, 8192, x);
+      tc::st_row8_bf16(ob + R_QG, i, c, 8192, x);
     }
   }
   static_assert(LD6 == SOLVE_LD, "solve layout");
@@ -168,9 +171,12 @@ __device__ __forceinline__ bool factor_chunk(const ChainParams& p, float* fac, i
     zero(acc);
     gemm<TD, NTD, 8, true>(acc, cols_scaled(view(sT, LD6, 1), sbeg), Kv, 64, warp, lane);
     if constexpr (D == 128) {
+      // (-W)^T [128 k][64 i]: element (i, c) of W at row c, column i
       each_pair<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float x0, float x1) {
-        *reinterpret_cast<uint32_t*>(ob + FB_NW + tc::sw128_off(i, c, 8192)) =
-            tc::pack_bf16x2(-x0, -x1);
+        *reinterpret_cast<__nv_bfloat16*>(ob + R_W + tc::sw128_off(c, i, 16384)) =
+            __float2bfloat16_rn(-x0);
+        *reinterpret_cast<__nv_bfloat16*>(ob + R_W + tc::sw128_off(c + 1, i, 16384)) =
+            __float2bfloat16_rn(-x1);
       });
     } else {
       each<TD, NTD, 8, true>(acc, warp, lane, [&](int i, int c, float& x) { oW[i * D + c] = x; });
@@ -386,12 +392,18 @@ static cudaError_t launch_chain_d(const ChainParams& p, float* fac, int64_t slot
 cudaError_t launch_mma_bwd_chain(const ChainParams& p, float* fac, int D, int64_t slots,
                                  cudaStream_t st) {
   if (D == 128) {
-    // factors (BF16 tiles) here, then the reverse chain on tcgen05 (bwd_chain_tc.cu)
-    const size_t smem = sizeof(float) * (3 * 64 * C_LD6 + 4 * 64) + 2 * 2 * 64 * (128 + 8);
-    auto kern = mma_bwd_factor_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTB, smem, st>>>(p, fac, slots);
+    // the chunk records: kept by the state replay, else made here; then the reverse chain
+    // on tcgen05 (bwd_chain_tc.cu)
+    cudaError_t e;
+    if (!p.fac_ready) {
+      const size_t smem = sizeof(float) * (3 * 64 * C_LD6 + 4 * 64) + 2 * 2 * 64 * (128 + 8);
+      auto kern = mma_bwd_factor_kernel<128>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (slots > 0) kern<<<dim3((unsigned)slot_grid(p, slots), p.H), NTB, smem, st>>>(p, fac, slots);
+    } else {
+      launch_tc_bwd_qg(p, fac, slots, st);   // the replay's records lack only Qg
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_tc_bwd_chain(p, fac, st);
   }

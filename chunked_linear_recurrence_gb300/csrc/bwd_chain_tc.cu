@@ -3,18 +3,20 @@
 //
 // StateFlow section 3.1, Eq. 6-7 (the chunk algebra differentiated): walking a sequence
 // backwards, per chunk with exit cotangent dS,
-//     dDelta^T = dO^T (scale Aqk) + (dS K^T) diag(dec)
-//     dS      <- e^{gamma_C} dS + dO^T Qg - dDelta^T W,     Qg = scale diag(e^gamma) Q,
+//     dDelta^T = scale dO^T Aqk + (dS K^T) diag(dec)
+//     dS      <- e^{gamma_C} dS + (diag(scale e^gamma) dO)^T Q - dDelta^T W,
 // and the cotangent left at the sequence start is d_initial_state.  One CTA per
 // (sequence, head) chain keeps dS FP32 in TMEM (the 128 v rows on the lanes, the 128 k
 // columns) with a BF16 copy there as the A operand of dS K^T.  Per chunk (all M = 128):
-//   P1  = dO^T (scale Aqk)      N = 64,  K = 64    (independent of dS: issued ahead)
+//   P1  = dO^T Aqk              N = 64,  K = 64    (independent of dS: issued ahead)
 //   X   = dS K^T                N = 64,  K = 128   (the chain's critical path)
-//   dS += dO^T Qg               N = 128, K = 64    (once the state warps scaled dS)
+//   dS += dO^T Qg               N = 128, K = 64    (Qg = scale diag(e^gamma) Q; once the
+//                                                   state warps scaled dS)
 //   dS += dDelta^T (-W)         N = 128, K = 64    (A: dDelta^T BF16 in TMEM)
-// The factors (scale Aqk, -W, Qg as BF16 tiles, the decays) are one record per chunk-head
-// from mma_bwd_factor_kernel<128>, copied in one bulk copy; dO and K come by TMA; two chunks
-// are in flight.  Each chunk's exit cotangent goes to the tape as the BF16 swizzled tile the
+// The factors are the backward's chunk records of chunk_record.cuh (Aqk = Ahat, (-W)^T, the
+// decays and Qg), kept by the state replay with Qg added by qg_kernel below (or made whole by
+// mma_bwd_factor_kernel<128>), one bulk copy each; K and dO come by TMA; two chunks are in
+// flight.  Each chunk's exit cotangent goes to the tape as the BF16 swizzled tile the
 // token-gradient kernel reads.
 //
 // Warps: 0 loads, 1 issues the products (one thread), 4-11 hold the cotangent (two
@@ -41,15 +43,15 @@ constexpr int D = 128;
 constexpr int NT = 384;
 constexpr int NB = 2;                   // chunk buffers
 constexpr uint32_t PANEL = 8192;        // 64-row tile panel
-constexpr uint32_t B_FAC = 0;           // the factor record (FB_* offsets)
-constexpr uint32_t B_K = 41984;         // K [64 j][128 k]
-constexpr uint32_t B_DO = 58368;        // dO [64 i][128 v]
-constexpr uint32_t BUF = 74752;
+constexpr uint32_t B_FAC = 0;           // the chunk record (R_* offsets, with Qg)
+constexpr uint32_t B_K = 50176;         // K [64 j][128 k]
+constexpr uint32_t B_DO = 66560;        // dO [64 i][128 v]
+constexpr uint32_t BUF = 82944;
 constexpr uint32_t O_BAR = NB * BUF;
 constexpr uint32_t SMEM_ALLOC = O_BAR + 256 + 1024;
-static_assert(B_K >= FB_BYTES && B_K % 1024 == 0 && B_DO == B_K + 2 * PANEL &&
+static_assert(B_K >= REC2_BYTES && B_K % 1024 == 0 && B_DO == B_K + 2 * PANEL &&
               BUF == B_DO + 2 * PANEL && BUF % 1024 == 0, "chain buffer");
-static_assert(FB_AQK % 1024 == 0 && FB_NW % 1024 == 0 && FB_QG % 1024 == 0, "tile alignment");
+static_assert(R_W % 1024 == 0 && R_AH % 1024 == 0 && R_QG % 1024 == 0, "tile alignment");
 static_assert(SMEM_ALLOC <= 232448, "shared memory");
 
 // TMEM columns (512 allocated)
@@ -62,7 +64,7 @@ constexpr uint32_t TM_DDB = 320;   // dDelta^T BF16 pairs (32 columns)
 constexpr uint32_t ID_P1 = idesc_bf16(128, 64, true, true);    // A, B MN-major
 constexpr uint32_t ID_X = idesc_bf16(128, 64, false, false);   // A in TMEM, B K-major
 constexpr uint32_t ID_U1 = idesc_bf16(128, 128, true, true);   // A, B MN-major, N = 128
-constexpr uint32_t ID_U2 = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
+constexpr uint32_t ID_U2 = idesc_bf16(128, 128, false, false); // A in TMEM, B K-major, N = 128
 
 enum { C_FULL = 0, C_LANDED = 2, C_FREE = 4, C_XDONE = 6, C_DREADY, C_SREADY, C_SSCALED,
        C_SUDONE, C_DRAIN, C_COUNT };
@@ -113,6 +115,57 @@ __device__ __forceinline__ void store_tile_row(uint8_t* row, int v, const uint32
   for (int c = 0; c < 8; ++c)
     *reinterpret_cast<uint4*>(row + ((c ^ (v & 7)) << 4)) =
         make_uint4(u[4 * c], u[4 * c + 1], u[4 * c + 2], u[4 * c + 3]);
+}
+
+// Qg = scale diag(e^gamma) Q of every chunk-head into its record (gamma: the in-chunk
+// cumulative gate; rows past the sequence end zero).  One CTA of 256 threads per (slot, head),
+// slots walked with a grid stride until the first empty one; thread t takes row t / 4 and
+// columns [32 (t mod 4), + 32).
+__global__ void __launch_bounds__(256) qg_kernel(const ChainParams p, uint8_t* fac, int64_t slots) {
+  __shared__ float se[64];
+  const int tid = threadIdx.x, lane = tid & 31, h = blockIdx.y, H = p.H;
+  const int hk = qk_head(h, H, p.HK);
+  const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
+    int n = -1;
+    int64_t bos = 0, eos = 0, ci = 0;
+    if (!locate_chunk(slot, p.B, p.T, p.cu, p.N, n, bos, eos, ci)) break;
+    const int64_t c0 = bos + ci * CHUNK;
+    const int L = (int)((eos - c0) < CHUNK ? (eos - c0) : CHUNK);
+    if (tid < 32) {
+      const int e0 = 2 * lane, e1 = e0 + 1;
+      const float g0 = e0 < L ? p.g[(size_t)(c0 + e0) * H + h] : 0.f;
+      const float g1 = e1 < L ? p.g[(size_t)(c0 + e1) * H + h] : 0.f;
+      float sum = g0 + g1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, sum, o);
+        if (lane >= o) sum += t;
+      }
+      const float excl = sum - (g0 + g1);
+      se[e0] = p.scale * expf(excl + g0);
+      se[e1] = p.scale * expf(excl + g0 + g1);
+    }
+    __syncthreads();
+    const int i = tid >> 2, c = 32 * (tid & 3);
+    uint8_t* tile = fac + ((size_t)slot * H + h) * REC2_BYTES + R_QG;
+    const float f = se[i];
+    const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(c0 + i) * p.HK + hk) * D + c);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint4 v4 = i < L ? src[cc] : make_uint4(0, 0, 0, 0);
+      const uint32_t va[4] = {v4.x, v4.y, v4.z, v4.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&va[e]));
+        x[2 * e] = f * fv.x;
+        x[2 * e + 1] = f * fv.y;
+      }
+      st_row8_bf16(tile, i, c + 8 * cc, PANEL, x);
+    }
+    __syncthreads();   // se is rewritten by the next chunk
+  }
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -171,9 +224,9 @@ __global__ void __launch_bounds__(NT, 1)
       if (part) landed ^= 1u << b;
       if (lane == 0) {
         const uint8_t* src =
-            reinterpret_cast<const uint8_t*>(fac) + ((size_t)(slot0 + ci) * H + h) * FB_BYTES;
-        mbar_arrive_expect_tx(bar, FB_BYTES + 4 * PANEL);
-        bulk_g2s(buf + B_FAC, src, FB_BYTES, bar);
+            reinterpret_cast<const uint8_t*>(fac) + ((size_t)(slot0 + ci) * H + h) * REC2_BYTES;
+        mbar_arrive_expect_tx(bar, REC2_BYTES + 4 * PANEL);
+        bulk_g2s(buf + B_FAC, src, REC2_BYTES, bar);
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           tma_load_3d(buf + B_K + pp * PANEL, &mk, bar, 64 * pp, hk, (int)c0);
@@ -187,8 +240,8 @@ __global__ void __launch_bounds__(NT, 1)
         if (!(ok = __shfl_sync(0xffffffffu, okl, 0) != 0)) break;
         const int per = (CHUNK - L) * 8;   // 16-byte chunks per panel
         for (int idx = lane; idx < 4 * per; idx += 32) {
-          const int tile = idx / per, rr = idx % per;
-          uint8_t* t = buf + ((tile >> 1) ? B_DO : B_K) + (tile & 1) * PANEL;
+          const int tile = idx / per, rr = idx % per;   // K, dO panels (contiguous)
+          uint8_t* t = buf + B_K + tile * PANEL;
           *reinterpret_cast<uint4*>(t + (L + rr / 8) * 128 + (rr % 8) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -219,9 +272,9 @@ __global__ void __launch_bounds__(NT, 1)
         if (!ok) break;
         tc_fence_after();
         {
-          // P1 = dO^T (scale Aqk)
+          // P1 = dO^T Aqk
           const uint64_t a = sdesc_sw128(buf + B_DO, PANEL, 1024);
-          const uint64_t bq = sdesc_sw128(buf + B_FAC + FB_AQK, PANEL, 1024);
+          const uint64_t bq = sdesc_sw128(buf + B_FAC + R_AH, PANEL, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tm + TM_P1, a + kstep_mn(kk), bq + kstep_mn(kk), ID_P1, kk > 0);
@@ -241,7 +294,7 @@ __global__ void __launch_bounds__(NT, 1)
         {
           // dS += dO^T Qg
           const uint64_t a = sdesc_sw128(buf + B_DO, PANEL, 1024);
-          const uint64_t bq = sdesc_sw128(buf + B_FAC + FB_QG, PANEL, 1024);
+          const uint64_t bq = sdesc_sw128(buf + B_FAC + R_QG, PANEL, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tm + TM_DS, a + kstep_mn(kk), bq + kstep_mn(kk), ID_U1, 1u);
@@ -249,11 +302,11 @@ __global__ void __launch_bounds__(NT, 1)
         if (!(ok = wait_bar(&bars[C_DREADY], s & 1, cx))) break;
         tc_fence_after();
         {
-          // dS += dDelta^T (-W)
-          const uint64_t bw = sdesc_sw128(buf + B_FAC + FB_NW, PANEL, 1024);
+          // dS += dDelta^T (-W): B = (-W)^T [128 k][64 i] read K-major
+          const uint64_t bw = sdesc_sw128(buf + B_FAC + R_W, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ta(tm + TM_DS, tm + TM_DDB + kk * 8, bw + kstep_mn(kk), ID_U2, 1u);
+            mma_bf16_ta(tm + TM_DS, tm + TM_DDB + kk * 8, bw + (uint64_t)(kk * 2), ID_U2, 1u);
           mma_commit(&bars[C_SUDONE]);
           mma_commit(&bars[C_FREE + b]);
         }
@@ -305,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1)
       named_bar(BAR_STATE, 256);
       if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
       if ((ok = group_wait(&bars[C_FULL], 0, cx))) {
-        const float g = reinterpret_cast<const float*>(sm + B_FAC + FB_VEC)[64];
+        const float g = reinterpret_cast<const float*>(sm + B_FAC + R_VEC + V_GC)[0];
 #pragma unroll
         for (int e = 0; e < 64; ++e) xv[e] *= g;
         tmem_st32(tl + TM_DS + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -321,17 +374,18 @@ __global__ void __launch_bounds__(NT, 1)
       if (!(ok = group_wait(&bars[C_XDONE], s & 1, cx))) break;
       tc_fence_after();
       {
-        // dDelta^T for columns [32w, 32w + 32): P1 + (dS K^T) diag(dec)
+        // dDelta^T for columns [32w, 32w + 32): scale P1 + (dS K^T) diag(dec)
         float a[32], x[32];
         tmem_ld32(tl + TM_P1 + 32 * w, a);
         tmem_ld32(tl + TM_X + 32 * w, x);
-        const float* dec = reinterpret_cast<const float*>(buf + B_FAC + FB_VEC) + 32 * w;
+        const float* dec = reinterpret_cast<const float*>(buf + B_FAC + R_VEC + V_DEC) + 32 * w;
+        const float scale = p.scale;
         tmem_ld_wait();
         uint32_t d[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          d[e] = pack_bf16x2(fmaf(dec[2 * e], x[2 * e], a[2 * e]),
-                             fmaf(dec[2 * e + 1], x[2 * e + 1], a[2 * e + 1]));
+          d[e] = pack_bf16x2(fmaf(dec[2 * e], x[2 * e], scale * a[2 * e]),
+                             fmaf(dec[2 * e + 1], x[2 * e + 1], scale * a[2 * e + 1]));
         tmem_st16(tl + TM_DDB + 16 * w, d);
       }
       tmem_st_wait();
@@ -357,7 +411,7 @@ __global__ void __launch_bounds__(NT, 1)
       store_tile_row(tape + (size_t)(nc - 2 - s) * tstride, v, u);
       const int s1 = s + 1;
       if (!(ok = group_wait(&bars[C_FULL + s1 % NB], (s1 / NB) & 1, cx))) break;
-      const float g = reinterpret_cast<const float*>(sm + (s1 % NB) * BUF + B_FAC + FB_VEC)[64];
+      const float g = reinterpret_cast<const float*>(sm + (s1 % NB) * BUF + B_FAC + R_VEC + V_GC)[0];
 #pragma unroll
       for (int e = 0; e < 64; ++e) xv[e] *= g;
       tmem_st32(tl + TM_DS + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -381,6 +435,13 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 }  // namespace
+
+cudaError_t launch_tc_bwd_qg(const ChainParams& p, float* fac, int64_t slots, cudaStream_t st) {
+  if (slots <= 0 || (int64_t)p.B * p.T == 0) return cudaSuccess;
+  qg_kernel<<<dim3((unsigned)slot_grid(p, slots), p.H), 256, 0, st>>>(
+      p, reinterpret_cast<uint8_t*>(fac), slots);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tc_bwd_chain(const ChainParams& p, const float* fac, cudaStream_t st) {
   const int chains = p.N * p.H;

@@ -52,6 +52,7 @@
 
 #include <mutex>
 
+#include "chunk_record.cuh"
 #include "common.cuh"
 #include "fwd_split.cuh"
 #include "tmap.cuh"
@@ -78,16 +79,7 @@ constexpr int MAX_NCH = 64;       // chain CTAs that own record streams, at most
 static_assert(SF_SUMMARY_CHAINS >= 1 && SF_SUMMARY_CHAINS <= MAX_NCH, "summary chain CTAs");
 constexpr int FLAG_STRIDE = 32;   // words between chain CTAs' flags: one 128-byte line each
 
-// ---- record (global ring slot, and the chain CTA's shared-memory copy) ----
-constexpr uint32_t R_W = 0;           // (-W)^T [128 k][64 i], one panel, 16 KB
-constexpr uint32_t R_T1 = 16384;      // T' [64 i][64 j], 8 KB
-constexpr uint32_t R_AH = 24576;      // Ahat [64 i][64 j], 8 KB
-constexpr uint32_t R_VEC = 32768;     // the decay vectors (FP32), at these offsets:
-constexpr uint32_t V_DEC = 0;         //   e^{gamma_C - gamma_j}, j < 64
-constexpr uint32_t V_EG = 256;        //   e^{gamma_i}, i < 64
-constexpr uint32_t V_GC = 512;        //   e^{gamma_C}
-constexpr uint32_t REC_BYTES = 33792;
-static_assert(REC_BYTES % 16 == 0 && V_GC + 4 <= REC_BYTES - R_VEC, "record layout");
+// ---- record (global ring slot, and the chain CTA's shared-memory copy): chunk_record.cuh
 
 // ---- state replay checkpoints: one BF16 [128 v][128 k] tile per chunk-head, two 64-column
 // panels of 128 rows x 128 bytes, 16-byte chunk c of row v at ((c ^ (v mod 8)) << 4) (the
@@ -212,6 +204,9 @@ struct SplitParams {
   __nv_bfloat16* out;        // or NULL (state replay: no output)
   float* final_state;        // or NULL
   float* ckpt;               // state replay: [slots,H] BF16 chunk-entry state tiles, else NULL
+  uint8_t* fac;              // state replay: [slots,H] copies of the chunk records (strided
+                             // REC2_BYTES; the backward's reverse chain reads Ahat, (-W)^T and
+                             // the decays, and Qg, which its own small kernel adds)
   int* status;               // workspace status word
   int* abort_g;              // global abort flag
   uint32_t* next_item;       // items claimed so far by the preparation CTAs
@@ -220,6 +215,7 @@ struct SplitParams {
   uint8_t* ring;             // [nch][NSLOT][REC_BYTES]
   const int32_t* cu;         // packed sequences: cu_seqlens [N+1], else NULL
   int* sstart;               // packed: [N*H] first stream position of each chain in its CTA
+  int* slot0;                // packed: [N] first backward slot of each sequence
   int* lenj;                 // packed: [nch] stream length of each chain CTA
   int* sortj;                // packed: [nch] chain CTAs by stream length, longest first
   // segment summaries (twin != 0): chain x = n H + h is token range n of `bounds`; chain
@@ -906,8 +902,10 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
 // warp's 4 KB of shared memory (already in the tile's swizzled order), and lane 0 sends
 // the 4 KB with one bulk copy (whole lines into L2).  The staging area is reused only
 // after the previous copy from it has been read; record_landed() waits for every copy.
-__device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* stage, int row0,
-                                           const uint32_t (&u)[32], int lane) {
+// kTwo: the same rows also to gtile2.
+template <bool kTwo>
+__device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* gtile2, uint8_t* stage,
+                                           int row0, const uint32_t (&u)[32], int lane) {
   if (lane == 0) bulk_wait_read_all();
   __syncwarp();
   uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
@@ -918,6 +916,7 @@ __device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* stage, int r
   __syncwarp();
   if (lane == 0) {
     bulk_s2g(gtile + (size_t)row0 * 128, stage, 4096);
+    if constexpr (kTwo) bulk_s2g(gtile2 + (size_t)row0 * 128, stage, 4096);
     bulk_commit();
   }
 }
@@ -1114,6 +1113,9 @@ __device__ __forceinline__ void lower(const float* AT, uint8_t* t1, uint8_t* t2,
 // decayed A and Ahat, the solve to T' and -T'', (-W)^T = K^T (-T'')^T; the record it
 // writes holds (-W)^T, T', Ahat and the decay vectors.
 // --------------------------------------------------------------------------
+// kCopy: the state replay, whose records are also kept per chunk-head for the backward (a
+// separate instantiation, so that the forward's preparation carries none of that code)
+template <bool kCopy>
 __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                          const CUtensorMap* tmQ4, const CUtensorMap* tmK4,
                                          const CUtensorMap* tmV4, const SplitParams& p,
@@ -1125,7 +1127,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
   // are read by two chain CTAs
   const bool summ = p.twin != 0;
   // item g -> (chain CTA, stream position, head, first row, length)
-  auto item = [&](long long g, int& jj, int& s, int& h, int& row0, int& L) {
+  // (fx: the index of the record's copy for the backward, slot * H + h, or -1)
+  auto item = [&](long long g, int& jj, int& s, int& h, int& row0, int& L, int& fx) {
     geo.item(g, jj, s);
     int x, c;
     geo.locate(jj, s, x, c);
@@ -1134,6 +1137,12 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     h = x % H;
     row0 = (int)(bos + (int64_t)c * CHUNK);
     L = (eos - row0) < CHUNK ? (int)(eos - row0) : CHUNK;
+    if constexpr (kCopy) {
+      const int n = x / H;
+      fx = ((geo.packed ? p.slot0[n] : n * geo.ncd) + c) * H + h;
+    } else {
+      fx = -1;
+    }
   };
   auto vec_of = [&](int pp, int use) {
     return reinterpret_cast<float*>(sm + pp * P_STRIDE + P_VEC + (use & 1) * P_VEC_SLOT);
@@ -1160,13 +1169,13 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // ahead so that their latency overlaps the waits), and its tiles warmed in L2 (V
       // for the chain CTA that will load it).
       struct Next {
-        int g, jj, s, h, hk, row0, L;   // hk: the query/key head of value head h
+        int g, jj, s, h, hk, row0, L, fx;   // hk: the query/key head of value head h
         float g0, g1, b0, b1;
       };
       auto fetch = [&](int g) {
-        Next n{g, 0, 0, 0, 0, 0, 0, 0.f, 0.f, 0.f, 0.f};
+        Next n{g, 0, 0, 0, 0, 0, 0, -1, 0.f, 0.f, 0.f, 0.f};
         if (g >= geo.total) return n;
-        item(g, n.jj, n.s, n.h, n.row0, n.L);
+        item(g, n.jj, n.s, n.h, n.row0, n.L, n.fx);
         n.hk = qk_of(p, n.h);
         const int e0 = 2 * lane, e1 = e0 + 1;
         const size_t o0 = (size_t)(n.row0 + e0) * H + n.h, o1 = (size_t)(n.row0 + e1) * H + n.h;
@@ -1247,6 +1256,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           vi[0] = done ? -1 : (int)gitem;
           vi[1] = jj;
           vi[2] = s;
+          vi[3] = cur.fx;
         }
         __syncwarp();
         if (!done) {
@@ -1357,6 +1367,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       if (gi < 0) break;
       const int jj = reinterpret_cast<const int*>(vs)[VEC_ITEM + 1];
       const int s = reinterpret_cast<const int*>(vs)[VEC_ITEM + 2];
+      const int fx = reinterpret_cast<const int*>(vs)[VEC_ITEM + 3];
       if (!(ok = group_wait(&bars[P_KQDONE + pp], use & 1, bid, 128, cx))) break;
       tc_fence_after();
       uint32_t ah[32];     // rows 64-127: this row of Ahat (BF16 pairs), stored at the end
@@ -1406,12 +1417,16 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // needs only the rows this warp wrote; meanwhile the Ahat warps store their rows to
       // the record's ring slot once the publisher has seen it free (s % NSLOT).
       uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
+      // state replay: the record's copy for the backward (Ahat, (-W)^T and the decays)
+      uint8_t* rec2 = kCopy ? p.fac + (size_t)fx * REC2_BYTES : nullptr;
       bool ok1 = true;
       if (arow) {
         solve::half(AT, base + P_T1, base + P_T2, vs, (warp & 3) & 1, lane);
       } else {
         ok1 = __all_sync(0xffffffffu, wait_bar(&bars[P_SLOTOK + pp], use & 1, cx)) != 0;
-        if (ok1 && !summ) store_rows(rec + R_AH, stage_ah, ((warp & 3) * 32) & 63, ah, lane);
+        if (ok1 && !summ)
+          store_rows<kCopy>(rec + R_AH, kCopy ? rec2 + R_AH : nullptr, stage_ah,
+                            ((warp & 3) * 32) & 63, ah, lane);
       }
       if (!(ok = named_bar_and(bid, 128, ok1))) {
         if (r == 0) raise_abort(cx);
@@ -1438,12 +1453,17 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         uint32_t u[32];
         tmem_ld64(tl + TP_WT, x);
         pack64(x, u);
-        store_rows(rec + R_W, stage, (warp & 3) * 32, u, lane);
+        store_rows<kCopy>(rec + R_W, kCopy ? rec2 + R_W : nullptr, stage, (warp & 3) * 32, u, lane);
       }
       // the decays e^{gamma_C - gamma_j}, e^{gamma_i} and e^{gamma_C}
       if (r < 64) reinterpret_cast<float*>(rec + R_VEC + V_DEC)[r] = vs[VEC_DEC + r];
       else reinterpret_cast<float*>(rec + R_VEC + V_EG)[r - 64] = vs[VEC_EG + r - 64];
       if (r == 0) reinterpret_cast<float*>(rec + R_VEC + V_GC)[0] = vs[VEC_EG + 63];
+      if constexpr (kCopy) {
+        if (r < 64) reinterpret_cast<float*>(rec2 + R_VEC + V_DEC)[r] = vs[VEC_DEC + r];
+        else reinterpret_cast<float*>(rec2 + R_VEC + V_EG)[r - 64] = vs[VEC_EG + r - 64];
+        if (r == 0) reinterpret_cast<float*>(rec2 + R_VEC + V_GC)[0] = vs[VEC_EG + 63];
+      }
       record_read(lane);     // the A/T and X areas, and T', are written again by the next item
       pend = true;
       tc_fence_before();
@@ -1521,6 +1541,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
   }
 }
 
+template <bool kCopy>
 __global__ void __launch_bounds__(NTHR, 1)
     gdn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -1592,7 +1613,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (is_chain)
     chain_cta(&tmQ4, &tmK4, &tmV4, &tmO, p, geo, sm, sb, bars, tm, cx);
   else
-    prep_cta(&tmQ, &tmK, &tmQ4, &tmK4, &tmV4, p, geo, sm, sb, bars, tm, cx);
+    prep_cta<kCopy>(&tmQ, &tmK, &tmQ4, &tmK4, &tmV4, p, geo, sm, sb, bars, tm, cx);
 
   tc_fence_before();
   __syncthreads();
@@ -1607,6 +1628,16 @@ __global__ void __launch_bounds__(NTHR, 1)
 __global__ void split_setup_kernel(const SplitParams p) {
   __shared__ int len_s[MAX_NCH];
   const int NH = p.N * p.H, nch = p.nch, tid = threadIdx.x;
+  if (p.fac && tid == 0) {
+    // the backward's slot numbering: each sequence's chunks follow those of the one before
+    int acc = 0;
+    for (int n = 0; n < p.N; ++n) {
+      p.slot0[n] = acc;
+      int64_t b, e;
+      chain_span(p, n * p.H, b, e);
+      acc += (int)n_chunks(e - b);
+    }
+  }
   for (int x = tid; x < NH; x += blockDim.x) {
     int64_t b, e;
     chain_span(p, x, b, e);
@@ -1659,7 +1690,7 @@ int summary_chain_ctas(int R, int H) {
 }
 size_t ws_ring_end(int nch) { return WS_RING + (size_t)nch * NSLOT * REC_BYTES; }
 size_t ws_total(int nch, int N, int H) {
-  return ws_ring_end(nch) + (((size_t)N * H + 2 * MAX_NCH) * sizeof(int) + 255) / 256 * 256;
+  return ws_ring_end(nch) + (((size_t)N * H + 2 * MAX_NCH + N) * sizeof(int) + 255) / 256 * 256;
 }
 
 // The launch shared by the forward, the state replay and the segment summaries: flags
@@ -1684,7 +1715,10 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   mq4 = mk4;
   if (q && (!make_bf16_map(&mq, q, rows, p.HK) || !make_bf16_map_4d(&mq4, q, rows, p.HK)))
     return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(gdn_fwd_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // the state replay that keeps the records for the backward takes the copying instantiation
+  const void* kern = p.fac ? reinterpret_cast<const void*>(gdn_fwd_split_kernel<true>)
+                           : reinterpret_cast<const void*>(gdn_fwd_split_kernel<false>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   char* w = reinterpret_cast<char*>(ws);
@@ -1701,6 +1735,7 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   p.sstart = reinterpret_cast<int*>(w + ws_ring_end(p.nch));
   p.lenj = p.sstart + (size_t)NH;
   p.sortj = p.lenj + MAX_NCH;
+  p.slot0 = p.sortj + MAX_NCH;
   p.nprep = nprep;
   p.wait_limit = kWaitLimitCycles;
   p.drop_item = -1;
@@ -1717,7 +1752,7 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   CUtensorMap mo = mk4;
   if (out && !make_bf16_map_4d(&mo, out, rows, p.H)) return cudaErrorInvalidValue;
   void* args[] = {&mq, &mk, &mq4, &mk4, &mv4, &mo, &p};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_fwd_split_kernel),
+  return cudaLaunchCooperativeKernel(kern,
                                      dim3(chain_blocks + nprep), dim3(NTHR), args, SMEM_ALLOC, st);
 }
 
@@ -1741,6 +1776,7 @@ cudaError_t launch_split_fwd(const ChainParams& cp, void* ws, int* status, cudaS
   p.out = reinterpret_cast<__nv_bfloat16*>(cp.out);
   p.final_state = cp.final_state;
   p.ckpt = cp.ckpt;
+  p.fac = cp.ckpt ? reinterpret_cast<uint8_t*>(cp.fac) : nullptr;
   p.pool = cp.pool;
   p.state_idx = cp.state_idx;
   p.has_init = cp.has_init;

@@ -33,6 +33,8 @@ struct ChainParams {
   float* dbeta;
   float* ds0;             // [N,H,V,K] or NULL
   float* fac;             // [slots,H] per-chunk backward factors (BF16 backward)
+  int fac_ready;          // BF16, K = 128: the state replay has written the chunk records to
+                          // fac (chunk_record.cuh), so the factor kernel is not run
   // paged state cache (forward): sequence n starts from pool[state_idx[n]] (zeros when
   // has_init[n] == 0) and leaves its final state there; state_idx[n] <= 0 marks padding:
   // zero output, the pool untouched.  p.s0 / p.final_state are then unused.

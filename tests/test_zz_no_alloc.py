@@ -62,7 +62,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(dtype, D, lengths):
 def test_noalloc_backward_rejects_shapes_beyond_its_scratch():
     import chunked_linear_recurrence_gb300 as sf
     lib = sf.load()
-    # 400 chunk-heads of 107,008 bytes: beyond the 32 MiB scratch
+    # 400 chunk-heads of 115,712 bytes: beyond the 32 MiB scratch
     inp = small_inputs(1, 64 * 400, 1, 128, torch.bfloat16, seed=3, grads=True)
     got = {n: torch.empty_like(inp[n if n != "dgate" else "gate"]) for n in
            ("q", "k", "v", "dgate", "beta")}
