@@ -429,9 +429,12 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
     return fail(SF_ERR_UNSUPPORTED, "%s: %s", fn, kNoTmaEncoder);
   cudaError_t e;
   if (bf16 && D == 128 && shape->T > 0) {
-    e = sfg::launch_split_fwd(p, ws + kStatusBytes + 2 * one + lay.fac,
-                              reinterpret_cast<int*>(workspace), cs);
+    char* split = ws + kStatusBytes + 2 * one + lay.fac;
+    e = sfg::launch_split_fwd(p, split, reinterpret_cast<int*>(workspace), cs);
     p.fac_ready = 1;    // the replay kept every chunk's record in p.fac
+    // the replay's ring is free once it has run: the fused backward's tape counts
+    if (!packed && lay.split >= (size_t)shape->N * shape->H * 128)
+      p.sync = reinterpret_cast<uint32_t*>(split);
   } else if (shape->T > 0) {
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);
   } else {

@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 
 #include "api_internal.cuh"
+#include "chain_tc.cuh"
 #include "common.cuh"
 #include "simt_chunk.cuh"
 #include "solve_tc.cuh"
@@ -176,16 +177,45 @@ __device__ __forceinline__ int colsum_col(int lane) {
 enum { B_SDO = 0, B_MMA, B_DRAIN, B_Q, B_K, B_V, B_COUNT };
 constexpr uint32_t TILE_BYTES = 32768;   // one BF16 [128][128] S or dSn tile
 
-// One chunk-head: backward slot, value head, query/key head, first row, length.
+// The launch that runs the reverse chain beside the gradients (dense inputs): CTAs
+// [0, nchain) are chain CTAs, one per (sequence, head) chain x; the others take chunk-heads
+// in the order the chains write their exit-cotangent tiles (chain x's count of written
+// tiles at tape[x * FLAG_STRIDE]).  nchain = 0: the gradients' own launch.
+struct Fuse {
+  int nchain;
+  uint32_t* tape;
+};
+constexpr int FLAG_STRIDE = 32;   // one 128-byte line per chain
+
+// One chunk-head: backward slot, value head, query/key head, first row, length; fused
+// launch: its chain x and the tape count its exit cotangent needs (x = -1 otherwise).
 struct Item {
   int64_t slot, c0;
-  int h, hk, L;
+  int h, hk, L, x;
+  uint32_t need;
   bool valid;
 };
 
-__device__ __forceinline__ Item locate_item(const ChainParams& p, int64_t item) {
+__device__ __forceinline__ Item locate_item(const ChainParams& p, int64_t item, const Fuse& f) {
   Item it{};
   it.valid = false;
+  it.x = -1;
+  if (f.nchain > 0) {
+    // the chains write chunk nc - 1 first: item = (step, chain), step-major
+    const int64_t nc = n_chunks(p.T), s = item / f.nchain;
+    if (s >= nc) return it;
+    const int x = (int)(item % f.nchain), n = x / p.H;
+    const int64_t ci = nc - 1 - s;
+    it.slot = (int64_t)n * nc + ci;
+    it.h = x % p.H;
+    it.hk = qk_head(it.h, p.H, p.HK);
+    it.c0 = (int64_t)n * p.T + ci * CHUNK;
+    it.L = (int)((p.T - ci * CHUNK) < CHUNK ? (p.T - ci * CHUNK) : CHUNK);
+    it.x = x;
+    it.need = (uint32_t)(s + 1);
+    it.valid = true;
+    return it;
+  }
   const int64_t slot = item / p.H;
   int n = -1;
   int64_t bos = 0, eos = 0, ci = 0;
@@ -214,6 +244,7 @@ struct Ctx {
   uint32_t pend;       // thread 0: copies issued and not yet waited for (1 << B_SDO | ...)
   float ng, nb;        // threads 0-63: the next chunk's gate and beta at this thread's row
   int* status;
+  const uint32_t* tape;  // fused launch: the chains' written-tile counts (FLAG_STRIDE apart)
   __device__ float* v(int which) const { return vec + which * 64; }
   // TMEM address of this warp's lane quarter at column `col`
   __device__ uint32_t ta(uint32_t col) const { return tm + ((uint32_t)(32 * q4) << 16) + col; }
@@ -252,9 +283,24 @@ __device__ __forceinline__ void st_row16(uint8_t* tile, int row, int c0, const f
   st_row8_bf16(tile, row, c0 + 8, X_PANEL, x + 8);
 }
 
-// Thread 0: the chunk's S and dSn tiles (bulk copies) and its dO tile (TMA).
-__device__ __forceinline__ void fetch_sdo(Ctx& c, const ChainParams& p, const Maps& m,
+// Thread 0: the chunk's S and dSn tiles (bulk copies) and its dO tile (TMA).  In the fused
+// launch, first the chain's tile count (bounded wait); false when that wait expired.
+__device__ __forceinline__ bool fetch_sdo(Ctx& c, const ChainParams& p, const Maps& m,
                                           const Item& it) {
+  if (it.x >= 0) {
+    const uint32_t* flag = c.tape + (size_t)it.x * FLAG_STRIDE;
+    if (ld_acquire_u32(flag) < it.need) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(flag) < it.need) {
+        __nanosleep(200);
+        if (globaltimer_ns() - t0 > WAIT_NS) {
+          note_timeout(c, 6);
+          return false;
+        }
+      }
+    }
+    fence_proxy_async_global();   // the chain's generic stores, then our bulk read
+  }
   const uint8_t* ck = reinterpret_cast<const uint8_t*>(p.ckpt);
   const uint8_t* tp = reinterpret_cast<const uint8_t*>(p.tape);
   const size_t off = ((size_t)it.slot * p.H + it.h) * TILE_BYTES;
@@ -265,6 +311,7 @@ __device__ __forceinline__ void fetch_sdo(Ctx& c, const ChainParams& p, const Ma
 #pragma unroll
   for (int pp = 0; pp < 2; ++pp)
     tma_load_3d(c.sm + O_DO + pp * X_PANEL, m.dout, &c.bars[B_SDO], 64 * pp, it.h, (int)it.c0);
+  return true;
 }
 // Thread 0: the chunk's Q tile.
 __device__ __forceinline__ void fetch_q(Ctx& c, const Maps& m, const Item& it) {
@@ -641,7 +688,7 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
   if (tid == 0 && nx.valid) {
     // the next chunk's S, dSn and dO (the last products reading this chunk's have completed)
     fence_proxy_async_smem();
-    fetch_sdo(c, p, m, nx);
+    ok = fetch_sdo(c, p, m, nx) && ok;
   }
   if (tid < 64 && nx.valid) fetch_gb(c, p, nx);
   if (q4 < 2) {
@@ -836,13 +883,26 @@ __device__ bool grad_chunk(Ctx& c, const ChainParams& p, const Maps& m, const It
   return ok;
 }
 
+// kFused: the CTAs below f.nchain run the reverse chain (chain_tc.cuh) over the records
+// `fac`; the others take the chunk-heads as their exit cotangents arrive.
+template <bool kFused>
 __global__ void __launch_bounds__(NT, 1)
     tc_bwd_grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv,
-                       const __grid_constant__ CUtensorMap mdo, const ChainParams p) {
+                       const __grid_constant__ CUtensorMap mdo, const ChainParams p,
+                       const float* fac, const Fuse f) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
   c.sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  if constexpr (kFused) {
+    if ((int)blockIdx.x < f.nchain) {
+      chaintc::chain_cta<true>(&mk, &mdo, p, fac, (int)blockIdx.x,
+                               f.tape + (size_t)blockIdx.x * FLAG_STRIDE, c.sm);
+      return;
+    }
+  }
+  const int64_t first = kFused ? (int64_t)blockIdx.x - f.nchain : (int64_t)blockIdx.x;
+  const int64_t stride = kFused ? (int64_t)gridDim.x - f.nchain : (int64_t)gridDim.x;
   c.sb = smem_u32(c.sm);
   c.bars = reinterpret_cast<uint64_t*>(c.sm + O_BAR);
   c.vec = reinterpret_cast<float*>(c.sm + O_VEC);
@@ -856,6 +916,7 @@ __global__ void __launch_bounds__(NT, 1)
   c.pend = 0;
   c.ng = c.nb = 0.f;
   c.status = p.status;
+  c.tape = f.tape;
   const Maps m{&mq, &mk, &mv, &mdo};
   uint32_t* tslot = reinterpret_cast<uint32_t*>(c.sm + O_BAR + 8 * B_COUNT);
   if (c.tid == 0) {
@@ -871,19 +932,22 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   c.tm = *tslot;
-  // chunk-heads blockIdx.x, blockIdx.x + gridDim.x, ... in the order (slot, head), until the
-  // first empty slot
-  Item it = locate_item(p, blockIdx.x);
+  // chunk-heads first, first + stride, ... in the order (slot, head) -- fused: (chain
+  // step, chain) -- until the first empty one
+  Item it = locate_item(p, first, f);
+  bool ok = true;
   if (c.tid == 0 && it.valid) {
-    fetch_sdo(c, p, m, it);
-    fetch_q(c, m, it);
-    fetch_k(c, m, it);
-    fetch_v(c, m, it);
+    ok = fetch_sdo(c, p, m, it);
+    if (ok) {
+      fetch_q(c, m, it);
+      fetch_k(c, m, it);
+      fetch_v(c, m, it);
+    }
   }
   if (c.tid < 64 && it.valid) fetch_gb(c, p, it);
-  bool ok = true;
-  for (int64_t item = blockIdx.x; it.valid; item += gridDim.x) {
-    const Item nx = locate_item(p, item + gridDim.x);
+  ok = __syncthreads_and(ok);
+  for (int64_t item = first; it.valid && ok; item += stride) {
+    const Item nx = locate_item(p, item + stride, f);
     ok = grad_chunk(c, p, m, it, nx);
     if (!ok) break;
     __syncthreads();   // the next chunk's vectors overwrite those read above
@@ -913,7 +977,7 @@ cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t
   if (!make_bf16_map(&mq, p.q, rows, p.HK) || !make_bf16_map(&mk, p.k, rows, p.HK) ||
       !make_bf16_map(&mv, p.v, rows, p.H) || !make_bf16_map(&mdo, p.dout, rows, p.H))
     return cudaErrorInvalidValue;
-  auto kern = tc_bwd_grad_kernel;
+  auto kern = tc_bwd_grad_kernel<false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (e != cudaSuccess) return e;
@@ -924,8 +988,44 @@ cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t
   // one persistent CTA per SM (the shared memory allows no second), at most one per item
   const int64_t items = slots * p.H;
   const int grid = (int)(items < nsm ? items : nsm);
-  if (grid > 0) kern<<<grid, NT, SMEM_ALLOC, st>>>(mq, mk, mv, mdo, p);
+  const Fuse f{0, nullptr};
+  const float* fac = nullptr;
+  if (grid > 0) kern<<<grid, NT, SMEM_ALLOC, st>>>(mq, mk, mv, mdo, p, fac, f);
   return cudaGetLastError();
+}
+
+bool tc_bwd_fusable(const ChainParams& p) {
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  const int chains = p.N * p.H;
+  return !p.cu && p.sync && p.B == p.N && chains >= 1 && chains <= 64 && nsm - chains >= 32 &&
+         (int64_t)p.B * p.T > 0;
+}
+
+cudaError_t launch_tc_bwd_fused(const ChainParams& p, const float* fac, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  const int rows = p.B * p.T;
+  if (!make_bf16_map(&mq, p.q, rows, p.HK) || !make_bf16_map(&mk, p.k, rows, p.HK) ||
+      !make_bf16_map(&mv, p.v, rows, p.H) || !make_bf16_map(&mdo, p.dout, rows, p.H))
+    return cudaErrorInvalidValue;
+  static_assert(chaintc::SMEM_ALLOC <= SMEM_ALLOC, "the chain CTAs fit the launch's smem");
+  const void* kern = reinterpret_cast<const void*>(tc_bwd_grad_kernel<true>);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_grad_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  Fuse f{p.N * p.H, p.sync};
+  e = cudaMemsetAsync(p.sync, 0, (size_t)f.nchain * FLAG_STRIDE * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  // cooperative: every chain CTA is resident with the gradient CTAs that wait for it
+  ChainParams pc = p;
+  void* args[] = {&mq, &mk, &mv, &mdo, &pc, const_cast<float**>(&fac), &f};
+  return cudaLaunchCooperativeKernel(kern, dim3(nsm), dim3(NT), args, SMEM_ALLOC, st);
 }
 
 }  // namespace sfg

@@ -14,6 +14,7 @@
 // the chunk's factors, which every CTA recomputes).
 #include <type_traits>
 
+#include "bwd_chain_tc.cuh"
 #include "common.cuh"
 #include "simt_chunk.cuh"
 
@@ -754,7 +755,13 @@ static cudaError_t launch_bwd_t(const ChainParams& p, int64_t slots, cudaStream_
                                 bool chain_only) {
   cudaError_t e;
   if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
-    // BF16: reverse chain and token gradients on the warp-level tensor cores
+    // K = V = 128, dense, records kept by the replay: the reverse chain and the token
+    // gradients in one tcgen05 launch
+    if (D == 128 && !chain_only && p.fac_ready && tc_bwd_fusable(p)) {
+      if ((e = launch_tc_bwd_qg(p, p.fac, slots, st)) != cudaSuccess) return e;
+      return launch_tc_bwd_fused(p, p.fac, st);
+    }
+    // BF16: reverse chain and token gradients on the tensor cores
     if ((e = launch_mma_bwd_chain(p, p.fac, D, slots, st)) != cudaSuccess) return e;
     if (chain_only) return cudaSuccess;
     // K = V = 128 (after the split kernel's replay): token gradients on tcgen05

@@ -48,6 +48,9 @@ struct ChainParams {
   int HK;                 // query/key heads (divides H): value head h reads h / (H / HK)
   float scale;
   int* status;            // the workspace's status words (kernels with bounded waits), or NULL
+  uint32_t* sync;         // BF16, K = 128, dense: scratch of N*H 128-byte lines (the reverse
+                          // chain's written-tile counts when it runs beside the gradients),
+                          // or NULL
 };
 
 // Query/key head of value head h.
@@ -91,5 +94,11 @@ cudaError_t launch_mma_bwd_grad(const ChainParams& p, bool bf16, int D, int64_t 
 // Per-chunk token gradients on tcgen05 (bwd_grad_tc.cu): BF16, K = V = 128, checkpoints and
 // tape as BF16 swizzled tiles.
 cudaError_t launch_tc_bwd_grad(const ChainParams& p, int64_t slots, cudaStream_t st);
+// Whether the reverse chain can run in the gradients' launch (dense inputs, p.sync set, at
+// most 64 chains and at least 32 SMs left for the gradients), and that launch: the chain
+// over the chunk records `fac` (with Qg) on CTAs [0, N*H), the gradients on the rest, each
+// chunk-head taken once its exit cotangent is written.
+bool tc_bwd_fusable(const ChainParams& p);
+cudaError_t launch_tc_bwd_fused(const ChainParams& p, const float* fac, cudaStream_t st);
 
 }  // namespace sfg
