@@ -433,7 +433,7 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape* shape, const void* q, const void*
     e = sfg::launch_split_fwd(p, split, reinterpret_cast<int*>(workspace), cs);
     p.fac_ready = 1;    // the replay kept every chunk's record in p.fac
     // the replay's ring is free once it has run: the fused backward's tape counts
-    if (!packed && lay.split >= (size_t)shape->N * shape->H * 128)
+    if (!packed && lay.split >= ((size_t)shape->N * shape->H + 1) * 128)
       p.sync = reinterpret_cast<uint32_t*>(split);
   } else if (shape->T > 0) {
     e = sfg::launch_simt_chain(p, sfg::MODE_REPLAY, bf16, D, shape->N, cs);

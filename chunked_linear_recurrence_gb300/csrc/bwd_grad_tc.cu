@@ -178,9 +178,10 @@ enum { B_SDO = 0, B_MMA, B_DRAIN, B_Q, B_K, B_V, B_COUNT };
 constexpr uint32_t TILE_BYTES = 32768;   // one BF16 [128][128] S or dSn tile
 
 // The launch that runs the reverse chain beside the gradients (dense inputs): CTAs
-// [0, nchain) are chain CTAs, one per (sequence, head) chain x; the others take chunk-heads
-// in the order the chains write their exit-cotangent tiles (chain x's count of written
-// tiles at tape[x * FLAG_STRIDE]).  nchain = 0: the gradients' own launch.
+// [0, nchain) run one (sequence, head) chain x each, then join the others in taking
+// chunk-heads, claimed one at a time from the counter tape[nchain * FLAG_STRIDE] in the
+// order the chains write their exit-cotangent tiles (chain x's count of written tiles at
+// tape[x * FLAG_STRIDE]).  nchain = 0: the gradients' own launch (a fixed grid stride).
 struct Fuse {
   int nchain;
   uint32_t* tape;
@@ -895,14 +896,10 @@ __global__ void __launch_bounds__(NT, 1)
   Ctx c;
   c.sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   if constexpr (kFused) {
-    if ((int)blockIdx.x < f.nchain) {
+    if ((int)blockIdx.x < f.nchain)
       chaintc::chain_cta<true>(&mk, &mdo, p, fac, (int)blockIdx.x,
                                f.tape + (size_t)blockIdx.x * FLAG_STRIDE, c.sm);
-      return;
-    }
   }
-  const int64_t first = kFused ? (int64_t)blockIdx.x - f.nchain : (int64_t)blockIdx.x;
-  const int64_t stride = kFused ? (int64_t)gridDim.x - f.nchain : (int64_t)gridDim.x;
   c.sb = smem_u32(c.sm);
   c.bars = reinterpret_cast<uint64_t*>(c.sm + O_BAR);
   c.vec = reinterpret_cast<float*>(c.sm + O_VEC);
@@ -919,7 +916,10 @@ __global__ void __launch_bounds__(NT, 1)
   c.tape = f.tape;
   const Maps m{&mq, &mk, &mv, &mdo};
   uint32_t* tslot = reinterpret_cast<uint32_t*>(c.sm + O_BAR + 8 * B_COUNT);
+  uint32_t* claim = tslot + 1;   // fused: the chunk-head claimed last
+  uint32_t* counter = f.tape + (size_t)f.nchain * FLAG_STRIDE;
   if (c.tid == 0) {
+    if constexpr (kFused) *claim = atomicAdd(counter, 2u);   // this chunk-head and the next
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&c.bars[b], 1);
     fence_mbar_init();
     prefetch_tmap(&mq);
@@ -932,9 +932,10 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   c.tm = *tslot;
-  // chunk-heads first, first + stride, ... in the order (slot, head) -- fused: (chain
-  // step, chain) -- until the first empty one
-  Item it = locate_item(p, first, f);
+  // chunk-heads blockIdx.x, + gridDim.x, ... in the order (slot, head) until the first empty
+  // one; fused: claimed in the order (chain step, chain)
+  int64_t next = kFused ? (int64_t)*claim + 1 : (int64_t)blockIdx.x + gridDim.x;
+  Item it = locate_item(p, kFused ? (int64_t)*claim : (int64_t)blockIdx.x, f);
   bool ok = true;
   if (c.tid == 0 && it.valid) {
     ok = fetch_sdo(c, p, m, it);
@@ -946,11 +947,14 @@ __global__ void __launch_bounds__(NT, 1)
   }
   if (c.tid < 64 && it.valid) fetch_gb(c, p, it);
   ok = __syncthreads_and(ok);
-  for (int64_t item = first; it.valid && ok; item += stride) {
-    const Item nx = locate_item(p, item + stride, f);
+  while (it.valid && ok) {
+    const Item nx = locate_item(p, next, f);
     ok = grad_chunk(c, p, m, it, nx);
     if (!ok) break;
+    // (every thread read *claim before grad_chunk's first CTA barrier)
+    if (kFused && c.tid == 0) *claim = atomicAdd(counter, 1u);
     __syncthreads();   // the next chunk's vectors overwrite those read above
+    next = kFused ? (int64_t)*claim : next + gridDim.x;
     it = nx;
   }
   if (!ok && c.tid == 0) {
@@ -1020,7 +1024,8 @@ cudaError_t launch_tc_bwd_fused(const ChainParams& p, const float* fac, cudaStre
       (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   Fuse f{p.N * p.H, p.sync};
-  e = cudaMemsetAsync(p.sync, 0, (size_t)f.nchain * FLAG_STRIDE * sizeof(uint32_t), st);
+  // the chains' tile counts and the claim counter
+  e = cudaMemsetAsync(p.sync, 0, (size_t)(f.nchain + 1) * FLAG_STRIDE * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   // cooperative: every chain CTA is resident with the gradient CTAs that wait for it
   ChainParams pc = p;

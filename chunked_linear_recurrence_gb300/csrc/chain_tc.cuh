@@ -130,7 +130,8 @@ __device__ __forceinline__ void publish_tape(uint32_t* flag, uint32_t count, int
 }
 
 // The chain x = n H + h of p: sm, 1024-aligned shared memory of SMEM_ALLOC bytes; tape_flag:
-// the published tape count (fused launch) or NULL.
+// the published tape count (fused launch) or NULL.  A fused launch's CTA leaves with its
+// TMEM freed, its barriers invalidated and 128 registers per thread.
 // Registers of the loader / issuer warpgroup in a fused launch.
 constexpr int kCtlRegs = 56;
 
@@ -410,6 +411,15 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* mk, const CUtensorM
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tm, 512);
+  if constexpr (kFused) {
+    // the CTA goes on to token gradients: 128 registers per thread again (the cotangent
+    // warps give theirs back first), and its barriers' memory is reused
+    if (warp >= 4 && warp < 12) reg_dealloc<128>();
+    else reg_alloc<128>();
+    if (tid == 0)
+      for (int i = 0; i < C_COUNT; ++i) mbar_inval(&bars[i]);
+    __syncthreads();
+  }
 }
 
 }  // namespace chaintc

@@ -48,9 +48,9 @@ struct ChainParams {
   int HK;                 // query/key heads (divides H): value head h reads h / (H / HK)
   float scale;
   int* status;            // the workspace's status words (kernels with bounded waits), or NULL
-  uint32_t* sync;         // BF16, K = 128, dense: scratch of N*H 128-byte lines (the reverse
-                          // chain's written-tile counts when it runs beside the gradients),
-                          // or NULL
+  uint32_t* sync;         // BF16, K = 128, dense: scratch of N*H + 1 128-byte lines (the
+                          // reverse chain's written-tile counts and a work counter when it
+                          // runs beside the gradients), or NULL
 };
 
 // Query/key head of value head h.
