@@ -66,8 +66,9 @@ using namespace tc;
 
 constexpr int D = 128;
 constexpr int NTHR = 512;
-constexpr int NSLOT = 8;          // ring slots per chain CTA
+constexpr int NSLOT = 16;         // ring slots per chain CTA
 constexpr int NBUF = 2;           // chunk buffers (record + K, Q, V tiles) of a chain CTA
+constexpr int NBUF_NO = 3;        // the same without output (no Q tile): replay, summaries
 constexpr int MAX_NCH = 64;       // chain CTAs that own record streams, at most
 // Stream-owning chain CTAs of a segment-summary launch, at most (each with a P twin).  The
 // summary's chains (two per (range, head), about 2 us per chunk step) and its preparation
@@ -94,17 +95,37 @@ __device__ __forceinline__ void store_ckpt_row(uint8_t* row, int v, const uint32
         make_uint4(u[4 * c], u[4 * c + 1], u[4 * c + 2], u[4 * c + 3]);
 }
 
-// ---- chain CTA shared memory: NBUF buffers, each the record then the K, Q, V tiles ----
+// ---- chain CTA shared memory: NBUF buffers, each the record then the K, Q, V tiles, and
+// two staging tiles of the output.  A launch without output has NBUF_NO buffers of the
+// record's (-W)^T, T' and decays (no Ahat), K and V, and the staging of one checkpoint tile.
 constexpr uint32_t C_K = 34816;       // K tile [64 tok][128 k]: 2 panels x 8 KB
 constexpr uint32_t C_Q = 51200;       // Q tile, same layout
 constexpr uint32_t C_V = 67584;       // V tile [64 tok][128 v]
 constexpr uint32_t C_T_PANEL = 8192;
 constexpr uint32_t C_BUF = 83968;     // buffer stride (1024-aligned)
 constexpr uint32_t C_OST = NBUF * C_BUF;   // two staging tiles of the output [64 tok][128 v]
-constexpr uint32_t C_BAR = C_OST + 2 * 16384;
+constexpr uint32_t C_VEC_NO = R_AH;   // no output: the decays where Ahat would be
+constexpr uint32_t C_K_NO = C_VEC_NO + (REC_BYTES - R_VEC);
+constexpr uint32_t C_V_NO = C_K_NO + 2 * C_T_PANEL;
+constexpr uint32_t C_BUF_NO = C_V_NO + 2 * C_T_PANEL;
+constexpr uint32_t C_CST = NBUF_NO * C_BUF_NO;   // checkpoint staging: 4 KB per state warp
+constexpr uint32_t C_BAR_OUT = C_OST + 2 * 16384, C_BAR_NO = C_CST + CKPT_TILE_BYTES;
+constexpr uint32_t C_BAR = C_BAR_OUT > C_BAR_NO ? C_BAR_OUT : C_BAR_NO;
 static_assert(C_K >= REC_BYTES && C_K % 1024 == 0 && C_BUF % 1024 == 0, "chain smem");
 static_assert(C_Q == C_K + 2 * C_T_PANEL && C_V == C_Q + 2 * C_T_PANEL &&
               C_BUF == C_V + 2 * C_T_PANEL, "chain tiles");
+static_assert(R_W == 0 && R_T1 == 16384 && R_AH == 24576 && C_K_NO % 1024 == 0 &&
+              C_BUF_NO % 1024 == 0, "chain smem without output");
+
+// Buffers of a chain CTA with (kOut) or without output products.
+template <bool kOut>
+struct ChainBufs {
+  static constexpr int NB = kOut ? NBUF : NBUF_NO;
+  static constexpr uint32_t STRIDE = kOut ? C_BUF : C_BUF_NO;
+  static constexpr uint32_t K = kOut ? C_K : C_K_NO;
+  static constexpr uint32_t V = kOut ? C_V : C_V_NO;
+  static constexpr uint32_t VEC = kOut ? R_VEC : C_VEC_NO;
+};
 
 // ---- preparation CTA shared memory, per pipeline (two pipelines) ----
 constexpr uint32_t P_KQ = 0;          // two [K;Q] tile buffers: 2 panels x 16 KB each
@@ -162,19 +183,19 @@ constexpr uint32_t ID_MG64 = idesc_bf16(128, 64, false, true);   // the same, N 
 // ---- mbarriers ----
 enum {
   // chain CTA
-  C_RECFULL = 0,   // [NBUF] the chunk's record and tiles in shared memory (tx, or the
-                   //        loader's arrival once a partial chunk's rows are zeroed)
-  C_RECFREE = 2,   // [NBUF] the chunk's last product done (MMA commit) + its output tile out
-  C_LANDED = 4,    // [NBUF] a partial chunk's copies landed (tx)
-  C_MERGED = 6,    // MMA: Delta accumulator U^T - S W^T complete
-  C_DREADY = 7,    // state: Delta BF16 operands in TMEM
-  C_SUDONE = 8,    // MMA: state update complete (and O1 of the chunk)
-  C_SREADY = 9,    // state: S BF16 operand in TMEM
-  C_SSCALED = 10,  // state: TMEM S scaled by e^{gamma_C} of the chunk
-  C_ODONE = 11,    // MMA: O1 and O2 of the chunk complete
-  C_OFREE = 12,    // out: O1 and O2 read
-  C_DRAIN = 13,    // MMA issuer, abort path only: every product it issued has completed
-  C_COUNT = 14,
+  C_RECFULL = 0,   // [3] the chunk's record and tiles in shared memory (tx, or the
+                   //     loader's arrival once a partial chunk's rows are zeroed)
+  C_RECFREE = 3,   // [3] the chunk's last product done (MMA commit) + its output tile out
+  C_LANDED = 6,    // [3] a partial chunk's copies landed (tx)
+  C_MERGED = 9,    // MMA: Delta accumulator U^T - S W^T complete
+  C_DREADY = 10,   // state: Delta BF16 operands in TMEM
+  C_SUDONE = 11,   // MMA: state update complete (and O1 of the chunk)
+  C_SREADY = 12,   // state: S BF16 operand in TMEM
+  C_SSCALED = 13,  // state: TMEM S scaled by e^{gamma_C} of the chunk
+  C_ODONE = 14,    // MMA: O1 and O2 of the chunk complete
+  C_OFREE = 15,    // out: O1 and O2 read
+  C_DRAIN = 16,    // MMA issuer, abort path only: every product it issued has completed
+  C_COUNT = 17,
   // preparation CTA
   P_FULL = 0,      // [2 pipelines][2 buffers] K and Q tiles landed (tx)
   P_HEAD = 4,      // [2][2 slots] controller: item slot, decay vectors, padding rows zeroed
@@ -190,8 +211,8 @@ enum {
   P_COUNT = 32
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
-static_assert(C_RECFREE == C_RECFULL + NBUF && C_LANDED == C_RECFREE + NBUF &&
-              C_MERGED == C_LANDED + NBUF, "chain barriers");
+static_assert(NBUF <= 3 && NBUF_NO <= 3 && C_RECFREE == C_RECFULL + 3 &&
+              C_LANDED == C_RECFREE + 3 && C_MERGED == C_LANDED + 3, "chain barriers");
 
 // named barriers
 constexpr int BAR_STATE = 1, BAR_OUT = 2;       // chain: 256, 128 threads
@@ -453,6 +474,7 @@ struct Geo {
 //   S   = e^{gamma_C} S + (Delta^T diag(dec)) K
 //   O2  = Delta^T Ahat^T                out = scale (e^{gamma_i} O1 + O2)
 // --------------------------------------------------------------------------
+template <bool kOut>
 __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                           const CUtensorMap* tmV, const CUtensorMap* tmO,
                                           const SplitParams& p, const Geo& geo, uint8_t* sm,
@@ -463,7 +485,10 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
   // segment summaries: chain CTA nch + j is the P twin of chain CTA j (same chains, same
   // records and ring); it reads (-W)^T and the decays only and has no output
   const bool summ = p.twin != 0, ptwin = summ && (int)blockIdx.x >= geo.nch;
-  const bool has_out = !summ && p.out != nullptr;   // the output products and stores
+  constexpr bool has_out = kOut;                     // the output products and stores
+  constexpr int NB = ChainBufs<kOut>::NB;
+  constexpr uint32_t BUF = ChainBufs<kOut>::STRIDE, CK = ChainBufs<kOut>::K,
+                     CV = ChainBufs<kOut>::V, RV = ChainBufs<kOut>::VEC;
   const bool need_v = !ptwin;                        // the value term U^T = V^T T'^T
   const int j = ptwin ? (int)blockIdx.x - geo.nch : (int)blockIdx.x;   // the stream's owner
   const int cnt = geo.chains_of(j);
@@ -476,7 +501,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
     reg_dealloc<RC_CTL>();
     if (warp == 0) {
       // ------------------------------------------------------------ loader
-      // Up to NBUF chunks in flight.  A ring slot is handed back (consumed) once its
+      // Up to NB chunks in flight.  A ring slot is handed back (consumed) once its
       // record has landed in shared memory: at the latest when the buffer is needed
       // again (then the chunk that used it is done), earlier if the copy is seen landed;
       // the slots landed by then go back with one release.  A chunk cut short by its
@@ -493,7 +518,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         st_release_u32(consumed_me, (uint32_t)n);
         rel = n;
       };
-      const uint32_t rec_tx = summ ? (ptwin ? 16384u : 24576u) + (REC_BYTES - R_VEC) : REC_BYTES;
+      // without output the record's Ahat is not needed (the P twin: no T' either)
+      const uint32_t rec_tx =
+          !has_out ? (ptwin ? 16384u : 24576u) + (REC_BYTES - R_VEC) : REC_BYTES;
       const uint32_t tx = rec_tx + 2 * C_T_PANEL * (1u + (need_v ? 1u : 0u) + (has_out ? 1u : 0u));
       int s = 0, t = 0, c = 0, ncx = 0, hk = 0, h = 0;
       int64_t bos = 0, eos = 0;
@@ -506,13 +533,13 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           hk = qk_of(p, h);
           c = 0;
         }
-        const int b = s % NBUF;
+        const int b = s % NB;
         const int row0 = (int)(bos + (int64_t)c * CHUNK);
         const int64_t rem = eos - (bos + (int64_t)c * CHUNK);
         const int L = rem < CHUNK ? (int)rem : CHUNK;
         const bool part = L < CHUNK;
         uint64_t* txbar = part ? &bars[C_LANDED + b] : &bars[C_RECFULL + b];
-        uint8_t* buf = sm + b * C_BUF;
+        uint8_t* buf = sm + b * BUF;
         // the record's flag first (usually set long before: its latency hides behind the
         // wait for the buffer), then the buffer, free once the chunk that used it has had
         // its products and its output read
@@ -520,23 +547,23 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           ok = flag_next >= (uint32_t)s + 1 || poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx);
           // the producer's plain stores before its release, then our bulk reads
           if (ok) fence_proxy_async_global();
-          ok = ok && (s < NBUF || wait_bar(&bars[C_RECFREE + b], ((s - NBUF) / NBUF) & 1, cx));
+          ok = ok && (s < NB || wait_bar(&bars[C_RECFREE + b], ((s - NB) / NB) & 1, cx));
         }
         if (!(ok = __shfl_sync(0xffffffffu, ok, 0) != 0)) break;
         part_of = (part_of & ~(1u << b)) | ((part ? 1u : 0u) << b);
         if (lane == 0) {
           mbar_arrive_expect_tx(txbar, tx);
           const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
-          if (!summ) {
+          if (has_out) {
             bulk_g2s(buf, src, REC_BYTES, txbar);
           } else {
-            // (-W)^T and, for the E chain, T' (contiguous), then the decays
+            // (-W)^T and, except for a P twin, T' (contiguous), then the decays
             bulk_g2s(buf + R_W, src + R_W, ptwin ? 16384u : 24576u, txbar);
-            bulk_g2s(buf + R_VEC, src + R_VEC, REC_BYTES - R_VEC, txbar);
+            bulk_g2s(buf + RV, src + R_VEC, REC_BYTES - R_VEC, txbar);
           }
-          tma_load_4d(buf + C_K, tmK, txbar, 0, row0, 0, hk);
+          tma_load_4d(buf + CK, tmK, txbar, 0, row0, 0, hk);
           if (has_out) tma_load_4d(buf + C_Q, tmQ, txbar, 0, row0, 0, hk);
-          if (need_v) tma_load_4d(buf + C_V, tmV, txbar, 0, row0, 0, h);
+          if (need_v) tma_load_4d(buf + CV, tmV, txbar, 0, row0, 0, h);
         }
         issued = s + 1;
         // the next record's flag, read now and looked at next time round
@@ -553,7 +580,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           const int ntile = need_v ? 4 : 2;
           for (int idx = lane; idx < ntile * per; idx += 32) {
             const int tile = idx / per, rr = idx % per;
-            uint8_t* base_t = buf + ((tile >> 1) ? C_V : C_K) + (tile & 1) * C_T_PANEL;
+            uint8_t* base_t = buf + ((tile >> 1) ? CV : CK) + (tile & 1) * C_T_PANEL;
             *reinterpret_cast<uint4*>(base_t + (L + rr / 8) * 128 + (rr % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
@@ -562,32 +589,32 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           if (lane == 0) mbar_arrive(&bars[C_RECFULL + b]);
         }
         if (lane == 0) {
-          // records up to s - NBUF have landed (their buffers came back); later ones are
+          // records up to s - NB have landed (their buffers came back); later ones are
           // tested against their buffers' current phases
           int n = rel;
-          if (s >= NBUF && n < s - NBUF + 1) n = s - NBUF + 1;
-          while (n < s && mbar_test(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1)) ++n;
+          if (s >= NB && n < s - NB + 1) n = s - NB + 1;
+          while (n < s && mbar_test(&bars[C_RECFULL + n % NB], (n / NB) & 1)) ++n;
           if (n >= rel + 2) release_to(n);   // two slots at a time (the ring has NSLOT)
         }
       }
       if (lane == 0) {
         if (ok && rel < len) {
-          // records before len - NBUF landed before their buffers were taken again (and a
+          // records before len - NB landed before their buffers were taken again (and a
           // parity wait on a buffer's older phase could be mistaken for its newer one), so
-          // only the last NBUF are waited for
-          for (int n = rel > len - NBUF ? rel : (len > NBUF ? len - NBUF : 0); n < len && ok; ++n)
-            ok = wait_bar(&bars[C_RECFULL + n % NBUF], (n / NBUF) & 1, cx);
+          // only the last NB are waited for
+          for (int n = rel > len - NB ? rel : (len > NB ? len - NB : 0); n < len && ok; ++n)
+            ok = wait_bar(&bars[C_RECFULL + n % NB], (n / NB) & 1, cx);
           if (ok) release_to(len);
         }
         if (!ok) {
           raise_abort(cx);
           // let every copy still in flight land before leaving
-          for (int q = issued > NBUF ? issued - NBUF : 0; q < issued; ++q) {
-            const int b = q % NBUF;
+          for (int q = issued > NB ? issued - NB : 0; q < issued; ++q) {
+            const int b = q % NB;
             if ((part_of >> b) & 1u)
               mbar_wait(&bars[C_LANDED + b], ((landed_uses >> b) & 1u) ^ 1u, 100000000ull);
             else
-              mbar_wait(&bars[C_RECFULL + b], (q / NBUF) & 1, 100000000ull);
+              mbar_wait(&bars[C_RECFULL + b], (q / NB) & 1, 100000000ull);
           }
         }
       }
@@ -598,9 +625,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       // condition in turn (a suspended wait leaves the issue slots to the other warps).
       if (lane == 0) {
         for (int s = 0; s < len; ++s) {
-          const int rb = s % NBUF;
-          const uint32_t buf = sb + rb * C_BUF;
-          if (!wait_bar(&bars[C_RECFULL + rb], (s / NBUF) & 1, cx)) {
+          const int rb = s % NB;
+          const uint32_t buf = sb + rb * BUF;
+          if (!wait_bar(&bars[C_RECFULL + rb], (s / NB) & 1, cx)) {
             raise_abort(cx);
             break;
           }
@@ -608,7 +635,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           if (need_v) {
             // U^T = V^T T'^T (the accumulator's previous contents were read before the
             // previous chunk's DREADY, which this thread waited for)
-            const uint64_t av = sdesc_sw128(buf + C_V, C_T_PANEL, 1024);
+            const uint64_t av = sdesc_sw128(buf + CV, C_T_PANEL, 1024);
             const uint64_t bt = sdesc_sw128(buf + R_T1, 0, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -649,7 +676,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
             break;
           }
           tc_fence_after();
-          const uint64_t bk = sdesc_sw128(buf + C_K, C_T_PANEL, 1024);
+          const uint64_t bk = sdesc_sw128(buf + CK, C_T_PANEL, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ta(tm + TM_S, tm + TM_DDB + kk * 8, bk + (uint64_t)(kk * 2048 >> 4), ID_MG, 1u);
@@ -710,6 +737,25 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
                                  (size_t)w * 16384 + (size_t)v * 128
                            : nullptr;
       const size_t ck_stride = (size_t)H * CKPT_TILE_BYTES;
+      // A checkpoint row.  Without output, each state warp's 32 rows (4 KB of one panel)
+      // go out by one bulk copy from the warp's staging area (direct stores from the 256
+      // threads stall the chain's own products and loads on this SM): stage_ckpt parks the
+      // row once the warp's previous copy has read the area, and after the next named
+      // barrier of the state warps send_ckpt sends the 4 KB from lane 0, whose row is the
+      // warp's first.
+      uint8_t* const stage = sm + C_CST + (st_t >> 5) * 4096;
+      auto stage_ckpt = [&](const uint32_t(&uu)[32]) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        store_ckpt_row(stage + lane * 128, v, uu);   // (v mod 8 == lane mod 8)
+        fence_proxy_async_smem();
+      };
+      auto send_ckpt = [&](uint8_t* row) {
+        if (lane == 0) {
+          bulk_s2g(row, stage, 4096);
+          bulk_commit();
+        }
+      };
       if (nc == 0) {
         // an empty sequence passes its initial state through (an empty range: the identity
         // map; an invalid range: NaN)
@@ -725,11 +771,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         }
         continue;
       }
-      if (!(ok = group_wait(&bars[C_RECFULL + sbase % NBUF], (sbase / NBUF) & 1, BAR_STATE, 256,
+      if (!(ok = group_wait(&bars[C_RECFULL + sbase % NB], (sbase / NB) & 1, BAR_STATE, 256,
                             cx)))
         break;
       {
-        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NBUF) * C_BUF + R_VEC + V_GC);
+        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NB) * BUF + RV + V_GC);
         float xv[64];
         if (s0p) {
           const float4* src = reinterpret_cast<const float4*>(s0p);
@@ -747,7 +793,15 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
         tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
         tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
-        if (ck) store_ckpt_row(ck, v, u);
+        if (ck) {
+          if constexpr (kOut) {
+            store_ckpt_row(ck, v, u);
+          } else {
+            stage_ckpt(u);
+            __syncwarp();
+            send_ckpt(ck);
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 64; ++e) xv[e] *= g0;
         tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -762,7 +816,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       }
       for (int c = 0; c < nc && ok; ++c) {
         const int s = sbase + c;
-        uint8_t* buf = sm + (s % NBUF) * C_BUF;
+        uint8_t* buf = sm + (s % NB) * BUF;
         if (!(ok = group_wait(&bars[C_MERGED], s & 1, BAR_STATE, 256, cx))) break;
         tc_fence_after();
         {
@@ -770,7 +824,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           // twin: -S W^T)
           float a[32];
           tmem_ld32(tl + TM_D + 32 * w, a);
-          const float* dec = reinterpret_cast<const float*>(buf + R_VEC + V_DEC) + 32 * w;
+          const float* dec = reinterpret_cast<const float*>(buf + RV + V_DEC) + 32 * w;
           tmem_ld_wait();
           uint32_t d1[16], d2[16];
 #pragma unroll
@@ -802,16 +856,20 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
           tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
           tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
+          if (!kOut && ck) stage_ckpt(u);
           tmem_st_wait();
           tc_fence_before();
           named_bar(BAR_STATE, 256);
           if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
           // state replay: the next chunk's entry state, written while its first product runs
-          if (ck) store_ckpt_row(ck + (size_t)(c + 1) * ck_stride, v, u);
+          if (ck) {
+            if constexpr (kOut) store_ckpt_row(ck + (size_t)(c + 1) * ck_stride, v, u);
+            else send_ckpt(ck + (size_t)(c + 1) * ck_stride);
+          }
           const int s1 = s + 1;
-          if (!(ok = group_wait(&bars[C_RECFULL + s1 % NBUF], (s1 / NBUF) & 1, BAR_STATE, 256, cx)))
+          if (!(ok = group_wait(&bars[C_RECFULL + s1 % NB], (s1 / NB) & 1, BAR_STATE, 256, cx)))
             break;
-          const float gn = *reinterpret_cast<const float*>(sm + (s1 % NBUF) * C_BUF + R_VEC + V_GC);
+          const float gn = *reinterpret_cast<const float*>(sm + (s1 % NB) * BUF + RV + V_GC);
 #pragma unroll
           for (int e = 0; e < 64; ++e) xv[e] *= gn;
           tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -824,6 +882,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       }
       sbase += nc;
     }
+    // every checkpoint copy has landed before the CTA leaves
+    if (!kOut && lane == 0) bulk_wait_all();
   } else {
     reg_dealloc<RC_OUT>();
     // -------------------------------------------------------------- output
@@ -842,8 +902,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
       for (int c = 0; c < nc; ++c, ++s) {
         if (!(ok = group_wait(&bars[C_ODONE], s & 1, BAR_OUT, 128, cx))) break;
         tc_fence_after();
-        const int rb = s % NBUF;
-        const float* eg = reinterpret_cast<const float*>(sm + rb * C_BUF + R_VEC + V_EG);
+        const int rb = s % NB;
+        const float* eg = reinterpret_cast<const float*>(sm + rb * BUF + RV + V_EG);
         const float sc = padded ? 0.f : p.scale;
         uint32_t ob[32];     // BF16 pairs: out rows 2e and 2e + 1 of this thread's column v
 #pragma unroll
@@ -1541,7 +1601,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
   }
 }
 
-template <bool kCopy>
+// kOut: the launch has output products (the forward); without them (state replay, segment
+// summaries) the chain CTAs keep three chunks in flight.
+template <bool kCopy, bool kOut>
 __global__ void __launch_bounds__(NTHR, 1)
     gdn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -1575,8 +1637,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
       // a record buffer is free once its chunk's products are done (MMA commit) and its
       // output tile, staged in it, has been read out (output warps)
-      // (summaries have no output)
-      for (int i = 0; i < NBUF; ++i) mbar_init(&bars[C_RECFREE + i], (p.twin || !p.out) ? 1 : 2);
+      for (int i = 0; i < 3; ++i) mbar_init(&bars[C_RECFREE + i], kOut ? 2 : 1);
     } else {
       for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
       mbar_init(&bars[P_KQFREE], 4);
@@ -1611,7 +1672,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   geo.init(p, len_s, sort_s);
 
   if (is_chain)
-    chain_cta(&tmQ4, &tmK4, &tmV4, &tmO, p, geo, sm, sb, bars, tm, cx);
+    chain_cta<kOut>(&tmQ4, &tmK4, &tmV4, &tmO, p, geo, sm, sb, bars, tm, cx);
   else
     prep_cta<kCopy>(&tmQ, &tmK, &tmQ4, &tmK4, &tmV4, p, geo, sm, sb, bars, tm, cx);
 
@@ -1716,8 +1777,12 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   if (q && (!make_bf16_map(&mq, q, rows, p.HK) || !make_bf16_map_4d(&mq4, q, rows, p.HK)))
     return cudaErrorInvalidValue;
   // the state replay that keeps the records for the backward takes the copying instantiation
-  const void* kern = p.fac ? reinterpret_cast<const void*>(gdn_fwd_split_kernel<true>)
-                           : reinterpret_cast<const void*>(gdn_fwd_split_kernel<false>);
+  const bool with_out = p.out && !p.twin;
+  if (p.fac && with_out) return cudaErrorInvalidValue;   // the replay has no output
+  const void* kern =
+      p.fac      ? reinterpret_cast<const void*>(gdn_fwd_split_kernel<true, false>)
+      : with_out ? reinterpret_cast<const void*>(gdn_fwd_split_kernel<false, true>)
+                 : reinterpret_cast<const void*>(gdn_fwd_split_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_ALLOC);
   if (e != cudaSuccess) return e;

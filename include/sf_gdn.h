@@ -258,9 +258,9 @@ sf_status sf_gdn_chunk_bwd(const sf_gdn_shape *shape, const void *q, const void 
  *  * Limit: shapes whose sf_gdn_bwd_workspace() exceeds
  *    SF_BWD_NOALLOC_SCRATCH_BYTES return SF_ERR_UNSUPPORTED.  For BF16 at
  *    K = V = 128 the scratch is 115,712 bytes per chunk-head (heads x
- *    B x ceil(T/64) dense, heads x (ceil(T/64) + N) packed) and 270,336 bytes
+ *    B x ceil(T/64) dense, heads x (ceil(T/64) + N) packed) and 540,672 bytes
  *    per (sequence, head) pair, up to 64 pairs, for the record ring of the
- *    state replay: one sequence of 2 heads fits up to T = 9024.
+ *    state replay: one sequence of 2 heads fits up to T = 8896.
  *  * The first call on a device looks up the array's device address for that
  *    device (cudaGetSymbolAddress, with the device current); make that first
  *    call before any stream capture.

@@ -106,10 +106,11 @@ def test_packed_backward_workspace_scales_with_tokens_not_sequences(lib):
     """Packed inputs (B = 1) need ceil(T/64) + N chunk slots, not N * ceil(T/64): eight
     sequences over T = 4096 at BF16, K = V = 128 cost seven chunk slots per head (115,712
     bytes each: checkpoint, cotangent, factors) and seven more replay-ring streams per head
-    (270,336 bytes each: 8 ring slots of 33,792-byte records) beyond one sequence -- not eight times as much."""
+    (540,672 bytes each: 16 ring slots of 33,792-byte records) beyond one sequence -- not
+    eight times as much."""
     one = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(T=4096, H=2, N=1)))
     eight = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(T=4096, H=2, N=8)))
-    assert eight - one == 7 * 2 * 115712 + 7 * 2 * 270336
+    assert eight - one == 7 * 2 * 115712 + 7 * 2 * 540672
     dense = lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(B=8, N=8, T=4096, H=2)))
     assert dense - eight == (8 * 64 - (64 + 8)) * 2 * 115712
 
