@@ -217,6 +217,7 @@ static_assert(NBUF <= 3 && NBUF_NO <= 3 && C_RECFREE == C_RECFULL + 3 &&
 // named barriers
 constexpr int BAR_STATE = 1, BAR_OUT = 2;       // chain: 256, 128 threads
 constexpr int BAR_PREP0 = 1;                    // preparation pipeline p: BAR_PREP0 + p
+constexpr int BAR_SOLVE0 = 3;                   // its solve's phase 2: BAR_SOLVE0 + p
 
 struct SplitParams {
   const float* g;
@@ -1011,12 +1012,12 @@ __device__ __forceinline__ void pack64(const float (&x)[64], uint32_t (&u)[32]) 
 // -T'' = -T diag(beta e^gamma) of the U and W products.  The blocking is that of
 // solve_tc.cuh -- 16x16 diagonal blocks by substitution in FP32, then
 // T_10 = -T_11 A_10 T_00 for the 32x32 halves and for the 64x64 matrix on TF32 mma --
-// arranged for four warps and a single barrier:
+// arranged for four warps, a barrier between the phases and a partial one inside phase 2:
 //  phase 1: warp p (p = 0, 1), which wrote rows 32p..32p+31 of A, inverts the half's
 //           two diagonal blocks (lanes 0-15 and 16-31, one column per lane, the block's
 //           A in registers) and merges them into the half's lower-left block;
-//  phase 2: warp w forms block (2 + w/2, w%2) of T[32:64, 0:32] =
-//           -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]).
+//  phase 2: one warp per 16x16 block of T[32:64, 0:32] = -T[32:64, 32:64] Y with
+//           Y = A[32:64, 0:32] T[0:32, 0:32], each forming one Y block first.
 // A product whose B operand is the previous product is taken in two steps: first the
 // transpose X^T = N^T M^T of the inner product (both operands from shared memory), then
 // the outer product with X^T's accumulator fragments as its B fragments -- valid once the
@@ -1137,21 +1138,52 @@ __device__ __forceinline__ void half(float* AT, uint8_t* t1, uint8_t* t2, const 
   put_block(AT, t1, t2, vs, o1, o0, ob, g, t);
 }
 
-// Phase 2 for the block (2 + MT, c) of T (one warp).
-template <int MT>
-__device__ __forceinline__ void lower(const float* AT, uint8_t* t1, uint8_t* t2, const float* vs,
-                                      int c, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  // X^T[c][kb] = sum_{j >= c} T[j][c]^T A[2 + kb][j]^T  (16x16 blocks, kb <= MT)
-  float xt[MT + 1][2][4] = {};
+// o += M N for 16x16 blocks M (rows i, columns k) and N (rows k, columns n) in shared
+// memory, with acc_nx's k-slot permutation on both operands.
+__device__ __forceinline__ void acc_nn(float (&o)[2][4], const float* M, const float* N, int g,
+                                       int t) {
 #pragma unroll
-  for (int kb = 0; kb <= MT; ++kb)
+  for (int s = 0; s < 2; ++s) {
+    const float2 r0 = *reinterpret_cast<const float2*>(M + g * L + 8 * s + 2 * t);
+    const float2 r1 = *reinterpret_cast<const float2*>(M + (g + 8) * L + 8 * s + 2 * t);
+    const uint32_t a0 = f2tf32(r0.x), a2 = f2tf32(r0.y), a1 = f2tf32(r1.x), a3 = f2tf32(r1.y);
+    const float* n0 = N + (8 * s + 2 * t) * L + g;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+      mma4(o[nt], a0, a1, a2, a3, f2tf32(n0[8 * nt]), f2tf32(n0[L + 8 * nt]));
+  }
+}
+
+// Phase 2 for the block (2 + M, c) of T (one warp), T[32:64, 0:32] = -T[32:64, 32:64] Y with
+// Y = A[32:64, 0:32] T[0:32, 0:32].  The warp forms its Y block (M, c) = sum_{j >= c}
+// A[2 + M][j] T[j][c] into the free upper-right quadrant of the A/T area (rows 16 M,
+// columns 32 + 16 c); block (2, c) needs only that one, block (3, c) also Y (0, c), for
+// which it waits on named barrier `yb` (the (2, c) warps arrive there once theirs is out).
+template <int M>
+__device__ __forceinline__ void lower(float* AT, uint8_t* t1, uint8_t* t2, const float* vs, int c,
+                                      int yb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float* Y = AT + 32 + 16 * c;
+  {
+    float y[2][4] = {};
     for (int j = c; j < 2; ++j)
-      acc_tt(xt[kb], AT + 16 * j * L + 16 * c, AT + (32 + 16 * kb) * L + 16 * j, g, t);
+      acc_nn(y, AT + (32 + 16 * M) * L + 16 * j, AT + 16 * j * L + 16 * c, g, t);
+    float* ym = Y + 16 * M * L;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      *reinterpret_cast<float2*>(ym + g * L + 8 * nt + 2 * t) = make_float2(y[nt][0], y[nt][1]);
+      *reinterpret_cast<float2*>(ym + (g + 8) * L + 8 * nt + 2 * t) =
+          make_float2(y[nt][2], y[nt][3]);
+    }
+  }
+  __syncwarp();
+  if (M == 0) named_bar_arrive(yb, 128);
+  else named_bar(yb, 128);
   float ob[2][4] = {};
 #pragma unroll
-  for (int kb = 0; kb <= MT; ++kb) acc_nx(ob, AT + (32 + 16 * MT) * L + 32 + 16 * kb, xt[kb], g, t);
-  put_block(nullptr, t1, t2, vs, 32 + 16 * MT, 16 * c, ob, g, t);
+  for (int kb = 0; kb <= M; ++kb)
+    acc_nn(ob, AT + (32 + 16 * M) * L + 32 + 16 * kb, Y + 16 * kb * L, g, t);
+  put_block(nullptr, t1, t2, vs, 32 + 16 * M, 16 * c, ob, g, t);
 }
 
 }  // namespace solve
@@ -1495,9 +1527,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       // the two heavier blocks (row block 3) go to sub-partitions 2, 3 in pipeline 0 and to
       // 0, 1 in pipeline 1, so that each sub-partition gets one of them
       if (((warp & 3) < 2) == (pp == 0))
-        solve::lower<0>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
+        solve::lower<0>(AT, base + P_T1, base + P_T2, vs, warp & 1, BAR_SOLVE0 + pp, lane);
       else
-        solve::lower<1>(AT, base + P_T1, base + P_T2, vs, warp & 1, lane);
+        solve::lower<1>(AT, base + P_T1, base + P_T2, vs, warp & 1, BAR_SOLVE0 + pp, lane);
       fence_proxy_async_smem();
       named_bar(bid, 128);
       if (r == 0) {
