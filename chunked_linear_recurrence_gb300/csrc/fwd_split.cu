@@ -772,11 +772,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         }
         continue;
       }
-      if (!(ok = group_wait(&bars[C_RECFULL + sbase % NB], (sbase / NB) & 1, BAR_STATE, 256,
-                            cx)))
-        break;
       {
-        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NB) * BUF + RV + V_GC);
+        // the entry state as the first product's BF16 operand needs nothing from the
+        // record, so it goes out before the first buffer has landed (the products of the
+        // CTA's previous chain that read it completed before that chain's last SUDONE);
+        // the FP32 copy is scaled by the chunk's e^{gamma_C} once the buffer is in
         float xv[64];
         if (s0p) {
           const float4* src = reinterpret_cast<const float4*>(s0p);
@@ -789,20 +789,26 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
 #pragma unroll
           for (int e = 0; e < 64; ++e) xv[e] = s_init(e);
         }
-        uint32_t u[32];
+        {
+          uint32_t u[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
-        tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
-        tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
-        if (ck) {
-          if constexpr (kOut) {
-            store_ckpt_row(ck, v, u);
-          } else {
-            stage_ckpt(u);
-            __syncwarp();
-            send_ckpt(ck);
+          for (int e = 0; e < 32; ++e) u[e] = pack_bf16x2(xv[2 * e], xv[2 * e + 1]);
+          tmem_st16(tl + TM_SB + 32 * w, *reinterpret_cast<const uint32_t(*)[16]>(u));
+          tmem_st16(tl + TM_SB + 32 * w + 16, *reinterpret_cast<const uint32_t(*)[16]>(u + 16));
+          if (ck) {
+            if constexpr (kOut) store_ckpt_row(ck, v, u);
+            else stage_ckpt(u);
           }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(BAR_STATE, 256);
+        if (st_t == 0) mbar_arrive(&bars[C_SREADY]);
+        if (!kOut && ck) send_ckpt(ck);
+        if (!(ok = group_wait(&bars[C_RECFULL + sbase % NB], (sbase / NB) & 1, BAR_STATE, 256,
+                              cx)))
+          break;
+        const float g0 = *reinterpret_cast<const float*>(sm + (sbase % NB) * BUF + RV + V_GC);
 #pragma unroll
         for (int e = 0; e < 64; ++e) xv[e] *= g0;
         tmem_st32(tl + TM_S + 64 * w, *reinterpret_cast<float(*)[32]>(xv));
@@ -810,10 +816,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         tmem_st_wait();
         tc_fence_before();
         named_bar(BAR_STATE, 256);
-        if (st_t == 0) {
-          mbar_arrive(&bars[C_SREADY]);
-          mbar_arrive(&bars[C_SSCALED]);
-        }
+        if (st_t == 0) mbar_arrive(&bars[C_SSCALED]);
       }
       for (int c = 0; c < nc && ok; ++c) {
         const int s = sbase + c;
@@ -1248,15 +1251,16 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       uint8_t* base = sm + pp * P_STRIDE;
       // pipeline 0 keeps [K;Q] in its tile rows, pipeline 1 [Q;K] (see the pipelines)
       const uint32_t kq_k = pp ? 8192u : 0u, kq_q = pp ? 0u : 8192u;
-      auto claim = [&]() -> int {
-        int g = 0;
-        if (lane == 0) g = (int)atomicAdd(p.next_item, 1u);
-        return __shfl_sync(0xffffffffu, g, 0);
-      };
+      // The first two items of every pipeline are fixed (pipeline q = 2 (CTA index) + pp
+      // of the 2 nprep takes items q and 2 nprep + q), so that the launch starts without
+      // waiting on the counter; the rest are claimed from it, after those 4 nprep.
+      const int nq = 2 * p.nprep, q = 2 * ((int)blockIdx.x - (p.nch * (p.twin ? 2 : 1))) + pp;
       // lane 0's claim in flight (its result is read one use later, so that the atomic's
       // round trip overlaps a whole use)
       auto claim_start = [&]() -> uint32_t { return lane == 0 ? atomicAdd(p.next_item, 1u) : 0u; };
-      auto claim_end = [&](uint32_t c) -> int { return __shfl_sync(0xffffffffu, (int)c, 0); };
+      auto claim_end = [&](uint32_t c) -> int {
+        return __shfl_sync(0xffffffffu, (int)c, 0) + 2 * nq;
+      };
       // An item's geometry, its gate/beta values (two tokens per lane, loaded one use
       // ahead so that their latency overlaps the waits), and its tiles warmed in L2 (V
       // for the chain CTA that will load it).
@@ -1283,11 +1287,10 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       int last = -1;                 // last use with a tile copy
       bool ok = true;
       // items are claimed three uses ahead: `cur` is this use's, `nxt` the next one's,
-      // and the claim in flight the one after (every claimed item below geo.total is
-      // processed: a pipeline's claims only grow, so once one is past the end, so are the
-      // ones after it)
-      Next cur = fetch(claim());
-      int gnn = claim();
+      // and the claim in flight the one after (every item below geo.total is processed: a
+      // pipeline's items only grow, so once one is past the end, so are the ones after it)
+      Next cur = fetch(q);
+      int gnn = nq + q;
       uint32_t inflight = claim_start();
       for (int use = 0; ok; ++use) {
         const bool done = cur.g >= geo.total;
