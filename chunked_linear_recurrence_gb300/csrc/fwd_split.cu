@@ -13,7 +13,7 @@
 // walking their chunks in order; the other CTAs are preparation CTAs that turn
 // chunks into "records" (the chunk's factors as ready-made BF16 tensor-core tiles) in
 // the order the chains consume them, two chunks in flight per CTA.  Records pass
-// through a per-chain-CTA ring of NSLOT slots in global memory (small enough to stay
+// through a per-chain-CTA ring of 8 or 16 slots in global memory (small enough to stay
 // in L2); a slot's `ready` flag (release/acquire) hands it to the chain CTA, which
 // copies it into shared memory with a bulk copy and hands the slot back through its
 // `consumed` counter.  This is StateFlow's split of Pre from ST (section 3.4.2,
@@ -66,7 +66,11 @@ using namespace tc;
 
 constexpr int D = 128;
 constexpr int NTHR = 512;
-constexpr int NSLOT = 16;         // ring slots per chain CTA
+// Ring slots per chain CTA: a launch with output (its preparation has little slack, and
+// 64 chain CTAs' rings of 8 stay in L2) takes NSLOT_OUT, the others (replay, summaries:
+// preparation ahead, a deeper ring hides the hand-over latency) NSLOT_MAX, which the
+// workspace always has room for.
+constexpr int NSLOT_OUT = 8, NSLOT_MAX = 16;
 constexpr int NBUF = 2;           // chunk buffers (record + K, Q, V tiles) of a chain CTA
 constexpr int NBUF_NO = 3;        // the same without output (no Q tile): replay, summaries
 constexpr int MAX_NCH = 64;       // chain CTAs that own record streams, at most
@@ -233,8 +237,9 @@ struct SplitParams {
   int* abort_g;              // global abort flag
   uint32_t* next_item;       // items claimed so far by the preparation CTAs
   uint32_t* consumed;        // [nch] records consumed (copied out), one line per chain CTA
-  uint32_t* ready;           // [nch] lines: [NSLOT] stream position + 1 of the slot's record
-  uint8_t* ring;             // [nch][NSLOT][REC_BYTES]
+  uint32_t* ready;           // [nch] lines: [nslot] stream position + 1 of the slot's record
+  uint8_t* ring;             // [nch][nslot][REC_BYTES]
+  int nslot;                 // ring slots per chain CTA (a power of two)
   const int32_t* cu;         // packed sequences: cu_seqlens [N+1], else NULL
   int* sstart;               // packed: [N*H] first stream position of each chain in its CTA
   int* slot0;                // packed: [N] first backward slot of each sequence
@@ -494,7 +499,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
   const int j = ptwin ? (int)blockIdx.x - geo.nch : (int)blockIdx.x;   // the stream's owner
   const int cnt = geo.chains_of(j);
   const int len = geo.len_of(j);
-  const uint8_t* ringj = p.ring + (size_t)j * NSLOT * REC_BYTES;
+  const uint8_t* ringj = p.ring + (size_t)j * p.nslot * REC_BYTES;
+  const int smask = p.nslot - 1;
   const uint32_t* readyj = p.ready + (size_t)j * FLAG_STRIDE;
   uint32_t* const consumed_me = p.consumed + (size_t)blockIdx.x * FLAG_STRIDE;
 
@@ -545,7 +551,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         // wait for the buffer), then the buffer, free once the chunk that used it has had
         // its products and its output read
         if (lane == 0) {
-          ok = flag_next >= (uint32_t)s + 1 || poll_ge(readyj + s % NSLOT, (uint32_t)s + 1, cx);
+          ok = flag_next >= (uint32_t)s + 1 || poll_ge(readyj + (s & smask), (uint32_t)s + 1, cx);
           // the producer's plain stores before its release, then our bulk reads
           if (ok) fence_proxy_async_global();
           ok = ok && (s < NB || wait_bar(&bars[C_RECFREE + b], ((s - NB) / NB) & 1, cx));
@@ -554,7 +560,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         part_of = (part_of & ~(1u << b)) | ((part ? 1u : 0u) << b);
         if (lane == 0) {
           mbar_arrive_expect_tx(txbar, tx);
-          const uint8_t* src = ringj + (size_t)(s % NSLOT) * REC_BYTES;
+          const uint8_t* src = ringj + (size_t)(s & smask) * REC_BYTES;
           if (has_out) {
             bulk_g2s(buf, src, REC_BYTES, txbar);
           } else {
@@ -568,7 +574,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
         }
         issued = s + 1;
         // the next record's flag, read now and looked at next time round
-        if (lane == 0 && s + 1 < len) flag_next = ld_acquire_u32(readyj + (s + 1) % NSLOT);
+        if (lane == 0 && s + 1 < len) flag_next = ld_acquire_u32(readyj + ((s + 1) & smask));
         if (part) {
           const uint32_t ph = (landed_uses >> b) & 1u;
           landed_uses ^= 1u << b;
@@ -595,7 +601,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap* tmQ, const CUtensor
           int n = rel;
           if (s >= NB && n < s - NB + 1) n = s - NB + 1;
           while (n < s && mbar_test(&bars[C_RECFULL + n % NB], (n / NB) & 1)) ++n;
-          if (n >= rel + 2) release_to(n);   // two slots at a time (the ring has NSLOT)
+          if (n >= rel + 2) release_to(n);   // two slots at a time (the ring has nslot)
         }
       }
       if (lane == 0) {
@@ -1510,8 +1516,8 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       if (lane == 0) mbar_arrive(&bars[P_KQFREE + pp]);
       // T = (I + A)^{-1} as T' = T diag(beta) and -T'' = -T diag(beta e^gamma).  Phase 1
       // needs only the rows this warp wrote; meanwhile the Ahat warps store their rows to
-      // the record's ring slot once the publisher has seen it free (s % NSLOT).
-      uint8_t* rec = p.ring + ((size_t)jj * NSLOT + s % NSLOT) * REC_BYTES;
+      // the record's ring slot once the publisher has seen it free (s mod nslot).
+      uint8_t* rec = p.ring + ((size_t)jj * p.nslot + (s & (p.nslot - 1))) * REC_BYTES;
       // state replay: the record's copy for the backward (Ahat, (-W)^T and the decays)
       uint8_t* rec2 = kCopy ? p.fac + (size_t)fx * REC2_BYTES : nullptr;
       bool ok1 = true;
@@ -1613,14 +1619,16 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
           if (pj >= 0) {
             if (!wait_bar(&bars[P_PUB + pp], (u - 1) & 1, cx)) { raise_abort(cx); break; }
             if (pg != p.drop_item)
-              st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + ps % NSLOT, (uint32_t)ps + 1);
+              st_release_u32(p.ready + (size_t)pj * FLAG_STRIDE + (ps & (p.nslot - 1)),
+                             (uint32_t)ps + 1);
             pj = -1;
           }
           if (g < 0) break;
-          const bool ok = s < NSLOT ||
-                          (poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, (uint32_t)(s - NSLOT + 1), cx) &&
+          const uint32_t need = (uint32_t)(s - p.nslot + 1);
+          const bool ok = s < p.nslot ||
+                          (poll_ge(p.consumed + (size_t)jj * FLAG_STRIDE, need, cx) &&
                            (!summ || poll_ge(p.consumed + (size_t)(jj + geo.nch) * FLAG_STRIDE,
-                                             (uint32_t)(s - NSLOT + 1), cx)));
+                                             need, cx)));
           if (!ok) {
             raise_abort(cx);
             break;
@@ -1784,7 +1792,7 @@ int summary_chain_ctas(int R, int H) {
   const long long k = (nh + SF_SUMMARY_CHAINS - 1) / SF_SUMMARY_CHAINS;
   return (int)((nh + k - 1) / k);
 }
-size_t ws_ring_end(int nch) { return WS_RING + (size_t)nch * NSLOT * REC_BYTES; }
+size_t ws_ring_end(int nch) { return WS_RING + (size_t)nch * NSLOT_MAX * REC_BYTES; }
 size_t ws_total(int nch, int N, int H) {
   return ws_ring_end(nch) + (((size_t)N * H + 2 * MAX_NCH + N) * sizeof(int) + 255) / 256 * 256;
 }
@@ -1832,6 +1840,7 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
   p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
   p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
+  p.nslot = with_out ? NSLOT_OUT : NSLOT_MAX;
   p.sstart = reinterpret_cast<int*>(w + ws_ring_end(p.nch));
   p.lenj = p.sstart + (size_t)NH;
   p.sortj = p.lenj + MAX_NCH;
