@@ -1308,6 +1308,26 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         const int jj = cur.jj, s = cur.s, hk = cur.hk, row0 = cur.row0, L = cur.L;
         const long long gitem = cur.g;
         const int ub = use & 1;        // vector slot and tile buffer of this use
+        // the [K;Q] tile first (it needs only the item's rows), then the vectors while it lands
+        uint8_t* const kq = base + P_KQ + ub * P_KQ_BUF;
+        if (!done) {
+          // tile buffer ub: the product that read it last, (-W)^T of item use - 2, is done
+          // (before the item's vector slot comes back, so this wait cannot hold that up)
+          if (use >= 2 &&
+              !(ok = warp_wait(&bars[P_ITEMFREE + 2 * pp + ub], ((use - 2) >> 1) & 1, cx)))
+            break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[P_FULL + 2 * pp + ub], 2 * 16384);
+#pragma unroll
+            for (int pnl = 0; pnl < 2; ++pnl) {
+              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
+                          row0);
+              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
+                          row0);
+            }
+          }
+          last = use;
+        }
         // the slot and the buffer are free once the item two uses back has finished (one
         // barrier per slot, so a phase can never be mistaken for the one two items later)
         if (use >= 2 && !(ok = warp_wait(&bars[P_VECFREE + 2 * pp + ub], ((use - 2) >> 1) & 1, cx)))
@@ -1361,22 +1381,6 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         }
         __syncwarp();
         if (!done) {
-          // tile buffer ub: the product that read it last, (-W)^T of item use - 2, is done
-          if (use >= 2 &&
-              !(ok = warp_wait(&bars[P_ITEMFREE + 2 * pp + ub], ((use - 2) >> 1) & 1, cx)))
-            break;
-          uint8_t* kq = base + P_KQ + ub * P_KQ_BUF;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[P_FULL + 2 * pp + ub], 2 * 16384);
-#pragma unroll
-            for (int pnl = 0; pnl < 2; ++pnl) {
-              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_k, tmK, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
-                          row0);
-              tma_load_3d(kq + pnl * P_KQ_PANEL + kq_q, tmQ, &bars[P_FULL + 2 * pp + ub], 64 * pnl, hk,
-                          row0);
-            }
-          }
-          last = use;
           if (L < CHUNK) {
             // rows past the sequence end: zero K and Q so they add nothing to any product
             if (!(ok = warp_wait(&bars[P_FULL + 2 * pp + ub], (use >> 1) & 1, cx))) break;
