@@ -204,14 +204,14 @@ enum {
   P_FULL = 0,      // [2 pipelines][2 buffers] K and Q tiles landed (tx)
   P_HEAD = 4,      // [2][2 slots] controller: item slot, decay vectors, padding rows zeroed
   P_KQDONE = 8,    // [2]
-  P_TT = 10,       // [2] T', -T'' written
   P_WDONE = 12,    // [2] (-W)^T complete
   P_ITEMFREE = 14, // [2][2 buffers] the tile buffer's last product, (-W)^T, done
   P_PUB = 18,      // [2] item's record landed (one arrival per warp): it may be released
   P_SLOTOK = 20,   // [2] publisher: the item's ring slot has been copied out by its chain CTA
   P_KQFREE = 22,   // [2] KQ accumulator of a pipeline read out (one arrival per warp)
   P_VECFREE = 24,  // [2][2] vector slot (pipeline, use % 2) free: its item finished
-  P_DRAIN = 28,    // [2][2] MMA issuers (KQ, W), abort path only: their products completed
+  P_DRAIN = 28,    // [2][2] MMA issuers (KQ, the pipeline's W), abort path only: their
+                   //        products completed
   P_COUNT = 32
 };
 static_assert(P_COUNT * 8 <= 256 && C_COUNT * 8 <= 256, "barrier area (TMEM address at +256)");
@@ -991,12 +991,6 @@ __device__ __forceinline__ void store_rows(uint8_t* gtile, uint8_t* gtile2, uint
   }
 }
 
-// The warp's record stores have read their staging areas.
-__device__ __forceinline__ void record_read(int lane) {
-  if (lane == 0) bulk_wait_read_all();
-  __syncwarp();
-}
-
 // The warp's record stores have landed in global memory; then lane 0 counts the warp in
 // on `pub` (four arrivals: the record may be released).
 __device__ __forceinline__ void record_landed(int lane, uint64_t* pub) {
@@ -1205,10 +1199,10 @@ __device__ __forceinline__ void lower(float* AT, uint8_t* t1, uint8_t* t2, const
 //     into one of two buffers;
 //   KQ issuer (warp 2p + 1): [K;Q] K^T of each item once its tiles have landed and the
 //     previous item's accumulator was read out -- typically during the previous solve;
-//   W issuer (warp 12 + p): (-W)^T of each item once its -T'' is written;
 //   publisher (warp 14 + p): the release of each finished record and the ring-slot check
 //     of the next;
-// and four warps (4-7, 8-11) that turn the products into the record.  Every role waits
+// and four warps (4-7, 8-11) that turn the products into the record, one of whose threads
+// issues (-W)^T as soon as the solve is done (warps 12, 13 are idle).  Every role waits
 // (suspended) only on what it needs, so none of them holds up another.
 // A pipeline's item u: [K;Q] K^T (issued while item u-1 is still in its solve), the
 // decayed A and Ahat, the solve to T' and -T'', (-W)^T = K^T (-T'')^T; the record it
@@ -1461,6 +1455,7 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     fence_proxy_async_smem();
     bool ok = true;
     bool pend = false;     // the previous item's record stores may be in flight
+    bool w_issued = false;     // thread r == 0: it has issued a (-W)^T product
     for (int use = 0; ok; ++use) {
       const float* vs = vec_of(pp, use);
       // the controller's item slot and vectors for this use (HEAD), then the chunk's
@@ -1546,7 +1541,20 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       fence_proxy_async_smem();
       named_bar(bid, 128);
       if (r == 0) {
-        mbar_arrive(&bars[P_TT + pp]);
+        // (-W)^T = K^T (-T'')^T, issued here as soon as -T'' is complete (the previous
+        // item's (-W)^T was read out before its last barrier); its commits tell this
+        // pipeline (WDONE) and the feeder (ITEMFREE: the tile buffer is free)
+        tc_fence_after();
+        const uint32_t kq = sb + pp * P_STRIDE + P_KQ + (use & 1) * P_KQ_BUF;
+        const uint64_t ak = sdesc_sw128(kq + (pp ? 8192u : 0u), P_KQ_PANEL, 1024);
+        const uint64_t b2 = sdesc_sw128(sb + pp * P_STRIDE + P_T2, 0, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tm + 256 * pp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2),
+                   ID_AMN, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[P_WDONE + pp]);
+        mma_commit(&bars[P_ITEMFREE + 2 * pp + (use & 1)]);
+        w_issued = true;
         // T' goes to the record as it is: the chain CTA's B operand of U^T = V^T T'^T
         bulk_s2g(rec + R_T1, base + P_T1, 8192);
         bulk_commit();
@@ -1569,7 +1577,9 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         else reinterpret_cast<float*>(rec2 + R_VEC + V_EG)[r - 64] = vs[VEC_EG + r - 64];
         if (r == 0) reinterpret_cast<float*>(rec2 + R_VEC + V_GC)[0] = vs[VEC_EG + 63];
       }
-      record_read(lane);     // the A/T and X areas, and T', are written again by the next item
+      // The A/T and X areas and T', which the next item writes again, are free once every
+      // warp has seen its own stores land (record_landed at the next item's start) and
+      // passed the KQDONE barrier after that; this barrier is for the vector slot.
       pend = true;
       tc_fence_before();
       named_bar(bid, 128);
@@ -1578,37 +1588,15 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
     // the last record (and, on the abort path, every bulk store) lands before leaving
     if (pend) record_landed(lane, &bars[P_PUB + pp]);
     else if (lane == 0) bulk_wait_all();
+    if (w_issued && *cx.abort_l) {
+      // leave no (-W)^T product running into the TMEM that the CTA frees on its way out
+      mma_commit(&bars[P_DRAIN + 2 * pp + 1]);
+      mbar_wait(&bars[P_DRAIN + 2 * pp + 1], 0, 100000000ull);
+    }
   } else {
     reg_dealloc<RP_AUX>();
     const int pp = warp & 1;
-    if (warp < 14) {
-      // ------------------------------------------------------------ W issuer
-      // (-W)^T = K^T (-T'')^T of item u once its -T'' is written (TT)
-      if (lane == 0) {
-        const uint32_t base = sb + pp * P_STRIDE, tp = tm + 256 * pp;
-        const uint32_t kq_k = pp ? 8192u : 0u;
-        for (int u = 0;; ++u) {
-          if (!wait_bar(&bars[P_HEAD + 2 * pp + (u & 1)], (u >> 1) & 1, cx)) { raise_abort(cx); break; }
-          if (reinterpret_cast<const int*>(vec_of(pp, u))[VEC_ITEM] < 0) break;
-          if (!wait_bar(&bars[P_TT + pp], u & 1, cx)) { raise_abort(cx); break; }
-          tc_fence_after();
-          const uint32_t kq = base + P_KQ + (u & 1) * P_KQ_BUF;
-          const uint64_t ak = sdesc_sw128(kq + kq_k, P_KQ_PANEL, 1024);
-          const uint64_t b2 = sdesc_sw128(base + P_T2, 0, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tp + TP_WT, ak + (uint64_t)(kk * 2048 >> 4), b2 + (uint64_t)(kk * 2), ID_AMN,
-                     kk > 0 ? 1u : 0u);
-          mma_commit(&bars[P_WDONE + pp]);
-          mma_commit(&bars[P_ITEMFREE + 2 * pp + (u & 1)]);
-        }
-        if (*cx.abort_l) {
-          mma_commit(&bars[P_DRAIN + 2 * pp + 1]);
-          mbar_wait(&bars[P_DRAIN + 2 * pp + 1], 0, 100000000ull);
-        }
-      }
-      __syncwarp();
-    } else {
+    if (warp >= 14) {
       // ------------------------------------------------------------ publisher
       // Record u-1 is released once its stores have landed (PUB: the pipeline's warps
       // arrive when they start item u), and item u's ring slot must have been copied out
