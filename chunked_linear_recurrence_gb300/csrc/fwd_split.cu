@@ -66,10 +66,11 @@ using namespace tc;
 
 constexpr int D = 128;
 constexpr int NTHR = 512;
-// Ring slots per chain CTA: a launch with output (its preparation has little slack, and
-// 64 chain CTAs' rings of 8 stay in L2) takes NSLOT_OUT, the others (replay, summaries:
-// preparation ahead, a deeper ring hides the hand-over latency) NSLOT_MAX, which the
-// workspace always has room for.
+// Ring slots per chain CTA: a dense launch with output and one chain per chain CTA (its
+// preparation has little slack, and 64 chain CTAs' rings of 8 stay in L2) takes
+// NSLOT_OUT; the others (replay, summaries: preparation ahead, a deeper ring hides the
+// hand-over latency; packed inputs and several chains per CTA: streams of different
+// lengths) NSLOT_MAX, which the workspace always has room for.
 constexpr int NSLOT_OUT = 8, NSLOT_MAX = 16;
 constexpr int NBUF = 2;           // chunk buffers (record + K, Q, V tiles) of a chain CTA
 constexpr int NBUF_NO = 3;        // the same without output (no Q tile): replay, summaries
@@ -1832,7 +1833,11 @@ cudaError_t launch_split(SplitParams& p, const void* q, const void* k, const voi
   p.consumed = reinterpret_cast<uint32_t*>(w + WS_CONSUMED);
   p.ready = reinterpret_cast<uint32_t*>(w + WS_READY);
   p.ring = reinterpret_cast<uint8_t*>(w + WS_RING);
-  p.nslot = with_out ? NSLOT_OUT : NSLOT_MAX;
+  // the short ring only where every chain CTA owns one chain of the same length (dense
+  // inputs, N H <= 64): with several chains per CTA, or packed lengths, the streams'
+  // lengths differ and the preparation needs the slack of the long one
+  const bool one_chain_each = !p.cu && !p.bounds && (long long)p.N * p.H <= MAX_NCH;
+  p.nslot = (with_out && one_chain_each) ? NSLOT_OUT : NSLOT_MAX;
   p.sstart = reinterpret_cast<int*>(w + ws_ring_end(p.nch));
   p.lenj = p.sstart + (size_t)NH;
   p.sortj = p.lenj + MAX_NCH;

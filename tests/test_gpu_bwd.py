@@ -69,3 +69,19 @@ def test_bwd_unsupported_f32_d128():
     with pytest.raises(sf.SfError) as ei:
         run_bwd(inp)
     assert ei.value.status == 2
+
+
+def test_bwd_bf16_one_long_chain():
+    """Dense K = V = 128 with one (sequence, head) chain of 32 chunks: in the launch that runs
+    the reverse chain beside the token gradients, every gradient CTA but the first waits for
+    that one chain's exit cotangents, in the order the chain writes them."""
+    inp = small_inputs(1, 2048, 1, 128, torch.bfloat16, seed=2048, grads=True)
+    check_bwd(inp, 2e-2)
+
+
+def test_bwd_bf16_sixty_four_chains():
+    """Dense K = V = 128 with 64 chains (B = 32, H = 2, a partial last chunk): the most
+    chains the shared launch takes; each chain CTA joins the token gradients after its
+    chain."""
+    inp = small_inputs(32, 130, 2, 128, torch.bfloat16, seed=64, grads=True)
+    check_bwd(inp, 2e-2)
