@@ -189,3 +189,12 @@ def test_bf16_128_without_tensor_map_encoder_is_unsupported(lib):
     for status, msg in zip(r[0::2], r[1::2]):
         assert status == 2, (status, msg)               # SF_ERR_UNSUPPORTED
         assert b"cuTensorMapEncodeTiled" in msg, msg
+
+
+def test_noalloc_scratch_capacity_matches_the_header(lib):
+    """The allocation-free backward takes shapes whose sf_gdn_bwd_workspace fits its fixed
+    scratch (SF_BWD_NOALLOC_SCRATCH_BYTES, 32 MiB); the header states that one sequence of
+    2 heads at BF16, K = V = 128 fits up to T = 8896, and no longer."""
+    scratch = 32 << 20
+    ws = lambda T: lib.sf_gdn_bwd_workspace(ctypes.byref(_shape(T=T, H=2, N=1)))
+    assert ws(8896) <= scratch < ws(8897)
