@@ -1295,11 +1295,6 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
       uint32_t inflight = claim_start();
       for (int use = 0; ok; ++use) {
         const bool done = cur.g >= geo.total;
-        const Next nxt = fetch(done ? cur.g : gnn);
-        if (!done && nxt.g < geo.total) {
-          gnn = claim_end(inflight);
-          inflight = claim_start();
-        }
         const int jj = cur.jj, s = cur.s, hk = cur.hk, row0 = cur.row0, L = cur.L;
         const long long gitem = cur.g;
         const int ub = use & 1;        // vector slot and tile buffer of this use
@@ -1392,6 +1387,13 @@ __device__ __forceinline__ void prep_cta(const CUtensorMap* tmQ, const CUtensorM
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[P_HEAD + 2 * pp + ub]);
         if (done) break;
+        // the next item's gate/beta loads and L2 prefetches, then the claim after it (the
+        // atomic's round trip is waited for only here, off the way to this use's HEAD)
+        const Next nxt = fetch(gnn);
+        if (nxt.g < geo.total) {
+          gnn = claim_end(inflight);
+          inflight = claim_start();
+        }
         cur = nxt;
       }
       // never leave with a tile copy in flight (the last two uses may each have one)
